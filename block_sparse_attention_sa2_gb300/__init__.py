@@ -1,0 +1,18 @@
+"""GB300 (sm_103a) hot path of SpargeAttention2: hybrid Top-k + Top-p block mask and
+trainable block-sparse attention, behind the C ABI of include/sa2.h.
+
+The Python surface is a thin ctypes binding (``sa2.py``); the library is built in-tree by
+``build_lib.build()``.
+"""
+from .sa2 import (  # noqa: F401
+    BlockMask,
+    Sa2Error,
+    attn_bwd,
+    attn_fwd,
+    blocks,
+    build_mask,
+    check_device,
+    device_status,
+    load_library,
+    make_shape,
+)

@@ -1,0 +1,146 @@
+// Host-side TMA descriptors and the element-wise kernels around the attention kernels:
+// fp32 -> bf16 staging of SA2_FP32 inputs, the backward's preprocessing
+// (D = rowsum(dO * O), zeroed fp32 dQ accumulator) and the dQ conversion.
+#include <algorithm>
+#include <cstring>
+#include <cudaTypedefs.h>
+
+#include "sa2_internal.h"
+
+namespace sa2 {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 [B, H, N, d] viewed as a 4-D tensor (d, N, H, B); boxes of 64 channels x box_rows
+// tokens with the 128-byte swizzle the tcgen05 descriptors expect.  Tokens past N read
+// as zero.
+bool make_token_map(CUtensorMap* map, const void* base, const ShapeArgs& s, int64_t sb, int64_t sh, int64_t sn,
+                    int box_rows) {
+  auto enc = encode_tiled();
+  if (!enc) return false;
+  std::memset(map, 0, sizeof(*map));
+  cuuint64_t dims[4] = {(cuuint64_t)s.d, (cuuint64_t)s.N, (cuuint64_t)s.H, (cuuint64_t)s.B};
+  cuuint64_t strides[3] = {(cuuint64_t)sn * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// fp32 token tensor (caller strides) -> contiguous bf16 [B, H, N, d].
+__global__ void to_bf16_kernel(const float* __restrict__ src, ShapeArgs s, __nv_bfloat16* __restrict__ dst) {
+  const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = i * 4;
+    const int c = (int)(e % s.d);
+    const int64_t t = e / s.d;
+    const int n = (int)(t % s.N);
+    const int64_t bh = t / s.N;
+    const int h = (int)(bh % s.H), b = (int)(bh / s.H);
+    const float4 v = *reinterpret_cast<const float4*>(src + b * s.sb + h * s.sh + (int64_t)n * s.sn + c);
+    uint2 w;
+    w.x = pack_bf16x2(v.x, v.y);
+    w.y = pack_bf16x2(v.z, v.w);
+    *reinterpret_cast<uint2*>(dst + e) = w;
+  }
+}
+
+cudaError_t launch_to_bf16(const float* src, const ShapeArgs& s, __nv_bfloat16* dst, cudaStream_t st) {
+  const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
+  const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 152 * 16);
+  to_bf16_kernel<<<blocks, 256, 0, st>>>(src, s, dst);
+  return cudaGetLastError();
+}
+
+template <typename T>
+__device__ __forceinline__ float ld_elem(const T* p);
+template <>
+__device__ __forceinline__ float ld_elem<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+// One warp per token row: D = sum_c dO[c] * O[c] (fp32), and the row of the fp32 dQ
+// accumulator set to zero.
+template <typename T>
+__global__ void bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dO, ShapeArgs s,
+                                      float* __restrict__ Dvec, float* __restrict__ dq_acc) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)s.B * s.H * s.N;
+  for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; row < rows;
+       row += (int64_t)gridDim.x * blockDim.x / 32) {
+    const int n = (int)(row % s.N);
+    const int64_t bh = row / s.N;
+    const int h = (int)(bh % s.H), b = (int)(bh / s.H);
+    const int64_t off = b * s.sb + h * s.sh + (int64_t)n * s.sn;
+    float acc = 0.f;
+    for (int c = lane; c < s.d; c += 32) acc += ld_elem<T>(o + off + c) * ld_elem<T>(dO + off + c);
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    if (lane == 0) Dvec[row] = acc;
+    float* dq = dq_acc + row * s.d;
+    for (int c = lane; c < s.d; c += 32) dq[c] = 0.f;
+  }
+}
+
+cudaError_t launch_bwd_preprocess(const ShapeArgs& s, const void* o, const void* dO, float* Dvec, float* dq_acc,
+                                  cudaStream_t st) {
+  const int64_t rows = (int64_t)s.B * s.H * s.N;
+  const int blocks = (int)std::min<int64_t>((rows * 32 + 255) / 256, 152 * 16);
+  if (s.dtype == 0)
+    bwd_preprocess_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
+                                                                 static_cast<const __nv_bfloat16*>(dO), s, Dvec,
+                                                                 dq_acc);
+  else
+    bwd_preprocess_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(o),
+                                                         static_cast<const float*>(dO), s, Dvec, dq_acc);
+  return cudaGetLastError();
+}
+
+// fp32 dQ accumulator (contiguous) -> dq in the call's dtype and strides.
+template <typename T>
+__global__ void dq_convert_kernel(const float* __restrict__ acc, ShapeArgs s, T* __restrict__ dq) {
+  const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = i * 4;
+    const int c = (int)(e % s.d);
+    const int64_t t = e / s.d;
+    const int n = (int)(t % s.N);
+    const int64_t bh = t / s.N;
+    const int h = (int)(bh % s.H), b = (int)(bh / s.H);
+    const float4 v = *reinterpret_cast<const float4*>(acc + e);
+    T* p = dq + b * s.sb + h * s.sh + (int64_t)n * s.sn + c;
+    if constexpr (sizeof(T) == 4) {
+      *reinterpret_cast<float4*>(p) = v;
+    } else {
+      uint2 w;
+      w.x = pack_bf16x2(v.x, v.y);
+      w.y = pack_bf16x2(v.z, v.w);
+      *reinterpret_cast<uint2*>(p) = w;
+    }
+  }
+}
+
+cudaError_t launch_dq_convert(const ShapeArgs& s, const float* dq_acc, void* dq, cudaStream_t st) {
+  const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
+  const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 152 * 16);
+  if (s.dtype == 0)
+    dq_convert_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(dq_acc, s, static_cast<__nv_bfloat16*>(dq));
+  else
+    dq_convert_kernel<float><<<blocks, 256, 0, st>>>(dq_acc, s, static_cast<float*>(dq));
+  return cudaGetLastError();
+}
+
+}  // namespace sa2

@@ -1,0 +1,339 @@
+// Block-sparse attention forward on sm_103a (tcgen05 + TMEM + TMA).
+//
+// gist.science explainer of SpargeAttention2 (arXiv 2602.13515), section 2.C: a
+// FlashAttention-style block-sparse kernel in which whole tiles are kept or skipped, and
+// skipped tiles cost neither matmul nor softmax.  Here each CTA owns one query block of
+// 128 rows and walks that block's list of kept 64-token key blocks.
+//
+// Roles (192 threads, 2 CTAs per SM):
+//   warp 0      TMA producer: Q once, then K_j / V_j per kept key block into NS stages
+//   warp 1      TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into a double
+//               buffered TMEM tile, O += P_j V_j with P_j read from TMEM
+//   warps 2..5  softmax: each thread owns one query row (its TMEM lane); online softmax in
+//               fp32 with exp2, P_j (bf16) written back over S_j in TMEM; epilogue O / l
+//
+// TMEM columns: S buffers at 0 and 64 (fp32, 64 columns each; P_j as packed bf16 pairs in
+// the first 32 columns of its S buffer), O at 128 (D columns).
+#include "sa2_internal.h"
+
+namespace sa2 {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kNumStages = 2;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 128;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: O and l are rescaled only past 2^8
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kPanels = D / 64;
+  static constexpr int kQBytes = 128 * 128 * kPanels;   // 128 rows x 128 B per panel
+  static constexpr int kKVBytes = 64 * 128 * kPanels;   // 64 rows x 128 B per panel
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffV = kOffK + kNumStages * kKVBytes;
+  static constexpr int kOffBar = kOffV + kNumStages * kKVBytes;
+  // barriers, TMEM slot and alignment slack; at least 80 KB so that no more than two CTAs
+  // (2 x 256 TMEM columns) share an SM
+  static constexpr int kBytes = (kOffBar + 256 + 1024) > 80 * 1024 ? (kOffBar + 256 + 1024) : 80 * 1024;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store_row_chunk(OutT* dst, const float* v);
+
+template <>
+__device__ __forceinline__ void store_row_chunk<__nv_bfloat16>(__nv_bfloat16* dst, const float* v) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    p[i] = w;
+  }
+}
+
+template <>
+__device__ __forceinline__ void store_row_chunk<float>(float* dst, const float* v) {
+  float4* p = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+template <int D, typename OutT>
+__global__ void __launch_bounds__(kThreads, 2)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mv, ShapeArgs s, FwdArgs a) {
+  using L = FwdSmem<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  // barrier slots
+  const uint32_t bar_q = smem_u32(&bars[0]);
+  auto bar_kfull = [&](int st) { return smem_u32(&bars[1 + st]); };
+  auto bar_vfull = [&](int st) { return smem_u32(&bars[1 + kNumStages + st]); };
+  auto bar_empty = [&](int st) { return smem_u32(&bars[1 + 2 * kNumStages + st]); };
+  auto bar_sfull = [&](int b) { return smem_u32(&bars[1 + 3 * kNumStages + b]); };
+  auto bar_pfull = [&](int b) { return smem_u32(&bars[3 + 3 * kNumStages + b]); };
+  const uint32_t bar_odone = smem_u32(&bars[5 + 3 * kNumStages]);
+  const uint32_t bar_drain = smem_u32(&bars[6 + 3 * kNumStages]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 128);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffBar + 192);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x / s.Tq;
+  const int qi = blockIdx.x % s.Tq;
+  const int b = bh / s.H, h = bh % s.H;
+  const int64_t rowid = (int64_t)bh * s.Tq + qi;
+  int nkv = a.row_cnt[rowid];
+  if (nkv < 0 || nkv > s.Tk) {
+    if (tid == 0) report_error(a.status, kDevErrBounds);
+    nkv = nkv < 0 ? 0 : s.Tk;
+  }
+  const int32_t* list = a.row_idx + rowid * s.Tk;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bar_q, 1);
+    for (int st = 0; st < kNumStages; ++st) {
+      mbar_init(bar_kfull(st), 1);
+      mbar_init(bar_vfull(st), 1);
+      mbar_init(bar_empty(st), 1);
+    }
+    for (int bb = 0; bb < 2; ++bb) {
+      mbar_init(bar_sfull(bb), 1);
+      mbar_init(bar_pfull(bb), 128);
+    }
+    mbar_init(bar_odone, 1);
+    mbar_init(bar_drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && nkv > 0) {
+      tma_prefetch_map(&mq);
+      tma_prefetch_map(&mk);
+      tma_prefetch_map(&mv);
+      mbar_arrive_expect_tx(bar_q, L::kQBytes);
+      for (int p = 0; p < L::kPanels; ++p)
+        tma_load_4d(sbase + L::kOffQ + p * 16384, &mq, bar_q, p * 64, qi * s.bq, h, b);
+      for (int j = 0; j < nkv; ++j) {
+        const int st = j % kNumStages;
+        if (j >= kNumStages && !mbar_wait(bar_empty(st), ((j / kNumStages) - 1) & 1, abort_flag)) break;
+        int kb = list[j];
+        if (kb < 0 || kb >= s.Tk) {
+          report_error(a.status, kDevErrBounds);
+          kb = 0;
+        }
+        mbar_arrive_expect_tx(bar_kfull(st), L::kKVBytes);
+        for (int p = 0; p < L::kPanels; ++p)
+          tma_load_4d(sbase + L::kOffK + st * L::kKVBytes + p * 8192, &mk, bar_kfull(st), p * 64, kb * 64, h, b);
+        mbar_arrive_expect_tx(bar_vfull(st), L::kKVBytes);
+        for (int p = 0; p < L::kPanels; ++p)
+          tma_load_4d(sbase + L::kOffV + st * L::kKVBytes + p * 8192, &mv, bar_vfull(st), p * 64, kb * 64, h, b);
+      }
+      // wait for the loads still in flight before the CTA may exit
+      const int first = nkv > kNumStages ? nkv - kNumStages : 0;
+      for (int j = first; j < nkv; ++j) {
+        const int st = j % kNumStages;
+        mbar_wait(bar_vfull(st), (j / kNumStages) & 1, abort_flag);
+        mbar_wait(bar_kfull(st), (j / kNumStages) & 1, abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------------- MMA issuer
+    if (lane == 0 && nkv > 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+      bool ok = mbar_wait(bar_q, 0, abort_flag);
+      for (int j = 0; ok && j <= nkv; ++j) {
+        if (j < nkv) {
+          const int st = j % kNumStages;
+          if (!mbar_wait(bar_kfull(st), (j / kNumStages) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t kbase = sbase + L::kOffK + st * L::kKVBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t adesc = smem_desc(sbase + L::kOffQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc(kbase + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024);
+            umma_ss(tmem + (j & 1) * 64, adesc, bdesc, idS, kk > 0);
+          }
+          umma_commit(bar_sfull(j & 1));
+        }
+        if (j >= 1) {
+          const int jj = j - 1;
+          const int st = jj % kNumStages;
+          if (!mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, abort_flag)) break;
+          if (!mbar_wait(bar_vfull(st), (jj / kNumStages) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t vbase = sbase + L::kOffV + st * L::kKVBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // V as the MN-major B operand: N = D (64-element groups 8 KB apart), K = 16 rows
+            const uint64_t bdesc = smem_desc(vbase + kk * 2048, 8192, 1024);
+            umma_ts(tmem + kColO, tmem + (jj & 1) * 64 + kk * 8, bdesc, idO, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(bar_empty(st));
+          umma_commit(bar_odone);
+        }
+      }
+      // every MMA issued by this thread has completed before TMEM is released
+      umma_commit(bar_drain);
+      mbar_wait(bar_drain, 0, abort_flag);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax rows
+    const int sub = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = 32 * sub + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * sub) << 16);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them is
+    // decided uniformly per warp (__all_sync / __any_sync).
+    for (int j = 0; j < nkv; ++j) {
+      const int bsel = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bsel), (j >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t u0[32], u1[32];
+      tmem_ld32(trow + bsel * 64, u0);
+      tmem_ld32(trow + bsel * 64 + 32, u1);
+      tmem_ld_wait(u0);
+      tmem_ld_wait(u1);
+      int kb = list[j];
+      kb = (kb < 0 || kb >= s.Tk) ? 0 : kb;
+      const int valid = min(64, s.N - kb * 64);
+      float x[64];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        x[c] = (c < valid) ? __uint_as_float(u0[c]) * a.scale_log2 : -INFINITY;
+        x[c + 32] = (c + 32 < valid) ? __uint_as_float(u1[c]) * a.scale_log2 : -INFINITY;
+      }
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
+      if (j == 0) {
+        m_used = mx;
+      } else {
+        const bool need = mx > m_used + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          // O must hold P_0..P_{j-1} V before it is rescaled; lanes that keep their max
+          // multiply by 1
+          const float alpha = need ? ex2(m_used - mx) : 1.f;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_odone, (j - 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(trow + kColO + c0, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(trow + kColO + c0, o);
+          }
+          tmem_st_wait();
+          if (need) {
+            l *= alpha;
+            m_used = mx;
+          }
+        }
+      }
+      uint32_t pk[32];
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(x[2 * c] - m_used);
+        const float p1 = ex2(x[2 * c + 1] - m_used);
+        lsum += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      l += lsum;
+      tmem_st32(trow + bsel * 64, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_pfull(bsel));
+    }
+    // ---- epilogue
+    const int64_t tok = (int64_t)qi * s.bq + r;
+    const bool row_valid = r < s.bq && tok < s.N;
+    OutT* orow = reinterpret_cast<OutT*>(a.o) + (int64_t)b * a.o_sb + (int64_t)h * a.o_sh + tok * a.o_sn;
+    if (nkv == 0) {
+      if (row_valid) {
+        float z[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) z[c] = 0.f;
+        for (int c0 = 0; c0 < D; c0 += 32) store_row_chunk<OutT>(orow + c0, z);
+        a.lse[(int64_t)bh * s.N + tok] = -INFINITY;
+      }
+    } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar_odone, (nkv - 1) & 1, abort_flag))) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(trow + kColO + c0, o);
+        tmem_ld_wait(o);
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(o[c]) * inv_l;
+        if (row_valid) store_row_chunk<OutT>(orow + c0, v);
+      }
+      if (row_valid) a.lse[(int64_t)bh * s.N + tok] = (m_used + __log2f(l)) * 0.69314718055994531f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) report_error(a.status, kDevErrTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, typename OutT>
+cudaError_t launch_fwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const FwdArgs& a, cudaStream_t st) {
+  const int smem = FwdSmem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)s.B * s.H * s.Tq;
+  attn_fwd_kernel<D, OutT><<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, s, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const FwdArgs& a, cudaStream_t st) {
+  if (s.d == 128)
+    return s.dtype == 0 ? launch_fwd_t<128, __nv_bfloat16>(s, mq, mk, mv, a, st)
+                        : launch_fwd_t<128, float>(s, mq, mk, mv, a, st);
+  return s.dtype == 0 ? launch_fwd_t<64, __nv_bfloat16>(s, mq, mk, mv, a, st)
+                      : launch_fwd_t<64, float>(s, mq, mk, mv, a, st);
+}
+
+}  // namespace sa2

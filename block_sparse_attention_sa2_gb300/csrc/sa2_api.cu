@@ -1,0 +1,320 @@
+// The C ABI (include/sa2.h): argument checks, workspace layout, tensor maps and launches.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sa2.h"
+#include "sa2_internal.h"
+
+using namespace sa2;
+
+namespace {
+
+// Device-side error word; kernels write the first error code into it.
+__device__ unsigned g_device_status;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices];
+std::once_flag g_status_once[kMaxDevices];
+
+unsigned* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::call_once(g_status_once[dev], [dev]() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess) g_status_ptr[dev] = static_cast<unsigned*>(p);
+  });
+  return g_status_ptr[dev];
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates a shape and fills the derived block counts.
+sa2_status check_shape(const sa2_shape* shape, ShapeArgs* s) {
+  if (!shape) return SA2_ERR_INVALID_ARG;
+  const sa2_shape& x = *shape;
+  if (x.B < 1 || x.H < 1 || x.N < 1 || x.reserved != 0) return SA2_ERR_INVALID_ARG;
+  if (x.dtype != SA2_BF16 && x.dtype != SA2_FP32) return SA2_ERR_UNSUPPORTED;
+  if (x.d != 64 && x.d != 128) return SA2_ERR_UNSUPPORTED;
+  if ((x.bq != 64 && x.bq != 128) || x.bk != 64) return SA2_ERR_UNSUPPORTED;
+  const int64_t esz = x.dtype == SA2_BF16 ? 2 : 4;
+  if (x.stride_n < x.d || x.stride_h < 1 || x.stride_b < 1) return SA2_ERR_INVALID_ARG;
+  if ((x.stride_n * esz) % 16 || (x.stride_h * esz) % 16 || (x.stride_b * esz) % 16) return SA2_ERR_ALIGNMENT;
+  s->B = x.B;
+  s->H = x.H;
+  s->N = x.N;
+  s->d = x.d;
+  s->bq = x.bq;
+  s->bk = x.bk;
+  s->Tq = (x.N + x.bq - 1) / x.bq;
+  s->Tk = (x.N + x.bk - 1) / x.bk;
+  s->dtype = x.dtype;
+  s->sb = x.stride_b;
+  s->sh = x.stride_h;
+  s->sn = x.stride_n;
+  if (s->Tk > 7680 || score_rows_per_cta(s->Tk, s->d) == 0) return SA2_ERR_UNSUPPORTED;
+  if ((int64_t)s->B * s->H * s->Tq >= (int64_t)1 << 31) return SA2_ERR_UNSUPPORTED;
+  return SA2_OK;
+}
+
+size_t token_elems(const ShapeArgs& s) { return (size_t)s.B * s.H * s.N * s.d; }
+
+sa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SA2_OK : SA2_ERR_CUDA; }
+
+struct MaskWs {
+  size_t qbar, kbar, mask, total;
+};
+MaskWs mask_ws(const ShapeArgs& s) {
+  MaskWs w;
+  w.qbar = 0;
+  w.kbar = align_up(w.qbar + sizeof(float) * (size_t)s.B * s.H * s.d * s.Tq);
+  w.mask = align_up(w.kbar + sizeof(float) * (size_t)s.B * s.H * s.d * s.Tk);
+  w.total = align_up(w.mask + (size_t)s.B * s.H * s.Tq * s.Tk);
+  return w;
+}
+
+struct FwdWs {
+  size_t q, k, v, total;
+};
+FwdWs fwd_ws(const ShapeArgs& s) {
+  FwdWs w{0, 0, 0, 0};
+  if (s.dtype == SA2_FP32) {
+    const size_t t = align_up(2 * token_elems(s));
+    w.q = 0;
+    w.k = t;
+    w.v = 2 * t;
+    w.total = 3 * t;
+  }
+  return w;
+}
+
+struct BwdWs {
+  size_t dq, D, q, k, v, dO, total;
+};
+BwdWs bwd_ws(const ShapeArgs& s) {
+  BwdWs w{};
+  w.dq = 0;
+  w.D = align_up(sizeof(float) * token_elems(s));
+  size_t end = align_up(w.D + sizeof(float) * (size_t)s.B * s.H * s.N);
+  if (s.dtype == SA2_FP32) {
+    const size_t t = align_up(2 * token_elems(s));
+    w.q = end;
+    w.k = end + t;
+    w.v = end + 2 * t;
+    w.dO = end + 3 * t;
+    end += 4 * t;
+  }
+  w.total = end;
+  return w;
+}
+
+// Tensor maps over bf16 token tensors: the caller's tensors for SA2_BF16, contiguous
+// staging copies for SA2_FP32.
+bool token_maps(const ShapeArgs& s, const void* base, bool contiguous, CUtensorMap* map, int box_rows) {
+  const int64_t sn = contiguous ? s.d : s.sn;
+  const int64_t sh = contiguous ? (int64_t)s.N * s.d : s.sh;
+  const int64_t sb = contiguous ? (int64_t)s.H * s.N * s.d : s.sb;
+  return make_token_map(map, base, s, sb, sh, sn, box_rows);
+}
+
+}  // namespace
+
+extern "C" {
+
+int sa2_version(void) { return 100; }
+
+const char* sa2_status_string(sa2_status st) {
+  switch (st) {
+    case SA2_OK: return "ok";
+    case SA2_ERR_INVALID_ARG: return "invalid argument";
+    case SA2_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case SA2_ERR_ALIGNMENT: return "pointer or stride not 16-byte aligned";
+    case SA2_ERR_WORKSPACE: return "workspace missing or too small";
+    case SA2_ERR_CUDA: return "CUDA error";
+    case SA2_ERR_TIMEOUT: return "device wait timed out";
+    case SA2_ERR_DEVICE_BOUNDS: return "block index out of range on the device";
+  }
+  return "unknown status";
+}
+
+size_t sa2_mask_workspace_size(const sa2_shape* shape) {
+  ShapeArgs s;
+  if (check_shape(shape, &s) != SA2_OK) return 0;
+  return mask_ws(s).total;
+}
+
+sa2_status sa2_build_mask(const sa2_shape* shape, const void* q, const void* k, float topk, float topp,
+                          const sa2_blockmask* out, void* ws, size_t ws_bytes, void* stream) {
+  ShapeArgs s;
+  sa2_status st = check_shape(shape, &s);
+  if (st != SA2_OK) return st;
+  if (!q || !k || !out || !out->row_cnt || !out->row_idx || !out->col_cnt || !out->col_idx)
+    return SA2_ERR_INVALID_ARG;
+  if (!std::isfinite(topk) || !std::isfinite(topp) || topk < 0.f || topk > 1.f || topp < 0.f || topp > 1.f)
+    return SA2_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(out->row_cnt) || !aligned16(out->row_idx) ||
+      !aligned16(out->col_cnt) || !aligned16(out->col_idx) || (out->mask && !aligned16(out->mask)) ||
+      (out->pooled_p && !aligned16(out->pooled_p)) || !aligned16(ws))
+    return SA2_ERR_ALIGNMENT;
+  const MaskWs w = mask_ws(s);
+  if (!ws || ws_bytes < w.total) return SA2_ERR_WORKSPACE;
+  SelectArgs sel;
+  const double Kd = std::ceil((double)topk * s.Tk - 1e-9);
+  sel.K = (int)std::fmin(std::fmax(Kd, 0.0), (double)s.Tk);
+  if (topp <= 0.f) {
+    sel.p_mode = 1;
+    sel.p_fix = 0;
+  } else if (topp >= 1.f) {
+    sel.p_mode = 2;
+    sel.p_fix = 0;
+  } else {
+    sel.p_mode = 0;
+    sel.p_fix = (unsigned long long)std::ldexp((double)topp, 60);
+  }
+  sel.inv_sqrt_d = (float)(1.0 / std::sqrt((double)s.d));
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  MaskOut mo;
+  mo.row_cnt = out->row_cnt;
+  mo.row_idx = out->row_idx;
+  mo.col_cnt = out->col_cnt;
+  mo.col_idx = out->col_idx;
+  mo.mask = out->mask ? out->mask : wsb + w.mask;
+  mo.pooled_p = out->pooled_p;
+  return cuda_status(launch_build_mask(s, q, k, sel, reinterpret_cast<float*>(wsb + w.qbar),
+                                       reinterpret_cast<float*>(wsb + w.kbar), mo,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+size_t sa2_fwd_workspace_size(const sa2_shape* shape) {
+  ShapeArgs s;
+  if (check_shape(shape, &s) != SA2_OK) return 0;
+  return fwd_ws(s).total;
+}
+
+sa2_status sa2_attn_fwd(const sa2_shape* shape, const void* q, const void* k, const void* v,
+                        const sa2_blockmask* mask, float softmax_scale, void* o, float* lse, void* ws,
+                        size_t ws_bytes, void* stream) {
+  ShapeArgs s;
+  sa2_status st = check_shape(shape, &s);
+  if (st != SA2_OK) return st;
+  if (!q || !k || !v || !o || !lse || !mask || !mask->row_cnt || !mask->row_idx) return SA2_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return SA2_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(mask->row_cnt) || !aligned16(mask->row_idx) || !aligned16(ws))
+    return SA2_ERR_ALIGNMENT;
+  const FwdWs w = fwd_ws(s);
+  if (w.total && (!ws || ws_bytes < w.total)) return SA2_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const void *qb = q, *kb = k, *vb = v;
+  const bool staged = s.dtype == SA2_FP32;
+  if (staged) {
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    __nv_bfloat16* qc = reinterpret_cast<__nv_bfloat16*>(wsb + w.q);
+    __nv_bfloat16* kc = reinterpret_cast<__nv_bfloat16*>(wsb + w.k);
+    __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(wsb + w.v);
+    if (launch_to_bf16(static_cast<const float*>(q), s, qc, cs) != cudaSuccess ||
+        launch_to_bf16(static_cast<const float*>(k), s, kc, cs) != cudaSuccess ||
+        launch_to_bf16(static_cast<const float*>(v), s, vc, cs) != cudaSuccess)
+      return SA2_ERR_CUDA;
+    qb = qc;
+    kb = kc;
+    vb = vc;
+  }
+  CUtensorMap mq, mk, mv;
+  if (!token_maps(s, qb, staged, &mq, 128) || !token_maps(s, kb, staged, &mk, 64) ||
+      !token_maps(s, vb, staged, &mv, 64))
+    return SA2_ERR_CUDA;
+  const float scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / std::sqrt((double)s.d));
+  FwdArgs a;
+  a.row_cnt = mask->row_cnt;
+  a.row_idx = mask->row_idx;
+  a.o = o;
+  a.lse = lse;
+  a.o_sb = s.sb;
+  a.o_sh = s.sh;
+  a.o_sn = s.sn;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status_ptr();
+  return cuda_status(launch_attn_fwd(s, mq, mk, mv, a, cs));
+}
+
+size_t sa2_bwd_workspace_size(const sa2_shape* shape) {
+  ShapeArgs s;
+  if (check_shape(shape, &s) != SA2_OK) return 0;
+  return bwd_ws(s).total;
+}
+
+sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dO, const sa2_blockmask* mask, float softmax_scale,
+                        void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+  ShapeArgs s;
+  sa2_status st = check_shape(shape, &s);
+  if (st != SA2_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !mask || !mask->col_cnt || !mask->col_idx)
+    return SA2_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return SA2_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(mask->col_cnt) ||
+      !aligned16(mask->col_idx) || !aligned16(ws))
+    return SA2_ERR_ALIGNMENT;
+  const BwdWs w = bwd_ws(s);
+  if (!ws || ws_bytes < w.total) return SA2_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* dq_acc = reinterpret_cast<float*>(wsb + w.dq);
+  float* Dvec = reinterpret_cast<float*>(wsb + w.D);
+  if (launch_bwd_preprocess(s, o, dO, Dvec, dq_acc, cs) != cudaSuccess) return SA2_ERR_CUDA;
+  const void *qb = q, *kb = k, *vb = v, *dob = dO;
+  const bool staged = s.dtype == SA2_FP32;
+  if (staged) {
+    __nv_bfloat16* c[4] = {reinterpret_cast<__nv_bfloat16*>(wsb + w.q), reinterpret_cast<__nv_bfloat16*>(wsb + w.k),
+                           reinterpret_cast<__nv_bfloat16*>(wsb + w.v), reinterpret_cast<__nv_bfloat16*>(wsb + w.dO)};
+    const void* src[4] = {q, k, v, dO};
+    for (int i = 0; i < 4; ++i)
+      if (launch_to_bf16(static_cast<const float*>(src[i]), s, c[i], cs) != cudaSuccess) return SA2_ERR_CUDA;
+    qb = c[0];
+    kb = c[1];
+    vb = c[2];
+    dob = c[3];
+  }
+  CUtensorMap mq, mk, mv, mdo;
+  if (!token_maps(s, qb, staged, &mq, 128) || !token_maps(s, kb, staged, &mk, 64) ||
+      !token_maps(s, vb, staged, &mv, 64) || !token_maps(s, dob, staged, &mdo, 128))
+    return SA2_ERR_CUDA;
+  const float scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / std::sqrt((double)s.d));
+  BwdArgs a;
+  a.col_cnt = mask->col_cnt;
+  a.col_idx = mask->col_idx;
+  a.lse = lse;
+  a.Dvec = Dvec;
+  a.dq_acc = dq_acc;
+  a.dk = dk;
+  a.dv = dv;
+  a.g_sb = s.sb;
+  a.g_sh = s.sh;
+  a.g_sn = s.sn;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status_ptr();
+  if (launch_attn_bwd(s, mq, mk, mv, mdo, a, cs) != cudaSuccess) return SA2_ERR_CUDA;
+  return cuda_status(launch_dq_convert(s, dq_acc, dq, cs));
+}
+
+sa2_status sa2_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SA2_ERR_CUDA;
+  unsigned* p = status_ptr();
+  if (!p) return SA2_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SA2_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SA2_ERR_CUDA;
+  }
+  return v == 0 ? SA2_OK : static_cast<sa2_status>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Internal declarations shared by the translation units of libsa2 (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "sa2_device.cuh"
+
+namespace sa2 {
+
+constexpr size_t kMaxDynSmem = 227 * 1024;
+
+// Shape of one call, with the derived block counts.  Strides are in elements.
+struct ShapeArgs {
+  int B, H, N, d, bq, bk, Tq, Tk, dtype;
+  int64_t sb, sh, sn;
+};
+
+// Selection parameters of the hybrid mask, prepared on the host.
+struct SelectArgs {
+  int K;                      // ceil(k * Tk) clamped to [0, Tk]
+  int p_mode;                 // 0: 0 < p < 1, 1: p <= 0 (m = 0), 2: p >= 1 (m = Tk)
+  unsigned long long p_fix;   // floor(p * 2^60), used when p_mode == 0
+  float inv_sqrt_d;           // 1/sqrt(d) rounded to fp32
+};
+
+struct MaskOut {
+  int32_t* row_cnt;
+  int32_t* row_idx;
+  int32_t* col_cnt;
+  int32_t* col_idx;
+  uint8_t* mask;      // never null here (workspace stands in when the caller passes null)
+  float* pooled_p;    // may be null
+};
+
+// Mask builder (mask_kernels.cu).
+int score_rows_per_cta(int Tk, int d);
+cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, const SelectArgs& sel,
+                              float* qbarT, float* kbarT, const MaskOut& out, cudaStream_t st);
+
+// Tensor maps of bf16 token tensors [B, H, N, d] (attn_common.cu).
+bool make_token_map(CUtensorMap* map, const void* base, const ShapeArgs& s, int64_t sb, int64_t sh, int64_t sn,
+                    int box_rows);
+
+// Element-wise helpers (attn_common.cu).
+cudaError_t launch_to_bf16(const float* src, const ShapeArgs& s, __nv_bfloat16* dst, cudaStream_t st);
+
+struct FwdArgs {
+  const int32_t* row_cnt;
+  const int32_t* row_idx;
+  void* o;           // output, dtype of the call
+  float* lse;        // [B, H, N]
+  int64_t o_sb, o_sh, o_sn;
+  float scale_log2;  // softmax scale * log2(e)
+  unsigned* status;
+};
+
+cudaError_t launch_attn_fwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const FwdArgs& a, cudaStream_t st);
+
+struct BwdArgs {
+  const int32_t* col_cnt;
+  const int32_t* col_idx;
+  const float* lse;   // [B, H, N]
+  const float* Dvec;  // [B, H, N] rowsum(dO * O)
+  float* dq_acc;      // [B, H, N, d] fp32, zeroed
+  void* dk;
+  void* dv;
+  int64_t g_sb, g_sh, g_sn;  // strides of dk / dv (dtype of the call)
+  float scale;
+  float scale_log2;
+  unsigned* status;
+};
+
+cudaError_t launch_bwd_preprocess(const ShapeArgs& s, const void* o, const void* dO, float* Dvec, float* dq_acc,
+                                  cudaStream_t st);
+cudaError_t launch_attn_bwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st);
+cudaError_t launch_dq_convert(const ShapeArgs& s, const float* dq_acc, void* dq, cudaStream_t st);
+
+}  // namespace sa2

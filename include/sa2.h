@@ -1,0 +1,179 @@
+/*
+ * sa2.h -- C ABI of the GB300 (sm_103a) hot path of SpargeAttention2: the hybrid
+ * Top-k + Top-p block mask and trainable block-sparse attention.
+ *
+ * Source of every operation: the pages on "SpargeAttention2: Trainable Sparse Attention
+ * via Hybrid Top-k+Top-p Masking and Distillation Fine-Tuning" (arXiv 2602.13515); the
+ * passage each entry point follows is cited at its declaration.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Token tensors (q, k, v, o, dO, dq, dk, dv) are [B, H, N, d] with element strides
+ *   stride_b, stride_h, stride_n (the last dimension is contiguous).  All token tensors of
+ *   one call share these strides.  dtype is SA2_BF16 or SA2_FP32 for all of them.
+ * - Blocks: query block i covers tokens [i*bq, min(N, (i+1)*bq)); key block j covers
+ *   [j*bk, min(N, (j+1)*bk)).  Tq = ceil(N/bq), Tk = ceil(N/bk).  The last block of each
+ *   may be partial.
+ * - Supported: d in {64, 128}; bq in {64, 128}; bk = 64; 1 <= N; Tk <= 7680.
+ * - Pointers are device pointers unless stated otherwise; every device pointer must be
+ *   16-byte aligned and every stride * element size a multiple of 16 bytes.
+ * - The caller owns every buffer, including the workspaces (sizes from the *_workspace_size
+ *   queries).  The library allocates no device memory; it keeps one device status word and
+ *   a few bytes of per-device set-up state.
+ * - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   Argument errors are returned before anything is launched.  Errors raised by a kernel
+ *   on the device (a bounded wait that timed out, a block index out of range) are recorded
+ *   in the status word and reported by sa2_get_device_status.
+ * - Attention is non-causal.  The softmax scale of the attention is an argument
+ *   (1/sqrt(d) when <= 0 is passed); the pooled scores always use 1/sqrt(d).
+ */
+#ifndef SA2_H_
+#define SA2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sa2_status {
+  SA2_OK = 0,
+  SA2_ERR_INVALID_ARG = 1, /* null pointer, negative size, k/p not finite, ... */
+  SA2_ERR_UNSUPPORTED = 2, /* d, bq, bk, dtype or size outside the supported set */
+  SA2_ERR_ALIGNMENT = 3,   /* a pointer or stride is not 16-byte aligned */
+  SA2_ERR_WORKSPACE = 4,   /* workspace missing or smaller than the size query returns */
+  SA2_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+  SA2_ERR_TIMEOUT = 6,     /* device: a bounded wait inside a kernel gave up */
+  SA2_ERR_DEVICE_BOUNDS = 7 /* device: a block list held an index out of range */
+} sa2_status;
+
+typedef enum sa2_dtype { SA2_BF16 = 0, SA2_FP32 = 1 } sa2_dtype;
+
+typedef struct sa2_shape {
+  int32_t B, H, N, d;
+  int32_t bq, bk;
+  int32_t dtype; /* sa2_dtype */
+  int32_t reserved; /* must be 0 */
+  int64_t stride_b, stride_h, stride_n; /* in elements */
+} sa2_shape;
+
+/*
+ * The block mask in compact form.  All arrays are device arrays owned by the caller.
+ *   row_cnt [B, H, Tq]      int32: number of kept key blocks of each query block
+ *   row_idx [B, H, Tq, Tk]  int32: the first row_cnt entries of each row are the kept key
+ *                                  blocks in ascending order; the rest is unspecified
+ *   col_cnt [B, H, Tk]      int32: number of query blocks that keep each key block
+ *   col_idx [B, H, Tk, Tq]  int32: the first col_cnt entries are those query blocks,
+ *                                  ascending; the rest is unspecified
+ *   mask    [B, H, Tq, Tk]  uint8: 1 = kept (optional output of sa2_build_mask; NULL skips)
+ *   pooled_p[B, H, Tq, Tk]  fp32 : the pooled probabilities P-bar (optional; NULL skips)
+ * sa2_attn_fwd reads row_cnt/row_idx; sa2_attn_bwd reads all four lists.
+ */
+typedef struct sa2_blockmask {
+  int32_t* row_cnt;
+  int32_t* row_idx;
+  int32_t* col_cnt;
+  int32_t* col_idx;
+  uint8_t* mask;
+  float* pooled_p;
+} sa2_blockmask;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int sa2_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* sa2_status_string(sa2_status status);
+
+/*
+ * Bytes of device workspace sa2_build_mask needs for this shape (the fp32 pooled queries
+ * and keys).  Returns 0 for an invalid shape.
+ */
+size_t sa2_mask_workspace_size(const sa2_shape* shape);
+
+/*
+ * sa2_build_mask -- the hybrid Top-k + Top-p block mask.
+ * gist.science explainer of the paper, section 2.A (hybrid Top-k + Top-p masking):
+ * P-bar is the attention map of block-pooled queries and keys; block j of row i is kept
+ * iff j is in Top-k(P-bar_i, k%) or in Top-p(P-bar_i, p%).  Section 1 of the same page
+ * defines Top-k (the k largest entries) and Top-p (the smallest set whose cumulative
+ * probability reaches p).
+ *
+ * Steps: q-bar_i, k-bar_j = means of Q and K over the valid tokens of each block (fp32);
+ * P-bar_i = softmax_j(q-bar_i . k-bar_j / sqrt(d)) (fp32); K = ceil(topk * Tk) clamped to
+ * [0, Tk]; m = length of the shortest prefix of the row sorted by P-bar descending (equal
+ * values by ascending block index) whose mass reaches topp (topp <= 0: m = 0; topp >= 1:
+ * m = Tk; a mass that never reaches topp: m = Tk); the row keeps the first max(K, m)
+ * blocks of that order.
+ *
+ *   q, k      token tensors (see conventions); read only
+ *   topk      k as a fraction of Tk, in [0, 1]
+ *   topp      p in [0, 1]
+ *   out       the lists to fill; row_cnt, row_idx, col_cnt, col_idx are required; mask and
+ *             pooled_p optional
+ *   ws        device workspace of at least sa2_mask_workspace_size(shape) bytes
+ */
+sa2_status sa2_build_mask(const sa2_shape* shape, const void* q, const void* k, float topk, float topp,
+                          const sa2_blockmask* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Bytes of device workspace sa2_attn_fwd needs (bf16 copies of q, k, v for SA2_FP32
+ * inputs; a per-row work order otherwise).
+ */
+size_t sa2_fwd_workspace_size(const sa2_shape* shape);
+
+/*
+ * sa2_attn_fwd -- block-sparse attention forward.
+ * gist.science explainer, section 2.C (efficient kernel implementation): a FlashAttention
+ * style block-sparse kernel; tiles are kept or skipped whole, and the matmul and softmax of
+ * skipped tiles are not computed.  Equals softmax attention with the scores of dropped
+ * blocks at -inf:
+ *   O_a = sum over kept key tokens c of exp(s_ac - LSE_a) v_c,  s_ac = scale * q_a . k_c,
+ *   LSE_a = log sum over kept c of exp(s_ac)   (natural log).
+ * A query block with no kept key block gets O = 0 and LSE = -inf.
+ * Computed in bf16 with fp32 accumulation and an fp32 online softmax (SA2_FP32 inputs are
+ * rounded to bf16 first).
+ *
+ *   q, k, v   token tensors; o: token tensor (output, same dtype); lse: [B, H, N] fp32 output
+ *   mask      row_cnt / row_idx of the block mask (e.g. from sa2_build_mask)
+ *   softmax_scale  scale of q.k (<= 0 means 1/sqrt(d))
+ */
+sa2_status sa2_attn_fwd(const sa2_shape* shape, const void* q, const void* k, const void* v,
+                        const sa2_blockmask* mask, float softmax_scale, void* o, float* lse, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/*
+ * Bytes of device workspace sa2_attn_bwd needs: the fp32 dQ accumulator [B, H, N, d],
+ * D = rowsum(dO * O) [B, H, N], and bf16 copies for SA2_FP32 inputs.
+ */
+size_t sa2_bwd_workspace_size(const sa2_shape* shape);
+
+/*
+ * sa2_attn_bwd -- backward of sa2_attn_fwd with the block mask held fixed.
+ * The abstract of the paper (shd-paper.top, fugumt.com and thelatestinai.com pages),
+ * contribution (ii): "an efficient trainable sparse attention implementation"; the pages
+ * do not spell the backward out, so this is the gradient of the forward above:
+ *   P = exp(s - LSE),  dV = P^T dO,  dP = dO V^T,  D_a = dO_a . O_a,
+ *   dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q,
+ * over kept tiles only.  Rows with LSE = -inf contribute nothing.
+ *
+ *   q, k, v, o, dO  token tensors (o and lse from sa2_attn_fwd); dq, dk, dv outputs
+ *   mask      all four lists of the block mask
+ *   ws        device workspace of at least sa2_bwd_workspace_size(shape) bytes
+ */
+sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dO, const sa2_blockmask* mask, float softmax_scale,
+                        void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronizes `stream`, then returns and clears the device status word of the current
+ * device: SA2_OK, SA2_ERR_TIMEOUT or SA2_ERR_DEVICE_BOUNDS (or SA2_ERR_CUDA when the
+ * synchronization itself fails).
+ */
+sa2_status sa2_get_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA2_H_ */

@@ -1,0 +1,124 @@
+"""GPU parity of sa2_build_mask against the fp64 oracle.
+
+Masks must match bit for bit except entries whose pooled probability lies within 1e-6 of
+the oracle row's selection threshold; those are logged.  The compact lists must list the
+CUDA path's own mask exactly, and P-bar must agree with the oracle's to fp32 accuracy."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+from tests.gpu_util import NEAR_THRESHOLD, check_lists_consistent, to_device
+from workload import CONFIGS, make_inputs
+from workload.gen import small_case
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def sa2():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_sparse_attention_sa2_gb300 as m
+    m.load_library()
+    return m
+
+
+def _compare(sa2, cfg, x, topk, topp, heads=None, log=None, check_lists=True):
+    torch = pytest.importorskip("torch")
+    q, k = to_device(x["q"]), to_device(x["k"])
+    bm = sa2.build_mask(q, k, topk, topp, bq=cfg.bq, bk=cfg.bk, want_pooled=True)
+    sa2.check_device()
+    torch.cuda.synchronize()
+    gmask = bm.mask.cpu().numpy()
+    gP = bm.pooled_p.cpu().numpy()
+    ref = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, topk, topp, heads=heads)
+    todo = heads or [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
+    n_exempt = 0
+    for (b, h) in todo:
+        P = ref["P"][b, h]
+        assert np.abs(gP[b, h] - P).max() <= 5e-6, "pooled probabilities differ beyond fp32 accuracy"
+        exempt, bad = O.compare_mask_head(P, ref["sel"][(b, h)], gmask[b, h], NEAR_THRESHOLD)
+        assert not bad, f"head {(b, h)}: mask entries differ away from the threshold: {bad[:5]}"
+        n_exempt += len(exempt)
+        if log is not None and exempt:
+            log.extend([(b, h) + e for e in exempt])
+    if check_lists:
+        check_lists_consistent(bm, cfg.B, cfg.H, cfg.Tq, cfg.Tk)
+    return bm, ref, n_exempt
+
+
+def test_mask_tiny_fp32_config(sa2):
+    cfg = CONFIGS[0]
+    x = make_inputs(cfg, tensors=("q", "k"))
+    _compare(sa2, cfg, x, cfg.topk, cfg.topp)
+
+
+@pytest.mark.parametrize("N,d,bq,dtype", [(1000, 128, 128, "bf16"), (777, 64, 64, "bf16"), (1000, 64, 128, "fp32"),
+                                          (64, 128, 128, "bf16"), (1, 128, 128, "bf16")])
+def test_mask_ragged_small_cases(sa2, N, d, bq, dtype):
+    cfg, x = small_case(f"ragged-{N}", 2, 3, N, d, dtype, bq, 64, seed=3)
+    for topk, topp in ((0.1, 0.5), (0.0, 0.9), (0.3, 0.0), (0.0, 0.0), (1.0, 0.3), (0.05, 1.0)):
+        _compare(sa2, cfg, x, topk, topp)
+
+
+def test_mask_failure_probe_sweep(sa2):
+    """Mask-failure probe (flat heads 0-3, sink heads 4-7): Top-k-only, Top-p-only, hybrid."""
+    cfg = CONFIGS[1]
+    x = make_inputs(cfg, tensors=("q", "k"))
+    log = []
+    summary = {}
+    for topk, topp in cfg.sweep:
+        K = O.topk_count(topk, cfg.Tk)
+        cnt = {}
+        for mode, (kk, pp) in (("topk", (topk, 0.0)), ("topp", (0.0, topp)), ("hybrid", (topk, topp))):
+            bm, _, _ = _compare(sa2, cfg, x, kk, pp, log=log)
+            cnt[mode] = bm.row_cnt.cpu().numpy()[0]  # [H, Tq]
+            summary[f"k={topk} p={topp} {mode}"] = [round(float(v), 2) for v in cnt[mode].mean(axis=1)]
+        assert (cnt["topk"] == K).all()
+        assert (cnt["topp"][4:] == 1).all()  # sink heads: one block already holds > 90 %
+        flat = cnt["topp"][:4].mean()
+        assert abs(flat - topp * cfg.Tk) <= 0.1 * topp * cfg.Tk + 1  # flat heads keep about p*Tk
+        assert (cnt["hybrid"] == np.maximum(cnt["topk"], cnt["topp"])).all()
+    print("exempt entries:", len(log), log[:10])
+    print(json.dumps(summary, indent=0))
+
+
+@pytest.mark.parametrize("ci", [2, 3])
+def test_mask_full_size_wan_shapes(sa2, ci):
+    """Full-size Wan-shaped workloads at the calibrated 95 % sparsity; the oracle checks a
+    few heads (P-bar, selection) and the lists are checked for internal consistency."""
+    cfg = CONFIGS[ci]
+    cal = json.load(open(os.path.join(GOLDEN, "calibration.json")))[str(ci)]["targets"]["0.95"]
+    heads = [(0, 0), (0, cfg.H // 2), (0, cfg.H - 1)]
+    x = make_inputs(cfg, tensors=("q", "k"), threads=16)
+    bm, ref, n_exempt = _compare(sa2, cfg, x, cal["k"], cal["p"], heads=heads, check_lists=False)
+    kept = bm.row_cnt.sum().item() / (cfg.B * cfg.H * cfg.Tq * cfg.Tk)
+    assert abs((1 - kept) - 0.95) < 0.01
+    # lists of two heads checked exhaustively
+    mask = bm.mask.cpu().numpy().astype(bool)
+    rc, cc = bm.row_cnt.cpu().numpy(), bm.col_cnt.cpu().numpy()
+    assert (rc == mask.sum(-1)).all() and (cc == mask.sum(-2)).all()
+    ri, ci_ = bm.row_idx.cpu().numpy(), bm.col_idx.cpu().numpy()
+    for (b, h) in heads[:2]:
+        for i in range(cfg.Tq):
+            assert (ri[b, h, i, :rc[b, h, i]] == np.nonzero(mask[b, h, i])[0]).all()
+        for j in range(cfg.Tk):
+            assert (ci_[b, h, j, :cc[b, h, j]] == np.nonzero(mask[b, h, :, j])[0]).all()
+    print(f"config {ci}: sparsity {1 - kept:.4f}, exempt {n_exempt}")
+
+
+def test_mask_rejects_bad_arguments(sa2):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros((1, 1, 128, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sa2.Sa2Error):
+        sa2.build_mask(q, q, 1.5, 0.5)
+    with pytest.raises(sa2.Sa2Error):
+        sa2.build_mask(q, q, 0.1, float("nan"))
+    with pytest.raises(sa2.Sa2Error):
+        sa2.build_mask(q, q, 0.1, 0.5, bk=32)
