@@ -24,6 +24,11 @@
 // the dQ tile out of TMEM into the atomics; finally dK, dV out of TMEM (one channel per
 // thread).
 //
+// All operands are fp16: the call's Q, K, V, dO arrive as fp16 copies (exact for bf16
+// inputs within the fp16 range) and P, dS are written as fp16.  P lies in [0, 1] and every
+// row of dS sums to zero, so dV and above all dQ = dS K cancel; fp16 keeps 11 significant
+// bits of P and dS against bf16's 8.
+//
 // The tiles are always 128 channels wide: for d = 64 the second channel panel is read past
 // the end of the tensor map and arrives as zeros, and the extra rows / columns of the
 // results are not stored.
@@ -162,9 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------------------- MMA issuer
     if (lane == 0 && nq > 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);
-      constexpr uint32_t idT = idesc_bf16_f32(128, 64, true, true);
-      constexpr uint32_t idQ = idesc_bf16_f32(128, 128, false, true);
+      constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
+      constexpr uint32_t idT = idesc_f16_f32(128, 64, true, true);
+      constexpr uint32_t idQ = idesc_f16_f32(128, 128, false, true);
       bool ok = mbar_wait(bar_kv, 0, abort_flag);
       for (int t = 0; ok && t <= nq; ++t) {
         if (t < nq) {
@@ -267,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pv[z] = p;
                 ds[z] = p * (__uint_as_float(dv[c]) - Dr);
               }
-              pw[e] = pack_bf16x2(pv[0], pv[1]);
-              dw[e] = pack_bf16x2(ds[0], ds[1]);
+              pw[e] = pack_f16x2(pv[0], pv[1]);
+              dw[e] = pack_f16x2(ds[0], ds[1]);
             }
             pk[half * 4 + c8] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
             dk[half * 4 + c8] = make_uint4(dw[0], dw[1], dw[2], dw[3]);

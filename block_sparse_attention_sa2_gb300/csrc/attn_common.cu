@@ -26,7 +26,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 // tokens with the 128-byte swizzle the tcgen05 descriptors expect.  Tokens past N read
 // as zero.
 bool make_token_map(CUtensorMap* map, const void* base, const ShapeArgs& s, int64_t sb, int64_t sh, int64_t sn,
-                    int box_rows) {
+                    int box_rows, bool f16) {
   auto enc = encode_tiled();
   if (!enc) return false;
   std::memset(map, 0, sizeof(*map));
@@ -34,15 +34,31 @@ bool make_token_map(CUtensorMap* map, const void* base, const ShapeArgs& s, int6
   cuuint64_t strides[3] = {(cuuint64_t)sn * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
   cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+  CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                   const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-// fp32 token tensor (caller strides) -> contiguous bf16 [B, H, N, d].
-__global__ void to_bf16_kernel(const float* __restrict__ src, ShapeArgs s, __nv_bfloat16* __restrict__ dst) {
+template <typename T>
+__device__ __forceinline__ float4 ld4(const T* p);
+template <>
+__device__ __forceinline__ float4 ld4<float>(const float* p) { return *reinterpret_cast<const float4*>(p); }
+template <>
+__device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                     __uint_as_float(w.y & 0xFFFF0000u));
+}
+
+// Token tensor (caller dtype and strides) -> contiguous fp16 [B, H, N, d].  bf16 values
+// within the fp16 range convert exactly; a value of magnitude above 65504 is saturated and
+// reported as a range error.
+template <typename T>
+__global__ void to_f16_kernel(const T* __restrict__ src, ShapeArgs s, __half* __restrict__ dst, unsigned* status) {
   const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
+  bool bad = false;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t e = i * 4;
     const int c = (int)(e % s.d);
@@ -50,18 +66,28 @@ __global__ void to_bf16_kernel(const float* __restrict__ src, ShapeArgs s, __nv_
     const int n = (int)(t % s.N);
     const int64_t bh = t / s.N;
     const int h = (int)(bh % s.H), b = (int)(bh / s.H);
-    const float4 v = *reinterpret_cast<const float4*>(src + b * s.sb + h * s.sh + (int64_t)n * s.sn + c);
+    float4 v = ld4<T>(src + b * s.sb + h * s.sh + (int64_t)n * s.sn + c);
+    const float lim = 65504.f;
+    bad |= !(fabsf(v.x) <= lim && fabsf(v.y) <= lim && fabsf(v.z) <= lim && fabsf(v.w) <= lim);
+    v.x = fminf(fmaxf(v.x, -lim), lim);
+    v.y = fminf(fmaxf(v.y, -lim), lim);
+    v.z = fminf(fmaxf(v.z, -lim), lim);
+    v.w = fminf(fmaxf(v.w, -lim), lim);
     uint2 w;
-    w.x = pack_bf16x2(v.x, v.y);
-    w.y = pack_bf16x2(v.z, v.w);
+    w.x = pack_f16x2(v.x, v.y);
+    w.y = pack_f16x2(v.z, v.w);
     *reinterpret_cast<uint2*>(dst + e) = w;
   }
+  if (bad) report_error(status, kDevErrRange);
 }
 
-cudaError_t launch_to_bf16(const float* src, const ShapeArgs& s, __nv_bfloat16* dst, cudaStream_t st) {
+cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsigned* status, cudaStream_t st) {
   const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
   const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 152 * 16);
-  to_bf16_kernel<<<blocks, 256, 0, st>>>(src, s, dst);
+  if (s.dtype == 0)
+    to_f16_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), s, dst, status);
+  else
+    to_f16_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(src), s, dst, status);
   return cudaGetLastError();
 }
 
@@ -71,12 +97,16 @@ template <>
 __device__ __forceinline__ float ld_elem<float>(const float* p) { return *p; }
 template <>
 __device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+template <>
+__device__ __forceinline__ float ld_elem<__half>(const __half* p) { return __half2float(*p); }
 
-// One warp per token row: D = sum_c dO[c] * O[c] (fp32), and the row of the fp32 dQ
-// accumulator set to zero.
-template <typename T>
-__global__ void bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dO, ShapeArgs s,
-                                      float* __restrict__ Dvec, float* __restrict__ dq_acc) {
+// One warp per token row: D = sum_c dO[c] * (O[c] + O_lo[c]) (fp32), and the row of the
+// fp32 dQ accumulator set to zero.  O has the call's dtype and strides; dO is the
+// contiguous fp16 copy the MMAs read, so that D matches the dO of dP = dO V^T.
+template <typename TO, typename TD>
+__global__ void bwd_preprocess_kernel(const TO* __restrict__ o, const __nv_bfloat16* __restrict__ o_lo,
+                                      const TD* __restrict__ dO, ShapeArgs s, int64_t d_sb, int64_t d_sh,
+                                      int64_t d_sn, float* __restrict__ Dvec, float* __restrict__ dq_acc) {
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)s.B * s.H * s.N;
   for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; row < rows;
@@ -85,8 +115,12 @@ __global__ void bwd_preprocess_kernel(const T* __restrict__ o, const T* __restri
     const int64_t bh = row / s.N;
     const int h = (int)(bh % s.H), b = (int)(bh / s.H);
     const int64_t off = b * s.sb + h * s.sh + (int64_t)n * s.sn;
+    const int64_t doff = b * d_sb + h * d_sh + (int64_t)n * d_sn;
     float acc = 0.f;
-    for (int c = lane; c < s.d; c += 32) acc += ld_elem<T>(o + off + c) * ld_elem<T>(dO + off + c);
+    for (int c = lane; c < s.d; c += 32) {
+      const float ov = ld_elem<TO>(o + off + c) + (o_lo ? __bfloat162float(o_lo[off + c]) : 0.f);
+      acc += ov * ld_elem<TD>(dO + doff + c);
+    }
 #pragma unroll
     for (int w = 16; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
     if (lane == 0) Dvec[row] = acc;
@@ -95,17 +129,18 @@ __global__ void bwd_preprocess_kernel(const T* __restrict__ o, const T* __restri
   }
 }
 
-cudaError_t launch_bwd_preprocess(const ShapeArgs& s, const void* o, const void* dO, float* Dvec, float* dq_acc,
-                                  cudaStream_t st) {
+cudaError_t launch_bwd_preprocess(const ShapeArgs& s, const void* o, const void* o_lo, const __half* dO16,
+                                  float* Dvec, float* dq_acc, cudaStream_t st) {
+  const __nv_bfloat16* lo = s.dtype == 0 ? static_cast<const __nv_bfloat16*>(o_lo) : nullptr;
   const int64_t rows = (int64_t)s.B * s.H * s.N;
   const int blocks = (int)std::min<int64_t>((rows * 32 + 255) / 256, 152 * 16);
+  const int64_t csb = (int64_t)s.H * s.N * s.d, csh = (int64_t)s.N * s.d, csn = s.d;
   if (s.dtype == 0)
-    bwd_preprocess_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
-                                                                 static_cast<const __nv_bfloat16*>(dO), s, Dvec,
-                                                                 dq_acc);
+    bwd_preprocess_kernel<__nv_bfloat16, __half><<<blocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(o), lo, dO16, s, csb, csh, csn, Dvec, dq_acc);
   else
-    bwd_preprocess_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(o),
-                                                         static_cast<const float*>(dO), s, Dvec, dq_acc);
+    bwd_preprocess_kernel<float, __half><<<blocks, 256, 0, st>>>(static_cast<const float*>(o), nullptr, dO16, s,
+                                                                 csb, csh, csn, Dvec, dq_acc);
   return cudaGetLastError();
 }
 

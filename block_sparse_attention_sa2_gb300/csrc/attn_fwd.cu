@@ -10,9 +10,13 @@
 //   warp 1      TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into a double
 //               buffered TMEM tile, O += P_j V_j with P_j read from TMEM
 //   warps 2..5  softmax: each thread owns one query row (its TMEM lane); online softmax in
-//               fp32 with exp2, P_j (bf16) written back over S_j in TMEM; epilogue O / l
+//               fp32 with exp2, P_j (fp16) written back over S_j in TMEM; epilogue O / l
 //
-// TMEM columns: S buffers at 0 and 64 (fp32, 64 columns each; P_j as packed bf16 pairs in
+// Operand types: S = Q K^T in bf16 (bf16 calls) or fp16 (fp32 calls, whose inputs arrive
+// as fp16 copies); P V always in fp16 with an fp16 copy of V: P lies in [0, 1], where fp16
+// keeps 11 significant bits against bf16's 8, and bf16 V converts to fp16 exactly.
+//
+// TMEM columns: S buffers at 0 and 64 (fp32, 64 columns each; P_j as packed fp16 pairs in
 // the first 32 columns of its S buffer), O at 128 (D columns).
 #include "sa2_internal.h"
 
@@ -62,6 +66,14 @@ __device__ __forceinline__ void store_row_chunk<__nv_bfloat16>(__nv_bfloat16* ds
   }
 }
 
+// Low-order part of a bf16 rounding: bf16(v - bf16(v)), so that hi + lo carries ~16 bits.
+__device__ __forceinline__ void store_residual_chunk(__nv_bfloat16* dst, const float* v) {
+  float r[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) r[c] = v[c] - __bfloat162float(__float2bfloat16_rn(v[c]));
+  store_row_chunk<__nv_bfloat16>(dst, r);
+}
+
 template <>
 __device__ __forceinline__ void store_row_chunk<float>(float* dst, const float* v) {
   float4* p = reinterpret_cast<float4*>(dst);
@@ -69,7 +81,7 @@ __device__ __forceinline__ void store_row_chunk<float>(float* dst, const float* 
   for (int i = 0; i < 8; ++i) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-template <int D, typename OutT>
+template <int D, typename OutT, bool S_F16>
 __global__ void __launch_bounds__(kThreads, 2)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, ShapeArgs s, FwdArgs a) {
@@ -162,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else if (warp == 1) {
     // -------------------------------------------------------------------- MMA issuer
     if (lane == 0 && nkv > 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idS = idesc_f32acc(128, 64, false, false, !S_F16);
+      constexpr uint32_t idO = idesc_f16_f32(128, D, false, true);
       bool ok = mbar_wait(bar_q, 0, abort_flag);
       for (int j = 0; ok && j <= nkv; ++j) {
         if (j < nkv) {
@@ -269,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float p0 = ex2(x[2 * c] - m_used);
         const float p1 = ex2(x[2 * c + 1] - m_used);
         lsum += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+        pk[c] = pack_f16x2(p0, p1);
       }
       l += lsum;
       tmem_st32(trow + bsel * 64, pk);
@@ -286,7 +298,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         float z[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) z[c] = 0.f;
-        for (int c0 = 0; c0 < D; c0 += 32) store_row_chunk<OutT>(orow + c0, z);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          store_row_chunk<OutT>(orow + c0, z);
+          if constexpr (sizeof(OutT) == 2) {
+            if (a.o_lo) store_row_chunk<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16*>(a.o_lo) + (int64_t)b * a.o_sb +
+                                                           (int64_t)h * a.o_sh + tok * a.o_sn + c0,
+                                                       z);
+          }
+        }
         a.lse[(int64_t)bh * s.N + tok] = -INFINITY;
       }
     } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar_odone, (nkv - 1) & 1, abort_flag))) {
@@ -300,7 +319,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         float v[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(o[c]) * inv_l;
-        if (row_valid) store_row_chunk<OutT>(orow + c0, v);
+        if (row_valid) {
+          store_row_chunk<OutT>(orow + c0, v);
+          if constexpr (sizeof(OutT) == 2) {
+            if (a.o_lo) store_residual_chunk(reinterpret_cast<__nv_bfloat16*>(a.o_lo) +
+                                                 (int64_t)b * a.o_sb + (int64_t)h * a.o_sh + tok * a.o_sn + c0,
+                                             v);
+          }
+        }
       }
       if (row_valid) a.lse[(int64_t)bh * s.N + tok] = (m_used + __log2f(l)) * 0.69314718055994531f;
     }
@@ -314,26 +340,28 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-template <int D, typename OutT>
+template <int D, typename OutT, bool S_F16>
 cudaError_t launch_fwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const FwdArgs& a, cudaStream_t st) {
   const int smem = FwdSmem<D>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = attn_fwd_kernel<D, OutT, S_F16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)s.B * s.H * s.Tq;
-  attn_fwd_kernel<D, OutT><<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, s, a);
+  kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, s, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attn_fwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                            const FwdArgs& a, cudaStream_t st) {
-  if (s.d == 128)
-    return s.dtype == 0 ? launch_fwd_t<128, __nv_bfloat16>(s, mq, mk, mv, a, st)
-                        : launch_fwd_t<128, float>(s, mq, mk, mv, a, st);
-  return s.dtype == 0 ? launch_fwd_t<64, __nv_bfloat16>(s, mq, mk, mv, a, st)
-                      : launch_fwd_t<64, float>(s, mq, mk, mv, a, st);
+cudaError_t launch_attn_fwd(const ShapeArgs& s, bool s_f16, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st) {
+  // bf16 calls: bf16 S, bf16 output; fp32 calls: fp16 S, fp32 output
+  if (!s_f16)
+    return s.d == 128 ? launch_fwd_t<128, __nv_bfloat16, false>(s, mq, mk, mv, a, st)
+                      : launch_fwd_t<64, __nv_bfloat16, false>(s, mq, mk, mv, a, st);
+  return s.d == 128 ? launch_fwd_t<128, float, true>(s, mq, mk, mv, a, st)
+                    : launch_fwd_t<64, float, true>(s, mq, mk, mv, a, st);
 }
 
 }  // namespace sa2

@@ -77,48 +77,47 @@ MaskWs mask_ws(const ShapeArgs& s) {
   return w;
 }
 
+// Forward workspace: fp16 copy of V (every call); fp16 copies of Q and K (fp32 calls).
 struct FwdWs {
-  size_t q, k, v, total;
+  size_t v16, q16, k16, total;
 };
 FwdWs fwd_ws(const ShapeArgs& s) {
-  FwdWs w{0, 0, 0, 0};
+  const size_t t = align_up(2 * token_elems(s));
+  FwdWs w{};
+  w.v16 = 0;
+  w.total = t;
   if (s.dtype == SA2_FP32) {
-    const size_t t = align_up(2 * token_elems(s));
-    w.q = 0;
-    w.k = t;
-    w.v = 2 * t;
+    w.q16 = t;
+    w.k16 = 2 * t;
     w.total = 3 * t;
   }
   return w;
 }
 
+// Backward workspace: fp32 dQ accumulator, D, and fp16 copies of Q, K, V, dO.
 struct BwdWs {
-  size_t dq, D, q, k, v, dO, total;
+  size_t dq, D, q16, k16, v16, do16, total;
 };
 BwdWs bwd_ws(const ShapeArgs& s) {
   BwdWs w{};
   w.dq = 0;
   w.D = align_up(sizeof(float) * token_elems(s));
-  size_t end = align_up(w.D + sizeof(float) * (size_t)s.B * s.H * s.N);
-  if (s.dtype == SA2_FP32) {
-    const size_t t = align_up(2 * token_elems(s));
-    w.q = end;
-    w.k = end + t;
-    w.v = end + 2 * t;
-    w.dO = end + 3 * t;
-    end += 4 * t;
-  }
-  w.total = end;
+  const size_t t = align_up(2 * token_elems(s));
+  w.q16 = align_up(w.D + sizeof(float) * (size_t)s.B * s.H * s.N);
+  w.k16 = w.q16 + t;
+  w.v16 = w.k16 + t;
+  w.do16 = w.v16 + t;
+  w.total = w.do16 + t;
   return w;
 }
 
-// Tensor maps over bf16 token tensors: the caller's tensors for SA2_BF16, contiguous
-// staging copies for SA2_FP32.
-bool token_maps(const ShapeArgs& s, const void* base, bool contiguous, CUtensorMap* map, int box_rows) {
-  const int64_t sn = contiguous ? s.d : s.sn;
-  const int64_t sh = contiguous ? (int64_t)s.N * s.d : s.sh;
-  const int64_t sb = contiguous ? (int64_t)s.H * s.N * s.d : s.sb;
-  return make_token_map(map, base, s, sb, sh, sn, box_rows);
+// Tensor maps over 16-bit token tensors: the caller's bf16 tensors (strided) or the
+// library's contiguous fp16 copies.
+bool caller_map(const ShapeArgs& s, const void* base, CUtensorMap* map, int box_rows) {
+  return make_token_map(map, base, s, s.sb, s.sh, s.sn, box_rows, false);
+}
+bool copy_map(const ShapeArgs& s, const void* base, CUtensorMap* map, int box_rows) {
+  return make_token_map(map, base, s, (int64_t)s.H * s.N * s.d, (int64_t)s.N * s.d, s.d, box_rows, true);
 }
 
 }  // namespace
@@ -137,6 +136,7 @@ const char* sa2_status_string(sa2_status st) {
     case SA2_ERR_CUDA: return "CUDA error";
     case SA2_ERR_TIMEOUT: return "device wait timed out";
     case SA2_ERR_DEVICE_BOUNDS: return "block index out of range on the device";
+    case SA2_ERR_RANGE: return "input magnitude beyond the fp16 range (saturated)";
   }
   return "unknown status";
 }
@@ -196,50 +196,48 @@ size_t sa2_fwd_workspace_size(const sa2_shape* shape) {
 }
 
 sa2_status sa2_attn_fwd(const sa2_shape* shape, const void* q, const void* k, const void* v,
-                        const sa2_blockmask* mask, float softmax_scale, void* o, float* lse, void* ws,
+                        const sa2_blockmask* mask, float softmax_scale, void* o, void* o_lo, float* lse, void* ws,
                         size_t ws_bytes, void* stream) {
   ShapeArgs s;
   sa2_status st = check_shape(shape, &s);
   if (st != SA2_OK) return st;
   if (!q || !k || !v || !o || !lse || !mask || !mask->row_cnt || !mask->row_idx) return SA2_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return SA2_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(o_lo) || !aligned16(lse) ||
       !aligned16(mask->row_cnt) || !aligned16(mask->row_idx) || !aligned16(ws))
     return SA2_ERR_ALIGNMENT;
   const FwdWs w = fwd_ws(s);
-  if (w.total && (!ws || ws_bytes < w.total)) return SA2_ERR_WORKSPACE;
+  if (!ws || ws_bytes < w.total) return SA2_ERR_WORKSPACE;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const void *qb = q, *kb = k, *vb = v;
-  const bool staged = s.dtype == SA2_FP32;
-  if (staged) {
-    uint8_t* wsb = static_cast<uint8_t*>(ws);
-    __nv_bfloat16* qc = reinterpret_cast<__nv_bfloat16*>(wsb + w.q);
-    __nv_bfloat16* kc = reinterpret_cast<__nv_bfloat16*>(wsb + w.k);
-    __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(wsb + w.v);
-    if (launch_to_bf16(static_cast<const float*>(q), s, qc, cs) != cudaSuccess ||
-        launch_to_bf16(static_cast<const float*>(k), s, kc, cs) != cudaSuccess ||
-        launch_to_bf16(static_cast<const float*>(v), s, vc, cs) != cudaSuccess)
-      return SA2_ERR_CUDA;
-    qb = qc;
-    kb = kc;
-    vb = vc;
-  }
+  unsigned* status = status_ptr();
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  __half* v16 = reinterpret_cast<__half*>(wsb + w.v16);
+  if (launch_to_f16(v, s, v16, status, cs) != cudaSuccess) return SA2_ERR_CUDA;
+  const bool f16_inputs = s.dtype == SA2_FP32;
   CUtensorMap mq, mk, mv;
-  if (!token_maps(s, qb, staged, &mq, 128) || !token_maps(s, kb, staged, &mk, 64) ||
-      !token_maps(s, vb, staged, &mv, 64))
-    return SA2_ERR_CUDA;
+  if (f16_inputs) {
+    __half* q16 = reinterpret_cast<__half*>(wsb + w.q16);
+    __half* k16 = reinterpret_cast<__half*>(wsb + w.k16);
+    if (launch_to_f16(q, s, q16, status, cs) != cudaSuccess || launch_to_f16(k, s, k16, status, cs) != cudaSuccess)
+      return SA2_ERR_CUDA;
+    if (!copy_map(s, q16, &mq, 128) || !copy_map(s, k16, &mk, 64)) return SA2_ERR_CUDA;
+  } else {
+    if (!caller_map(s, q, &mq, 128) || !caller_map(s, k, &mk, 64)) return SA2_ERR_CUDA;
+  }
+  if (!copy_map(s, v16, &mv, 64)) return SA2_ERR_CUDA;
   const float scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / std::sqrt((double)s.d));
   FwdArgs a;
   a.row_cnt = mask->row_cnt;
   a.row_idx = mask->row_idx;
   a.o = o;
+  a.o_lo = s.dtype == SA2_BF16 ? o_lo : nullptr;
   a.lse = lse;
   a.o_sb = s.sb;
   a.o_sh = s.sh;
   a.o_sn = s.sn;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.status = status_ptr();
-  return cuda_status(launch_attn_fwd(s, mq, mk, mv, a, cs));
+  a.status = status;
+  return cuda_status(launch_attn_fwd(s, f16_inputs, mq, mk, mv, a, cs));
 }
 
 size_t sa2_bwd_workspace_size(const sa2_shape* shape) {
@@ -249,41 +247,36 @@ size_t sa2_bwd_workspace_size(const sa2_shape* shape) {
 }
 
 sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, const void* v, const void* o,
-                        const float* lse, const void* dO, const sa2_blockmask* mask, float softmax_scale,
-                        void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+                        const void* o_lo, const float* lse, const void* dO, const sa2_blockmask* mask,
+                        float softmax_scale, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
   ShapeArgs s;
   sa2_status st = check_shape(shape, &s);
   if (st != SA2_OK) return st;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !mask || !mask->col_cnt || !mask->col_idx)
     return SA2_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return SA2_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(o_lo) || !aligned16(lse) ||
+      !aligned16(dO) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(mask->col_cnt) ||
       !aligned16(mask->col_idx) || !aligned16(ws))
     return SA2_ERR_ALIGNMENT;
   const BwdWs w = bwd_ws(s);
   if (!ws || ws_bytes < w.total) return SA2_ERR_WORKSPACE;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  unsigned* status = status_ptr();
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* dq_acc = reinterpret_cast<float*>(wsb + w.dq);
   float* Dvec = reinterpret_cast<float*>(wsb + w.D);
-  if (launch_bwd_preprocess(s, o, dO, Dvec, dq_acc, cs) != cudaSuccess) return SA2_ERR_CUDA;
-  const void *qb = q, *kb = k, *vb = v, *dob = dO;
-  const bool staged = s.dtype == SA2_FP32;
-  if (staged) {
-    __nv_bfloat16* c[4] = {reinterpret_cast<__nv_bfloat16*>(wsb + w.q), reinterpret_cast<__nv_bfloat16*>(wsb + w.k),
-                           reinterpret_cast<__nv_bfloat16*>(wsb + w.v), reinterpret_cast<__nv_bfloat16*>(wsb + w.dO)};
-    const void* src[4] = {q, k, v, dO};
-    for (int i = 0; i < 4; ++i)
-      if (launch_to_bf16(static_cast<const float*>(src[i]), s, c[i], cs) != cudaSuccess) return SA2_ERR_CUDA;
-    qb = c[0];
-    kb = c[1];
-    vb = c[2];
-    dob = c[3];
-  }
+  __half* c16[4] = {reinterpret_cast<__half*>(wsb + w.q16), reinterpret_cast<__half*>(wsb + w.k16),
+                    reinterpret_cast<__half*>(wsb + w.v16), reinterpret_cast<__half*>(wsb + w.do16)};
+  const void* src[4] = {q, k, v, dO};
+  for (int i = 0; i < 4; ++i)
+    if (launch_to_f16(src[i], s, c16[i], status, cs) != cudaSuccess) return SA2_ERR_CUDA;
+  // D = rowsum(dO * O) from the same fp16 dO the MMAs read
+  if (launch_bwd_preprocess(s, o, o_lo, c16[3], Dvec, dq_acc, cs) != cudaSuccess) return SA2_ERR_CUDA;
   CUtensorMap mq, mk, mv, mdo;
-  if (!token_maps(s, qb, staged, &mq, 128) || !token_maps(s, kb, staged, &mk, 64) ||
-      !token_maps(s, vb, staged, &mv, 64) || !token_maps(s, dob, staged, &mdo, 128))
+  if (!copy_map(s, c16[0], &mq, 128) || !copy_map(s, c16[1], &mk, 64) || !copy_map(s, c16[2], &mv, 64) ||
+      !copy_map(s, c16[3], &mdo, 128))
     return SA2_ERR_CUDA;
   const float scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / std::sqrt((double)s.d));
   BwdArgs a;
@@ -299,7 +292,7 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   a.g_sn = s.sn;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.status = status_ptr();
+  a.status = status;
   if (launch_attn_bwd(s, mq, mk, mv, mdo, a, cs) != cudaSuccess) return SA2_ERR_CUDA;
   return cuda_status(launch_dq_convert(s, dq_acc, dq, cs));
 }

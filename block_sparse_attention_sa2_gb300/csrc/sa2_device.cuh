@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda.h>
 
 namespace sa2 {
@@ -13,6 +14,7 @@ namespace sa2 {
 // Device error codes written into the library's status word (same values as sa2_status).
 constexpr unsigned kDevErrTimeout = 6u;
 constexpr unsigned kDevErrBounds = 7u;
+constexpr unsigned kDevErrRange = 8u;
 
 // A wait on an mbarrier gives up after this many nanoseconds of %globaltimer; legitimate
 // waits in these kernels last microseconds.
@@ -113,11 +115,18 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator.
-// a_mn / b_mn select the MN-major ("transposed") operand layouts.
+// Instruction descriptor of kind::f16 with an fp32 accumulator; A and B are both bf16
+// (bf16 = true) or both fp16.  a_mn / b_mn select the MN-major ("transposed") operand
+// layouts.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn, bool b_mn, bool bf16) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+  return idesc_f32acc(M, N, a_mn, b_mn, true);
+}
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_f32acc(M, N, a_mn, b_mn, false);
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -201,6 +210,11 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 

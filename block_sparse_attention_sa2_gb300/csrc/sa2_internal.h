@@ -43,23 +43,26 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
 
 // Tensor maps of bf16 token tensors [B, H, N, d] (attn_common.cu).
 bool make_token_map(CUtensorMap* map, const void* base, const ShapeArgs& s, int64_t sb, int64_t sh, int64_t sn,
-                    int box_rows);
+                    int box_rows, bool f16);
 
 // Element-wise helpers (attn_common.cu).
-cudaError_t launch_to_bf16(const float* src, const ShapeArgs& s, __nv_bfloat16* dst, cudaStream_t st);
+cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsigned* status, cudaStream_t st);
 
 struct FwdArgs {
   const int32_t* row_cnt;
   const int32_t* row_idx;
   void* o;           // output, dtype of the call
+  void* o_lo;        // optional bf16 residual O - bf16(O) (bf16 calls only), or null
   float* lse;        // [B, H, N]
   int64_t o_sb, o_sh, o_sn;
   float scale_log2;  // softmax scale * log2(e)
   unsigned* status;
 };
 
-cudaError_t launch_attn_fwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                            const FwdArgs& a, cudaStream_t st);
+// S = Q K^T reads bf16 Q and K (s_f16 = false, bf16 calls) or their fp16 copies (fp32
+// calls); P V always reads fp16 P and V.
+cudaError_t launch_attn_fwd(const ShapeArgs& s, bool s_f16, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st);
 
 struct BwdArgs {
   const int32_t* col_cnt;
@@ -75,8 +78,8 @@ struct BwdArgs {
   unsigned* status;
 };
 
-cudaError_t launch_bwd_preprocess(const ShapeArgs& s, const void* o, const void* dO, float* Dvec, float* dq_acc,
-                                  cudaStream_t st);
+cudaError_t launch_bwd_preprocess(const ShapeArgs& s, const void* o, const void* o_lo, const __half* dO16,
+                                  float* Dvec, float* dq_acc, cudaStream_t st);
 cudaError_t launch_attn_bwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_dq_convert(const ShapeArgs& s, const float* dq_acc, void* dq, cudaStream_t st);

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libsa2.so")
 
 SA2_BF16, SA2_FP32 = 0, 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace", 5: "cuda",
-          6: "device timeout", 7: "device bounds"}
+          6: "device timeout", 7: "device bounds", 8: "input beyond fp16 range"}
 
 
 class Sa2Error(RuntimeError):
@@ -63,9 +63,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sa2_build_mask.restype = ctypes.c_int
     lib.sa2_build_mask.argtypes = [S, P, P, F, F, M, P, Z, P]
     lib.sa2_attn_fwd.restype = ctypes.c_int
-    lib.sa2_attn_fwd.argtypes = [S, P, P, P, M, F, P, P, P, Z, P]
+    lib.sa2_attn_fwd.argtypes = [S, P, P, P, M, F, P, P, P, P, Z, P]
     lib.sa2_attn_bwd.restype = ctypes.c_int
-    lib.sa2_attn_bwd.argtypes = [S, P, P, P, P, P, P, M, F, P, P, P, P, Z, P]
+    lib.sa2_attn_bwd.argtypes = [S, P, P, P, P, P, P, P, M, F, P, P, P, P, Z, P]
     lib.sa2_get_device_status.restype = ctypes.c_int
     lib.sa2_get_device_status.argtypes = [P]
     _lib = lib
@@ -157,8 +157,9 @@ def build_mask(q: torch.Tensor, k: torch.Tensor, topk: float, topp: float, bq: i
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: BlockMask, bq: int = 128, bk: int = 64,
              scale: Optional[float] = None, o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-             ws: Optional[torch.Tensor] = None, stream=None):
-    """sa2_attn_fwd: block-sparse attention forward; returns (O, LSE)."""
+             o_lo: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None, stream=None):
+    """sa2_attn_fwd: block-sparse attention forward; returns (O, LSE).  Pass ``o_lo`` (a
+    tensor like q) to also receive the low-order bf16 part of O for the backward."""
     lib = load_library()
     shp = make_shape(q, bq, bk)
     B, H, N, d = q.shape
@@ -170,13 +171,14 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: BlockMask,
         ws = workspace(lib.sa2_fwd_workspace_size(ctypes.byref(shp)), q.device)
     m = mask.struct()
     _check("sa2_attn_fwd", lib.sa2_attn_fwd(ctypes.byref(shp), q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                            ctypes.byref(m), float(scale or 0.0), o.data_ptr(), lse.data_ptr(),
-                                            ws.data_ptr(), ws.numel(), _stream(stream)))
+                                            ctypes.byref(m), float(scale or 0.0), o.data_ptr(), _ptr(o_lo),
+                                            lse.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
     return o, lse
 
 
 def attn_bwd(q, k, v, o, lse, do, mask: BlockMask, bq: int = 128, bk: int = 64, scale: Optional[float] = None,
-             dq=None, dk=None, dv=None, ws: Optional[torch.Tensor] = None, stream=None):
+             o_lo: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None, ws: Optional[torch.Tensor] = None,
+             stream=None):
     """sa2_attn_bwd: gradients (dQ, dK, dV) of the block-sparse attention, mask fixed."""
     lib = load_library()
     shp = make_shape(q, bq, bk)
@@ -187,9 +189,9 @@ def attn_bwd(q, k, v, o, lse, do, mask: BlockMask, bq: int = 128, bk: int = 64, 
         ws = workspace(lib.sa2_bwd_workspace_size(ctypes.byref(shp)), q.device)
     m = mask.struct()
     _check("sa2_attn_bwd", lib.sa2_attn_bwd(ctypes.byref(shp), q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                            o.data_ptr(), lse.data_ptr(), do.data_ptr(), ctypes.byref(m),
-                                            float(scale or 0.0), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                                            ws.data_ptr(), ws.numel(), _stream(stream)))
+                                            o.data_ptr(), _ptr(o_lo), lse.data_ptr(), do.data_ptr(),
+                                            ctypes.byref(m), float(scale or 0.0), dq.data_ptr(), dk.data_ptr(),
+                                            dv.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
     return dq, dk, dv
 
 

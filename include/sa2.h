@@ -45,7 +45,8 @@ typedef enum sa2_status {
   SA2_ERR_WORKSPACE = 4,   /* workspace missing or smaller than the size query returns */
   SA2_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
   SA2_ERR_TIMEOUT = 6,     /* device: a bounded wait inside a kernel gave up */
-  SA2_ERR_DEVICE_BOUNDS = 7 /* device: a block list held an index out of range */
+  SA2_ERR_DEVICE_BOUNDS = 7, /* device: a block list held an index out of range */
+  SA2_ERR_RANGE = 8          /* device: an attention input exceeded the fp16 range (saturated) */
 } sa2_status;
 
 typedef enum sa2_dtype { SA2_BF16 = 0, SA2_FP32 = 1 } sa2_dtype;
@@ -117,8 +118,8 @@ sa2_status sa2_build_mask(const sa2_shape* shape, const void* q, const void* k, 
                           const sa2_blockmask* out, void* ws, size_t ws_bytes, void* stream);
 
 /*
- * Bytes of device workspace sa2_attn_fwd needs (bf16 copies of q, k, v for SA2_FP32
- * inputs; a per-row work order otherwise).
+ * Bytes of device workspace sa2_attn_fwd needs: an fp16 copy of v, plus fp16 copies of q
+ * and k for SA2_FP32 inputs.
  */
 size_t sa2_fwd_workspace_size(const sa2_shape* shape);
 
@@ -131,20 +132,27 @@ size_t sa2_fwd_workspace_size(const sa2_shape* shape);
  *   O_a = sum over kept key tokens c of exp(s_ac - LSE_a) v_c,  s_ac = scale * q_a . k_c,
  *   LSE_a = log sum over kept c of exp(s_ac)   (natural log).
  * A query block with no kept key block gets O = 0 and LSE = -inf.
- * Computed in bf16 with fp32 accumulation and an fp32 online softmax (SA2_FP32 inputs are
- * rounded to bf16 first).
+ * Arithmetic: S = Q K^T on the tensor cores in bf16 (SA2_BF16) or fp16 (SA2_FP32 inputs,
+ * rounded to fp16 first), fp32 accumulation, fp32 online softmax, then P V with P and V in
+ * fp16 (P lies in [0, 1]; bf16 V converts to fp16 exactly).  Attention inputs must lie
+ * within the fp16 range (|x| <= 65504); larger values are saturated and reported as
+ * SA2_ERR_RANGE through sa2_get_device_status.
  *
  *   q, k, v   token tensors; o: token tensor (output, same dtype); lse: [B, H, N] fp32 output
+ *   o_lo      optional (NULL skips; ignored for SA2_FP32): token tensor that receives the
+ *             low-order bf16 part of O, bf16(O - bf16(O)), with the strides of o.  Handing
+ *             it to sa2_attn_bwd makes its D = rowsum(dO * O) accurate to ~16 bits instead
+ *             of bf16's 8, which matters where dS = P (dP - D) cancels (sink-dominated rows).
  *   mask      row_cnt / row_idx of the block mask (e.g. from sa2_build_mask)
  *   softmax_scale  scale of q.k (<= 0 means 1/sqrt(d))
  */
 sa2_status sa2_attn_fwd(const sa2_shape* shape, const void* q, const void* k, const void* v,
-                        const sa2_blockmask* mask, float softmax_scale, void* o, float* lse, void* ws,
-                        size_t ws_bytes, void* stream);
+                        const sa2_blockmask* mask, float softmax_scale, void* o, void* o_lo, float* lse,
+                        void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Bytes of device workspace sa2_attn_bwd needs: the fp32 dQ accumulator [B, H, N, d],
- * D = rowsum(dO * O) [B, H, N], and bf16 copies for SA2_FP32 inputs.
+ * D = rowsum(dO * O) [B, H, N], and fp16 copies of q, k, v and dO.
  */
 size_t sa2_bwd_workspace_size(const sa2_shape* shape);
 
@@ -157,13 +165,20 @@ size_t sa2_bwd_workspace_size(const sa2_shape* shape);
  *   dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q,
  * over kept tiles only.  Rows with LSE = -inf contribute nothing.
  *
- *   q, k, v, o, dO  token tensors (o and lse from sa2_attn_fwd); dq, dk, dv outputs
- *   mask      all four lists of the block mask
+ * Every product runs on the tensor cores in fp16 (q, k, v, dO converted; P and dS written
+ * in fp16, which keeps 11 significant bits where the rows of dS cancel in dQ = dS K) with
+ * fp32 accumulation; dQ is accumulated across key blocks in fp32.
+ *
+ *   q, k, v, o, dO  token tensors (o, o_lo and lse from sa2_attn_fwd); dq, dk, dv outputs
+ *   o_lo      optional residual of O from sa2_attn_fwd (NULL: D uses O alone)
+ *   mask      all four lists of the block mask; the column lists must be the transpose of
+ *             the row lists the forward used
  *   ws        device workspace of at least sa2_bwd_workspace_size(shape) bytes
  */
 sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, const void* v, const void* o,
-                        const float* lse, const void* dO, const sa2_blockmask* mask, float softmax_scale,
-                        void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+                        const void* o_lo, const float* lse, const void* dO, const sa2_blockmask* mask,
+                        float softmax_scale, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                        void* stream);
 
 /*
  * Synchronizes `stream`, then returns and clears the device status word of the current

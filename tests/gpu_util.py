@@ -7,7 +7,9 @@ import torch
 
 import oracle as O
 
-# Parity bar for bf16 attention outputs and gradients (max |delta| and sum|delta| / sum|ref|).
+# Parity bar for bf16 attention outputs and gradients: max |delta| <= 2e-2 at unit scale,
+# i.e. |delta| <= 2e-2 * max(1, |ref|) element by element (a bf16 result of magnitude >= 8
+# is 0.03-0.06 per ulp, so a flat 2e-2 cannot hold there), and sum|delta| / sum|ref| <= 5e-3.
 MAX_ABS = 2e-2
 MEAN_REL = 5e-3
 # Pooled probabilities within this distance of a row's selection threshold may be decided
@@ -36,15 +38,18 @@ def blockmask_from_oracle(mask: np.ndarray, device="cuda"):
 
 
 def errors(got: np.ndarray, ref: np.ndarray):
+    """(max |d| / max(1, |ref|), sum|d| / sum|ref|)."""
     d = np.abs(got - ref)
     denom = np.abs(ref).sum()
-    return float(d.max()) if d.size else 0.0, float(d.sum() / denom) if denom > 0 else float(d.sum())
+    scaled = d / np.maximum(1.0, np.abs(ref))
+    return float(scaled.max()) if d.size else 0.0, float(d.sum() / denom) if denom > 0 else float(d.sum())
 
 
 def assert_close(name: str, got: np.ndarray, ref: np.ndarray, max_abs=MAX_ABS, mean_rel=MEAN_REL):
     mx, mr = errors(got, ref)
     assert np.isfinite(got).all(), f"{name}: non-finite values"
-    assert mx <= max_abs and mr <= mean_rel, f"{name}: max|d| {mx:.3e} (<= {max_abs}), mean rel {mr:.3e} (<= {mean_rel})"
+    assert mx <= max_abs and mr <= mean_rel, \
+        f"{name}: max|d|/max(1,|ref|) {mx:.3e} (<= {max_abs}), mean rel {mr:.3e} (<= {mean_rel})"
     return mx, mr
 
 

@@ -1,0 +1,139 @@
+"""GPU parity of sa2_attn_bwd against the fp64 oracle.
+
+Forward then backward run on the CUDA path with the oracle's mask; the oracle computes
+dQ, dK, dV from the same inputs.  Bar on each gradient: max |d| <= 2e-2 and
+sum|d| / sum|ref| <= 5e-3.  fp32 inputs: the reference is the oracle on the fp16-rounded
+inputs (the library's documented staging), plus a looser check on the exact inputs."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.gpu_util import assert_close, blockmask_from_oracle, to_device, to_f64
+from workload import CONFIGS, make_inputs
+from workload.gen import small_case
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+FP32_INPUT_MAX_ABS = 6e-2
+
+
+@pytest.fixture(scope="module")
+def sa2():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_sparse_attention_sa2_gb300 as m
+    m.load_library()
+    return m
+
+
+def attn_inputs(x):
+    """fp32 inputs rounded to fp16 (the library's documented staging); bf16 as they are."""
+    return {t: (a.astype(np.float16).astype(np.float32) if a.dtype == np.float32 else a) for t, a in x.items()}
+
+
+def _run(sa2, cfg, x, mask, scale=None):
+    q, k, v, do = (to_device(x[t]) for t in ("q", "k", "v", "do"))
+    bm = blockmask_from_oracle(mask)
+    o_lo = torch.empty_like(q) if q.dtype == torch.bfloat16 else None
+    o, lse = sa2.attn_fwd(q, k, v, bm, bq=cfg.bq, bk=cfg.bk, scale=scale, o_lo=o_lo)
+    dq, dk, dv = sa2.attn_bwd(q, k, v, o, lse, do, bm, bq=cfg.bq, bk=cfg.bk, scale=scale, o_lo=o_lo)
+    sa2.check_device()
+    return to_f64(dq), to_f64(dk), to_f64(dv)
+
+
+def _full_check(sa2, cfg, x, mask, scale=None):
+    g = _run(sa2, cfg, x, mask, scale)
+    xa = attn_inputs(x)
+    ref = O.attn_bwd(xa["q"], xa["k"], xa["v"], xa["do"], mask, cfg.bq, cfg.bk, scale)
+    for name, got, want in zip(("dQ", "dK", "dV"), g, ref):
+        for b in range(cfg.B):
+            for h in range(cfg.H):
+                assert_close(f"{cfg.name} b{b}h{h} {name}", got[b, h], want[b, h])
+    if cfg.dtype == "fp32":
+        exact = O.attn_bwd(x["q"], x["k"], x["v"], x["do"], mask, cfg.bq, cfg.bk, scale)
+        for name, got, want in zip(("dQ", "dK", "dV"), g, exact):
+            assert_close(f"{cfg.name} {name} vs exact fp32", got, want, max_abs=FP32_INPUT_MAX_ABS)
+    return g
+
+
+def test_bwd_tiny_fp32_config(sa2):
+    cfg = CONFIGS[0]
+    x = make_inputs(cfg)
+    mask = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, cfg.topk, cfg.topp)["mask"]
+    _full_check(sa2, cfg, x, mask)
+
+
+@pytest.mark.parametrize("N,d,bq,dtype", [(1000, 128, 128, "bf16"), (777, 64, 64, "bf16"), (1000, 64, 128, "fp32"),
+                                          (1100, 128, 64, "fp32"), (130, 128, 128, "bf16"), (1, 64, 128, "bf16")])
+def test_bwd_ragged_small_cases(sa2, N, d, bq, dtype):
+    cfg, x = small_case(f"ragged-{N}", 2, 2, N, d, dtype, bq, 64, seed=5)
+    for topk, topp in ((0.2, 0.6), (1.0, 0.0), (0.0, 0.3)):
+        mask = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, topk, topp)["mask"]
+        _full_check(sa2, cfg, x, mask)
+
+
+def test_bwd_random_masks_empty_rows_unused_keys_and_scale(sa2):
+    cfg, x = small_case("random-mask", 1, 3, 700, 128, "bf16", 128, 64, seed=7)
+    rng = np.random.default_rng(1)
+    mask = (rng.random((1, 3, cfg.Tq, cfg.Tk)) < 0.3).astype(np.uint8)
+    mask[0, 0, 2] = 0  # a query block that keeps nothing
+    mask[0, 2, :, 4] = 0  # a key block kept by nobody: dK = dV = 0
+    mask[0, 1] = 0
+    g = _full_check(sa2, cfg, x, mask)
+    assert not g[1][0, 2, 4 * 64:5 * 64].any() and not g[2][0, 2, 4 * 64:5 * 64].any()
+    _full_check(sa2, cfg, x, mask, scale=0.05)
+
+
+def test_bwd_gradient_invariants_on_gpu(sa2):
+    """Every row of dS sums to zero and every row of P to one: the keys' dK sum to ~0 and
+    the keys' dV sum to the queries' dO (rows that keep something)."""
+    cfg, x = small_case("invariants", 1, 2, 1024, 128, "bf16", 128, 64, seed=13)
+    mask = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, 0.25, 0.5)["mask"]
+    dq, dk, dv = _run(sa2, cfg, x, mask)
+    do = O.to_f64(x["do"])
+    for h in range(cfg.H):
+        assert np.abs(dk[0, h].sum(axis=0)).max() < 0.1
+        np.testing.assert_allclose(dv[0, h].sum(axis=0), do[0, h].sum(axis=0), atol=0.25, rtol=2e-2)
+
+
+def _sampled_check(sa2, cfg, x, mask, heads, rows, key_blocks):
+    dq, dk, dv = _run(sa2, cfg, x, mask)
+    for (b, h) in heads:
+        q, k, v, do = (O.to_f64(x[t][b, h]) for t in ("q", "k", "v", "do"))
+        rdq = O.attn_bwd_dq_rows(q, k, v, do, mask[b, h], cfg.bq, cfg.bk, rows)
+        assert_close(f"{cfg.name} h{h} dQ rows", dq[b, h, rows], rdq)
+        cols = np.concatenate([np.arange(j * cfg.bk, min(cfg.N, (j + 1) * cfg.bk)) for j in key_blocks])
+        rdk, rdv = O.attn_bwd_dkdv_cols(q, k, v, do, mask[b, h], cfg.bq, cfg.bk, cols)
+        assert_close(f"{cfg.name} h{h} dK cols", dk[b, h, cols], rdk)
+        assert_close(f"{cfg.name} h{h} dV cols", dv[b, h, cols], rdv)
+
+
+def test_bwd_mask_probe_config_sampled(sa2):
+    cfg = CONFIGS[1]
+    x = make_inputs(cfg)
+    mask = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, 0.05, 0.9)["mask"]
+    rows = np.concatenate([np.arange(0, 130), np.arange(cfg.N - 130, cfg.N)])
+    _sampled_check(sa2, cfg, x, mask, [(0, 0), (0, 5)], rows, [0, 1, 63, cfg.Tk - 1])
+
+
+@pytest.mark.parametrize("ci", [2, 3])
+def test_bwd_full_size_wan_shapes_sampled(sa2, ci):
+    """Full size with the calibrated 95 % mask of two heads (the other heads keep a
+    diagonal band); sampled query rows and key blocks recomputed by the oracle."""
+    cfg = CONFIGS[ci]
+    cal = json.load(open(os.path.join(GOLDEN, "calibration.json")))[str(ci)]["targets"]["0.95"]
+    x = make_inputs(cfg, threads=16)
+    heads = [(0, 1), (0, cfg.H - 1)]
+    ref = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, cal["k"], cal["p"], heads=heads)
+    mask = ref["mask"].copy()
+    for h in range(cfg.H):
+        if (0, h) not in heads:
+            for i in range(cfg.Tq):
+                mask[0, h, i, max(0, 2 * i - 3): 2 * i + 5] = 1
+    rows = np.concatenate([np.arange(0, 64), np.arange(cfg.N // 2, cfg.N // 2 + 32), np.arange(cfg.N - 64, cfg.N)])
+    _sampled_check(sa2, cfg, x, mask, heads, rows, [0, cfg.Tk // 2, cfg.Tk - 1])
