@@ -1,0 +1,400 @@
+"""Benchmark of the SpargeAttention2 hot path on GB300.
+
+One step = the whole hot path over one batch of synthetic input: the hybrid Top-k + Top-p
+block mask (sa2_build_mask), the block-sparse forward (sa2_attn_fwd) and the backward
+(sa2_attn_bwd), on a Wan2.1-14B-720p-shaped attention layer (B=1, H=40, N=75600 tokens of
+a 21x45x80 latent, d=128, bf16, 128x64 blocks) at the calibrated 95 % block sparsity.
+
+Metric: kept-tile TFLOP/s of forward + backward (4 + 10 flops per kept query-key pair per
+channel, over valid tokens only), whole job over all ranks.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this method has) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workload import CONFIGS, make_inputs  # noqa: E402
+
+FWD_FLOPS, BWD_FLOPS = 4, 10  # per kept (query, key) pair and channel
+
+# DRAM bytes of one attn_bwd launch from an ncu capture (profiles/attn_bwd_ncu.md); null
+# once the kernel source differs from the one measured.
+BWD_TRAFFIC = None
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--sparsity", type=float, default=0.95)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-qblocks", type=int, default=4, help="query blocks of the oracle sample")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return a
+
+
+def calibration(ci: int, sparsity: float):
+    path = os.path.join(ROOT, "tests", "golden", "calibration.json")
+    cal = json.load(open(path))
+    entry = cal[str(ci)]["targets"][f"{sparsity:.2f}"]
+    return float(entry["k"]), float(entry["p"])
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def cpu_threads() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------- kept work
+
+def tile_sizes(cfg):
+    rq = np.minimum(cfg.bq, cfg.N - np.arange(cfg.Tq) * cfg.bq).astype(np.float64)
+    rk = np.minimum(cfg.bk, cfg.N - np.arange(cfg.Tk) * cfg.bk).astype(np.float64)
+    return rq, rk
+
+
+def kept_pairs(cfg, mask_u8) -> float:
+    """Sum over kept tiles of (valid query rows x valid key columns)."""
+    rq, rk = tile_sizes(cfg)
+    m = mask_u8.reshape(-1, cfg.Tq, cfg.Tk).astype(np.float64)
+    return float(np.einsum("gij,i,j->", m, rq, rk))
+
+
+# --------------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(cfg, x, topk, topp, qblocks):
+    """The oracle on a bounded sample of the workload: the mask of head 0 (pooling, pooled
+    softmax, selection over all its rows), then forward and backward of the listed query
+    blocks of head 0.  Returns (seconds, kept flops of the sampled rows, description)."""
+    import oracle as O
+    t0 = time.perf_counter()
+    q, k, v, do = (O.to_f64(x[t][0, 0]) for t in ("q", "k", "v", "do"))
+    r = O.build_mask_head(q, k, cfg.bq, cfg.bk, topk, topp)
+    mask = r["mask"]
+    rq, rk = tile_sizes(cfg)
+    flops = 0.0
+    for i in qblocks:
+        rows = np.arange(i * cfg.bq, min(cfg.N, (i + 1) * cfg.bq))
+        O.attn_fwd_head(q, k, v, mask, cfg.bq, cfg.bk, rows=rows)
+        O.attn_bwd_rows(q, k, v, do, mask, cfg.bq, cfg.bk, rows)
+        flops += (FWD_FLOPS + BWD_FLOPS) * cfg.d * rq[i] * float((mask[i] * rk).sum())
+    dt = time.perf_counter() - t0
+    desc = (f"oracle (numpy fp64) mask of head 0 + forward/backward of query blocks {list(qblocks)} of head 0 "
+            f"({len(qblocks) * cfg.bq} query rows against all {cfg.N} keys)")
+    return dt, flops, desc
+
+
+def spread_qblocks(cfg, n):
+    return sorted(set(int(round(v)) for v in np.linspace(0, cfg.Tq - 1, n)))
+
+
+# ---------------------------------------------------------------------- clock sampler
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id):
+        self.bus_id = (bus_id or "").lower()
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        lines = [ln.strip() for ln in open(self.f.name) if ln.strip()]
+        os.unlink(self.f.name)
+        rows = [[c.strip() for c in ln.split(",")] for ln in lines]
+        mine = [r for r in rows if len(r) >= 10 and (not self.bus_id or self.bus_id[-12:] in r[1].lower())]
+        if not mine:
+            mine = [r for r in rows if len(r) >= 10 and r[0] == "0"]
+        sm = [float(r[2]) for r in mine if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in mine if r[3].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in mine for i in range(4) if r[6 + i].lower().startswith("active")})
+        # samples under load: the upper half of the observed clocks (the bench keeps the GPU busy)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- native
+
+def run_native(a, rank, world):
+    import torch
+    import block_sparse_attention_sa2_gb300 as sa2
+    from block_sparse_attention_sa2_gb300 import build_lib
+
+    if not build_lib.up_to_date():
+        if rank == 0:
+            build_lib.build()
+        if world > 1:
+            torch.distributed.barrier()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    cfg = CONFIGS[a.config]
+    topk, topp = calibration(a.config, a.sparsity)
+    x = make_inputs(cfg, threads=os.cpu_count() or 8)
+
+    def pinned(arr):
+        t = torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    host = {t: pinned(x[t]) for t in ("q", "k", "v", "do")}
+    d = {t: host[t].to(dev) for t in host}
+    stream = torch.cuda.current_stream()
+    B, H, N, D = d["q"].shape
+    bm = sa2.BlockMask.empty(B, H, cfg.Tq, cfg.Tk, dev, mask=True)
+    lib = sa2.load_library()
+    shp = sa2.make_shape(d["q"], cfg.bq, cfg.bk)
+    import ctypes
+    ws_m = sa2.workspace(lib.sa2_mask_workspace_size(ctypes.byref(shp)), dev)
+    ws_f = sa2.workspace(lib.sa2_fwd_workspace_size(ctypes.byref(shp)), dev)
+    ws_b = sa2.workspace(lib.sa2_bwd_workspace_size(ctypes.byref(shp)), dev)
+    o, o_lo = torch.empty_like(d["q"]), torch.empty_like(d["q"])
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+
+    def step(src):
+        sa2.build_mask(src["q"], src["k"], topk, topp, bq=cfg.bq, bk=cfg.bk, out=bm, ws=ws_m)
+        sa2.attn_fwd(src["q"], src["k"], src["v"], bm, bq=cfg.bq, bk=cfg.bk, o=o, lse=lse, o_lo=o_lo, ws=ws_f)
+        sa2.attn_bwd(src["q"], src["k"], src["v"], o, lse, src["do"], bm, bq=cfg.bq, bk=cfg.bk, o_lo=o_lo,
+                     dq=dq, dk=dk, dv=dv, ws=ws_b)
+
+    for _ in range(a.warmup):
+        step(d)
+    sa2.check_device()
+    torch.cuda.synchronize()
+    mask_np = bm.mask.cpu().numpy()
+    pairs = kept_pairs(cfg, mask_np)
+    sparsity = 1.0 - float(bm.row_cnt.sum().item()) / (B * H * cfg.Tq * cfg.Tk)
+    flops_step = (FWD_FLOPS + BWD_FLOPS) * D * pairs
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        pass
+    clocks = ClockSampler(bus)
+    if rank == 0:
+        clocks.start()
+    sa2.profiler_enable(True)
+    sa2.profiler_collect()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
+    ev0.record(stream)
+    for _ in range(a.steps):
+        step(d)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    if world > 1:
+        torch.distributed.barrier()
+    sa2.profiler_enable(False)
+    prof = sa2.profiler_collect()
+    sa2.check_device()
+    ms = ev0.elapsed_time(ev1)
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+    clk = clocks.stop() if rank == 0 else None
+
+    # ---- end to end through the public API with host buffers
+    e2e_steps = max(1, a.e2e_steps)
+    hout = {n: torch.empty_like(host["q"]).pin_memory() for n in ("o", "dq", "dk", "dv")}
+    dst = {t: torch.empty_like(d[t]) for t in d}
+    h2d = sum(host[t].numel() * host[t].element_size() for t in host)
+    d2h = sum(hout[n].numel() * hout[n].element_size() for n in hout)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for t in host:
+            dst[t].copy_(host[t], non_blocking=True)
+        step(dst)
+        for n, src_t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+            hout[n].copy_(src_t, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e2e_ms = float(te.item()) / e2e_steps
+    sa2.check_device()
+
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    value = world * flops_step * a.steps / (ms_max * 1e-3) / 1e12
+    kernels = {n: {"launches": c, "ms_per_launch": (m / c if c else 0.0), "total_ms": m} for n, (c, m) in prof.items()}
+    launches = sum(c for c, _ in prof.values())
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
+    algo = {"attn_bwd": BWD_FLOPS * D * pairs, "attn_fwd": FWD_FLOPS * D * pairs}
+    c, m = prof[dom]
+    if dom in algo and c > 0 and m > 0:
+        achieved = algo[dom] / ((m / c) * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": BWD_TRAFFIC if dom == "attn_bwd" else None,
+                "peak_source": f"{peaks['source']} bf16 dense, sustained (fp16 MMAs: same nominal rate)",
+                "algorithmic_flops_per_launch": algo[dom]}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": None, "traffic": None}
+    # mask builder against HBM: it reads Q and K once and writes the mask and lists
+    qk_bytes = 2 * B * H * N * D * 2
+    out_bytes = B * H * cfg.Tq * cfg.Tk + 4 * 2 * float(bm.row_cnt.sum().item()) + 4 * B * H * (cfg.Tq + cfg.Tk)
+    mask_ms = sum(prof[k][1] for k in ("pool", "score_select", "csc")) / a.steps
+    mask_gbs = (qk_bytes + out_bytes) / (mask_ms * 1e-3) / 1e9 if mask_ms > 0 else None
+    fwd_ms = (prof["attn_fwd"][1]) / a.steps
+    bwd_ms = prof["attn_bwd"][1] / a.steps
+    line = {
+        "metric": "block-sparse attn fwd+bwd TFLOPS over kept tiles (whole hot path: mask + fwd + bwd) at 95% sparsity",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": ms_max / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in/out; tcgen05 MMAs bf16 (S) and fp16 (P, dS), fp32 accumulate", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} attention layer: B={B}, H={H}, N={N} (latent 21x45x80), d={D}, bf16, "
+                               f"blocks {cfg.bq}x{cfg.bk}",
+                   "block_sparsity": sparsity, "topk": topk, "topp": topp, "seed": 0,
+                   "l2": "inputs larger than L2 (Q,K,V,dO = %.1f GB per step); no flush" % (4 * B * H * N * D * 2 / 1e9),
+                   "step": "sa2_build_mask + sa2_attn_fwd + sa2_attn_bwd", "parallelism": f"replicas x{world}"},
+        "kept_tflop_per_step": flops_step / 1e12,
+        "dense_equiv_tflops": world * (FWD_FLOPS + BWD_FLOPS) * D * float(N) * N * B * H * a.steps / (ms_max * 1e-3) / 1e12,
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "mask_ms": mask_ms,
+        "fwd_tflops": FWD_FLOPS * D * pairs / (fwd_ms * 1e-3) / 1e12 if fwd_ms > 0 else None,
+        "bwd_tflops": BWD_FLOPS * D * pairs / (bwd_ms * 1e-3) / 1e12 if bwd_ms > 0 else None,
+        "mask_builder": {"ms": mask_ms, "achieved_gbs": mask_gbs, "peak_gbs": peaks["hbm_gbs"],
+                         "frac": mask_gbs / peaks["hbm_gbs"] if mask_gbs else None, "bytes": qk_bytes + out_bytes},
+        "roofline": roof,
+        "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "kernels": kernels,
+        "clocks": clk,
+    }
+    if world == 1 and not a.no_cpu_baseline:
+        secs, cflops, desc = oracle_sample(cfg, x, topk, topp, spread_qblocks(cfg, a.cpu_qblocks))
+        line["cpu_baseline"] = {"value": cflops / secs / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+                                "kind": "oracle", "sample": desc, "seconds": secs}
+    return line
+
+
+# ------------------------------------------------------------------------- reference
+
+def run_reference(a, rank, world):
+    if rank != 0:
+        return None
+    cfg = CONFIGS[a.config]
+    topk, topp = calibration(a.config, a.sparsity)
+    x = make_inputs(cfg, tensors=("q", "k", "v", "do"), heads=[(0, 0)])
+    qb = spread_qblocks(cfg, 2)
+    for _ in range(a.warmup):
+        oracle_sample(cfg, x, topk, topp, qb)
+    t0 = time.perf_counter()
+    flops = 0.0
+    desc = ""
+    for _ in range(a.steps):
+        _, f, desc = oracle_sample(cfg, x, topk, topp, qb)
+        flops += f
+    secs = time.perf_counter() - t0
+    value = flops / secs / 1e12
+    return {
+        "impl": "reference",
+        "metric": "block-sparse attn fwd+bwd TFLOPS over kept tiles (whole hot path: mask + fwd + bwd) at 95% sparsity",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": secs * 1e3 / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} attention layer (bounded oracle sample per step)",
+                   "topk": topk, "topp": topp, "seed": 0},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    a = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        backend = "nccl" if a.impl == "native" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group(backend)
+    line = run_reference(a, rank, world) if a.impl == "reference" else run_native(a, rank, world)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -15,4 +15,7 @@ from .sa2 import (  # noqa: F401
     device_status,
     load_library,
     make_shape,
+    profiler_collect,
+    profiler_enable,
+    workspace,
 )

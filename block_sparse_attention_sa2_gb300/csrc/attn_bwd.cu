@@ -358,7 +358,9 @@ cudaError_t launch_bwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtens
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)s.B * s.H * s.Tk;
+  prof_start(st, kAttnBwd);
   attn_bwd_kernel<GT><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, s, a);
+  prof_stop(st, kAttnBwd);
   return cudaGetLastError();
 }
 

@@ -84,10 +84,12 @@ __global__ void to_f16_kernel(const T* __restrict__ src, ShapeArgs s, __half* __
 cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsigned* status, cudaStream_t st) {
   const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
   const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 152 * 16);
+  prof_start(st, kToF16);
   if (s.dtype == 0)
     to_f16_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), s, dst, status);
   else
     to_f16_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(src), s, dst, status);
+  prof_stop(st, kToF16);
   return cudaGetLastError();
 }
 
@@ -135,12 +137,14 @@ cudaError_t launch_bwd_preprocess(const ShapeArgs& s, const void* o, const void*
   const int64_t rows = (int64_t)s.B * s.H * s.N;
   const int blocks = (int)std::min<int64_t>((rows * 32 + 255) / 256, 152 * 16);
   const int64_t csb = (int64_t)s.H * s.N * s.d, csh = (int64_t)s.N * s.d, csn = s.d;
+  prof_start(st, kBwdPre);
   if (s.dtype == 0)
     bwd_preprocess_kernel<__nv_bfloat16, __half><<<blocks, 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(o), lo, dO16, s, csb, csh, csn, Dvec, dq_acc);
   else
     bwd_preprocess_kernel<float, __half><<<blocks, 256, 0, st>>>(static_cast<const float*>(o), nullptr, dO16, s,
                                                                  csb, csh, csn, Dvec, dq_acc);
+  prof_stop(st, kBwdPre);
   return cudaGetLastError();
 }
 
@@ -171,10 +175,12 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, ShapeArgs s, T*
 cudaError_t launch_dq_convert(const ShapeArgs& s, const float* dq_acc, void* dq, cudaStream_t st) {
   const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
   const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 152 * 16);
+  prof_start(st, kDqConvert);
   if (s.dtype == 0)
     dq_convert_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(dq_acc, s, static_cast<__nv_bfloat16*>(dq));
   else
     dq_convert_kernel<float><<<blocks, 256, 0, st>>>(dq_acc, s, static_cast<float*>(dq));
+  prof_stop(st, kDqConvert);
   return cudaGetLastError();
 }
 

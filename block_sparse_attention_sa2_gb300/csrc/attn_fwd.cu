@@ -348,7 +348,9 @@ cudaError_t launch_fwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtens
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)s.B * s.H * s.Tq;
+  prof_start(st, kAttnFwd);
   kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, s, a);
+  prof_stop(st, kAttnFwd);
   return cudaGetLastError();
 }
 

@@ -318,19 +318,23 @@ static cudaError_t launch_score(const float* qbarT, const float* kbarT, const Sh
                                        (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((s.Tq + RQ - 1) / RQ, s.B * s.H);
+  prof_start(st, kScoreSelect);
   score_select_kernel<RQ><<<grid, kScoreThreads, smem, st>>>(qbarT, kbarT, s, sel, out);
+  prof_stop(st, kScoreSelect);
   return cudaGetLastError();
 }
 
 cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, const SelectArgs& sel,
                               float* qbarT, float* kbarT, const MaskOut& out, cudaStream_t st) {
   dim3 pgrid(s.Tq + s.Tk, s.B * s.H);
+  prof_start(st, kPool);
   if (s.dtype == 0)
     pool_kernel<__nv_bfloat16><<<pgrid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(q),
                                                        static_cast<const __nv_bfloat16*>(k), s, qbarT, kbarT);
   else
     pool_kernel<float><<<pgrid, 256, 0, st>>>(static_cast<const float*>(q), static_cast<const float*>(k), s, qbarT,
                                               kbarT);
+  prof_stop(st, kPool);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int rq = score_rows_per_cta(s.Tk, s.d);
@@ -342,7 +346,9 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
     e = launch_score<4>(qbarT, kbarT, s, sel, out, st);
   if (e != cudaSuccess) return e;
   dim3 cgrid((s.Tk + 127) / 128, s.B * s.H);
+  prof_start(st, kCsc);
   csc_kernel<<<cgrid, 128, 0, st>>>(s, out.mask, out.col_cnt, out.col_idx);
+  prof_stop(st, kCsc);
   return cudaGetLastError();
 }
 

@@ -13,6 +13,11 @@ namespace sa2 {
 
 constexpr size_t kMaxDynSmem = 227 * 1024;
 
+// Launch profiler (profiler.cu): kernel ids and the brackets every launch wrapper calls.
+enum KernelId { kPool = 0, kScoreSelect, kCsc, kToF16, kAttnFwd, kBwdPre, kAttnBwd, kDqConvert, kNumKernelIds };
+void prof_start(cudaStream_t st, int id);
+void prof_stop(cudaStream_t st, int id);
+
 // Shape of one call, with the derived block counts.  Strides are in elements.
 struct ShapeArgs {
   int B, H, N, d, bq, bk, Tq, Tk, dtype;

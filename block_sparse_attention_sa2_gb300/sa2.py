@@ -36,6 +36,10 @@ class Shape(ctypes.Structure):
                 ("stride_n", ctypes.c_int64)]
 
 
+class KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
+
+
 class BlockMaskStruct(ctypes.Structure):
     _fields_ = [("row_cnt", ctypes.c_void_p), ("row_idx", ctypes.c_void_p), ("col_cnt", ctypes.c_void_p),
                 ("col_idx", ctypes.c_void_p), ("mask", ctypes.c_void_p), ("pooled_p", ctypes.c_void_p)]
@@ -68,6 +72,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sa2_attn_bwd.argtypes = [S, P, P, P, P, P, P, P, M, F, P, P, P, P, Z, P]
     lib.sa2_get_device_status.restype = ctypes.c_int
     lib.sa2_get_device_status.argtypes = [P]
+    lib.sa2_profiler_enable.restype = None
+    lib.sa2_profiler_enable.argtypes = [ctypes.c_int]
+    lib.sa2_profiler_collect.restype = ctypes.c_int
+    lib.sa2_profiler_collect.argtypes = [ctypes.POINTER(KernelTime), ctypes.c_int]
     _lib = lib
     return lib
 
@@ -198,6 +206,22 @@ def attn_bwd(q, k, v, o, lse, do, mask: BlockMask, bq: int = 128, bk: int = 64, 
 def device_status(stream=None) -> int:
     """sa2_get_device_status: synchronizes the stream and returns (and clears) the status."""
     return load_library().sa2_get_device_status(_stream(stream))
+
+
+def profiler_enable(on: bool = True):
+    """sa2_profiler_enable: bracket every later kernel launch with CUDA events."""
+    load_library().sa2_profiler_enable(1 if on else 0)
+
+
+def profiler_collect() -> dict:
+    """sa2_profiler_collect: {kernel name: (launches, total device ms)} since the last call."""
+    lib = load_library()
+    n = lib.sa2_profiler_collect(None, 0)
+    arr = (KernelTime * n)()
+    got = lib.sa2_profiler_collect(arr, n)
+    if got < 0:
+        raise Sa2Error("sa2_profiler_collect", 5)
+    return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(got)}
 
 
 def check_device(stream=None):

@@ -181,6 +181,25 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
                         void* stream);
 
 /*
+ * Launch profiler (instrumentation of this library; the pages have no counterpart).
+ * sa2_profiler_enable(1) makes every later kernel launch of the library record a CUDA
+ * event before and after it on its stream; sa2_profiler_enable(0) stops that.
+ * sa2_profiler_collect waits for the recorded events, writes up to max_entries records
+ * (one per kernel of the library: name, launches, summed device milliseconds) and clears
+ * them; it returns the number of records written, or -1 when an event could not be read.
+ * With out == NULL it returns the number of kernels and leaves the records in place.  Not thread-safe against concurrent
+ * launches from several host threads on different streams of the same kernel.
+ */
+typedef struct sa2_kernel_time {
+  const char* name; /* static string */
+  int launches;
+  double total_ms;
+} sa2_kernel_time;
+
+void sa2_profiler_enable(int on);
+int sa2_profiler_collect(sa2_kernel_time* out, int max_entries);
+
+/*
  * Synchronizes `stream`, then returns and clears the device status word of the current
  * device: SA2_OK, SA2_ERR_TIMEOUT or SA2_ERR_DEVICE_BOUNDS (or SA2_ERR_CUDA when the
  * synchronization itself fails).

@@ -271,6 +271,22 @@ def attn_bwd_dq_rows(q, k, v, do, block_mask, bq, bk, rows, scale=None):
     return scale * (dS @ k)
 
 
+def attn_bwd_rows(q, k, v, do, block_mask, bq, bk, rows, scale=None):
+    """The backward restricted to the listed query rows: their dQ rows, and their
+    contributions to dK and dV (the gradient is a sum over query rows, so contributions of
+    a partition of the rows add up to the full dK, dV).  Returns (dQ_rows, dK_part, dV_part)."""
+    N, d = k.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rows = np.asarray(rows)
+    allowed = token_mask(block_mask, N, bq, bk, rows)
+    P, _ = _masked_softmax_rows((q[rows] @ k.T) * scale, allowed)
+    o = P @ v
+    dP = do[rows] @ v.T
+    D = (do[rows] * o).sum(axis=1)
+    dS = P * (dP - D[:, None])
+    return scale * (dS @ k), scale * (dS.T @ q[rows]), P.T @ do[rows]
+
+
 def attn_bwd_dkdv_cols(q, k, v, do, block_mask, bq, bk, cols, scale=None):
     """dK and dV of the listed key tokens only.  Every query row that keeps one of these
     keys is recomputed in full (its softmax needs the whole row)."""

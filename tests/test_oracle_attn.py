@@ -171,6 +171,20 @@ def test_row_and_column_sampled_versions_equal_the_full_computation():
     np.testing.assert_allclose(dv_c, dv[cols], rtol=1e-12, atol=1e-13)
 
 
+def test_row_partition_of_the_backward_adds_up():
+    q, k, v, do, mask = _rand_case(14, N=50, d=8, bq=16, bk=8, density=0.5)
+    dq, dk, dv = O.attn_bwd_head(q, k, v, do, mask, 16, 8)
+    parts = [np.arange(0, 16), np.arange(16, 40), np.arange(40, 50)]
+    dk_sum, dv_sum = np.zeros_like(dk), np.zeros_like(dv)
+    for rows in parts:
+        dq_r, dk_p, dv_p = O.attn_bwd_rows(q, k, v, do, mask, 16, 8, rows)
+        np.testing.assert_allclose(dq_r, dq[rows], rtol=1e-12, atol=1e-13)
+        dk_sum += dk_p
+        dv_sum += dv_p
+    np.testing.assert_allclose(dk_sum, dk, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dv_sum, dv, rtol=1e-12, atol=1e-13)
+
+
 def test_batched_wrappers_and_bf16_widening():
     from workload import bf16_round_bits
     rng = np.random.default_rng(12)
