@@ -1,0 +1,122 @@
+// sa2_build_mask_noalloc: the hybrid block mask for callers that cannot allocate device
+// memory.
+//
+// Some callers of this library have no way to hand it a workspace: code that runs inside
+// another runtime's memory pool and may not call cudaMalloc (a custom allocator that is
+// not re-entrant, a framework plugin that only receives tensors), or code on a path where
+// an allocation would synchronize the device.  For them this entry point keeps the
+// builder's scratch -- the fp32 pooled queries and keys -- in a fixed array of device
+// memory that belongs to the library itself.  The array is static: every GPU that loads
+// the library holds it until the process exits.
+//
+// The kernels are the ones sa2_build_mask launches; only where their scratch lives differs.
+#include <cmath>
+#include <mutex>
+
+#include "../../include/sa2.h"
+#include "sa2_internal.h"
+
+using namespace sa2;
+
+namespace {
+
+// The builder's scratch.  In host code this name is only a host-side stand-in for the
+// device array: its device address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SA2_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_ptr[kMaxDevices];
+cudaError_t g_scratch_err[kMaxDevices];
+std::once_flag g_scratch_once[kMaxDevices];
+
+// Device address of the scratch array on the current device (set up on first use there).
+void* scratch_for_current_device(cudaError_t* err) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::call_once(g_scratch_once[dev], [dev]() {
+    void* p = nullptr;
+    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    g_scratch_ptr[dev] = g_scratch_err[dev] == cudaSuccess ? p : nullptr;
+  });
+  *err = g_scratch_err[dev];
+  return g_scratch_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" sa2_status sa2_build_mask_noalloc(const sa2_shape* shape, const void* q, const void* k, float topk,
+                                             float topp, const sa2_blockmask* out, void* stream) {
+  if (!shape || !q || !k || !out || !out->row_cnt || !out->row_idx || !out->col_cnt || !out->col_idx || !out->mask)
+    return SA2_ERR_INVALID_ARG;
+  const sa2_shape& x = *shape;
+  if (x.B < 1 || x.H < 1 || x.N < 1 || x.reserved != 0) return SA2_ERR_INVALID_ARG;
+  if (x.dtype != SA2_BF16 && x.dtype != SA2_FP32) return SA2_ERR_UNSUPPORTED;
+  if (x.d != 64 && x.d != 128) return SA2_ERR_UNSUPPORTED;
+  if ((x.bq != 64 && x.bq != 128) || x.bk != 64) return SA2_ERR_UNSUPPORTED;
+  const int64_t esz = x.dtype == SA2_BF16 ? 2 : 4;
+  if (x.stride_n < x.d || x.stride_h < 1 || x.stride_b < 1) return SA2_ERR_INVALID_ARG;
+  if ((x.stride_n * esz) % 16 || (x.stride_h * esz) % 16 || (x.stride_b * esz) % 16) return SA2_ERR_ALIGNMENT;
+  if (!std::isfinite(topk) || !std::isfinite(topp) || topk < 0.f || topk > 1.f || topp < 0.f || topp > 1.f)
+    return SA2_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(out->row_cnt) || !aligned16(out->row_idx) ||
+      !aligned16(out->col_cnt) || !aligned16(out->col_idx) || !aligned16(out->mask) ||
+      (out->pooled_p && !aligned16(out->pooled_p)))
+    return SA2_ERR_ALIGNMENT;
+
+  ShapeArgs s;
+  s.B = x.B;
+  s.H = x.H;
+  s.N = x.N;
+  s.d = x.d;
+  s.bq = x.bq;
+  s.bk = x.bk;
+  s.Tq = (x.N + x.bq - 1) / x.bq;
+  s.Tk = (x.N + x.bk - 1) / x.bk;
+  s.dtype = x.dtype;
+  s.sb = x.stride_b;
+  s.sh = x.stride_h;
+  s.sn = x.stride_n;
+  if (s.Tk > 7680 || score_rows_per_cta(s.Tk, s.d) == 0) return SA2_ERR_UNSUPPORTED;
+
+  // pooled queries [B*H, d, Tq] then pooled keys [B*H, d, Tk], fp32, each 256-aligned
+  const size_t qbar_bytes = (sizeof(float) * (size_t)s.B * s.H * s.d * s.Tq + 255) / 256 * 256;
+  const size_t kbar_bytes = sizeof(float) * (size_t)s.B * s.H * s.d * s.Tk;
+  if (qbar_bytes + kbar_bytes > (size_t)SA2_NOALLOC_SCRATCH_BYTES) return SA2_ERR_WORKSPACE;
+
+  cudaError_t err = cudaSuccess;
+  unsigned char* scratch = static_cast<unsigned char*>(scratch_for_current_device(&err));
+  if (!scratch) return SA2_ERR_CUDA;
+
+  SelectArgs sel;
+  const double Kd = std::ceil((double)topk * s.Tk - 1e-9);
+  sel.K = (int)std::fmin(std::fmax(Kd, 0.0), (double)s.Tk);
+  if (topp <= 0.f) {
+    sel.p_mode = 1;
+    sel.p_fix = 0;
+  } else if (topp >= 1.f) {
+    sel.p_mode = 2;
+    sel.p_fix = 0;
+  } else {
+    sel.p_mode = 0;
+    sel.p_fix = (unsigned long long)std::ldexp((double)topp, 60);
+  }
+  sel.inv_sqrt_d = (float)(1.0 / std::sqrt((double)s.d));
+  MaskOut mo;
+  mo.row_cnt = out->row_cnt;
+  mo.row_idx = out->row_idx;
+  mo.col_cnt = out->col_cnt;
+  mo.col_idx = out->col_idx;
+  mo.mask = out->mask;
+  mo.pooled_p = out->pooled_p;
+  // The pooling kernel writes every pooled element the scoring kernel reads, so nothing in
+  // the scratch has to start at zero.
+  err = launch_build_mask(s, q, k, sel, reinterpret_cast<float*>(scratch),
+                          reinterpret_cast<float*>(scratch + qbar_bytes), mo, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SA2_OK : SA2_ERR_CUDA;
+}

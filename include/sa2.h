@@ -118,6 +118,30 @@ sa2_status sa2_build_mask(const sa2_shape* shape, const void* q, const void* k, 
                           const sa2_blockmask* out, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * sa2_build_mask_noalloc -- sa2_build_mask for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point; it exists for callers that are not
+ * allowed to call cudaMalloc or hand the library a workspace: code running under another
+ * runtime's memory pool or a non-re-entrant custom allocator, plugins that only receive
+ * tensors, and paths where an allocation would synchronize the device.
+ *
+ * Same computation and outputs as sa2_build_mask, except that the builder's scratch (the
+ * fp32 pooled queries and keys, B*H*d*(Tq+Tk) floats) lives in a static device array of
+ * SA2_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the library
+ * holds until the process exits.  Nothing is allocated: no cudaMalloc, no cudaFree.
+ *   - out->mask is required here (the u8 mask is built in place of the workspace copy).
+ *   - A shape whose scratch exceeds SA2_NOALLOC_SCRATCH_BYTES is rejected with
+ *     SA2_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address on that device (the
+ *     device must be current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.  Calls whose
+ *     kernels overlap on the GPU (different streams, no ordering between them) race on it:
+ *     order them on one stream or with events.
+ */
+#define SA2_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+sa2_status sa2_build_mask_noalloc(const sa2_shape* shape, const void* q, const void* k, float topk, float topp,
+                                  const sa2_blockmask* out, void* stream);
+
+/*
  * Bytes of device workspace sa2_attn_fwd needs: an fp16 copy of v, plus fp16 copies of q
  * and k for SA2_FP32 inputs.
  */
