@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-qblocks", type=int, default=4, help="query blocks of the oracle sample")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="heads of the workload (default: all); a smaller case for profiler captures")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -78,6 +80,19 @@ def cpu_threads() -> int:
         if os.environ.get(var, "").isdigit():
             return int(os.environ[var])
     return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------- ranks and timing
+
+def reduce_max_over_ranks(value: float, device) -> float:
+    """The slowest rank's time: every rank contributes its own and gets the maximum back
+    (a reduction of one scalar for timing only; the data path has no collective)."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 
 # ----------------------------------------------------------------------- kept work
@@ -193,6 +208,9 @@ def run_native(a, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     cfg = CONFIGS[a.config]
+    if a.heads:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, H=a.heads)
     topk, topp = calibration(a.config, a.sparsity)
     x = make_inputs(cfg, threads=os.cpu_count() or 8)
 
@@ -256,11 +274,7 @@ def run_native(a, rank, world):
     sa2.profiler_enable(False)
     prof = sa2.profiler_collect()
     sa2.check_device()
-    ms = ev0.elapsed_time(ev1)
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = reduce_max_over_ranks(ev0.elapsed_time(ev1), dev)
     clk = clocks.stop() if rank == 0 else None
 
     # ---- end to end through the public API with host buffers
@@ -282,10 +296,7 @@ def run_native(a, rank, world):
             hout[n].copy_(src_t, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_ms = float(te.item()) / e2e_steps
+    e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1), dev) / e2e_steps
     sa2.check_device()
 
     if rank != 0:
