@@ -35,8 +35,8 @@ from workload import CONFIGS, make_inputs  # noqa: E402
 
 FWD_FLOPS, BWD_FLOPS = 4, 10  # per kept (query, key) pair and channel
 
-# DRAM bytes of one attn_bwd launch from an ncu capture (profiles/attn_bwd_ncu.md); null
-# once the kernel source differs from the one measured.
+# DRAM bytes of one attn_bwd_dkdv launch from an ncu capture (profiles/); null until the
+# current kernel has been captured.
 BWD_TRAFFIC = None
 
 
@@ -306,13 +306,15 @@ def run_native(a, rank, world):
     kernels = {n: {"launches": c, "ms_per_launch": (m / c if c else 0.0), "total_ms": m} for n, (c, m) in prof.items()}
     launches = sum(c for c, _ in prof.values())
     dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
-    algo = {"attn_bwd": BWD_FLOPS * D * pairs, "attn_fwd": FWD_FLOPS * D * pairs}
+    # algorithmic flops of each attention kernel over kept tiles: the forward's 2 GEMMs, the
+    # dK/dV kernel's 4 (S, dP, dV^T, dK^T), the dQ kernel's 3 (S, dP, dQ)
+    algo = {"attn_fwd": FWD_FLOPS * D * pairs, "attn_bwd_dkdv": 8 * D * pairs, "attn_bwd_dq": 6 * D * pairs}
     c, m = prof[dom]
     if dom in algo and c > 0 and m > 0:
         achieved = algo[dom] / ((m / c) * 1e-3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": BWD_TRAFFIC if dom == "attn_bwd" else None,
+                "frac": achieved / peak, "traffic": BWD_TRAFFIC if dom == "attn_bwd_dkdv" else None,
                 "peak_source": f"{peaks['source']} bf16 dense, sustained (fp16 MMAs: same nominal rate)",
                 "algorithmic_flops_per_launch": algo[dom]}
     else:
@@ -324,7 +326,7 @@ def run_native(a, rank, world):
     mask_ms = sum(prof[k][1] for k in ("pool", "score_select", "csc")) / a.steps
     mask_gbs = (qk_bytes + out_bytes) / (mask_ms * 1e-3) / 1e9 if mask_ms > 0 else None
     fwd_ms = (prof["attn_fwd"][1]) / a.steps
-    bwd_ms = prof["attn_bwd"][1] / a.steps
+    bwd_ms = (prof["attn_bwd_dkdv"][1] + prof["attn_bwd_dq"][1]) / a.steps
     line = {
         "metric": "block-sparse attn fwd+bwd TFLOPS over kept tiles (whole hot path: mask + fwd + bwd) at 95% sparsity",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,

@@ -1,10 +1,10 @@
-// Block-sparse attention backward on sm_103a (tcgen05 + TMEM + TMA).
+// Block-sparse attention backward, dK / dV part, on sm_103a (tcgen05 + TMEM + TMA).
 //
 // The abstract of SpargeAttention2 (arXiv 2602.13515), contribution (ii), calls the sparse
 // attention trainable; the pages do not spell out its backward, so this is the gradient of
 // the forward with the block mask held fixed:
 //   P = exp(s - LSE), dV = P^T dO, dP = dO V^T, dS = P * (dP - D), D = rowsum(dO * O),
-//   dQ = scale dS K, dK = scale dS^T Q,
+//   dK = scale dS^T Q   (dQ = scale dS K is the job of attn_bwd_dq.cu),
 // computed over kept tiles only (gist.science explainer, section 2.C: skipped tiles cost
 // nothing).
 //
@@ -14,24 +14,21 @@
 //   dP  = dO_i V_j^T     M = 128, N = 64, K = d                      (A, B K-major)
 //   dV^T += dO_i^T P     M = d, N = 64, K = 128 query rows           (A, B MN-major)
 //   dK^T += Q_i^T dS     M = d, N = 64, K = 128                      (A, B MN-major)
-//   dQ_i  = dS K_j       M = 128, N = d, K = 64                      (A K-major, B MN-major)
-// dV^T and dK^T accumulate in TMEM across the whole list; each dQ_i tile is added to an
-// fp32 accumulator in global memory with vector atomics.
+// dV^T and dK^T accumulate in TMEM across the whole list and are written once at the end,
+// so the kernel needs no cross-CTA reduction.
 //
 // Roles (192 threads, 1 CTA per SM): warp 0 TMA producer (K_j, V_j once; Q_i, dO_i per list
 // entry into 2 stages), warp 1 TMEM owner and MMA issuer, warps 2..5 one query row per
-// thread: P and dS from S, dP, LSE and D, written as bf16 into swizzled shared tiles; then
-// the dQ tile out of TMEM into the atomics; finally dK, dV out of TMEM (one channel per
-// thread).
+// thread: P and dS from S, dP, LSE and D (prefetched one list entry ahead), written as fp16
+// into 128-byte-swizzled shared tiles; finally dK, dV out of TMEM (one channel per thread).
 //
 // All operands are fp16: the call's Q, K, V, dO arrive as fp16 copies (exact for bf16
-// inputs within the fp16 range) and P, dS are written as fp16.  P lies in [0, 1] and every
-// row of dS sums to zero, so dV and above all dQ = dS K cancel; fp16 keeps 11 significant
+// inputs within the fp16 range) and P, dS are written as fp16, which keeps 11 significant
 // bits of P and dS against bf16's 8.
 //
 // The tiles are always 128 channels wide: for d = 64 the second channel panel is read past
-// the end of the tensor map and arrives as zeros, and the extra rows / columns of the
-// results are not stored.
+// the end of the tensor map and arrives as zeros, and the extra rows of the results are not
+// stored.
 #include "sa2_internal.h"
 
 namespace sa2 {
@@ -42,9 +39,8 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM columns
 constexpr uint32_t kColS = 0;     // 2 x 64
 constexpr uint32_t kColDP = 128;  // 2 x 64
-constexpr uint32_t kColDQ = 256;  // 128
-constexpr uint32_t kColDV = 384;  // 64 (lanes = channels)
-constexpr uint32_t kColDK = 448;  // 64
+constexpr uint32_t kColDV = 256;  // 64 (lanes = channels)
+constexpr uint32_t kColDK = 320;  // 64
 
 // shared memory (bytes from the 1024-aligned base)
 constexpr int kOffK = 0;                  // 64 rows x 2 panels of 128 B = 16 KB
@@ -83,7 +79,7 @@ __device__ __forceinline__ void store_elem<__nv_bfloat16>(__nv_bfloat16* p, floa
 
 template <typename GT>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo, ShapeArgs s,
                     BwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -95,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_empty = [&](int st) { return smem_u32(&bars[3 + st]); };
   auto bar_sfull = [&](int b) { return smem_u32(&bars[5 + b]); };
   const uint32_t bar_pready = smem_u32(&bars[7]);
-  const uint32_t bar_dqfull = smem_u32(&bars[8]);
+  const uint32_t bar_pdsfree = smem_u32(&bars[8]);  // the MMAs that read P / dS have completed
   const uint32_t bar_drain = smem_u32(&bars[9]);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 192);
@@ -122,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_sfull(st), 1);
     }
     mbar_init(bar_pready, 128);
-    mbar_init(bar_dqfull, 1);
+    mbar_init(bar_pdsfree, 1);
     mbar_init(bar_drain, 1);
     fence_barrier_init();
   }
@@ -169,7 +165,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && nq > 0) {
       constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
       constexpr uint32_t idT = idesc_f16_f32(128, 64, true, true);
-      constexpr uint32_t idQ = idesc_f16_f32(128, 128, false, true);
       bool ok = mbar_wait(bar_kv, 0, abort_flag);
       for (int t = 0; ok && t <= nq; ++t) {
         if (t < nq) {
@@ -212,15 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = smem_desc(sbase + kOffDS + kk * 2048, 1024, 1024);
             umma_ss(tmem + kColDK, adesc, bdesc, idT, (u > 0 || kk > 0) ? 1u : 0u);
           }
-          // dQ_i = dS K: K = 64 keys in steps of 16; K_j as the MN-major B operand
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = smem_desc(sbase + kOffDS + kk * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc(sbase + kOffK + kk * 2048, 8192, 1024);
-            umma_ss(tmem + kColDQ, adesc, bdesc, idQ, kk > 0);
-          }
           umma_commit(bar_empty(st));
-          umma_commit(bar_dqfull);
+          umma_commit(bar_pdsfree);
         }
       }
       umma_commit(bar_drain);
@@ -232,86 +220,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = 32 * sub + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * sub) << 16);
     const float lse_scale = 1.4426950408889634f;
+    // LSE and D of this thread's row for list entry t are loaded one entry ahead, and the
+    // query block of entry t two entries ahead, so no dependent global load sits on the path
+    // from one tile to the next
+    auto row_stats = [&](int t, int qi, float& lse2, float& Dr, bool& valid) {
+      qi = (qi < 0 || qi >= s.Tq) ? 0 : qi;
+      const int64_t tok = (int64_t)qi * s.bq + r;
+      valid = t < nq && r < s.bq && tok < s.N;
+      lse2 = valid ? a.lse[(int64_t)bh * s.N + tok] * lse_scale : 0.f;
+      Dr = valid ? a.Dvec[(int64_t)bh * s.N + tok] : 0.f;
+    };
+    float n_lse2, n_D;
+    bool n_valid;
+    row_stats(0, nq > 0 ? list[0] : 0, n_lse2, n_D, n_valid);
+    int qi_ahead = nq > 1 ? list[1] : 0;
     bool ok = true;
-    int prev_tok = -1;  // token of this thread's row in the previous tile (-1: not stored)
-    for (int t = 0; t <= nq && ok; ++t) {
+    for (int t = 0; t < nq; ++t) {
+      const float lse2 = n_lse2, Dr = n_D;
+      const bool row_valid = n_valid;
+      const int qi_next = qi_ahead;
+      qi_ahead = t + 2 < nq ? list[t + 2] : 0;
+      row_stats(t + 1, qi_next, n_lse2, n_D, n_valid);
       uint4 pk[8], dk[8];
-      int tok_valid = -1;
-      if (t < nq) {
-        const int st = t & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(st), (t >> 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        int qi = list[t];
-        qi = (qi < 0 || qi >= s.Tq) ? 0 : qi;
-        const int64_t tok = (int64_t)qi * s.bq + r;
-        const bool row_valid = r < s.bq && tok < s.N;
-        const float lse2 = row_valid ? a.lse[(int64_t)bh * s.N + tok] * lse_scale : 0.f;
-        const float Dr = row_valid ? a.Dvec[(int64_t)bh * s.N + tok] : 0.f;
-        tok_valid = row_valid ? (int)tok : -1;
+      const int st = t & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(st), (t >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(trow + kColS + st * 64 + half * 32, sv);
-          tmem_ld32(trow + kColDP + st * 64 + half * 32, dv);
-          tmem_ld_wait(sv);
-          tmem_ld_wait(dv);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(trow + kColS + st * 64 + half * 32, sv);
+        tmem_ld32(trow + kColDP + st * 64 + half * 32, dv);
+        tmem_ld_wait(sv);
+        tmem_ld_wait(dv);
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            uint32_t pw[4], dw[4];
+        for (int c8 = 0; c8 < 4; ++c8) {
+          uint32_t pw[4], dw[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float pv[2], ds[2];
+          for (int e = 0; e < 4; ++e) {
+            float pv[2], ds[2];
 #pragma unroll
-              for (int z = 0; z < 2; ++z) {
-                const int c = c8 * 8 + e * 2 + z;
-                const bool cv = row_valid && (half * 32 + c) < kv_valid;
-                const float p = cv ? ex2(__uint_as_float(sv[c]) * a.scale_log2 - lse2) : 0.f;
-                pv[z] = p;
-                ds[z] = p * (__uint_as_float(dv[c]) - Dr);
-              }
-              pw[e] = pack_f16x2(pv[0], pv[1]);
-              dw[e] = pack_f16x2(ds[0], ds[1]);
+            for (int z = 0; z < 2; ++z) {
+              const int c = c8 * 8 + e * 2 + z;
+              const bool cv = row_valid && (half * 32 + c) < kv_valid;
+              const float p = cv ? ex2(__uint_as_float(sv[c]) * a.scale_log2 - lse2) : 0.f;
+              pv[z] = p;
+              ds[z] = p * (__uint_as_float(dv[c]) - Dr);
             }
-            pk[half * 4 + c8] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            dk[half * 4 + c8] = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+            pw[e] = pack_f16x2(pv[0], pv[1]);
+            dw[e] = pack_f16x2(ds[0], ds[1]);
           }
+          pk[half * 4 + c8] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          dk[half * 4 + c8] = make_uint4(dw[0], dw[1], dw[2], dw[3]);
         }
       }
-      if (t >= 1) {
-        // dQ of the previous tile: out of TMEM, scaled, added to the fp32 accumulator
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_dqfull, (t - 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        float* dst = a.dq_acc + ((int64_t)bh * s.N + (prev_tok < 0 ? 0 : prev_tok)) * s.d;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(trow + kColDQ + c0, o);
-          tmem_ld_wait(o);
-          if (prev_tok >= 0 && c0 < s.d) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              atomicAdd(reinterpret_cast<float4*>(dst + c0 + c),
-                        make_float4(__uint_as_float(o[c]) * a.scale, __uint_as_float(o[c + 1]) * a.scale,
-                                    __uint_as_float(o[c + 2]) * a.scale, __uint_as_float(o[c + 3]) * a.scale));
-          }
-        }
+      // the MMAs that read the previous P / dS tiles must have completed
+      if (t >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_pdsfree, (t - 1) & 1, abort_flag))) {
+        ok = false;
+        break;
       }
-      if (t < nq) {
-        // every MMA that read the previous P / dS tiles has completed (dq_full above)
-        st_swizzled_row(smem + kOffP, r, pk);
-        st_swizzled_row(smem + kOffDS, r, dk);
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(bar_pready);
-        prev_tok = tok_valid;
-      }
+      st_swizzled_row(smem + kOffP, r, pk);
+      st_swizzled_row(smem + kOffDS, r, dk);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_pready);
     }
+    if (ok && nq > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_pdsfree, (nq - 1) & 1, abort_flag));
     // ---- dK, dV of this key block: thread = channel (TMEM lane), columns = keys
     const int c = r;
     GT* dkp = reinterpret_cast<GT*>(a.dk) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + c;
@@ -323,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_elem<GT>(dvp + (int64_t)(kj * 64 + kv) * a.g_sn, 0.f);
         }
     } else if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint32_t kvv[32], vvv[32];
@@ -355,11 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <typename GT>
 cudaError_t launch_bwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  auto kern = attn_bwd_dkdv_kernel<GT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)s.B * s.H * s.Tk;
   prof_start(st, kAttnBwd);
-  attn_bwd_kernel<GT><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, s, a);
+  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, s, a);
   prof_stop(st, kAttnBwd);
   return cudaGetLastError();
 }

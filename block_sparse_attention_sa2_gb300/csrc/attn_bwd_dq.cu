@@ -1,0 +1,312 @@
+// Block-sparse attention backward, dQ part, on sm_103a (tcgen05 + TMEM + TMA).
+//
+// dQ = scale * dS K with dS = P * (dP - D), P = exp(s - LSE), dP = dO V^T: the gradient of
+// the block-sparse forward with respect to Q (the abstract of SpargeAttention2, arXiv
+// 2602.13515, contribution (ii): trainable sparse attention; gist.science explainer,
+// section 2.C: whole tiles kept or skipped).  Each CTA owns one query block of 128 rows and
+// walks that block's list of kept key blocks -- the forward's traversal -- so dQ
+// accumulates in TMEM over the whole list and is written once: no cross-CTA reduction.
+//
+// Roles (320 threads, 1 CTA per SM): warp 0 TMA (Q and dO once, K_j / V_j per kept block
+// into 2 stages), warp 1 TMEM owner and MMA issuer, and two row warpgroups (warps 2..5 and
+// 6..9) that take the list entries in turn (entry j -> group j % 2, TMEM buffer j % 2), one
+// query row per thread, so that one group's exp / dS work overlaps the other's.
+// Per kept key block j:
+//   S_j  = Q K_j^T     M = 128, N = 64, K = d     (A, B K-major, fp16)
+//   dP_j = dO V_j^T    M = 128, N = 64, K = d     (A, B K-major, fp16)
+//   row threads: P = exp2(S * scale*log2e - LSE*log2e), dS = P (dP - D), dS as fp16 pairs
+//                written over S_j in TMEM
+//   dQ  += dS_j K_j    M = 128, N = d, K = 64     (A = dS from TMEM, B = K_j MN-major)
+// TMEM columns: S at 0 / 64, dP at 128 / 192 (double-buffered), dQ at 256 (d columns).
+#include "sa2_internal.h"
+
+namespace sa2 {
+namespace {
+
+constexpr int kThreads = 320;
+// K_j feeds S_j and, after the softmax, dQ += dS_j K_j, so its ring is deep; V_j only feeds
+// dP_j and is released right after it
+constexpr int kKStages = 4;
+constexpr int kVStages = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+
+template <int D>
+struct DqSmem {
+  static constexpr int kPanels = D / 64;
+  static constexpr int kQBytes = 128 * 128 * kPanels;  // 128 rows x 128 B per panel
+  static constexpr int kKVBytes = 64 * 128 * kPanels;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kOffQ + kQBytes;
+  static constexpr int kOffK = kOffDO + kQBytes;
+  static constexpr int kOffV = kOffK + kKStages * kKVBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
+  static constexpr int kBytes = kOffBar + 256 + 1024;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store_chunk(OutT* dst, const float* v);
+template <>
+__device__ __forceinline__ void store_chunk<__nv_bfloat16>(__nv_bfloat16* dst, const float* v) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    p[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+}
+template <>
+__device__ __forceinline__ void store_chunk<float>(float* dst, const float* v) {
+  float4* p = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+template <int D, typename OutT>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                       const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo, ShapeArgs s,
+                       DqArgs a) {
+  using L = DqSmem<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  const uint32_t bar_q = smem_u32(&bars[0]);
+  auto bar_kfull = [&](int st) { return smem_u32(&bars[1 + st]); };
+  auto bar_kempty = [&](int st) { return smem_u32(&bars[5 + st]); };
+  auto bar_vfull = [&](int st) { return smem_u32(&bars[9 + st]); };
+  auto bar_vempty = [&](int st) { return smem_u32(&bars[11 + st]); };
+  auto bar_sfull = [&](int b) { return smem_u32(&bars[13 + b]); };
+  auto bar_pfull = [&](int b) { return smem_u32(&bars[15 + b]); };
+  const uint32_t bar_dq = smem_u32(&bars[17]);
+  const uint32_t bar_drain = smem_u32(&bars[18]);
+  // 19 barriers occupy the first 152 bytes of the 256-byte barrier area
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 224);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffBar + 240);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x / s.Tq;
+  const int qi = blockIdx.x % s.Tq;
+  const int b = bh / s.H, h = bh % s.H;
+  const int64_t rowid = (int64_t)bh * s.Tq + qi;
+  int nkv = a.row_cnt[rowid];
+  if (nkv < 0 || nkv > s.Tk) {
+    if (tid == 0) report_error(a.status, kDevErrBounds);
+    nkv = nkv < 0 ? 0 : s.Tk;
+  }
+  const int32_t* list = a.row_idx + rowid * s.Tk;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bar_q, 1);
+    for (int st = 0; st < kKStages; ++st) {
+      mbar_init(bar_kfull(st), 1);
+      mbar_init(bar_kempty(st), 1);
+    }
+    for (int st = 0; st < kVStages; ++st) {
+      mbar_init(bar_vfull(st), 1);
+      mbar_init(bar_vempty(st), 1);
+    }
+    for (int bb = 0; bb < 2; ++bb) {
+      mbar_init(bar_sfull(bb), 1);
+      mbar_init(bar_pfull(bb), 128);
+    }
+    mbar_init(bar_dq, 1);
+    mbar_init(bar_drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && nkv > 0) {
+      tma_prefetch_map(&mk);
+      tma_prefetch_map(&mv);
+      mbar_arrive_expect_tx(bar_q, 2 * L::kQBytes);
+      for (int p = 0; p < L::kPanels; ++p) {
+        tma_load_4d(sbase + L::kOffQ + p * 16384, &mq, bar_q, p * 64, qi * s.bq, h, b);
+        tma_load_4d(sbase + L::kOffDO + p * 16384, &mdo, bar_q, p * 64, qi * s.bq, h, b);
+      }
+      for (int j = 0; j < nkv; ++j) {
+        const int ks = j % kKStages, vs = j % kVStages;
+        int kb = list[j];
+        if (kb < 0 || kb >= s.Tk) {
+          report_error(a.status, kDevErrBounds);
+          kb = 0;
+        }
+        if (j >= kKStages && !mbar_wait(bar_kempty(ks), ((j / kKStages) - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(bar_kfull(ks), L::kKVBytes);
+        for (int p = 0; p < L::kPanels; ++p)
+          tma_load_4d(sbase + L::kOffK + ks * L::kKVBytes + p * 8192, &mk, bar_kfull(ks), p * 64, kb * 64, h, b);
+        if (j >= kVStages && !mbar_wait(bar_vempty(vs), ((j / kVStages) - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(bar_vfull(vs), L::kKVBytes);
+        for (int p = 0; p < L::kPanels; ++p)
+          tma_load_4d(sbase + L::kOffV + vs * L::kKVBytes + p * 8192, &mv, bar_vfull(vs), p * 64, kb * 64, h, b);
+      }
+      const int kfirst = nkv > kKStages ? nkv - kKStages : 0;
+      for (int j = kfirst; j < nkv; ++j) mbar_wait(bar_kfull(j % kKStages), (j / kKStages) & 1, abort_flag);
+      const int vfirst = nkv > kVStages ? nkv - kVStages : 0;
+      for (int j = vfirst; j < nkv; ++j) mbar_wait(bar_vfull(j % kVStages), (j / kVStages) & 1, abort_flag);
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------------- MMA issuer
+    if (lane == 0 && nkv > 0) {
+      constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
+      constexpr uint32_t idQ = idesc_f16_f32(128, D, false, true);
+      bool ok = mbar_wait(bar_q, 0, abort_flag);
+      for (int j = 0; ok && j <= nkv; ++j) {
+        if (j < nkv) {
+          const int ks = j % kKStages, vs = j % kVStages, bb = j & 1;
+          if (!mbar_wait(bar_kfull(ks), (j / kKStages) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t kbase = sbase + L::kOffK + ks * L::kKVBytes;
+          const uint32_t vbase = sbase + L::kOffV + vs * L::kKVBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColS + bb * 64, smem_desc(sbase + L::kOffQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
+                    smem_desc(kbase + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024), idS, kk > 0);
+          if (!mbar_wait(bar_vfull(vs), (j / kVStages) & 1, abort_flag)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColDP + bb * 64, smem_desc(sbase + L::kOffDO + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
+                    smem_desc(vbase + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024), idS, kk > 0);
+          umma_commit(bar_sfull(bb));
+          umma_commit(bar_vempty(vs));
+        }
+        if (j >= 1) {
+          const int jj = j - 1, ks = jj % kKStages, bb = jj & 1;
+          if (!mbar_wait(bar_pfull(bb), (jj >> 1) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t kbase = sbase + L::kOffK + ks * L::kKVBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_ts(tmem + kColDQ, tmem + kColS + bb * 64 + kk * 8, smem_desc(kbase + kk * 2048, 8192, 1024), idQ,
+                    (jj > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar_kempty(ks));
+        }
+      }
+      umma_commit(bar_dq);
+      umma_commit(bar_drain);
+      mbar_wait(bar_drain, 0, abort_flag);
+    }
+  } else {
+    // -------------------------------------------------------------- query-row threads
+    const int wg = (warp - 2) >> 2;  // row warpgroup 0 or 1
+    const int sub = warp & 3;
+    const int r = 32 * sub + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * sub) << 16);
+    const int64_t tok = (int64_t)qi * s.bq + r;
+    const bool row_valid = r < s.bq && tok < s.N;
+    const float lse2 = row_valid ? a.lse[(int64_t)bh * s.N + tok] * 1.4426950408889634f : 0.f;
+    const float Dr = row_valid ? a.Dvec[(int64_t)bh * s.N + tok] : 0.f;
+    bool ok = true;
+    const int bb = wg;  // this group's TMEM buffer
+    int next_kb = wg < nkv ? list[wg] : 0;
+    for (int j = wg; j < nkv; j += 2) {
+      int kb = next_kb;
+      if (j + 2 < nkv) next_kb = list[j + 2];
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bb), (j >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      kb = (kb < 0 || kb >= s.Tk) ? 0 : kb;
+      const int kv_valid = min(64, s.N - kb * 64);
+      uint32_t pk[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(trow + kColS + bb * 64 + half * 32, sv);
+        tmem_ld32(trow + kColDP + bb * 64 + half * 32, dv);
+        tmem_ld_wait(sv);
+        tmem_ld_wait(dv);
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float ds[2];
+#pragma unroll
+          for (int z = 0; z < 2; ++z) {
+            const bool cv = row_valid && (half * 32 + c + z) < kv_valid;
+            const float p = cv ? ex2(__uint_as_float(sv[c + z]) * a.scale_log2 - lse2) : 0.f;
+            ds[z] = p * (__uint_as_float(dv[c + z]) - Dr);
+          }
+          pk[half * 16 + c / 2] = pack_f16x2(ds[0], ds[1]);
+        }
+      }
+      tmem_st32(trow + kColS + bb * 64, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_pfull(bb));
+    }
+    // ---- epilogue: dQ = scale * (dS K) accumulated over the list; each group stores half
+    // of the channels of every row
+    OutT* dqrow = reinterpret_cast<OutT*>(a.dq) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + tok * a.g_sn;
+    const int c_begin = wg * (D / 2), c_end = c_begin + D / 2;
+    if (nkv == 0) {
+      if (row_valid) {
+        float z[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) z[c] = 0.f;
+        for (int c0 = c_begin; c0 < c_end; c0 += 32) store_chunk<OutT>(dqrow + c0, z);
+      }
+    } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar_dq, 0, abort_flag))) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c0 = c_begin; c0 < c_end; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(trow + kColDQ + c0, o);
+        tmem_ld_wait(o);
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(o[c]) * a.scale;
+        if (row_valid) store_chunk<OutT>(dqrow + c0, v);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) report_error(a.status, kDevErrTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, typename OutT>
+cudaError_t launch_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                     const CUtensorMap& mdo, const DqArgs& a, cudaStream_t st) {
+  const int smem = DqSmem<D>::kBytes;
+  auto kern = attn_bwd_dq_kernel<D, OutT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  prof_start(st, kAttnBwdDq);
+  kern<<<(unsigned)((long long)s.B * s.H * s.Tq), kThreads, smem, st>>>(mq, mk, mv, mdo, s, a);
+  prof_stop(st, kAttnBwdDq);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_dq(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk,
+                               const CUtensorMap& mv, const CUtensorMap& mdo, const DqArgs& a, cudaStream_t st) {
+  if (s.d == 128)
+    return s.dtype == 0 ? launch_t<128, __nv_bfloat16>(s, mq, mk, mv, mdo, a, st)
+                        : launch_t<128, float>(s, mq, mk, mv, mdo, a, st);
+  return s.dtype == 0 ? launch_t<64, __nv_bfloat16>(s, mq, mk, mv, mdo, a, st)
+                      : launch_t<64, float>(s, mq, mk, mv, mdo, a, st);
+}
+
+}  // namespace sa2

@@ -102,13 +102,12 @@ __device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16* p) 
 template <>
 __device__ __forceinline__ float ld_elem<__half>(const __half* p) { return __half2float(*p); }
 
-// One warp per token row: D = sum_c dO[c] * (O[c] + O_lo[c]) (fp32), and the row of the
-// fp32 dQ accumulator set to zero.  O has the call's dtype and strides; dO is the
-// contiguous fp16 copy the MMAs read, so that D matches the dO of dP = dO V^T.
-template <typename TO, typename TD>
+// One warp per token row: D = sum_c dO[c] * (O[c] + O_lo[c]) (fp32).  O has the call's
+// dtype and strides; dO is the contiguous fp16 copy the MMAs read, so that D matches the dO
+// of dP = dO V^T.
+template <typename TO>
 __global__ void bwd_preprocess_kernel(const TO* __restrict__ o, const __nv_bfloat16* __restrict__ o_lo,
-                                      const TD* __restrict__ dO, ShapeArgs s, int64_t d_sb, int64_t d_sh,
-                                      int64_t d_sn, float* __restrict__ Dvec, float* __restrict__ dq_acc) {
+                                      const __half* __restrict__ dO, ShapeArgs s, float* __restrict__ Dvec) {
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)s.B * s.H * s.N;
   for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; row < rows;
@@ -117,70 +116,30 @@ __global__ void bwd_preprocess_kernel(const TO* __restrict__ o, const __nv_bfloa
     const int64_t bh = row / s.N;
     const int h = (int)(bh % s.H), b = (int)(bh / s.H);
     const int64_t off = b * s.sb + h * s.sh + (int64_t)n * s.sn;
-    const int64_t doff = b * d_sb + h * d_sh + (int64_t)n * d_sn;
+    const __half* drow = dO + row * s.d;
     float acc = 0.f;
     for (int c = lane; c < s.d; c += 32) {
       const float ov = ld_elem<TO>(o + off + c) + (o_lo ? __bfloat162float(o_lo[off + c]) : 0.f);
-      acc += ov * ld_elem<TD>(dO + doff + c);
+      acc += ov * __half2float(drow[c]);
     }
 #pragma unroll
     for (int w = 16; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
     if (lane == 0) Dvec[row] = acc;
-    float* dq = dq_acc + row * s.d;
-    for (int c = lane; c < s.d; c += 32) dq[c] = 0.f;
   }
 }
 
 cudaError_t launch_bwd_preprocess(const ShapeArgs& s, const void* o, const void* o_lo, const __half* dO16,
-                                  float* Dvec, float* dq_acc, cudaStream_t st) {
+                                  float* Dvec, cudaStream_t st) {
   const __nv_bfloat16* lo = s.dtype == 0 ? static_cast<const __nv_bfloat16*>(o_lo) : nullptr;
   const int64_t rows = (int64_t)s.B * s.H * s.N;
   const int blocks = (int)std::min<int64_t>((rows * 32 + 255) / 256, 152 * 16);
-  const int64_t csb = (int64_t)s.H * s.N * s.d, csh = (int64_t)s.N * s.d, csn = s.d;
   prof_start(st, kBwdPre);
   if (s.dtype == 0)
-    bwd_preprocess_kernel<__nv_bfloat16, __half><<<blocks, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(o), lo, dO16, s, csb, csh, csn, Dvec, dq_acc);
+    bwd_preprocess_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o), lo, dO16,
+                                                                 s, Dvec);
   else
-    bwd_preprocess_kernel<float, __half><<<blocks, 256, 0, st>>>(static_cast<const float*>(o), nullptr, dO16, s,
-                                                                 csb, csh, csn, Dvec, dq_acc);
+    bwd_preprocess_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(o), nullptr, dO16, s, Dvec);
   prof_stop(st, kBwdPre);
-  return cudaGetLastError();
-}
-
-// fp32 dQ accumulator (contiguous) -> dq in the call's dtype and strides.
-template <typename T>
-__global__ void dq_convert_kernel(const float* __restrict__ acc, ShapeArgs s, T* __restrict__ dq) {
-  const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t e = i * 4;
-    const int c = (int)(e % s.d);
-    const int64_t t = e / s.d;
-    const int n = (int)(t % s.N);
-    const int64_t bh = t / s.N;
-    const int h = (int)(bh % s.H), b = (int)(bh / s.H);
-    const float4 v = *reinterpret_cast<const float4*>(acc + e);
-    T* p = dq + b * s.sb + h * s.sh + (int64_t)n * s.sn + c;
-    if constexpr (sizeof(T) == 4) {
-      *reinterpret_cast<float4*>(p) = v;
-    } else {
-      uint2 w;
-      w.x = pack_bf16x2(v.x, v.y);
-      w.y = pack_bf16x2(v.z, v.w);
-      *reinterpret_cast<uint2*>(p) = w;
-    }
-  }
-}
-
-cudaError_t launch_dq_convert(const ShapeArgs& s, const float* dq_acc, void* dq, cudaStream_t st) {
-  const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
-  const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 152 * 16);
-  prof_start(st, kDqConvert);
-  if (s.dtype == 0)
-    dq_convert_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(dq_acc, s, static_cast<__nv_bfloat16*>(dq));
-  else
-    dq_convert_kernel<float><<<blocks, 256, 0, st>>>(dq_acc, s, static_cast<float*>(dq));
-  prof_stop(st, kDqConvert);
   return cudaGetLastError();
 }
 

@@ -92,13 +92,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   // barrier slots
   const uint32_t bar_q = smem_u32(&bars[0]);
+  // K_j is released as soon as S_j has been computed, V_j only after P_j V_j: separate
+  // rings keep the K loads running ahead of the softmax
   auto bar_kfull = [&](int st) { return smem_u32(&bars[1 + st]); };
   auto bar_vfull = [&](int st) { return smem_u32(&bars[1 + kNumStages + st]); };
-  auto bar_empty = [&](int st) { return smem_u32(&bars[1 + 2 * kNumStages + st]); };
-  auto bar_sfull = [&](int b) { return smem_u32(&bars[1 + 3 * kNumStages + b]); };
-  auto bar_pfull = [&](int b) { return smem_u32(&bars[3 + 3 * kNumStages + b]); };
-  const uint32_t bar_odone = smem_u32(&bars[5 + 3 * kNumStages]);
-  const uint32_t bar_drain = smem_u32(&bars[6 + 3 * kNumStages]);
+  auto bar_kempty = [&](int st) { return smem_u32(&bars[1 + 2 * kNumStages + st]); };
+  auto bar_vempty = [&](int st) { return smem_u32(&bars[1 + 3 * kNumStages + st]); };
+  auto bar_sfull = [&](int b) { return smem_u32(&bars[1 + 4 * kNumStages + b]); };
+  auto bar_pfull = [&](int b) { return smem_u32(&bars[3 + 4 * kNumStages + b]); };
+  const uint32_t bar_odone = smem_u32(&bars[5 + 4 * kNumStages]);
+  const uint32_t bar_drain = smem_u32(&bars[6 + 4 * kNumStages]);
+  // 15 barriers occupy the first 120 bytes of the 256-byte barrier area
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffBar + 192);
 
@@ -120,7 +124,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int st = 0; st < kNumStages; ++st) {
       mbar_init(bar_kfull(st), 1);
       mbar_init(bar_vfull(st), 1);
-      mbar_init(bar_empty(st), 1);
+      mbar_init(bar_kempty(st), 1);
+      mbar_init(bar_vempty(st), 1);
     }
     for (int bb = 0; bb < 2; ++bb) {
       mbar_init(bar_sfull(bb), 1);
@@ -150,15 +155,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_4d(sbase + L::kOffQ + p * 16384, &mq, bar_q, p * 64, qi * s.bq, h, b);
       for (int j = 0; j < nkv; ++j) {
         const int st = j % kNumStages;
-        if (j >= kNumStages && !mbar_wait(bar_empty(st), ((j / kNumStages) - 1) & 1, abort_flag)) break;
+        const uint32_t ph = ((j / kNumStages) - 1) & 1;
         int kb = list[j];
         if (kb < 0 || kb >= s.Tk) {
           report_error(a.status, kDevErrBounds);
           kb = 0;
         }
+        if (j >= kNumStages && !mbar_wait(bar_kempty(st), ph, abort_flag)) break;
         mbar_arrive_expect_tx(bar_kfull(st), L::kKVBytes);
         for (int p = 0; p < L::kPanels; ++p)
           tma_load_4d(sbase + L::kOffK + st * L::kKVBytes + p * 8192, &mk, bar_kfull(st), p * 64, kb * 64, h, b);
+        if (j >= kNumStages && !mbar_wait(bar_vempty(st), ph, abort_flag)) break;
         mbar_arrive_expect_tx(bar_vfull(st), L::kKVBytes);
         for (int p = 0; p < L::kPanels; ++p)
           tma_load_4d(sbase + L::kOffV + st * L::kKVBytes + p * 8192, &mv, bar_vfull(st), p * 64, kb * 64, h, b);
@@ -190,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             umma_ss(tmem + (j & 1) * 64, adesc, bdesc, idS, kk > 0);
           }
           umma_commit(bar_sfull(j & 1));
+          umma_commit(bar_kempty(st));
         }
         if (j >= 1) {
           const int jj = j - 1;
@@ -204,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint64_t bdesc = smem_desc(vbase + kk * 2048, 8192, 1024);
             umma_ts(tmem + kColO, tmem + (jj & 1) * 64 + kk * 8, bdesc, idO, (jj > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(bar_empty(st));
+          umma_commit(bar_vempty(st));
           umma_commit(bar_odone);
         }
       }
@@ -221,8 +229,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = true;
     // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them is
     // decided uniformly per warp (__all_sync / __any_sync).
+    int next_kb = nkv > 0 ? list[0] : 0;  // key block of the next entry, loaded one entry ahead
     for (int j = 0; j < nkv; ++j) {
       const int bsel = j & 1;
+      int kb = next_kb;
+      if (j + 1 < nkv) next_kb = list[j + 1];
       if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bsel), (j >> 1) & 1, abort_flag))) {
         ok = false;
         break;
@@ -233,7 +244,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       tmem_ld32(trow + bsel * 64 + 32, u1);
       tmem_ld_wait(u0);
       tmem_ld_wait(u1);
-      int kb = list[j];
       kb = (kb < 0 || kb >= s.Tk) ? 0 : kb;
       const int valid = min(64, s.N - kb * 64);
       float x[64];

@@ -24,7 +24,7 @@ std::vector<Record> g_done;         // stopped, not yet collected
 std::vector<cudaEvent_t> g_pool;    // events ready for reuse
 
 const char* kNames[kNumKernelIds] = {"pool", "score_select", "csc", "to_f16", "attn_fwd",
-                                     "bwd_preprocess", "attn_bwd", "dq_convert"};
+                                     "bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq"};
 
 cudaEvent_t take_event() {
   if (!g_pool.empty()) {

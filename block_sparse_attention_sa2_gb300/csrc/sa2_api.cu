@@ -94,16 +94,15 @@ FwdWs fwd_ws(const ShapeArgs& s) {
   return w;
 }
 
-// Backward workspace: fp32 dQ accumulator, D, and fp16 copies of Q, K, V, dO.
+// Backward workspace: D and fp16 copies of Q, K, V, dO.
 struct BwdWs {
-  size_t dq, D, q16, k16, v16, do16, total;
+  size_t D, q16, k16, v16, do16, total;
 };
 BwdWs bwd_ws(const ShapeArgs& s) {
   BwdWs w{};
-  w.dq = 0;
-  w.D = align_up(sizeof(float) * token_elems(s));
+  w.D = 0;
   const size_t t = align_up(2 * token_elems(s));
-  w.q16 = align_up(w.D + sizeof(float) * (size_t)s.B * s.H * s.N);
+  w.q16 = align_up(sizeof(float) * (size_t)s.B * s.H * s.N);
   w.k16 = w.q16 + t;
   w.v16 = w.k16 + t;
   w.do16 = w.v16 + t;
@@ -252,20 +251,20 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   ShapeArgs s;
   sa2_status st = check_shape(shape, &s);
   if (st != SA2_OK) return st;
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !mask || !mask->col_cnt || !mask->col_idx)
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !mask || !mask->col_cnt || !mask->col_idx ||
+      !mask->row_cnt || !mask->row_idx)
     return SA2_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return SA2_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(o_lo) || !aligned16(lse) ||
       !aligned16(dO) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(mask->col_cnt) ||
-      !aligned16(mask->col_idx) || !aligned16(ws))
+      !aligned16(mask->col_idx) || !aligned16(mask->row_cnt) || !aligned16(mask->row_idx) || !aligned16(ws))
     return SA2_ERR_ALIGNMENT;
   const BwdWs w = bwd_ws(s);
   if (!ws || ws_bytes < w.total) return SA2_ERR_WORKSPACE;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   unsigned* status = status_ptr();
   uint8_t* wsb = static_cast<uint8_t*>(ws);
-  float* dq_acc = reinterpret_cast<float*>(wsb + w.dq);
   float* Dvec = reinterpret_cast<float*>(wsb + w.D);
   __half* c16[4] = {reinterpret_cast<__half*>(wsb + w.q16), reinterpret_cast<__half*>(wsb + w.k16),
                     reinterpret_cast<__half*>(wsb + w.v16), reinterpret_cast<__half*>(wsb + w.do16)};
@@ -273,7 +272,7 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   for (int i = 0; i < 4; ++i)
     if (launch_to_f16(src[i], s, c16[i], status, cs) != cudaSuccess) return SA2_ERR_CUDA;
   // D = rowsum(dO * O) from the same fp16 dO the MMAs read
-  if (launch_bwd_preprocess(s, o, o_lo, c16[3], Dvec, dq_acc, cs) != cudaSuccess) return SA2_ERR_CUDA;
+  if (launch_bwd_preprocess(s, o, o_lo, c16[3], Dvec, cs) != cudaSuccess) return SA2_ERR_CUDA;
   CUtensorMap mq, mk, mv, mdo;
   if (!copy_map(s, c16[0], &mq, 128) || !copy_map(s, c16[1], &mk, 64) || !copy_map(s, c16[2], &mv, 64) ||
       !copy_map(s, c16[3], &mdo, 128))
@@ -284,7 +283,6 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   a.col_idx = mask->col_idx;
   a.lse = lse;
   a.Dvec = Dvec;
-  a.dq_acc = dq_acc;
   a.dk = dk;
   a.dv = dv;
   a.g_sb = s.sb;
@@ -294,7 +292,19 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   if (launch_attn_bwd(s, mq, mk, mv, mdo, a, cs) != cudaSuccess) return SA2_ERR_CUDA;
-  return cuda_status(launch_dq_convert(s, dq_acc, dq, cs));
+  DqArgs g;
+  g.row_cnt = mask->row_cnt;
+  g.row_idx = mask->row_idx;
+  g.lse = lse;
+  g.Dvec = Dvec;
+  g.dq = dq;
+  g.g_sb = s.sb;
+  g.g_sh = s.sh;
+  g.g_sn = s.sn;
+  g.scale = scale;
+  g.scale_log2 = a.scale_log2;
+  g.status = status;
+  return cuda_status(launch_attn_bwd_dq(s, mq, mk, mv, mdo, g, cs));
 }
 
 sa2_status sa2_get_device_status(void* stream) {

@@ -14,7 +14,7 @@ namespace sa2 {
 constexpr size_t kMaxDynSmem = 227 * 1024;
 
 // Launch profiler (profiler.cu): kernel ids and the brackets every launch wrapper calls.
-enum KernelId { kPool = 0, kScoreSelect, kCsc, kToF16, kAttnFwd, kBwdPre, kAttnBwd, kDqConvert, kNumKernelIds };
+enum KernelId { kPool = 0, kScoreSelect, kCsc, kToF16, kAttnFwd, kBwdPre, kAttnBwd, kAttnBwdDq, kNumKernelIds };
 void prof_start(cudaStream_t st, int id);
 void prof_stop(cudaStream_t st, int id);
 
@@ -74,7 +74,6 @@ struct BwdArgs {
   const int32_t* col_idx;
   const float* lse;   // [B, H, N]
   const float* Dvec;  // [B, H, N] rowsum(dO * O)
-  float* dq_acc;      // [B, H, N, d] fp32, zeroed
   void* dk;
   void* dv;
   int64_t g_sb, g_sh, g_sn;  // strides of dk / dv (dtype of the call)
@@ -83,10 +82,23 @@ struct BwdArgs {
   unsigned* status;
 };
 
+struct DqArgs {
+  const int32_t* row_cnt;
+  const int32_t* row_idx;
+  const float* lse;
+  const float* Dvec;
+  void* dq;
+  int64_t g_sb, g_sh, g_sn;
+  float scale;
+  float scale_log2;
+  unsigned* status;
+};
+
 cudaError_t launch_bwd_preprocess(const ShapeArgs& s, const void* o, const void* o_lo, const __half* dO16,
-                                  float* Dvec, float* dq_acc, cudaStream_t st);
+                                  float* Dvec, cudaStream_t st);
 cudaError_t launch_attn_bwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st);
-cudaError_t launch_dq_convert(const ShapeArgs& s, const float* dq_acc, void* dq, cudaStream_t st);
+cudaError_t launch_attn_bwd_dq(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk,
+                               const CUtensorMap& mv, const CUtensorMap& mdo, const DqArgs& a, cudaStream_t st);
 
 }  // namespace sa2
