@@ -171,6 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j < nkv) {
           const int ks = j % kKStages, vs = j % kVStages, bb = j & 1;
           if (!mbar_wait(bar_kfull(ks), (j / kKStages) & 1, abort_flag)) break;
+          // S_j overwrites the TMEM buffer whose dS_{j-2} the MMA dQ += dS_{j-2} K_{j-2}
+          // read: a later tcgen05.mma is not ordered after an earlier one's TMEM operand
+          // reads, so wait for that MMA (its commit releases K_{j-2})
+          if (j >= 2 && !mbar_wait(bar_kempty((j - 2) % kKStages), ((j - 2) / kKStages) & 1, abort_flag)) break;
           tc_fence_after();
           const uint32_t kbase = sbase + L::kOffK + ks * L::kKVBytes;
           const uint32_t vbase = sbase + L::kOffV + vs * L::kKVBytes;

@@ -54,91 +54,150 @@ __device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16* p) {
 
 // Token tensor (caller dtype and strides) -> contiguous fp16 [B, H, N, d].  bf16 values
 // within the fp16 range convert exactly; a value of magnitude above 65504 is saturated and
-// reported as a range error.
+// reported as a range error.  Each thread converts 8 consecutive channels of one token; for
+// contiguous inputs the source offset is the destination offset.
 template <typename T>
-__global__ void to_f16_kernel(const T* __restrict__ src, ShapeArgs s, __half* __restrict__ dst, unsigned* status) {
-  const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
+__device__ __forceinline__ void ld8(const T* p, float* v);
+template <>
+__device__ __forceinline__ void ld8<float>(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void ld8<__nv_bfloat16>(const __nv_bfloat16* p, float* v) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(u[i] << 16);
+    v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 to_f16x8(float* v, bool& bad) {
+  const float lim = 65504.f;
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    bad |= !(fabsf(v[i]) <= lim);
+    v[i] = fminf(fmaxf(v[i], -lim), lim);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = pack_f16x2(v[2 * i], v[2 * i + 1]);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename T, bool CONTIG>
+__global__ void __launch_bounds__(256) to_f16_kernel(const T* __restrict__ src, ShapeArgs s, __half* __restrict__ dst,
+                                                     unsigned* status) {
+  const int64_t items = (int64_t)s.B * s.H * s.N * s.d / 8;
+  const int per_row = s.d / 8;
   bool bad = false;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t e = i * 4;
-    const int c = (int)(e % s.d);
-    const int64_t t = e / s.d;
-    const int n = (int)(t % s.N);
-    const int64_t bh = t / s.N;
-    const int h = (int)(bh % s.H), b = (int)(bh / s.H);
-    float4 v = ld4<T>(src + b * s.sb + h * s.sh + (int64_t)n * s.sn + c);
-    const float lim = 65504.f;
-    bad |= !(fabsf(v.x) <= lim && fabsf(v.y) <= lim && fabsf(v.z) <= lim && fabsf(v.w) <= lim);
-    v.x = fminf(fmaxf(v.x, -lim), lim);
-    v.y = fminf(fmaxf(v.y, -lim), lim);
-    v.z = fminf(fmaxf(v.z, -lim), lim);
-    v.w = fminf(fmaxf(v.w, -lim), lim);
-    uint2 w;
-    w.x = pack_f16x2(v.x, v.y);
-    w.y = pack_f16x2(v.z, v.w);
-    *reinterpret_cast<uint2*>(dst + e) = w;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < items; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = i * 8;
+    int64_t off = e;
+    if (!CONTIG) {
+      const int64_t row = i / per_row;
+      const int c = (int)(i - row * per_row) * 8;
+      const int64_t bh = row / s.N;
+      const int n = (int)(row - bh * s.N);
+      off = (bh / s.H) * s.sb + (bh % s.H) * s.sh + (int64_t)n * s.sn + c;
+    }
+    float v[8];
+    ld8<T>(src + off, v);
+    *reinterpret_cast<uint4*>(dst + e) = to_f16x8(v, bad);
   }
   if (bad) report_error(status, kDevErrRange);
 }
 
+static bool contiguous(const ShapeArgs& s) {
+  return s.sn == s.d && s.sh == (int64_t)s.N * s.d && s.sb == (int64_t)s.H * s.N * s.d;
+}
+
+static int grid_for(int64_t items) { return (int)std::min<int64_t>((items + 255) / 256, 152 * 8); }
+
 cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsigned* status, cudaStream_t st) {
-  const int64_t n4 = (int64_t)s.B * s.H * s.N * s.d / 4;
-  const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 152 * 16);
+  const int blocks = grid_for((int64_t)s.B * s.H * s.N * s.d / 8);
+  const bool c = contiguous(s);
   prof_start(st, kToF16);
-  if (s.dtype == 0)
-    to_f16_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), s, dst, status);
-  else
-    to_f16_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(src), s, dst, status);
+  if (s.dtype == 0) {
+    auto p = static_cast<const __nv_bfloat16*>(src);
+    if (c)
+      to_f16_kernel<__nv_bfloat16, true><<<blocks, 256, 0, st>>>(p, s, dst, status);
+    else
+      to_f16_kernel<__nv_bfloat16, false><<<blocks, 256, 0, st>>>(p, s, dst, status);
+  } else {
+    auto p = static_cast<const float*>(src);
+    if (c)
+      to_f16_kernel<float, true><<<blocks, 256, 0, st>>>(p, s, dst, status);
+    else
+      to_f16_kernel<float, false><<<blocks, 256, 0, st>>>(p, s, dst, status);
+  }
   prof_stop(st, kToF16);
   return cudaGetLastError();
 }
 
+// Backward preparation of dO, one pass: the contiguous fp16 copy of dO the MMAs read and
+// D = sum_c dO16[c] * (O[c] + O_lo[c]) in fp32, so that D matches the dO of dP = dO V^T.
+// Sixteen threads per token (8 channels each, d = 128) or eight (d = 64).
 template <typename T>
-__device__ __forceinline__ float ld_elem(const T* p);
-template <>
-__device__ __forceinline__ float ld_elem<float>(const float* p) { return *p; }
-template <>
-__device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-template <>
-__device__ __forceinline__ float ld_elem<__half>(const __half* p) { return __half2float(*p); }
-
-// One warp per token row: D = sum_c dO[c] * (O[c] + O_lo[c]) (fp32).  O has the call's
-// dtype and strides; dO is the contiguous fp16 copy the MMAs read, so that D matches the dO
-// of dP = dO V^T.
-template <typename TO>
-__global__ void bwd_preprocess_kernel(const TO* __restrict__ o, const __nv_bfloat16* __restrict__ o_lo,
-                                      const __half* __restrict__ dO, ShapeArgs s, float* __restrict__ Dvec) {
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(256) do_prep_kernel(const T* __restrict__ dO, const T* __restrict__ o,
+                                                      const __nv_bfloat16* __restrict__ o_lo, ShapeArgs s,
+                                                      __half* __restrict__ dO16, float* __restrict__ Dvec,
+                                                      unsigned* status) {
+  const int per_row = s.d / 8;  // threads per token: 16 or 8, a power of two within a warp
   const int64_t rows = (int64_t)s.B * s.H * s.N;
-  for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; row < rows;
-       row += (int64_t)gridDim.x * blockDim.x / 32) {
-    const int n = (int)(row % s.N);
-    const int64_t bh = row / s.N;
-    const int h = (int)(bh % s.H), b = (int)(bh / s.H);
-    const int64_t off = b * s.sb + h * s.sh + (int64_t)n * s.sn;
-    const __half* drow = dO + row * s.d;
+  const int64_t items = rows * per_row;
+  bool bad = false;
+  // warps walk whole groups of 32 items (2 or 4 tokens), so the loop and the shuffles below
+  // are uniform across each warp
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  for (int64_t wbase = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) - lane; wbase < items; wbase += stride) {
+    const int64_t i = wbase + lane;
+    const bool live = i < items;
     float acc = 0.f;
-    for (int c = lane; c < s.d; c += 32) {
-      const float ov = ld_elem<TO>(o + off + c) + (o_lo ? __bfloat162float(o_lo[off + c]) : 0.f);
-      acc += ov * __half2float(drow[c]);
-    }
+    int64_t row = 0;
+    if (live) {
+      row = i / per_row;
+      const int c = (int)(i - row * per_row) * 8;
+      const int64_t bh = row / s.N;
+      const int n = (int)(row - bh * s.N);
+      const int64_t off = (bh / s.H) * s.sb + (bh % s.H) * s.sh + (int64_t)n * s.sn + c;
+      float g[8], ov[8];
+      ld8<T>(dO + off, g);
+      ld8<T>(o + off, ov);
+      if (o_lo) {
+        float lo[8];
+        ld8<__nv_bfloat16>(o_lo + off, lo);
 #pragma unroll
-    for (int w = 16; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-    if (lane == 0) Dvec[row] = acc;
+        for (int k = 0; k < 8; ++k) ov[k] += lo[k];
+      }
+      const uint4 h = to_f16x8(g, bad);
+      *reinterpret_cast<uint4*>(dO16 + row * s.d + c) = h;
+      const __half* hh = reinterpret_cast<const __half*>(&h);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc += __half2float(hh[k]) * ov[k];
+    }
+    for (int w = per_row / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    if (live && (lane & (per_row - 1)) == 0) Dvec[row] = acc;
   }
+  if (bad) report_error(status, kDevErrRange);
 }
 
-cudaError_t launch_bwd_preprocess(const ShapeArgs& s, const void* o, const void* o_lo, const __half* dO16,
-                                  float* Dvec, cudaStream_t st) {
-  const __nv_bfloat16* lo = s.dtype == 0 ? static_cast<const __nv_bfloat16*>(o_lo) : nullptr;
-  const int64_t rows = (int64_t)s.B * s.H * s.N;
-  const int blocks = (int)std::min<int64_t>((rows * 32 + 255) / 256, 152 * 16);
+cudaError_t launch_do_prep(const ShapeArgs& s, const void* dO, const void* o, const void* o_lo, __half* dO16,
+                           float* Dvec, unsigned* status, cudaStream_t st) {
+  const int64_t items = (int64_t)s.B * s.H * s.N * (s.d / 8);
+  const int blocks = grid_for(items);
   prof_start(st, kBwdPre);
   if (s.dtype == 0)
-    bwd_preprocess_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o), lo, dO16,
-                                                                 s, Dvec);
+    do_prep_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(dO),
+                                                          static_cast<const __nv_bfloat16*>(o),
+                                                          static_cast<const __nv_bfloat16*>(o_lo), s, dO16, Dvec,
+                                                          status);
   else
-    bwd_preprocess_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(o), nullptr, dO16, s, Dvec);
+    do_prep_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(dO), static_cast<const float*>(o),
+                                                  nullptr, s, dO16, Dvec, status);
   prof_stop(st, kBwdPre);
   return cudaGetLastError();
 }

@@ -24,7 +24,7 @@ namespace sa2 {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kNumStages = 2;
+constexpr int kNumStages = 2;  // also the number of S/P buffers in TMEM (the waits rely on it)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O and l are rescaled only past 2^8
@@ -188,6 +188,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (j < nkv) {
           const int st = j % kNumStages;
           if (!mbar_wait(bar_kfull(st), (j / kNumStages) & 1, abort_flag)) break;
+          // S_j overwrites the TMEM buffer whose P_{j-2} the MMA P_{j-2} V_{j-2} read: a
+          // later tcgen05.mma is not ordered after an earlier one's TMEM operand reads, so
+          // wait for that MMA to complete (its commit also releases V_{j-2}; buffer and
+          // V stage have the same index, both rings being 2 deep)
+          if (j >= 2 && !mbar_wait(bar_vempty(st), ((j - 2) / kNumStages) & 1, abort_flag)) break;
           tc_fence_after();
           const uint32_t kbase = sbase + L::kOffK + st * L::kKVBytes;
 #pragma unroll
@@ -263,6 +268,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           // O must hold P_0..P_{j-1} V before it is rescaled; lanes that keep their max
           // multiply by 1
           const float alpha = need ? ex2(m_used - mx) : 1.f;
+          // S_j was issued only after P_{j-2} V_{j-2} completed, so o_done is at most one
+          // phase behind j - 1 here and the parity wait is exact
           if (!__all_sync(0xffffffffu, mbar_wait(bar_odone, (j - 1) & 1, abort_flag))) {
             ok = false;
             break;
@@ -318,7 +325,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         a.lse[(int64_t)bh * s.N + tok] = -INFINITY;
       }
-    } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar_odone, (nkv - 1) & 1, abort_flag))) {
+    } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar_drain, 0, abort_flag))) {
+      // bar_drain completes once, after the last MMA.  (A parity wait on o_done is only
+      // valid while that barrier is at most one phase behind the awaited phase; here the
+      // last two P V MMAs may both still be pending.)
       tc_fence_after();
       const float inv_l = 1.f / l;
 #pragma unroll 1

@@ -91,10 +91,15 @@ __global__ void __launch_bounds__(256) pool_kernel(const T* __restrict__ q, cons
 constexpr int kScoreThreads = 256;
 constexpr int kKeyChunk = 128;
 
-// Fixed-point mass of a non-negative fp32 probability: floor(P * 2^60).  Exact for
-// P >= 2^-37; smaller values lose less than 2^-60.
+// Fixed-point mass of a non-negative fp32 probability given by its bit pattern:
+// floor(P * 2^60), from the exponent and mantissa with integer shifts (P <= 1, so the
+// result fits in 61 bits).  Exact for P >= 2^-37; smaller values lose less than 2^-60.
 __device__ __forceinline__ unsigned long long mass_fix(uint32_t key) {
-  return __float2ull_rz(__uint_as_float(key) * 1152921504606846976.0f);
+  const int e = (int)(key >> 23);  // biased exponent; sign bit is 0
+  if (e == 0) return 0ull;         // zero or subnormal: below 2^-126
+  const unsigned long long m = (unsigned long long)((key & 0x7FFFFFu) | 0x800000u);
+  const int sh = e - 90;           // P * 2^60 = m * 2^(e - 127 - 23 + 60)
+  return sh >= 0 ? (m << sh) : (sh > -64 ? (m >> (-sh)) : 0ull);
 }
 
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {

@@ -268,11 +268,12 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   float* Dvec = reinterpret_cast<float*>(wsb + w.D);
   __half* c16[4] = {reinterpret_cast<__half*>(wsb + w.q16), reinterpret_cast<__half*>(wsb + w.k16),
                     reinterpret_cast<__half*>(wsb + w.v16), reinterpret_cast<__half*>(wsb + w.do16)};
-  const void* src[4] = {q, k, v, dO};
-  for (int i = 0; i < 4; ++i)
+  const void* src[3] = {q, k, v};
+  for (int i = 0; i < 3; ++i)
     if (launch_to_f16(src[i], s, c16[i], status, cs) != cudaSuccess) return SA2_ERR_CUDA;
-  // D = rowsum(dO * O) from the same fp16 dO the MMAs read
-  if (launch_bwd_preprocess(s, o, o_lo, c16[3], Dvec, cs) != cudaSuccess) return SA2_ERR_CUDA;
+  // fp16 dO and D = rowsum(dO * O) from that same fp16 dO, in one pass
+  if (launch_do_prep(s, dO, o, s.dtype == SA2_BF16 ? o_lo : nullptr, c16[3], Dvec, status, cs) != cudaSuccess)
+    return SA2_ERR_CUDA;
   CUtensorMap mq, mk, mv, mdo;
   if (!copy_map(s, c16[0], &mq, 128) || !copy_map(s, c16[1], &mk, 64) || !copy_map(s, c16[2], &mv, 64) ||
       !copy_map(s, c16[3], &mdo, 128))

@@ -94,8 +94,9 @@ struct DqArgs {
   unsigned* status;
 };
 
-cudaError_t launch_bwd_preprocess(const ShapeArgs& s, const void* o, const void* o_lo, const __half* dO16,
-                                  float* Dvec, cudaStream_t st);
+// dO -> fp16 copy and D = rowsum(dO * (O + O_lo)) in one pass (attn_common.cu).
+cudaError_t launch_do_prep(const ShapeArgs& s, const void* dO, const void* o, const void* o_lo, __half* dO16,
+                           float* Dvec, unsigned* status, cudaStream_t st);
 cudaError_t launch_attn_bwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_attn_bwd_dq(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk,
