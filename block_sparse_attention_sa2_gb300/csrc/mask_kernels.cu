@@ -45,7 +45,7 @@ __device__ __forceinline__ void load_vec<float>(const float* p, float* out) {
 // the Tq query blocks then the Tk key blocks; blockIdx.y is b*H + h.
 template <typename T>
 __global__ void __launch_bounds__(256) pool_kernel(const T* __restrict__ q, const T* __restrict__ k,
-                                                   ShapeArgs s, float* __restrict__ qbarT,
+                                                   ShapeArgs s, int tq_pad, int tk_pad, float* __restrict__ qbarT,
                                                    float* __restrict__ kbarT) {
   constexpr int VEC = 16 / sizeof(T);
   __shared__ float part[256 * VEC];
@@ -80,8 +80,8 @@ __global__ void __launch_bounds__(256) pool_kernel(const T* __restrict__ q, cons
     float sum = 0.f;
     for (int r = 0; r < rpp; ++r) sum += part[r * s.d + tid];
     const float mean = sum / static_cast<float>(nrows);
-    const int nblk = is_q ? s.Tq : s.Tk;
-    float* out = (is_q ? qbarT : kbarT) + ((int64_t)bh * s.d + tid) * nblk + blk;
+    const int pitch = is_q ? tq_pad : tk_pad;
+    float* out = (is_q ? qbarT : kbarT) + ((int64_t)bh * s.d + tid) * pitch + blk;
     *out = mean;
   }
 }
@@ -134,11 +134,11 @@ __device__ __forceinline__ Predicate count_mass(const uint32_t* keys, int Tk, ui
 
 template <int RQ>
 __global__ void __launch_bounds__(kScoreThreads, 1)
-    score_select_kernel(const float* __restrict__ qbarT, const float* __restrict__ kbarT, ShapeArgs s,
-                        SelectArgs sel, MaskOut out) {
+    score_select_kernel(const float* __restrict__ qbarT, const float* __restrict__ kbarT, ShapeArgs s, int tq_pad,
+                        int tk_pad, SelectArgs sel, MaskOut out) {
   extern __shared__ __align__(16) float smem[];
   const int Tk = s.Tk;
-  const int Tk_pad = ((Tk + kKeyChunk - 1) / kKeyChunk) * kKeyChunk;
+  const int Tk_pad = tk_pad;  // multiple of kKeyChunk; pooled keys past Tk are never read back
   float* qs = smem;                  // [d][RQ]
   float* ks = qs + s.d * RQ;         // [d][kKeyChunk]
   float* S = ks + s.d * kKeyChunk;   // [RQ][Tk_pad]
@@ -147,19 +147,35 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int nrow = min(RQ, s.Tq - i0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // q-bar tile, transposed: qs[c][r]
-  for (int idx = tid; idx < s.d * RQ; idx += kScoreThreads) {
-    const int c = idx / RQ, r = idx % RQ;
-    qs[idx] = r < nrow ? qbarT[((int64_t)bh * s.d + c) * s.Tq + i0 + r] : 0.f;
+  // q-bar tile, transposed: qs[c][r] (rows past Tq hold padding and are never used)
+  constexpr int QV = RQ / 4;  // float4 per channel row of the tile
+  for (int idx = tid; idx < s.d * QV; idx += kScoreThreads) {
+    const int c = idx / QV, r4 = idx % QV;
+    reinterpret_cast<float4*>(qs)[idx] =
+        *reinterpret_cast<const float4*>(qbarT + ((int64_t)bh * s.d + c) * tq_pad + i0 + 4 * r4);
   }
   // ---- pooled scores S[r][j] = (q-bar_r . k-bar_j) / sqrt(d), fp32 FMA in channel order
   constexpr int RPT = RQ / 4;  // rows per thread
   const int tr = tid / 64, tj = tid % 64;
+  const float* kbase = kbarT + (int64_t)bh * s.d * Tk_pad;
   for (int j0 = 0; j0 < Tk; j0 += kKeyChunk) {
     __syncthreads();
-    for (int idx = tid; idx < s.d * kKeyChunk; idx += kScoreThreads) {
-      const int c = idx / kKeyChunk, j = idx % kKeyChunk;
-      ks[idx] = (j0 + j < Tk) ? kbarT[((int64_t)bh * s.d + c) * Tk + j0 + j] : 0.f;
+    // the chunk is d x 128 floats = d*32 float4: d/8 per thread, all loads in flight at once
+    for (int base = 0; base < s.d * 32; base += kScoreThreads * 16) {
+      float4 v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int idx = base + u * kScoreThreads + tid;
+        if (idx < s.d * 32) {
+          const int c = idx >> 5, j4 = idx & 31;
+          v[u] = *reinterpret_cast<const float4*>(kbase + (int64_t)c * Tk_pad + j0 + 4 * j4);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int idx = base + u * kScoreThreads + tid;
+        if (idx < s.d * 32) reinterpret_cast<float4*>(ks)[idx] = v[u];
+      }
     }
     __syncthreads();
     float acc[RPT][2];
@@ -169,11 +185,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     for (int c = 0; c < s.d; ++c) {
       const float k0 = ks[c * kKeyChunk + tj];
       const float k1 = ks[c * kKeyChunk + tj + 64];
+      float qv[RPT];
+      if constexpr (RPT == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(qs + c * RQ + tr * 4);
+        qv[0] = t.x; qv[1] = t.y; qv[2] = t.z; qv[3] = t.w;
+      } else if constexpr (RPT == 2) {
+        const float2 t = *reinterpret_cast<const float2*>(qs + c * RQ + tr * 2);
+        qv[0] = t.x; qv[1] = t.y;
+      } else {
+        qv[0] = qs[c * RQ + tr];
+      }
 #pragma unroll
       for (int a = 0; a < RPT; ++a) {
-        const float qv = qs[c * RQ + tr * RPT + a];
-        acc[a][0] = fmaf(qv, k0, acc[a][0]);
-        acc[a][1] = fmaf(qv, k1, acc[a][1]);
+        acc[a][0] = fmaf(qv[a], k0, acc[a][0]);
+        acc[a][1] = fmaf(qv[a], k1, acc[a][1]);
       }
     }
 #pragma unroll
@@ -301,18 +326,24 @@ __global__ void __launch_bounds__(128) csc_kernel(ShapeArgs s, const uint8_t* __
 
 // ------------------------------------------------------------------------------- host
 
-int score_rows_per_cta(int Tk, int d) {
-  const int Tk_pad = ((Tk + kKeyChunk - 1) / kKeyChunk) * kKeyChunk;
-  for (int rq : {16, 8, 4}) {
-    const size_t bytes = sizeof(float) * ((size_t)d * rq + (size_t)d * kKeyChunk + (size_t)rq * Tk_pad);
-    if (bytes <= kMaxDynSmem) return rq;
-  }
-  return 0;
+int mask_tq_pad(int Tq) { return (Tq + 15) / 16 * 16; }
+int mask_tk_pad(int Tk) { return (Tk + kKeyChunk - 1) / kKeyChunk * kKeyChunk; }
+
+size_t mask_pooled_bytes(const ShapeArgs& s, size_t* kbar_offset) {
+  const size_t q = (sizeof(float) * (size_t)s.B * s.H * s.d * mask_tq_pad(s.Tq) + 255) / 256 * 256;
+  const size_t k = sizeof(float) * (size_t)s.B * s.H * s.d * mask_tk_pad(s.Tk);
+  if (kbar_offset) *kbar_offset = q;
+  return q + k;
 }
 
 static size_t score_smem_bytes(int rq, int Tk, int d) {
-  const int Tk_pad = ((Tk + kKeyChunk - 1) / kKeyChunk) * kKeyChunk;
-  return sizeof(float) * ((size_t)d * rq + (size_t)d * kKeyChunk + (size_t)rq * Tk_pad);
+  return sizeof(float) * ((size_t)d * rq + (size_t)d * kKeyChunk + (size_t)rq * mask_tk_pad(Tk));
+}
+
+int score_rows_per_cta(int Tk, int d) {
+  for (int rq : {16, 8, 4})
+    if (score_smem_bytes(rq, Tk, d) <= kMaxDynSmem) return rq;
+  return 0;
 }
 
 template <int RQ>
@@ -324,21 +355,28 @@ static cudaError_t launch_score(const float* qbarT, const float* kbarT, const Sh
   if (e != cudaSuccess) return e;
   dim3 grid((s.Tq + RQ - 1) / RQ, s.B * s.H);
   prof_start(st, kScoreSelect);
-  score_select_kernel<RQ><<<grid, kScoreThreads, smem, st>>>(qbarT, kbarT, s, sel, out);
+  score_select_kernel<RQ><<<grid, kScoreThreads, smem, st>>>(qbarT, kbarT, s, mask_tq_pad(s.Tq),
+                                                              mask_tk_pad(s.Tk), sel, out);
   prof_stop(st, kScoreSelect);
   return cudaGetLastError();
 }
 
 cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, const SelectArgs& sel,
-                              float* qbarT, float* kbarT, const MaskOut& out, cudaStream_t st) {
+                              void* pooled, const MaskOut& out, cudaStream_t st) {
+  size_t koff = 0;
+  mask_pooled_bytes(s, &koff);
+  float* qbarT = static_cast<float*>(pooled);
+  float* kbarT = reinterpret_cast<float*>(static_cast<uint8_t*>(pooled) + koff);
+  const int tqp = mask_tq_pad(s.Tq), tkp = mask_tk_pad(s.Tk);
   dim3 pgrid(s.Tq + s.Tk, s.B * s.H);
   prof_start(st, kPool);
   if (s.dtype == 0)
     pool_kernel<__nv_bfloat16><<<pgrid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(q),
-                                                       static_cast<const __nv_bfloat16*>(k), s, qbarT, kbarT);
+                                                       static_cast<const __nv_bfloat16*>(k), s, tqp, tkp, qbarT,
+                                                       kbarT);
   else
-    pool_kernel<float><<<pgrid, 256, 0, st>>>(static_cast<const float*>(q), static_cast<const float*>(k), s, qbarT,
-                                              kbarT);
+    pool_kernel<float><<<pgrid, 256, 0, st>>>(static_cast<const float*>(q), static_cast<const float*>(k), s, tqp, tkp,
+                                              qbarT, kbarT);
   prof_stop(st, kPool);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

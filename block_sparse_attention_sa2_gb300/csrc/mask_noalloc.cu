@@ -84,10 +84,8 @@ extern "C" sa2_status sa2_build_mask_noalloc(const sa2_shape* shape, const void*
   s.sn = x.stride_n;
   if (s.Tk > 7680 || score_rows_per_cta(s.Tk, s.d) == 0) return SA2_ERR_UNSUPPORTED;
 
-  // pooled queries [B*H, d, Tq] then pooled keys [B*H, d, Tk], fp32, each 256-aligned
-  const size_t qbar_bytes = (sizeof(float) * (size_t)s.B * s.H * s.d * s.Tq + 255) / 256 * 256;
-  const size_t kbar_bytes = sizeof(float) * (size_t)s.B * s.H * s.d * s.Tk;
-  if (qbar_bytes + kbar_bytes > (size_t)SA2_NOALLOC_SCRATCH_BYTES) return SA2_ERR_WORKSPACE;
+  // pooled queries then pooled keys, fp32, as the builder lays them out
+  if (mask_pooled_bytes(s, nullptr) > (size_t)SA2_NOALLOC_SCRATCH_BYTES) return SA2_ERR_WORKSPACE;
 
   cudaError_t err = cudaSuccess;
   unsigned char* scratch = static_cast<unsigned char*>(scratch_for_current_device(&err));
@@ -114,9 +112,9 @@ extern "C" sa2_status sa2_build_mask_noalloc(const sa2_shape* shape, const void*
   mo.col_idx = out->col_idx;
   mo.mask = out->mask;
   mo.pooled_p = out->pooled_p;
-  // The pooling kernel writes every pooled element the scoring kernel reads, so nothing in
-  // the scratch has to start at zero.
-  err = launch_build_mask(s, q, k, sel, reinterpret_cast<float*>(scratch),
-                          reinterpret_cast<float*>(scratch + qbar_bytes), mo, static_cast<cudaStream_t>(stream));
+  // The pooling kernel writes every pooled element whose scores are used (the scoring
+  // kernel also reads the padding past Tq / Tk, but discards what it computes from it), so
+  // nothing in the scratch has to start at zero.
+  err = launch_build_mask(s, q, k, sel, scratch, mo, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SA2_OK : SA2_ERR_CUDA;
 }

@@ -66,13 +66,12 @@ size_t token_elems(const ShapeArgs& s) { return (size_t)s.B * s.H * s.N * s.d; }
 sa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SA2_OK : SA2_ERR_CUDA; }
 
 struct MaskWs {
-  size_t qbar, kbar, mask, total;
+  size_t pooled, mask, total;
 };
 MaskWs mask_ws(const ShapeArgs& s) {
   MaskWs w;
-  w.qbar = 0;
-  w.kbar = align_up(w.qbar + sizeof(float) * (size_t)s.B * s.H * s.d * s.Tq);
-  w.mask = align_up(w.kbar + sizeof(float) * (size_t)s.B * s.H * s.d * s.Tk);
+  w.pooled = 0;
+  w.mask = align_up(mask_pooled_bytes(s, nullptr));
   w.total = align_up(w.mask + (size_t)s.B * s.H * s.Tq * s.Tk);
   return w;
 }
@@ -183,9 +182,7 @@ sa2_status sa2_build_mask(const sa2_shape* shape, const void* q, const void* k, 
   mo.col_idx = out->col_idx;
   mo.mask = out->mask ? out->mask : wsb + w.mask;
   mo.pooled_p = out->pooled_p;
-  return cuda_status(launch_build_mask(s, q, k, sel, reinterpret_cast<float*>(wsb + w.qbar),
-                                       reinterpret_cast<float*>(wsb + w.kbar), mo,
-                                       static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_build_mask(s, q, k, sel, wsb + w.pooled, mo, static_cast<cudaStream_t>(stream)));
 }
 
 size_t sa2_fwd_workspace_size(const sa2_shape* shape) {

@@ -43,8 +43,11 @@ struct MaskOut {
 
 // Mask builder (mask_kernels.cu).
 int score_rows_per_cta(int Tk, int d);
-cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, const SelectArgs& sel,
-                              float* qbarT, float* kbarT, const MaskOut& out, cudaStream_t st);
+// Bytes of the pooled scratch (q-bar then k-bar, fp32, channel-major with padded pitches);
+// *kbar_offset receives the byte offset of k-bar.
+size_t mask_pooled_bytes(const ShapeArgs& s, size_t* kbar_offset);
+cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, const SelectArgs& sel, void* pooled,
+                              const MaskOut& out, cudaStream_t st);
 
 // Tensor maps of bf16 token tensors [B, H, N, d] (attn_common.cu).
 bool make_token_map(CUtensorMap* map, const void* base, const ShapeArgs& s, int64_t sb, int64_t sh, int64_t sn,
