@@ -8,49 +8,59 @@
 // computed over kept tiles only (gist.science explainer, section 2.C: skipped tiles cost
 // nothing).
 //
-// Each CTA owns one key block j (64 tokens) and walks the list of query blocks that keep
-// it (the column list of the mask).  Every GEMM has M = 128:
-//   S   = Q_i K_j^T      M = 128 query rows, N = 64 keys, K = d     (A, B K-major)
-//   dP  = dO_i V_j^T     M = 128, N = 64, K = d                      (A, B K-major)
-//   dV^T += dO_i^T P     M = d, N = 64, K = 128 query rows           (A, B MN-major)
-//   dK^T += Q_i^T dS     M = d, N = 64, K = 128                      (A, B MN-major)
-// dV^T and dK^T accumulate in TMEM across the whole list and are written once at the end,
-// so the kernel needs no cross-CTA reduction.
+// Each CTA owns a pair of adjacent key blocks (2m, 2m+1: 128 keys) and walks the union of
+// their two column lists (built by pair_union_kernel below) in sub-tiles of 64 query rows.
+// The products are formed transposed, keys along the 128 TMEM lanes:
+//   S^T  = K Q_u^T    M = 128 keys, N = 64 queries, K = d   (A, B from shared memory)
+//   dP^T = V dO_u^T   M = 128, N = 64, K = d
+//   dV  += P^T dO_u   M = 128 keys, N = d, K = 64 queries   (A = P^T from TMEM)
+//   dK  += dS^T Q_u   M = 128, N = d, K = 64                 (A = dS^T from TMEM)
+// so P^T and dS^T never go through shared memory: the element-wise warps read S^T and dP^T
+// out of TMEM, and write P^T and dS^T back over them as fp16.  For a query block kept by
+// only one of the two key blocks the other block's 64 key rows get P = 0 (a warp-uniform
+// choice: they are whole warps), which is the price of the pairing -- about a fifth more
+// MMA work on the Wan-like masks -- against a tensor-core step that is twice as wide.
 //
-// Roles (192 threads, 1 CTA per SM): warp 0 TMA producer (K_j, V_j once; Q_i, dO_i per list
-// entry into 2 stages), warp 1 TMEM owner and MMA issuer, warps 2..5 one query row per
-// thread: P and dS from S, dP, LSE and D (prefetched one list entry ahead), written as fp16
-// into 128-byte-swizzled shared tiles; finally dK, dV out of TMEM (one channel per thread).
+// TMEM (512 columns): S^T / P^T double-buffered (2 x 64), dP^T / dS^T double-buffered
+// (2 x 64), dV and dK accumulators (128 each, lanes = keys, columns = channels).
+// Shared memory: K and V of the pair (32 KB each) and a 4-deep ring of query sub-tiles
+// (Q 16 KB, dO 16 KB, and the sub-tile's log2(e)*LSE and D vectors, 512 B).
+//
+// Roles (320 threads, 1 CTA per SM): warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer, warps 2..9 element-wise (thread = key row; warps 2-5 take query columns 0-31 of
+// the sub-tile, warps 6-9 columns 32-63), then the dK / dV epilogue.
 //
 // All operands are fp16: the call's Q, K, V, dO arrive as fp16 copies (exact for bf16
 // inputs within the fp16 range) and P, dS are written as fp16, which keeps 11 significant
 // bits of P and dS against bf16's 8.
 //
 // The tiles are always 128 channels wide: for d = 64 the second channel panel is read past
-// the end of the tensor map and arrives as zeros, and the extra rows of the results are not
-// stored.
+// the end of the tensor map and arrives as zeros, and the extra columns of the results are
+// not stored.
 #include "sa2_internal.h"
 
 namespace sa2 {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kStages = 4;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns
-constexpr uint32_t kColS = 0;     // 2 x 64
-constexpr uint32_t kColDP = 128;  // 2 x 64
-constexpr uint32_t kColDV = 256;  // 64 (lanes = channels)
-constexpr uint32_t kColDK = 320;  // 64
+constexpr uint32_t kColS = 0;     // 2 x 64: S^T, then P^T (fp16 pairs) in place
+constexpr uint32_t kColDP = 128;  // 2 x 64: dP^T, then dS^T in place
+constexpr uint32_t kColDV = 256;  // 128
+constexpr uint32_t kColDK = 384;  // 128
 
 // shared memory (bytes from the 1024-aligned base)
-constexpr int kOffK = 0;                  // 64 rows x 2 panels of 128 B = 16 KB
-constexpr int kOffV = 16384;              // 16 KB
-constexpr int kOffStage = 32768;          // 2 stages x (Q 32 KB + dO 32 KB)
-constexpr int kStageBytes = 65536;
-constexpr int kOffP = kOffStage + 2 * kStageBytes;  // 128 rows x 128 B (swizzled) = 16 KB
-constexpr int kOffDS = kOffP + 16384;
-constexpr int kOffBar = kOffDS + 16384;
+constexpr int kOffK = 0;         // 128 key rows x 2 channel panels of 128 B (panel = 16 KB)
+constexpr int kOffV = 32768;
+constexpr int kOffStage = 65536;  // stage: Q (2 panels x 64 rows x 128 B), dO (same), stats
+constexpr int kStageQ = 0, kStageDO = 16384, kStageStats = 32768;
+constexpr int kStageBytes = 33792;
+constexpr uint32_t kStageTx = 2 * 16384 + 512;
+constexpr int kOffBar = kOffStage + kStages * kStageBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;
+static_assert(kSmemBytes <= (int)kMaxDynSmem, "shared memory");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -58,67 +68,108 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// Shared-memory descriptor offsets (16-byte units) of k-step kk (16 channels) in a
+// K-major 128-byte-swizzled tile with `rows` rows per channel panel.
+__device__ __forceinline__ constexpr uint64_t kstep_off(int kk, int rows) {
+  return (uint64_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
 }
 
-// Row r of a 128-row tile with 128-byte rows in the 128-byte swizzle: 16-byte chunk c lands
-// at chunk c ^ (r % 8).
-__device__ __forceinline__ void st_swizzled_row(uint8_t* tile, int r, const uint4 (&v)[8]) {
-  uint8_t* row = tile + r * 128;
+template <typename GT>
+__device__ __forceinline__ void store_row64(GT* p, const uint32_t (&x)[32], const uint32_t (&y)[32], float mul);
+template <>
+__device__ __forceinline__ void store_row64<__nv_bfloat16>(__nv_bfloat16* p, const uint32_t (&x)[32],
+                                                           const uint32_t (&y)[32], float mul) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = v[c];
+  for (int c = 0; c < 4; ++c) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(x[8 * c + 0]) * mul, __uint_as_float(x[8 * c + 1]) * mul);
+    w.y = pack_bf16x2(__uint_as_float(x[8 * c + 2]) * mul, __uint_as_float(x[8 * c + 3]) * mul);
+    w.z = pack_bf16x2(__uint_as_float(x[8 * c + 4]) * mul, __uint_as_float(x[8 * c + 5]) * mul);
+    w.w = pack_bf16x2(__uint_as_float(x[8 * c + 6]) * mul, __uint_as_float(x[8 * c + 7]) * mul);
+    *reinterpret_cast<uint4*>(p + 8 * c) = w;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(y[8 * c + 0]) * mul, __uint_as_float(y[8 * c + 1]) * mul);
+    w.y = pack_bf16x2(__uint_as_float(y[8 * c + 2]) * mul, __uint_as_float(y[8 * c + 3]) * mul);
+    w.z = pack_bf16x2(__uint_as_float(y[8 * c + 4]) * mul, __uint_as_float(y[8 * c + 5]) * mul);
+    w.w = pack_bf16x2(__uint_as_float(y[8 * c + 6]) * mul, __uint_as_float(y[8 * c + 7]) * mul);
+    *reinterpret_cast<uint4*>(p + 32 + 8 * c) = w;
+  }
+}
+template <>
+__device__ __forceinline__ void store_row64<float>(float* p, const uint32_t (&x)[32], const uint32_t (&y)[32],
+                                                   float mul) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<float4*>(p + 4 * c) =
+        make_float4(__uint_as_float(x[4 * c]) * mul, __uint_as_float(x[4 * c + 1]) * mul,
+                    __uint_as_float(x[4 * c + 2]) * mul, __uint_as_float(x[4 * c + 3]) * mul);
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<float4*>(p + 32 + 4 * c) =
+        make_float4(__uint_as_float(y[4 * c]) * mul, __uint_as_float(y[4 * c + 1]) * mul,
+                    __uint_as_float(y[4 * c + 2]) * mul, __uint_as_float(y[4 * c + 3]) * mul);
 }
 
-template <typename T>
-__device__ __forceinline__ void store_elem(T* p, float v);
-template <>
-__device__ __forceinline__ void store_elem<float>(float* p, float v) { *p = v; }
-template <>
-__device__ __forceinline__ void store_elem<__nv_bfloat16>(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+template <typename GT>
+__device__ __forceinline__ void zero_row64(GT* p) {
+  constexpr int kVec = 16 / sizeof(GT);
+#pragma unroll
+  for (int c = 0; c < 64 / kVec; ++c) *reinterpret_cast<uint4*>(p + kVec * c) = make_uint4(0, 0, 0, 0);
+}
 
 template <typename GT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo, ShapeArgs s,
-                    BwdArgs a) {
+                         const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+                         ShapeArgs s, BwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   const uint32_t bar_kv = smem_u32(&bars[0]);
   auto bar_full = [&](int st) { return smem_u32(&bars[1 + st]); };
-  auto bar_empty = [&](int st) { return smem_u32(&bars[3 + st]); };
-  auto bar_sfull = [&](int b) { return smem_u32(&bars[5 + b]); };
-  const uint32_t bar_pready = smem_u32(&bars[7]);
-  const uint32_t bar_pdsfree = smem_u32(&bars[8]);  // the MMAs that read P / dS have completed
-  const uint32_t bar_drain = smem_u32(&bars[9]);
+  auto bar_empty = [&](int st) { return smem_u32(&bars[5 + st]); };
+  auto bar_sfull = [&](int b) { return smem_u32(&bars[9 + b]); };
+  auto bar_pready = [&](int b) { return smem_u32(&bars[11 + b]); };
+  auto bar_bfree = [&](int b) { return smem_u32(&bars[13 + b]); };  // MMAs reading buffer b done
+  const uint32_t bar_drain = smem_u32(&bars[15]);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 192);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x / s.Tk;
-  const int kj = blockIdx.x % s.Tk;
+  // pair-major order: the pairs holding the first key blocks of every head (where
+  // attention sinks, and so the longest lists, usually sit) start first
+  const int BH = s.B * s.H;
+  const int Tp = (s.Tk + 1) >> 1;
+  const int m = blockIdx.x / BH;
+  const int bh = blockIdx.x % BH;
   const int b = bh / s.H, h = bh % s.H;
-  const int64_t colid = (int64_t)bh * s.Tk + kj;
-  int nq = a.col_cnt[colid];
-  if (nq < 0 || nq > s.Tq) {
+  const int64_t pid = (int64_t)bh * Tp + m;
+  int nu = a.pair_cnt[pid];
+  if (nu < 0 || nu > s.Tq) {
     if (tid == 0) report_error(a.status, kDevErrBounds);
-    nq = nq < 0 ? 0 : s.Tq;
+    nu = nu < 0 ? 0 : s.Tq;
   }
-  const int32_t* list = a.col_idx + colid * s.Tq;
-  const int kv_valid = min(64, s.N - kj * 64);
+  const uint32_t* list = a.pair_idx + pid * s.Tq;
+  const int sub_shift = s.bq == 128 ? 1 : 0;  // 64-row sub-tiles per query block: 2 or 1
+  const int nsub = nu << sub_shift;
+  const int Tsub = s.Tq << sub_shift;
 
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(bar_kv, 1);
-    for (int st = 0; st < 2; ++st) {
+    for (int st = 0; st < kStages; ++st) {
       mbar_init(bar_full(st), 1);
       mbar_init(bar_empty(st), 1);
-      mbar_init(bar_sfull(st), 1);
     }
-    mbar_init(bar_pready, 128);
-    mbar_init(bar_pdsfree, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_sfull(i), 1);
+      mbar_init(bar_pready(i), 256);
+      mbar_init(bar_bfree(i), 1);
+    }
     mbar_init(bar_drain, 1);
     fence_barrier_init();
   }
@@ -133,191 +184,186 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0 && nq > 0) {
-      tma_prefetch_map(&mq);
-      tma_prefetch_map(&mdo);
-      mbar_arrive_expect_tx(bar_kv, 32768);
-      for (int p = 0; p < 2; ++p) {
-        tma_load_4d(sbase + kOffK + p * 8192, &mk, bar_kv, p * 64, kj * 64, h, b);
-        tma_load_4d(sbase + kOffV + p * 8192, &mv, bar_kv, p * 64, kj * 64, h, b);
+    if (nsub > 0) {
+      if (lane == 0) {
+        tma_prefetch_map(&mq);
+        tma_prefetch_map(&mdo);
+        mbar_arrive_expect_tx(bar_kv, 65536);
+        for (int p = 0; p < 2; ++p)
+          for (int r = 0; r < 2; ++r) {
+            tma_load_4d(sbase + kOffK + p * 16384 + r * 8192, &mk, bar_kv, p * 64, m * 128 + r * 64, h, b);
+            tma_load_4d(sbase + kOffV + p * 16384 + r * 8192, &mv, bar_kv, p * 64, m * 128 + r * 64, h, b);
+          }
       }
-      for (int t = 0; t < nq; ++t) {
-        const int st = t & 1;
-        if (t >= 2 && !mbar_wait(bar_empty(st), ((t >> 1) - 1) & 1, abort_flag)) break;
-        int qi = list[t];
-        if (qi < 0 || qi >= s.Tq) {
-          report_error(a.status, kDevErrBounds);
+      uint32_t chunk = 0;  // list entries t0 + lane of the current 32-entry chunk
+      bool ok = true;
+      for (int u = 0; u < nsub; ++u) {
+        const int t = u >> sub_shift, hh = u & sub_shift;
+        if ((t & 31) == 0 && hh == 0) chunk = t + lane < nu ? list[t + lane] : 0u;
+        int qi = (int)(__shfl_sync(0xffffffffu, chunk, t & 31) & 0x3FFFFFFFu);
+        if (qi >= s.Tq) {
+          if (lane == 0) report_error(a.status, kDevErrBounds);
           qi = 0;
         }
-        const uint32_t stg = sbase + kOffStage + st * kStageBytes;
-        mbar_arrive_expect_tx(bar_full(st), kStageBytes);
-        for (int p = 0; p < 2; ++p) {
-          tma_load_4d(stg + p * 16384, &mq, bar_full(st), p * 64, qi * s.bq, h, b);
-          tma_load_4d(stg + 32768 + p * 16384, &mdo, bar_full(st), p * 64, qi * s.bq, h, b);
+        const int st = u & (kStages - 1);
+        if (u >= kStages && !__all_sync(0xffffffffu, mbar_wait(bar_empty(st), ((u >> 2) - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
         }
+        if (lane == 0) {
+          const uint32_t stg = sbase + kOffStage + st * kStageBytes;
+          const int row = (qi << sub_shift) + hh;  // 64-row sub-tile index within the head
+          mbar_arrive_expect_tx(bar_full(st), kStageTx);
+          for (int p = 0; p < 2; ++p) {
+            tma_load_4d(stg + kStageQ + p * 8192, &mq, bar_full(st), p * 64, row * 64, h, b);
+            tma_load_4d(stg + kStageDO + p * 8192, &mdo, bar_full(st), p * 64, row * 64, h, b);
+          }
+          bulk_load(stg + kStageStats, a.stats + ((int64_t)bh * Tsub + row) * 128, 512, bar_full(st));
+        }
+        __syncwarp();
       }
-      const int first = nq > 2 ? nq - 2 : 0;
-      for (int t = first; t < nq; ++t) mbar_wait(bar_full(t & 1), (t >> 1) & 1, abort_flag);
-      mbar_wait(bar_kv, 0, abort_flag);
+      // no copy may still be in flight when the CTA exits
+      if (ok && lane == 0) {
+        const int first = nsub > kStages ? nsub - kStages : 0;
+        for (int u = first; u < nsub; ++u) mbar_wait(bar_full(u & (kStages - 1)), (u >> 2) & 1, abort_flag);
+        mbar_wait(bar_kv, 0, abort_flag);
+      }
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------------- MMA issuer
-    if (lane == 0 && nq > 0) {
+    if (lane == 0 && nsub > 0) {
       constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
-      constexpr uint32_t idT = idesc_f16_f32(128, 64, true, true);
+      constexpr uint32_t idG = idesc_f16_f32(128, 128, false, true);
+      const uint64_t kd = smem_desc(sbase + kOffK, 16, 1024), vd = smem_desc(sbase + kOffV, 16, 1024);
       bool ok = mbar_wait(bar_kv, 0, abort_flag);
-      for (int t = 0; ok && t <= nq; ++t) {
-        if (t < nq) {
-          const int st = t & 1;
-          if (!mbar_wait(bar_full(st), (t >> 1) & 1, abort_flag)) break;
+      for (int u = 0; ok && u <= nsub; ++u) {
+        if (u < nsub) {
+          const int st = u & (kStages - 1), bb = u & 1;
+          if (!mbar_wait(bar_full(st), (u >> 2) & 1, abort_flag)) break;
+          // buffer bb was last read by the dV / dK MMAs of sub-tile u - 2
+          if (u >= 2 && !mbar_wait(bar_bfree(bb), ((u >> 1) - 1) & 1, abort_flag)) break;
           tc_fence_after();
-          const uint32_t qs = sbase + kOffStage + st * kStageBytes, dos = qs + 32768;
+          const uint32_t stg = sbase + kOffStage + st * kStageBytes;
+          const uint64_t qd = smem_desc(stg + kStageQ, 16, 1024), dod = smem_desc(stg + kStageDO, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            const uint32_t koff = (kk >> 2) * 8192 + (kk & 3) * 32;
-            umma_ss(tmem + kColS + st * 64, smem_desc(qs + off, 16, 1024), smem_desc(sbase + kOffK + koff, 16, 1024),
-                    idS, kk > 0);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(tmem + kColS + bb * 64, kd + kstep_off(kk, 128), qd + kstep_off(kk, 64), idS, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            const uint32_t koff = (kk >> 2) * 8192 + (kk & 3) * 32;
-            umma_ss(tmem + kColDP + st * 64, smem_desc(dos + off, 16, 1024),
-                    smem_desc(sbase + kOffV + koff, 16, 1024), idS, kk > 0);
-          }
-          umma_commit(bar_sfull(st));
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ss(tmem + kColDP + bb * 64, vd + kstep_off(kk, 128), dod + kstep_off(kk, 64), idS, kk > 0);
+          umma_commit(bar_sfull(bb));
         }
-        if (t >= 1) {
-          const int u = t - 1;
-          const int st = u & 1;
-          if (!mbar_wait(bar_pready, u & 1, abort_flag)) break;
+        if (u >= 1) {
+          const int w = u - 1;
+          const int st = w & (kStages - 1), bb = w & 1;
+          if (!mbar_wait(bar_pready(bb), (w >> 1) & 1, abort_flag)) break;
           tc_fence_after();
-          const uint32_t qs = sbase + kOffStage + st * kStageBytes, dos = qs + 32768;
-          // dV^T += dO^T P and dK^T += Q^T dS: K = 128 query rows in steps of 16
+          const uint32_t stg = sbase + kOffStage + st * kStageBytes;
+          // B = dO_w / Q_w read MN-major: 16 query rows (2048 B) per k-step, channel panels
+          // 8 KB apart
+          const uint64_t dod = smem_desc(stg + kStageDO, 8192, 1024), qd = smem_desc(stg + kStageQ, 8192, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t adesc = smem_desc(dos + kk * 2048, 16384, 1024);
-            const uint64_t bdesc = smem_desc(sbase + kOffP + kk * 2048, 1024, 1024);
-            umma_ss(tmem + kColDV, adesc, bdesc, idT, (u > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t col = bb * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
+            umma_ts(tmem + kColDV, tmem + kColS + col, dod + (uint64_t)(kk * 128), idG, (w > 0 || kk > 0) ? 1u : 0u);
           }
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t adesc = smem_desc(qs + kk * 2048, 16384, 1024);
-            const uint64_t bdesc = smem_desc(sbase + kOffDS + kk * 2048, 1024, 1024);
-            umma_ss(tmem + kColDK, adesc, bdesc, idT, (u > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t col = bb * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
+            umma_ts(tmem + kColDK, tmem + kColDP + col, qd + (uint64_t)(kk * 128), idG, (w > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(bar_empty(st));
-          umma_commit(bar_pdsfree);
+          umma_commit(bar_bfree(bb));
         }
       }
       umma_commit(bar_drain);
       mbar_wait(bar_drain, 0, abort_flag);
     }
   } else {
-    // -------------------------------------------------------------- query-row threads
-    const int sub = warp & 3;
-    const int r = 32 * sub + lane;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * sub) << 16);
-    const float lse_scale = 1.4426950408889634f;
-    // LSE and D of this thread's row for list entry t are loaded one entry ahead, and the
-    // query block of entry t two entries ahead, so no dependent global load sits on the path
-    // from one tile to the next
-    auto row_stats = [&](int t, int qi, float& lse2, float& Dr, bool& valid) {
-      qi = (qi < 0 || qi >= s.Tq) ? 0 : qi;
-      const int64_t tok = (int64_t)qi * s.bq + r;
-      valid = t < nq && r < s.bq && tok < s.N;
-      lse2 = valid ? a.lse[(int64_t)bh * s.N + tok] * lse_scale : 0.f;
-      Dr = valid ? a.Dvec[(int64_t)bh * s.N + tok] : 0.f;
-    };
-    float n_lse2, n_D;
-    bool n_valid;
-    row_stats(0, nq > 0 ? list[0] : 0, n_lse2, n_D, n_valid);
-    int qi_ahead = nq > 1 ? list[1] : 0;
+    // ------------------------------------------------------------- element-wise warps
+    const int q4 = warp & 3;          // TMEM lane quarter
+    const int g = (warp - 2) >> 2;    // query columns 32g .. 32g+31 of each sub-tile
+    const int r = 32 * q4 + lane;     // key row of the pair
+    const int half = r >> 6;          // 0: key block 2m, 1: key block 2m+1
+    const int key = m * 128 + r;
+    const bool key_valid = key < s.N;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q4) << 16);
     bool ok = true;
-    for (int t = 0; t < nq; ++t) {
-      const float lse2 = n_lse2, Dr = n_D;
-      const bool row_valid = n_valid;
-      const int qi_next = qi_ahead;
-      qi_ahead = t + 2 < nq ? list[t + 2] : 0;
-      row_stats(t + 1, qi_next, n_lse2, n_D, n_valid);
-      uint4 pk[8], dk[8];
-      const int st = t & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(st), (t >> 1) & 1, abort_flag))) {
+    uint32_t e_next = nu > 0 ? list[0] : 0u;
+    uint32_t e = 0;
+    for (int u = 0; u < nsub; ++u) {
+      const int t = u >> sub_shift;
+      if ((u & sub_shift) == 0) {
+        e = e_next;
+        e_next = t + 1 < nu ? list[t + 1] : 0u;
+      }
+      const bool keep = ((e >> (30 + half)) & 1u) != 0;  // same for the whole warp
+      const int st = u & (kStages - 1), bb = u & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bb), (u >> 1) & 1, abort_flag) &&
+                                       mbar_wait(bar_full(st), (u >> 2) & 1, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
+      uint32_t sv[32], dv[32];
+      tmem_ld32(trow + kColS + bb * 64 + 32 * g, sv);
+      tmem_ld32(trow + kColDP + bb * 64 + 32 * g, dv);
+      const float4* l4 = reinterpret_cast<const float4*>(smem + kOffStage + st * kStageBytes + kStageStats) + 8 * g;
+      const float4* d4 = l4 + 16;
+      tmem_ld_wait(sv);
+      tmem_ld_wait(dv);
+      uint32_t pw[16], dw[16];
+      if (keep) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(trow + kColS + st * 64 + half * 32, sv);
-        tmem_ld32(trow + kColDP + st * 64 + half * 32, dv);
-        tmem_ld_wait(sv);
-        tmem_ld_wait(dv);
+        for (int j = 0; j < 8; ++j) {
+          const float4 L = l4[j], D = d4[j];
+          const float lv[4] = {L.x, L.y, L.z, L.w}, Dv[4] = {D.x, D.y, D.z, D.w};
+          float pv[4], ds[4];
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint32_t pw[4], dw[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float pv[2], ds[2];
-#pragma unroll
-            for (int z = 0; z < 2; ++z) {
-              const int c = c8 * 8 + e * 2 + z;
-              const bool cv = row_valid && (half * 32 + c) < kv_valid;
-              const float p = cv ? ex2(__uint_as_float(sv[c]) * a.scale_log2 - lse2) : 0.f;
-              pv[z] = p;
-              ds[z] = p * (__uint_as_float(dv[c]) - Dr);
-            }
-            pw[e] = pack_f16x2(pv[0], pv[1]);
-            dw[e] = pack_f16x2(ds[0], ds[1]);
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const int c = 4 * j + e4;
+            const float p = key_valid ? ex2(fmaf(__uint_as_float(sv[c]), a.scale_log2, -lv[e4])) : 0.f;
+            pv[e4] = p;
+            ds[e4] = p * (__uint_as_float(dv[c]) - Dv[e4]);
           }
-          pk[half * 4 + c8] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-          dk[half * 4 + c8] = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+          pw[2 * j] = pack_f16x2(pv[0], pv[1]);
+          pw[2 * j + 1] = pack_f16x2(pv[2], pv[3]);
+          dw[2 * j] = pack_f16x2(ds[0], ds[1]);
+          dw[2 * j + 1] = pack_f16x2(ds[2], ds[3]);
         }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pw[j] = dw[j] = 0u;
       }
-      // the MMAs that read the previous P / dS tiles must have completed
-      if (t >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_pdsfree, (t - 1) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      st_swizzled_row(smem + kOffP, r, pk);
-      st_swizzled_row(smem + kOffDS, r, dk);
-      fence_proxy_async_smem();
+      tmem_st16(trow + kColS + bb * 64 + 32 * g, pw);
+      tmem_st16(trow + kColDP + bb * 64 + 32 * g, dw);
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_pready);
+      mbar_arrive(bar_pready(bb));
     }
-    if (ok && nq > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_pdsfree, (nq - 1) & 1, abort_flag));
-    // ---- dK, dV of this key block: thread = channel (TMEM lane), columns = keys
-    const int c = r;
-    GT* dkp = reinterpret_cast<GT*>(a.dk) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + c;
-    GT* dvp = reinterpret_cast<GT*>(a.dv) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + c;
-    if (nq == 0) {
-      if (c < s.d)
-        for (int kv = 0; kv < kv_valid; ++kv) {
-          store_elem<GT>(dkp + (int64_t)(kj * 64 + kv) * a.g_sn, 0.f);
-          store_elem<GT>(dvp + (int64_t)(kj * 64 + kv) * a.g_sn, 0.f);
-        }
-    } else if (__all_sync(0xffffffffu, ok)) {
-      tc_fence_after();
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        uint32_t kvv[32], vvv[32];
-        tmem_ld32(trow + kColDK + half * 32, kvv);
-        tmem_ld32(trow + kColDV + half * 32, vvv);
-        tmem_ld_wait(kvv);
-        tmem_ld_wait(vvv);
-        if (c < s.d) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int kv = half * 32 + e;
-            if (kv < kv_valid) {
-              store_elem<GT>(dkp + (int64_t)(kj * 64 + kv) * a.g_sn, __uint_as_float(kvv[e]) * a.scale);
-              store_elem<GT>(dvp + (int64_t)(kj * 64 + kv) * a.g_sn, __uint_as_float(vvv[e]));
-            }
-          }
-        }
+    // ---- dK, dV of the pair: thread = key row, 64 channels 64g .. 64g+63
+    const int c0 = 64 * g;
+    GT* dkp = reinterpret_cast<GT*>(a.dk) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + (int64_t)key * a.g_sn + c0;
+    GT* dvp = reinterpret_cast<GT*>(a.dv) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + (int64_t)key * a.g_sn + c0;
+    const bool store = key_valid && c0 < s.d;
+    if (nsub == 0) {
+      if (store) {
+        zero_row64<GT>(dkp);
+        zero_row64<GT>(dvp);
       }
+    } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar_drain, 0, abort_flag))) {
+      tc_fence_after();
+      uint32_t x[32], y[32];
+      tmem_ld32(trow + kColDK + c0, x);
+      tmem_ld32(trow + kColDK + c0 + 32, y);
+      tmem_ld_wait(x);
+      tmem_ld_wait(y);
+      if (store) store_row64<GT>(dkp, x, y, a.scale);
+      tmem_ld32(trow + kColDV + c0, x);
+      tmem_ld32(trow + kColDV + c0 + 32, y);
+      tmem_ld_wait(x);
+      tmem_ld_wait(y);
+      if (store) store_row64<GT>(dvp, x, y, 1.f);
     }
   }
   tc_fence_before();
@@ -329,23 +375,99 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Union of the column lists of key blocks 2m and 2m+1, one warp per pair: the query blocks
+// are marked in two bitmaps and read back in ascending order, each entry tagged with the
+// blocks that keep it (bit 30: block 2m, bit 31: block 2m+1).
+constexpr int kUnionWarps = 4;
+constexpr int kMaxTqWords = 240;  // Tq <= 7680
+
+__global__ void __launch_bounds__(32 * kUnionWarps) pair_union_kernel(const int32_t* __restrict__ col_cnt,
+                                                                     const int32_t* __restrict__ col_idx, ShapeArgs s,
+                                                                     int32_t* __restrict__ pair_cnt,
+                                                                     uint32_t* __restrict__ pair_idx,
+                                                                     unsigned* status) {
+  __shared__ uint32_t bits[kUnionWarps][2][kMaxTqWords];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Tp = (s.Tk + 1) >> 1;
+  const int64_t pid = (int64_t)blockIdx.x * kUnionWarps + warp;
+  if (pid >= (int64_t)s.B * s.H * Tp) return;  // whole warps only; no block-wide barrier below
+  const int64_t bh = pid / Tp;
+  const int m = (int)(pid - bh * Tp);
+  const int nw = (s.Tq + 31) >> 5;
+  for (int w = lane; w < nw; w += 32) bits[warp][0][w] = bits[warp][1][w] = 0u;
+  __syncwarp();
+  bool bad = false;
+  for (int half = 0; half < 2; ++half) {
+    const int j = 2 * m + half;
+    if (j >= s.Tk) break;
+    const int64_t col = bh * s.Tk + j;
+    int cnt = col_cnt[col];
+    if (cnt < 0 || cnt > s.Tq) {
+      bad = true;
+      cnt = cnt < 0 ? 0 : s.Tq;
+    }
+    const int32_t* li = col_idx + col * s.Tq;
+    for (int i = lane; i < cnt; i += 32) {
+      const int qi = li[i];
+      if (qi < 0 || qi >= s.Tq) {
+        bad = true;
+        continue;
+      }
+      atomicOr(&bits[warp][half][qi >> 5], 1u << (qi & 31));
+    }
+  }
+  __syncwarp();
+  uint32_t* out = pair_idx + pid * s.Tq;
+  int base = 0;
+  for (int w0 = 0; w0 < nw; w0 += 32) {
+    const int w = w0 + lane;
+    const uint32_t x = w < nw ? bits[warp][0][w] : 0u, y = w < nw ? bits[warp][1][w] : 0u;
+    uint32_t un = x | y;
+    const int n = __popc(un);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int pos = base + incl - n;
+    while (un) {
+      const int bit = __ffs(un) - 1;
+      un &= un - 1;
+      out[pos++] = (uint32_t)(w * 32 + bit) | (((x >> bit) & 1u) << 30) | (((y >> bit) & 1u) << 31);
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) pair_cnt[pid] = base;
+  if (bad) report_error(status, kDevErrBounds);
+}
+
 template <typename GT>
 cudaError_t launch_bwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st) {
-  auto kern = attn_bwd_dkdv_kernel<GT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const long long pairs = (long long)s.B * s.H * ((s.Tk + 1) / 2);
+  prof_start(st, kBwdPairs);
+  pair_union_kernel<<<(unsigned)((pairs + kUnionWarps - 1) / kUnionWarps), 32 * kUnionWarps, 0, st>>>(
+      a.col_cnt, a.col_idx, s, a.pair_cnt, a.pair_idx, a.status);
+  prof_stop(st, kBwdPairs);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)s.B * s.H * s.Tk;
+  auto kern = attn_bwd_dkdv_kernel<GT>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
   prof_start(st, kAttnBwd);
-  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, s, a);
+  kern<<<(unsigned)pairs, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, s, a);
   prof_stop(st, kAttnBwd);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+size_t bwd_pair_entries(const ShapeArgs& s) { return (size_t)s.B * s.H * ((s.Tk + 1) / 2) * s.Tq; }
+
 cudaError_t launch_attn_bwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st) {
+  if (s.Tq > 32 * kMaxTqWords) return cudaErrorInvalidValue;
   return s.dtype == 0 ? launch_bwd_t<__nv_bfloat16>(s, mq, mk, mv, mdo, a, st)
                       : launch_bwd_t<float>(s, mq, mk, mv, mdo, a, st);
 }

@@ -215,8 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * sub) << 16);
     const int64_t tok = (int64_t)qi * s.bq + r;
     const bool row_valid = r < s.bq && tok < s.N;
-    const float lse2 = row_valid ? a.lse[(int64_t)bh * s.N + tok] * 1.4426950408889634f : 0.f;
-    const float Dr = row_valid ? a.Dvec[(int64_t)bh * s.N + tok] : 0.f;
+    // statistics record of this row: 64-row sub-tile (qi * bq + r) / 64 of the head
+    const float* rec = a.stats + ((int64_t)bh * (s.Tq * (s.bq / 64)) + ((qi * s.bq + r) >> 6)) * 128 + (r & 63);
+    const float lse2 = row_valid ? rec[0] : 0.f;
+    const float Dr = row_valid ? rec[64] : 0.f;
     bool ok = true;
     const int bb = wg;  // this group's TMEM buffer
     int next_kb = wg < nkv ? list[wg] : 0;

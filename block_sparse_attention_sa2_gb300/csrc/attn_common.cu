@@ -1,6 +1,6 @@
 // Host-side TMA descriptors and the element-wise kernels around the attention kernels:
-// fp32 -> bf16 staging of SA2_FP32 inputs, the backward's preprocessing
-// (D = rowsum(dO * O), zeroed fp32 dQ accumulator) and the dQ conversion.
+// fp16 copies of the token tensors, and the backward's preprocessing (fp16 dO, D =
+// rowsum(dO * O) and log2(e) * LSE per row).
 #include <algorithm>
 #include <cstring>
 #include <cudaTypedefs.h>
@@ -142,12 +142,14 @@ cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsi
 // Sixteen threads per token (8 channels each, d = 128) or eight (d = 64).
 template <typename T>
 __global__ void __launch_bounds__(256) do_prep_kernel(const T* __restrict__ dO, const T* __restrict__ o,
-                                                      const __nv_bfloat16* __restrict__ o_lo, ShapeArgs s,
-                                                      __half* __restrict__ dO16, float* __restrict__ Dvec,
+                                                      const __nv_bfloat16* __restrict__ o_lo,
+                                                      const float* __restrict__ lse, ShapeArgs s,
+                                                      __half* __restrict__ dO16, float* __restrict__ stats,
                                                       unsigned* status) {
   const int per_row = s.d / 8;  // threads per token: 16 or 8, a power of two within a warp
   const int64_t rows = (int64_t)s.B * s.H * s.N;
   const int64_t items = rows * per_row;
+  const int Tsub = s.Tq * (s.bq / 64);
   bool bad = false;
   // warps walk whole groups of 32 items (2 or 4 tokens), so the loop and the shuffles below
   // are uniform across each warp
@@ -157,12 +159,13 @@ __global__ void __launch_bounds__(256) do_prep_kernel(const T* __restrict__ dO, 
     const int64_t i = wbase + lane;
     const bool live = i < items;
     float acc = 0.f;
-    int64_t row = 0;
+    int64_t row = 0, bh = 0;
+    int n = 0;
     if (live) {
       row = i / per_row;
       const int c = (int)(i - row * per_row) * 8;
-      const int64_t bh = row / s.N;
-      const int n = (int)(row - bh * s.N);
+      bh = row / s.N;
+      n = (int)(row - bh * s.N);
       const int64_t off = (bh / s.H) * s.sb + (bh % s.H) * s.sh + (int64_t)n * s.sn + c;
       float g[8], ov[8];
       ld8<T>(dO + off, g);
@@ -180,24 +183,37 @@ __global__ void __launch_bounds__(256) do_prep_kernel(const T* __restrict__ dO, 
       for (int k = 0; k < 8; ++k) acc += __half2float(hh[k]) * ov[k];
     }
     for (int w = per_row / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-    if (live && (lane & (per_row - 1)) == 0) Dvec[row] = acc;
+    if (live && (lane & (per_row - 1)) == 0) {
+      float* rec = stats + ((int64_t)bh * Tsub + (n >> 6)) * 128 + (n & 63);
+      rec[0] = lse[row] * 1.4426950408889634f;
+      rec[64] = acc;
+    }
+  }
+  // rows of the last sub-tiles past N: +inf makes their P exactly 0
+  const int pad = Tsub * 64 - s.N;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)s.B * s.H * pad; i += stride) {
+    const int64_t bh = i / pad;
+    const int n = s.N + (int)(i - bh * pad);
+    float* rec = stats + ((int64_t)bh * Tsub + (n >> 6)) * 128 + (n & 63);
+    rec[0] = __int_as_float(0x7f800000);
+    rec[64] = 0.f;
   }
   if (bad) report_error(status, kDevErrRange);
 }
 
-cudaError_t launch_do_prep(const ShapeArgs& s, const void* dO, const void* o, const void* o_lo, __half* dO16,
-                           float* Dvec, unsigned* status, cudaStream_t st) {
+cudaError_t launch_do_prep(const ShapeArgs& s, const void* dO, const void* o, const void* o_lo, const float* lse,
+                           __half* dO16, float* stats, unsigned* status, cudaStream_t st) {
   const int64_t items = (int64_t)s.B * s.H * s.N * (s.d / 8);
   const int blocks = grid_for(items);
   prof_start(st, kBwdPre);
   if (s.dtype == 0)
     do_prep_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(dO),
                                                           static_cast<const __nv_bfloat16*>(o),
-                                                          static_cast<const __nv_bfloat16*>(o_lo), s, dO16, Dvec,
-                                                          status);
+                                                          static_cast<const __nv_bfloat16*>(o_lo), lse, s, dO16,
+                                                          stats, status);
   else
     do_prep_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(dO), static_cast<const float*>(o),
-                                                  nullptr, s, dO16, Dvec, status);
+                                                  nullptr, lse, s, dO16, stats, status);
   prof_stop(st, kBwdPre);
   return cudaGetLastError();
 }

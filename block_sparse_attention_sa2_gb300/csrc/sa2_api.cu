@@ -93,15 +93,18 @@ FwdWs fwd_ws(const ShapeArgs& s) {
   return w;
 }
 
-// Backward workspace: D and fp16 copies of Q, K, V, dO.
+// Backward workspace: per-row statistics, the pair-union lists of the dK / dV kernel, and
+// fp16 copies of Q, K, V, dO.
 struct BwdWs {
-  size_t D, q16, k16, v16, do16, total;
+  size_t stats, pair_cnt, pair_idx, q16, k16, v16, do16, total;
 };
 BwdWs bwd_ws(const ShapeArgs& s) {
   BwdWs w{};
-  w.D = 0;
   const size_t t = align_up(2 * token_elems(s));
-  w.q16 = align_up(sizeof(float) * (size_t)s.B * s.H * s.N);
+  w.stats = 0;
+  w.pair_cnt = align_up(sizeof(float) * (size_t)bwd_stats_floats(s));
+  w.pair_idx = w.pair_cnt + align_up(sizeof(int32_t) * (size_t)s.B * s.H * ((s.Tk + 1) / 2));
+  w.q16 = w.pair_idx + align_up(sizeof(uint32_t) * bwd_pair_entries(s));
   w.k16 = w.q16 + t;
   w.v16 = w.k16 + t;
   w.do16 = w.v16 + t;
@@ -262,25 +265,28 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   unsigned* status = status_ptr();
   uint8_t* wsb = static_cast<uint8_t*>(ws);
-  float* Dvec = reinterpret_cast<float*>(wsb + w.D);
+  float* stats = reinterpret_cast<float*>(wsb + w.stats);
   __half* c16[4] = {reinterpret_cast<__half*>(wsb + w.q16), reinterpret_cast<__half*>(wsb + w.k16),
                     reinterpret_cast<__half*>(wsb + w.v16), reinterpret_cast<__half*>(wsb + w.do16)};
   const void* src[3] = {q, k, v};
   for (int i = 0; i < 3; ++i)
     if (launch_to_f16(src[i], s, c16[i], status, cs) != cudaSuccess) return SA2_ERR_CUDA;
-  // fp16 dO and D = rowsum(dO * O) from that same fp16 dO, in one pass
-  if (launch_do_prep(s, dO, o, s.dtype == SA2_BF16 ? o_lo : nullptr, c16[3], Dvec, status, cs) != cudaSuccess)
+  // fp16 dO, and D = rowsum(dO * O) from that same fp16 dO, in one pass
+  if (launch_do_prep(s, dO, o, s.dtype == SA2_BF16 ? o_lo : nullptr, lse, c16[3], stats, status, cs) !=
+      cudaSuccess)
     return SA2_ERR_CUDA;
-  CUtensorMap mq, mk, mv, mdo;
-  if (!copy_map(s, c16[0], &mq, 128) || !copy_map(s, c16[1], &mk, 64) || !copy_map(s, c16[2], &mv, 64) ||
-      !copy_map(s, c16[3], &mdo, 128))
+  // the dK / dV kernel reads 64-row query sub-tiles, the dQ kernel 128-row query tiles
+  CUtensorMap mq64, mdo64, mq, mk, mv, mdo;
+  if (!copy_map(s, c16[0], &mq64, 64) || !copy_map(s, c16[3], &mdo64, 64) || !copy_map(s, c16[0], &mq, 128) ||
+      !copy_map(s, c16[1], &mk, 64) || !copy_map(s, c16[2], &mv, 64) || !copy_map(s, c16[3], &mdo, 128))
     return SA2_ERR_CUDA;
   const float scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / std::sqrt((double)s.d));
   BwdArgs a;
   a.col_cnt = mask->col_cnt;
   a.col_idx = mask->col_idx;
-  a.lse = lse;
-  a.Dvec = Dvec;
+  a.pair_cnt = reinterpret_cast<int32_t*>(wsb + w.pair_cnt);
+  a.pair_idx = reinterpret_cast<uint32_t*>(wsb + w.pair_idx);
+  a.stats = stats;
   a.dk = dk;
   a.dv = dv;
   a.g_sb = s.sb;
@@ -289,12 +295,11 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
-  if (launch_attn_bwd(s, mq, mk, mv, mdo, a, cs) != cudaSuccess) return SA2_ERR_CUDA;
+  if (launch_attn_bwd(s, mq64, mk, mv, mdo64, a, cs) != cudaSuccess) return SA2_ERR_CUDA;
   DqArgs g;
   g.row_cnt = mask->row_cnt;
   g.row_idx = mask->row_idx;
-  g.lse = lse;
-  g.Dvec = Dvec;
+  g.stats = stats;
   g.dq = dq;
   g.g_sb = s.sb;
   g.g_sh = s.sh;

@@ -14,7 +14,9 @@ namespace sa2 {
 constexpr size_t kMaxDynSmem = 227 * 1024;
 
 // Launch profiler (profiler.cu): kernel ids and the brackets every launch wrapper calls.
-enum KernelId { kPool = 0, kScoreSelect, kCsc, kToF16, kAttnFwd, kBwdPre, kAttnBwd, kAttnBwdDq, kNumKernelIds };
+enum KernelId {
+  kPool = 0, kScoreSelect, kCsc, kToF16, kAttnFwd, kBwdPre, kAttnBwd, kAttnBwdDq, kBwdPairs, kNumKernelIds
+};
 void prof_start(cudaStream_t st, int id);
 void prof_stop(cudaStream_t st, int id);
 
@@ -72,11 +74,18 @@ struct FwdArgs {
 cudaError_t launch_attn_fwd(const ShapeArgs& s, bool s_f16, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st);
 
+// Per-row statistics of the backward, one record per 64-row query sub-tile:
+// stats[(bh * Tsub + r) * 128 + i] = log2(e) * LSE of row 64 r + i (+inf past N), and
+// stats[... + 64 + i] = D of that row (0 past N), with Tsub = Tq * bq / 64.
+inline int64_t bwd_stats_floats(const ShapeArgs& s) { return (int64_t)s.B * s.H * s.Tq * (s.bq / 64) * 128; }
+
 struct BwdArgs {
-  const int32_t* col_cnt;
+  const int32_t* col_cnt;  // mask column lists: input of the pair-union pass
   const int32_t* col_idx;
-  const float* lse;   // [B, H, N]
-  const float* Dvec;  // [B, H, N] rowsum(dO * O)
+  int32_t* pair_cnt;       // [B*H, ceil(Tk/2)] union lengths (workspace)
+  uint32_t* pair_idx;      // [B*H, ceil(Tk/2), Tq] union entries: q block | bit 30 kept by
+                           // block 2m | bit 31 kept by block 2m+1 (workspace)
+  const float* stats;      // per-row statistics, layout above
   void* dk;
   void* dv;
   int64_t g_sb, g_sh, g_sn;  // strides of dk / dv (dtype of the call)
@@ -88,8 +97,7 @@ struct BwdArgs {
 struct DqArgs {
   const int32_t* row_cnt;
   const int32_t* row_idx;
-  const float* lse;
-  const float* Dvec;
+  const float* stats;
   void* dq;
   int64_t g_sb, g_sh, g_sn;
   float scale;
@@ -97,9 +105,13 @@ struct DqArgs {
   unsigned* status;
 };
 
-// dO -> fp16 copy and D = rowsum(dO * (O + O_lo)) in one pass (attn_common.cu).
-cudaError_t launch_do_prep(const ShapeArgs& s, const void* dO, const void* o, const void* o_lo, __half* dO16,
-                           float* Dvec, unsigned* status, cudaStream_t st);
+// Entries of BwdArgs::pair_idx.
+size_t bwd_pair_entries(const ShapeArgs& s);
+
+// dO -> fp16 copy, D = rowsum(dO * (O + O_lo)) and log2(e) * LSE into the per-row
+// statistics, in one pass (attn_common.cu).
+cudaError_t launch_do_prep(const ShapeArgs& s, const void* dO, const void* o, const void* o_lo, const float* lse,
+                           __half* dO16, float* stats, unsigned* status, cudaStream_t st);
 cudaError_t launch_attn_bwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_attn_bwd_dq(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk,

@@ -175,23 +175,27 @@ sa2_status sa2_attn_fwd(const sa2_shape* shape, const void* q, const void* k, co
                         void* ws, size_t ws_bytes, void* stream);
 
 /*
- * Bytes of device workspace sa2_attn_bwd needs: the fp32 dQ accumulator [B, H, N, d],
- * D = rowsum(dO * O) [B, H, N], and fp16 copies of q, k, v and dO.
+ * Bytes of device workspace sa2_attn_bwd needs: per-row statistics (log2(e) * LSE and
+ * D = rowsum(dO * O), padded to whole 64-row query sub-tiles), the merged column lists of
+ * each pair of adjacent key blocks ([B, H, ceil(Tk/2), Tq] uint32 plus their lengths), and
+ * fp16 copies of q, k, v and dO.
  */
 size_t sa2_bwd_workspace_size(const sa2_shape* shape);
 
 /*
  * sa2_attn_bwd -- backward of sa2_attn_fwd with the block mask held fixed.
  * The abstract of the paper (shd-paper.top, fugumt.com and thelatestinai.com pages),
- * contribution (ii): "an efficient trainable sparse attention implementation"; the pages
- * do not spell the backward out, so this is the gradient of the forward above:
+ * contribution (ii), makes the sparse attention trainable; the pages do not spell the
+ * backward out, so this is the gradient of the forward above:
  *   P = exp(s - LSE),  dV = P^T dO,  dP = dO V^T,  D_a = dO_a . O_a,
  *   dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q,
  * over kept tiles only.  Rows with LSE = -inf contribute nothing.
  *
  * Every product runs on the tensor cores in fp16 (q, k, v, dO converted; P and dS written
  * in fp16, which keeps 11 significant bits where the rows of dS cancel in dQ = dS K) with
- * fp32 accumulation; dQ is accumulated across key blocks in fp32.
+ * fp32 accumulation in tensor memory: dK and dV per pair of key blocks across its query
+ * blocks, dQ per query block across its key blocks, so no output is reduced across CTAs
+ * and the result does not depend on scheduling.
  *
  *   q, k, v, o, dO  token tensors (o, o_lo and lse from sa2_attn_fwd); dq, dk, dv outputs
  *   o_lo      optional residual of O from sa2_attn_fwd (NULL: D uses O alone)
