@@ -16,19 +16,23 @@
 //   dV  += P^T dO_u   M = 128 keys, N = d, K = 64 queries   (A = P^T from TMEM)
 //   dK  += dS^T Q_u   M = 128, N = d, K = 64                 (A = dS^T from TMEM)
 // so P^T and dS^T never go through shared memory: the element-wise warps read S^T and dP^T
-// out of TMEM, and write P^T and dS^T back over them as fp16.  For a query block kept by
+// out of TMEM and write P^T and dS^T back into TMEM as fp16.  For a query block kept by
 // only one of the two key blocks the other block's 64 key rows get P = 0 (a warp-uniform
 // choice: they are whole warps), which is the price of the pairing -- about a fifth more
 // MMA work on the Wan-like masks -- against a tensor-core step that is twice as wide.
 //
-// TMEM (512 columns): S^T / P^T double-buffered (2 x 64), dP^T / dS^T double-buffered
-// (2 x 64), dV and dK accumulators (128 each, lanes = keys, columns = channels).
+// TMEM (512 columns): S^T and dP^T (64 columns each, single), P^T and dS^T as fp16 pairs
+// (32 columns each, double-buffered), dV and dK accumulators (128 each, lanes = keys,
+// columns = channels).  S^T / dP^T are free again as soon as the element-wise warps hold
+// them in registers, so the next sub-tile's S^T, dP^T MMAs never wait for the dV, dK
+// MMAs to complete: the tensor pipe runs S/dP(u+1) behind dV/dK(u-1) without draining.
 // Shared memory: K and V of the pair (32 KB each) and a 4-deep ring of query sub-tiles
 // (Q 16 KB, dO 16 KB, and the sub-tile's log2(e)*LSE and D vectors, 512 B).
 //
 // Roles (320 threads, 1 CTA per SM): warp 0 TMA producer, warp 1 TMEM owner and MMA
-// issuer, warps 2..9 element-wise (thread = key row; warps 2-5 take query columns 0-31 of
-// the sub-tile, warps 6-9 columns 32-63), then the dK / dV epilogue.
+// issuer (converged, one elect.sync lane issuing), warps 2..9 element-wise (thread = key
+// row; warps 2-5 take query columns 0-31 of the sub-tile, warps 6-9 columns 32-63), then
+// the dK / dV epilogue.
 //
 // All operands are fp16: the call's Q, K, V, dO arrive as fp16 copies (exact for bf16
 // inputs within the fp16 range) and P, dS are written as fp16, which keeps 11 significant
@@ -46,8 +50,10 @@ constexpr int kThreads = 320;
 constexpr int kStages = 4;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns
-constexpr uint32_t kColS = 0;     // 2 x 64: S^T, then P^T (fp16 pairs) in place
-constexpr uint32_t kColDP = 128;  // 2 x 64: dP^T, then dS^T in place
+constexpr uint32_t kColS = 0;     // 64: S^T
+constexpr uint32_t kColDP = 64;   // 64: dP^T
+constexpr uint32_t kColP = 128;   // 2 x 32: P^T, fp16 pairs
+constexpr uint32_t kColDS = 192;  // 2 x 32: dS^T, fp16 pairs
 constexpr uint32_t kColDV = 256;  // 128
 constexpr uint32_t kColDK = 384;  // 128
 
@@ -66,12 +72,6 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// Shared-memory descriptor offsets (16-byte units) of k-step kk (16 channels) in a
-// K-major 128-byte-swizzled tile with `rows` rows per channel panel.
-__device__ __forceinline__ constexpr uint64_t kstep_off(int kk, int rows) {
-  return (uint64_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
 }
 
 template <typename GT>
@@ -132,9 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_kv = smem_u32(&bars[0]);
   auto bar_full = [&](int st) { return smem_u32(&bars[1 + st]); };
   auto bar_empty = [&](int st) { return smem_u32(&bars[5 + st]); };
-  auto bar_sfull = [&](int b) { return smem_u32(&bars[9 + b]); };
-  auto bar_pready = [&](int b) { return smem_u32(&bars[11 + b]); };
-  auto bar_bfree = [&](int b) { return smem_u32(&bars[13 + b]); };  // MMAs reading buffer b done
+  const uint32_t bar_sfull = smem_u32(&bars[9]);   // S^T, dP^T of the current sub-tile in TMEM
+  const uint32_t bar_sfree = smem_u32(&bars[10]);  // ... and read out by the element-wise warps
+  auto bar_pready = [&](int b) { return smem_u32(&bars[11 + b]); };  // P^T, dS^T buffer b written
+  auto bar_pfree = [&](int b) { return smem_u32(&bars[13 + b]); };   // MMAs reading buffer b done
   const uint32_t bar_drain = smem_u32(&bars[15]);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 192);
@@ -165,10 +166,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_full(st), 1);
       mbar_init(bar_empty(st), 1);
     }
+    mbar_init(bar_sfull, 1);
+    mbar_init(bar_sfree, 256);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_sfull(i), 1);
       mbar_init(bar_pready(i), 256);
-      mbar_init(bar_bfree(i), 1);
+      mbar_init(bar_pfree(i), 1);
     }
     mbar_init(bar_drain, 1);
     fence_barrier_init();
@@ -231,52 +233,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------------- MMA issuer
-    if (lane == 0 && nsub > 0) {
+    if (nsub > 0) {  // the whole warp runs the loop; one elected lane issues
       constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
       constexpr uint32_t idG = idesc_f16_f32(128, 128, false, true);
       const uint64_t kd = smem_desc(sbase + kOffK, 16, 1024), vd = smem_desc(sbase + kOffV, 16, 1024);
-      bool ok = mbar_wait(bar_kv, 0, abort_flag);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar_kv, 0, abort_flag));
       for (int u = 0; ok && u <= nsub; ++u) {
         if (u < nsub) {
-          const int st = u & (kStages - 1), bb = u & 1;
-          if (!mbar_wait(bar_full(st), (u >> 2) & 1, abort_flag)) break;
-          // buffer bb was last read by the dV / dK MMAs of sub-tile u - 2
-          if (u >= 2 && !mbar_wait(bar_bfree(bb), ((u >> 1) - 1) & 1, abort_flag)) break;
+          const int st = u & (kStages - 1);
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (u >> 2) & 1, abort_flag))) break;
+          // S^T / dP^T of sub-tile u - 1 must have been read out of TMEM
+          if (u >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_sfree, (u - 1) & 1, abort_flag))) break;
           tc_fence_after();
           const uint32_t stg = sbase + kOffStage + st * kStageBytes;
           const uint64_t qd = smem_desc(stg + kStageQ, 16, 1024), dod = smem_desc(stg + kStageDO, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss(tmem + kColS + bb * 64, kd + kstep_off(kk, 128), qd + kstep_off(kk, 64), idS, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss(tmem + kColDP + bb * 64, vd + kstep_off(kk, 128), dod + kstep_off(kk, 64), idS, kk > 0);
-          umma_commit(bar_sfull(bb));
+          if (elect_one()) {
+            mma_ss_kmajor<idS, 128, 64, 8>(tmem + kColS, kd, qd);
+            mma_ss_kmajor<idS, 128, 64, 8>(tmem + kColDP, vd, dod);
+            umma_commit(bar_sfull);
+          }
+          __syncwarp();
         }
         if (u >= 1) {
           const int w = u - 1;
           const int st = w & (kStages - 1), bb = w & 1;
-          if (!mbar_wait(bar_pready(bb), (w >> 1) & 1, abort_flag)) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (w >> 1) & 1, abort_flag))) break;
           tc_fence_after();
           const uint32_t stg = sbase + kOffStage + st * kStageBytes;
           // B = dO_w / Q_w read MN-major: 16 query rows (2048 B) per k-step, channel panels
-          // 8 KB apart
+          // 8 KB apart; A = P^T / dS^T of buffer bb, 8 columns (16 queries) per k-step
           const uint64_t dod = smem_desc(stg + kStageDO, 8192, 1024), qd = smem_desc(stg + kStageQ, 8192, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t col = bb * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
-            umma_ts(tmem + kColDV, tmem + kColS + col, dod + (uint64_t)(kk * 128), idG, (w > 0 || kk > 0) ? 1u : 0u);
+          if (elect_one()) {
+            mma_ts_bmn<idG, 4>(tmem + kColDV, tmem + kColP + bb * 32, dod, w == 0);
+            mma_ts_bmn<idG, 4>(tmem + kColDK, tmem + kColDS + bb * 32, qd, w == 0);
+            umma_commit(bar_empty(st));
+            umma_commit(bar_pfree(bb));
           }
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t col = bb * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
-            umma_ts(tmem + kColDK, tmem + kColDP + col, qd + (uint64_t)(kk * 128), idG, (w > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(bar_empty(st));
-          umma_commit(bar_bfree(bb));
+          __syncwarp();
         }
       }
-      umma_commit(bar_drain);
+      if (elect_one()) umma_commit(bar_drain);
+      __syncwarp();
       mbar_wait(bar_drain, 0, abort_flag);
     }
   } else {
@@ -299,19 +296,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool keep = ((e >> (30 + half)) & 1u) != 0;  // same for the whole warp
       const int st = u & (kStages - 1), bb = u & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bb), (u >> 1) & 1, abort_flag) &&
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull, u & 1, abort_flag) &&
                                        mbar_wait(bar_full(st), (u >> 2) & 1, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sv[32], dv[32];
-      tmem_ld32(trow + kColS + bb * 64 + 32 * g, sv);
-      tmem_ld32(trow + kColDP + bb * 64 + 32 * g, dv);
+      tmem_ld32(trow + kColS + 32 * g, sv);
+      tmem_ld32(trow + kColDP + 32 * g, dv);
       const float4* l4 = reinterpret_cast<const float4*>(smem + kOffStage + st * kStageBytes + kStageStats) + 8 * g;
       const float4* d4 = l4 + 16;
       tmem_ld_wait(sv);
       tmem_ld_wait(dv);
+      tc_fence_before();
+      mbar_arrive(bar_sfree);
       uint32_t pw[16], dw[16];
       if (keep) {
 #pragma unroll
@@ -335,8 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) pw[j] = dw[j] = 0u;
       }
-      tmem_st16(trow + kColS + bb * 64 + 32 * g, pw);
-      tmem_st16(trow + kColDP + bb * 64 + 32 * g, dw);
+      // buffer bb was last read by the dV / dK MMAs of sub-tile u - 2
+      if (u >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_pfree(bb), ((u >> 1) - 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st16(trow + kColP + bb * 32 + 16 * g, pw);
+      tmem_st16(trow + kColDS + bb * 32 + 16 * g, dw);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_pready(bb));

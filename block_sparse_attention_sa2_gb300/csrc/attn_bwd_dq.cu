@@ -162,49 +162,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = vfirst; j < nkv; ++j) mbar_wait(bar_vfull(j % kVStages), (j / kVStages) & 1, abort_flag);
     }
   } else if (warp == 1) {
-    // -------------------------------------------------------------------- MMA issuer
-    if (lane == 0 && nkv > 0) {
+    // ------------------------------------------------- MMA issuer (whole warp, one lane issues)
+    if (nkv > 0) {
       constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
       constexpr uint32_t idQ = idesc_f16_f32(128, D, false, true);
-      bool ok = mbar_wait(bar_q, 0, abort_flag);
+      const uint64_t qd = smem_desc(sbase + L::kOffQ, 16, 1024), dod = smem_desc(sbase + L::kOffDO, 16, 1024);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag));
       for (int j = 0; ok && j <= nkv; ++j) {
         if (j < nkv) {
           const int ks = j % kKStages, vs = j % kVStages, bb = j & 1;
-          if (!mbar_wait(bar_kfull(ks), (j / kKStages) & 1, abort_flag)) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_kfull(ks), (j / kKStages) & 1, abort_flag))) break;
           // S_j overwrites the TMEM buffer whose dS_{j-2} the MMA dQ += dS_{j-2} K_{j-2}
           // read: a later tcgen05.mma is not ordered after an earlier one's TMEM operand
           // reads, so wait for that MMA (its commit releases K_{j-2})
-          if (j >= 2 && !mbar_wait(bar_kempty((j - 2) % kKStages), ((j - 2) / kKStages) & 1, abort_flag)) break;
+          if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_kempty((j - 2) % kKStages),
+                                                           ((j - 2) / kKStages) & 1, abort_flag)))
+            break;
           tc_fence_after();
-          const uint32_t kbase = sbase + L::kOffK + ks * L::kKVBytes;
-          const uint32_t vbase = sbase + L::kOffV + vs * L::kKVBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + kColS + bb * 64, smem_desc(sbase + L::kOffQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
-                    smem_desc(kbase + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024), idS, kk > 0);
-          if (!mbar_wait(bar_vfull(vs), (j / kVStages) & 1, abort_flag)) break;
+          const uint64_t kd = smem_desc(sbase + L::kOffK + ks * L::kKVBytes, 16, 1024);
+          const uint64_t vd = smem_desc(sbase + L::kOffV + vs * L::kKVBytes, 16, 1024);
+          if (elect_one()) mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qd, kd);
+          __syncwarp();
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_vfull(vs), (j / kVStages) & 1, abort_flag))) break;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + kColDP + bb * 64, smem_desc(sbase + L::kOffDO + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
-                    smem_desc(vbase + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024), idS, kk > 0);
-          umma_commit(bar_sfull(bb));
-          umma_commit(bar_vempty(vs));
+          if (elect_one()) {
+            mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColDP + bb * 64, dod, vd);
+            umma_commit(bar_sfull(bb));
+            umma_commit(bar_vempty(vs));
+          }
+          __syncwarp();
         }
         if (j >= 1) {
           const int jj = j - 1, ks = jj % kKStages, bb = jj & 1;
-          if (!mbar_wait(bar_pfull(bb), (jj >> 1) & 1, abort_flag)) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_pfull(bb), (jj >> 1) & 1, abort_flag))) break;
           tc_fence_after();
-          const uint32_t kbase = sbase + L::kOffK + ks * L::kKVBytes;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_ts(tmem + kColDQ, tmem + kColS + bb * 64 + kk * 8, smem_desc(kbase + kk * 2048, 8192, 1024), idQ,
-                    (jj > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar_kempty(ks));
+          // K as the MN-major B operand: N = D (64-element groups 8 KB apart), K = 16 keys
+          const uint64_t kmn = smem_desc(sbase + L::kOffK + ks * L::kKVBytes, 8192, 1024);
+          if (elect_one()) {
+            mma_ts_bmn<idQ, 4>(tmem + kColDQ, tmem + kColS + bb * 64, kmn, jj == 0);
+            umma_commit(bar_kempty(ks));
+          }
+          __syncwarp();
         }
       }
-      umma_commit(bar_dq);
-      umma_commit(bar_drain);
+      if (elect_one()) {
+        umma_commit(bar_dq);
+        umma_commit(bar_drain);
+      }
+      __syncwarp();
       mbar_wait(bar_drain, 0, abort_flag);
     }
   } else {

@@ -179,50 +179,52 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   } else if (warp == 1) {
-    // -------------------------------------------------------------------- MMA issuer
-    if (lane == 0 && nkv > 0) {
+    // ------------------------------------------------- MMA issuer (whole warp, one lane issues)
+    if (nkv > 0) {
       constexpr uint32_t idS = idesc_f32acc(128, 64, false, false, !S_F16);
       constexpr uint32_t idO = idesc_f16_f32(128, D, false, true);
-      bool ok = mbar_wait(bar_q, 0, abort_flag);
+      const uint64_t qd = smem_desc(sbase + L::kOffQ, 16, 1024);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag));
       for (int j = 0; ok && j <= nkv; ++j) {
         if (j < nkv) {
           const int st = j % kNumStages;
-          if (!mbar_wait(bar_kfull(st), (j / kNumStages) & 1, abort_flag)) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_kfull(st), (j / kNumStages) & 1, abort_flag))) break;
           // S_j overwrites the TMEM buffer whose P_{j-2} the MMA P_{j-2} V_{j-2} read: a
           // later tcgen05.mma is not ordered after an earlier one's TMEM operand reads, so
           // wait for that MMA to complete (its commit also releases V_{j-2}; buffer and
           // V stage have the same index, both rings being 2 deep)
-          if (j >= 2 && !mbar_wait(bar_vempty(st), ((j - 2) / kNumStages) & 1, abort_flag)) break;
+          if (j >= 2 &&
+              !__all_sync(0xffffffffu, mbar_wait(bar_vempty(st), ((j - 2) / kNumStages) & 1, abort_flag)))
+            break;
           tc_fence_after();
-          const uint32_t kbase = sbase + L::kOffK + st * L::kKVBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t adesc = smem_desc(sbase + L::kOffQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc(kbase + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024);
-            umma_ss(tmem + (j & 1) * 64, adesc, bdesc, idS, kk > 0);
+          const uint64_t kd = smem_desc(sbase + L::kOffK + st * L::kKVBytes, 16, 1024);
+          if (elect_one()) {
+            mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + (j & 1) * 64, qd, kd);
+            umma_commit(bar_sfull(j & 1));
+            umma_commit(bar_kempty(st));
           }
-          umma_commit(bar_sfull(j & 1));
-          umma_commit(bar_kempty(st));
+          __syncwarp();
         }
         if (j >= 1) {
           const int jj = j - 1;
           const int st = jj % kNumStages;
-          if (!mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, abort_flag)) break;
-          if (!mbar_wait(bar_vfull(st), (jj / kNumStages) & 1, abort_flag)) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, abort_flag) &&
+                                           mbar_wait(bar_vfull(st), (jj / kNumStages) & 1, abort_flag)))
+            break;
           tc_fence_after();
-          const uint32_t vbase = sbase + L::kOffV + st * L::kKVBytes;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // V as the MN-major B operand: N = D (64-element groups 8 KB apart), K = 16 rows
-            const uint64_t bdesc = smem_desc(vbase + kk * 2048, 8192, 1024);
-            umma_ts(tmem + kColO, tmem + (jj & 1) * 64 + kk * 8, bdesc, idO, (jj > 0 || kk > 0) ? 1u : 0u);
+          // V as the MN-major B operand: N = D (64-element groups 8 KB apart), K = 16 rows
+          const uint64_t vd = smem_desc(sbase + L::kOffV + st * L::kKVBytes, 8192, 1024);
+          if (elect_one()) {
+            mma_ts_bmn<idO, 4>(tmem + kColO, tmem + (jj & 1) * 64, vd, jj == 0);
+            umma_commit(bar_vempty(st));
+            umma_commit(bar_odone);
           }
-          umma_commit(bar_vempty(st));
-          umma_commit(bar_odone);
+          __syncwarp();
         }
       }
-      // every MMA issued by this thread has completed before TMEM is released
-      umma_commit(bar_drain);
+      // every MMA issued by this warp has completed before TMEM is released
+      if (elect_one()) umma_commit(bar_drain);
+      __syncwarp();
       mbar_wait(bar_drain, 0, abort_flag);
     }
   } else {

@@ -172,6 +172,29 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// Descriptor offset (16-byte units) of k-step kk (16 elements of 2 bytes) in a K-major
+// 128-byte-swizzled tile whose channel panels hold `rows` rows each.
+__host__ __device__ constexpr uint64_t kmajor_kstep(int kk, int rows) {
+  return (uint64_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
+}
+
+// The k-steps of one product, unrolled at compile time so every descriptor offset and
+// accumulate flag is an immediate and the MMAs issue back to back.
+// SS form, A and B K-major (A_ROWS / B_ROWS rows per channel panel); the first k-step
+// overwrites D.
+template <uint32_t IDESC, int A_ROWS, int B_ROWS, int KSTEPS, int KK = 0>
+__device__ __forceinline__ void mma_ss_kmajor(uint32_t d, uint64_t a, uint64_t b) {
+  umma_ss(d, a + kmajor_kstep(KK, A_ROWS), b + kmajor_kstep(KK, B_ROWS), IDESC, KK > 0 ? 1u : 0u);
+  if constexpr (KK + 1 < KSTEPS) mma_ss_kmajor<IDESC, A_ROWS, B_ROWS, KSTEPS, KK + 1>(d, a, b);
+}
+// TS form: A from TMEM (8 columns of fp16 pairs per k-step), B MN-major with 16 rows
+// (2048 bytes) per k-step.  The first k-step overwrites D when `fresh`, else accumulates.
+template <uint32_t IDESC, int KSTEPS, int KK = 0>
+__device__ __forceinline__ void mma_ts_bmn(uint32_t d, uint32_t a, uint64_t b, bool fresh) {
+  umma_ts(d, a + KK * 8, b + (uint64_t)(KK * 128), IDESC, KK > 0 ? 1u : (fresh ? 0u : 1u));
+  if constexpr (KK + 1 < KSTEPS) mma_ts_bmn<IDESC, KSTEPS, KK + 1>(d, a, b, fresh);
+}
+
 // Arrive (once) on an mbarrier when every tcgen05 operation issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -237,5 +260,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ int elect_lane0() { return (threadIdx.x & 31) == 0; }
+
+// elect.sync: true in exactly one lane of a converged warp.  tcgen05.mma issued this way,
+// with the whole warp running the issuing loop, issues markedly faster than from a lane
+// the rest of its warp has branched away from.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}\n" : "=r"(pred));
+  return pred != 0;
+}
 
 }  // namespace sa2
