@@ -29,10 +29,11 @@
 // Shared memory: K and V of the pair (32 KB each) and a 4-deep ring of query sub-tiles
 // (Q 16 KB, dO 16 KB, and the sub-tile's log2(e)*LSE and D vectors, 512 B).
 //
-// Roles (320 threads, 1 CTA per SM): warp 0 TMA producer, warp 1 TMEM owner and MMA
-// issuer (converged, one elect.sync lane issuing), warps 2..9 element-wise (thread = key
-// row; warps 2-5 take query columns 0-31 of the sub-tile, warps 6-9 columns 32-63), then
-// the dK / dV epilogue.
+// Roles (352 threads, 1 CTA per SM): warp 0 TMA producer, warp 1 TMEM owner and issuer
+// of the S^T / dP^T MMAs, warp 2 issuer of the dV / dK MMAs (each converged, one
+// elect.sync lane issuing), warps 3..10 element-wise (thread = key row; warps 3-6 take
+// query columns 0-31 of the sub-tile, warps 7-10 columns 32-63), then the dK / dV
+// epilogue.
 //
 // All operands are fp16: the call's Q, K, V, dO arrive as fp16 copies (exact for bf16
 // inputs within the fp16 range) and P, dS are written as fp16, which keeps 11 significant
@@ -46,7 +47,7 @@
 namespace sa2 {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kStages = 4;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns
@@ -136,8 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_sfree = smem_u32(&bars[10]);  // ... and read out by the element-wise warps
   auto bar_pready = [&](int b) { return smem_u32(&bars[11 + b]); };  // P^T, dS^T buffer b written
   auto bar_pfree = [&](int b) { return smem_u32(&bars[13 + b]); };   // MMAs reading buffer b done
-  const uint32_t bar_drain = smem_u32(&bars[15]);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 128);
+  const uint32_t bar_drain = smem_u32(&bars[15]);   // every dV / dK MMA completed
+  const uint32_t bar_sdrain = smem_u32(&bars[16]);  // every S^T / dP^T MMA completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 160);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 192);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -173,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_pfree(i), 1);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_sdrain, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -232,46 +235,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // -------------------------------------------------------------------- MMA issuer
-    if (nsub > 0) {  // the whole warp runs the loop; one elected lane issues
+    // ------------------------------------------------------- S^T, dP^T issuer (warp 1)
+    // The whole warp runs the loop and one elected lane issues.  tcgen05.mma issue stalls
+    // while the MMA queue is full, so a single issuer that also waits on barriers between
+    // its groups lets the tensor pipe drain; with S/dP and dV/dK issued by two warps, one
+    // of them is always queued behind the other's MMAs.
+    if (nsub > 0) {
       constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
-      constexpr uint32_t idG = idesc_f16_f32(128, 128, false, true);
       const uint64_t kd = smem_desc(sbase + kOffK, 16, 1024), vd = smem_desc(sbase + kOffV, 16, 1024);
       bool ok = __all_sync(0xffffffffu, mbar_wait(bar_kv, 0, abort_flag));
-      for (int u = 0; ok && u <= nsub; ++u) {
-        if (u < nsub) {
-          const int st = u & (kStages - 1);
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (u >> 2) & 1, abort_flag))) break;
-          // S^T / dP^T of sub-tile u - 1 must have been read out of TMEM
-          if (u >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_sfree, (u - 1) & 1, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t stg = sbase + kOffStage + st * kStageBytes;
-          const uint64_t qd = smem_desc(stg + kStageQ, 16, 1024), dod = smem_desc(stg + kStageDO, 16, 1024);
-          if (elect_one()) {
-            mma_ss_kmajor<idS, 128, 64, 8>(tmem + kColS, kd, qd);
-            mma_ss_kmajor<idS, 128, 64, 8>(tmem + kColDP, vd, dod);
-            umma_commit(bar_sfull);
-          }
-          __syncwarp();
+      for (int u = 0; ok && u < nsub; ++u) {
+        const int st = u & (kStages - 1);
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (u >> 2) & 1, abort_flag))) break;
+        // S^T / dP^T of sub-tile u - 1 must have been read out of TMEM
+        if (u >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_sfree, (u - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t stg = sbase + kOffStage + st * kStageBytes;
+        const uint64_t qd = smem_desc(stg + kStageQ, 16, 1024), dod = smem_desc(stg + kStageDO, 16, 1024);
+        if (elect_one()) {
+          mma_ss_kmajor<idS, 128, 64, 8>(tmem + kColS, kd, qd);
+          mma_ss_kmajor<idS, 128, 64, 8>(tmem + kColDP, vd, dod);
+          umma_commit(bar_sfull);
         }
-        if (u >= 1) {
-          const int w = u - 1;
-          const int st = w & (kStages - 1), bb = w & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (w >> 1) & 1, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t stg = sbase + kOffStage + st * kStageBytes;
-          // B = dO_w / Q_w read MN-major: 16 query rows (2048 B) per k-step, channel panels
-          // 8 KB apart; A = P^T / dS^T of buffer bb, 8 columns (16 queries) per k-step
-          const uint64_t dod = smem_desc(stg + kStageDO, 8192, 1024), qd = smem_desc(stg + kStageQ, 8192, 1024);
-          if (elect_one()) {
-            mma_ts_bmn<idG, 4>(tmem + kColDV, tmem + kColP + bb * 32, dod, w == 0);
-            mma_ts_bmn<idG, 4>(tmem + kColDK, tmem + kColDS + bb * 32, qd, w == 0);
-            umma_commit(bar_empty(st));
-            umma_commit(bar_pfree(bb));
-          }
-          __syncwarp();
-        }
+        __syncwarp();
       }
+      // no MMA of this warp may still run when TMEM is released (matters on the abort path)
+      if (elect_one()) umma_commit(bar_sdrain);
+      __syncwarp();
+      mbar_wait(bar_sdrain, 0, abort_flag);
+    }
+  } else if (warp == 2) {
+    // --------------------------------------------------------- dV, dK issuer (warp 2)
+    if (nsub > 0) {
+      constexpr uint32_t idG = idesc_f16_f32(128, 128, false, true);
+      for (int w = 0; w < nsub; ++w) {
+        const int st = w & (kStages - 1), bb = w & 1;
+        // P^T / dS^T of sub-tile w written (the stage's load completed long before)
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (w >> 1) & 1, abort_flag) &&
+                                         mbar_wait(bar_full(st), (w >> 2) & 1, abort_flag)))
+          break;
+        tc_fence_after();
+        const uint32_t stg = sbase + kOffStage + st * kStageBytes;
+        // B = dO_w / Q_w read MN-major: 16 query rows (2048 B) per k-step, channel panels
+        // 8 KB apart; A = P^T / dS^T of buffer bb, 8 columns (16 queries) per k-step
+        const uint64_t dod = smem_desc(stg + kStageDO, 8192, 1024), qd = smem_desc(stg + kStageQ, 8192, 1024);
+        if (elect_one()) {
+          mma_ts_bmn<idG, 4>(tmem + kColDV, tmem + kColP + bb * 32, dod, w == 0);
+          mma_ts_bmn<idG, 4>(tmem + kColDK, tmem + kColDS + bb * 32, qd, w == 0);
+          umma_commit(bar_empty(st));
+          umma_commit(bar_pfree(bb));
+        }
+        __syncwarp();
+      }
+      // the S^T / dP^T MMAs all completed before the last P^T was written, so this commit
+      // covers every MMA of the CTA
       if (elect_one()) umma_commit(bar_drain);
       __syncwarp();
       mbar_wait(bar_drain, 0, abort_flag);
@@ -279,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------- element-wise warps
     const int q4 = warp & 3;          // TMEM lane quarter
-    const int g = (warp - 2) >> 2;    // query columns 32g .. 32g+31 of each sub-tile
+    const int g = (warp - 3) >> 2;    // query columns 32g .. 32g+31 of each sub-tile
     const int r = 32 * q4 + lane;     // key row of the pair
     const int half = r >> 6;          // 0: key block 2m, 1: key block 2m+1
     const int key = m * 128 + r;
