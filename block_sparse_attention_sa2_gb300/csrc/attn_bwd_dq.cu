@@ -7,29 +7,34 @@
 // walks that block's list of kept key blocks -- the forward's traversal -- so dQ
 // accumulates in TMEM over the whole list and is written once: no cross-CTA reduction.
 //
-// Roles (320 threads, 1 CTA per SM): warp 0 TMA (Q and dO once, K_j / V_j per kept block
-// into 2 stages), warp 1 TMEM owner and MMA issuer, and two row warpgroups (warps 2..5 and
-// 6..9) that take the list entries in turn (entry j -> group j % 2, TMEM buffer j % 2), one
-// query row per thread, so that one group's exp / dS work overlaps the other's.
+// Roles (352 threads, 1 CTA per SM): warp 0 TMA (Q and dO once, K_j / V_j per kept block
+// into 4 / 2 stages), warp 1 TMEM owner and issuer of the S_j / dP_j MMAs, warp 2 issuer of
+// the dQ MMAs (each converged, one elect.sync lane issuing: two issuers keep the MMA queue
+// fed while either waits on a barrier), and two row warpgroups (warps 3..6 and 7..10) that
+// take the list entries in turn (entry j -> group j % 2, TMEM buffers j % 2), one query row
+// per thread, so that one group's exp / dS work overlaps the other's.
 // Per kept key block j:
 //   S_j  = Q K_j^T     M = 128, N = 64, K = d     (A, B K-major, fp16)
 //   dP_j = dO V_j^T    M = 128, N = 64, K = d     (A, B K-major, fp16)
 //   row threads: P = exp2(S * scale*log2e - LSE*log2e), dS = P (dP - D), dS as fp16 pairs
-//                written over S_j in TMEM
+//                into their own TMEM buffer
 //   dQ  += dS_j K_j    M = 128, N = d, K = 64     (A = dS from TMEM, B = K_j MN-major)
-// TMEM columns: S at 0 / 64, dP at 128 / 192 (double-buffered), dQ at 256 (d columns).
+// TMEM columns: S at 0 / 64, dP at 128 / 192, dS at 256 / 288 (all double-buffered), dQ at
+// 384 (d columns).  S_j / dP_j may overwrite their buffers as soon as the row threads have
+// read S_{j-2} / dP_{j-2} out; only the row threads wait for dQ_{j-2} to complete before
+// writing dS_j, so the tensor pipe never drains to let an MMA overwrite an operand.
 #include "sa2_internal.h"
 
 namespace sa2 {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 // K_j feeds S_j and, after the softmax, dQ += dS_j K_j, so its ring is deep; V_j only feeds
 // dP_j and is released right after it
 constexpr int kKStages = 4;
 constexpr int kVStages = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 384;
 
 template <int D>
 struct DqSmem {
@@ -82,11 +87,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_kempty = [&](int st) { return smem_u32(&bars[5 + st]); };
   auto bar_vfull = [&](int st) { return smem_u32(&bars[9 + st]); };
   auto bar_vempty = [&](int st) { return smem_u32(&bars[11 + st]); };
-  auto bar_sfull = [&](int b) { return smem_u32(&bars[13 + b]); };
-  auto bar_pfull = [&](int b) { return smem_u32(&bars[15 + b]); };
-  const uint32_t bar_dq = smem_u32(&bars[17]);
-  const uint32_t bar_drain = smem_u32(&bars[18]);
-  // 19 barriers occupy the first 152 bytes of the 256-byte barrier area
+  auto bar_sfull = [&](int b) { return smem_u32(&bars[13 + b]); };   // S_j, dP_j in TMEM
+  auto bar_sfree = [&](int b) { return smem_u32(&bars[15 + b]); };   // ... read out by the rows
+  auto bar_pready = [&](int b) { return smem_u32(&bars[17 + b]); };  // dS_j written
+  auto bar_pfree = [&](int b) { return smem_u32(&bars[19 + b]); };   // dQ MMA reading dS_j done
+  const uint32_t bar_dq = smem_u32(&bars[21]);
+  const uint32_t bar_drain = smem_u32(&bars[22]);
+  const uint32_t bar_sdrain = smem_u32(&bars[23]);
+  // 24 barriers occupy the first 192 bytes of the 256-byte barrier area
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 224);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffBar + 240);
 
@@ -115,10 +123,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int bb = 0; bb < 2; ++bb) {
       mbar_init(bar_sfull(bb), 1);
-      mbar_init(bar_pfull(bb), 128);
+      mbar_init(bar_sfree(bb), 128);
+      mbar_init(bar_pready(bb), 128);
+      mbar_init(bar_pfree(bb), 1);
     }
     mbar_init(bar_dq, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_sdrain, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -162,49 +173,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = vfirst; j < nkv; ++j) mbar_wait(bar_vfull(j % kVStages), (j / kVStages) & 1, abort_flag);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------- MMA issuer (whole warp, one lane issues)
+    // ------------------------------------------------------------ S_j, dP_j issuer
     if (nkv > 0) {
       constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
-      constexpr uint32_t idQ = idesc_f16_f32(128, D, false, true);
       const uint64_t qd = smem_desc(sbase + L::kOffQ, 16, 1024), dod = smem_desc(sbase + L::kOffDO, 16, 1024);
       bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag));
-      for (int j = 0; ok && j <= nkv; ++j) {
-        if (j < nkv) {
-          const int ks = j % kKStages, vs = j % kVStages, bb = j & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_kfull(ks), (j / kKStages) & 1, abort_flag))) break;
-          // S_j overwrites the TMEM buffer whose dS_{j-2} the MMA dQ += dS_{j-2} K_{j-2}
-          // read: a later tcgen05.mma is not ordered after an earlier one's TMEM operand
-          // reads, so wait for that MMA (its commit releases K_{j-2})
-          if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_kempty((j - 2) % kKStages),
-                                                           ((j - 2) / kKStages) & 1, abort_flag)))
-            break;
-          tc_fence_after();
-          const uint64_t kd = smem_desc(sbase + L::kOffK + ks * L::kKVBytes, 16, 1024);
-          const uint64_t vd = smem_desc(sbase + L::kOffV + vs * L::kKVBytes, 16, 1024);
-          if (elect_one()) mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qd, kd);
-          __syncwarp();
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_vfull(vs), (j / kVStages) & 1, abort_flag))) break;
-          tc_fence_after();
-          if (elect_one()) {
-            mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColDP + bb * 64, dod, vd);
-            umma_commit(bar_sfull(bb));
-            umma_commit(bar_vempty(vs));
-          }
-          __syncwarp();
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int ks = j % kKStages, vs = j % kVStages, bb = j & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_kfull(ks), (j / kKStages) & 1, abort_flag))) break;
+        // buffer bb held S_{j-2} / dP_{j-2}: the row threads must have read them out
+        if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_sfree(bb), ((j >> 1) - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint64_t kd = smem_desc(sbase + L::kOffK + ks * L::kKVBytes, 16, 1024);
+        const uint64_t vd = smem_desc(sbase + L::kOffV + vs * L::kKVBytes, 16, 1024);
+        if (elect_one()) mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qd, kd);
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_vfull(vs), (j / kVStages) & 1, abort_flag))) break;
+        tc_fence_after();
+        if (elect_one()) {
+          mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColDP + bb * 64, dod, vd);
+          umma_commit(bar_sfull(bb));
+          umma_commit(bar_vempty(vs));
         }
-        if (j >= 1) {
-          const int jj = j - 1, ks = jj % kKStages, bb = jj & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_pfull(bb), (jj >> 1) & 1, abort_flag))) break;
-          tc_fence_after();
-          // K as the MN-major B operand: N = D (64-element groups 8 KB apart), K = 16 keys
-          const uint64_t kmn = smem_desc(sbase + L::kOffK + ks * L::kKVBytes, 8192, 1024);
-          if (elect_one()) {
-            mma_ts_bmn<idQ, 4>(tmem + kColDQ, tmem + kColS + bb * 64, kmn, jj == 0);
-            umma_commit(bar_kempty(ks));
-          }
-          __syncwarp();
-        }
+        __syncwarp();
       }
+      // no MMA of this warp may still run when TMEM is released (matters on the abort path)
+      if (elect_one()) umma_commit(bar_sdrain);
+      __syncwarp();
+      mbar_wait(bar_sdrain, 0, abort_flag);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ dQ issuer
+    if (nkv > 0) {
+      constexpr uint32_t idQ = idesc_f16_f32(128, D, false, true);
+      for (int j = 0; j < nkv; ++j) {
+        const int ks = j % kKStages, bb = j & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (j >> 1) & 1, abort_flag) &&
+                                         mbar_wait(bar_kfull(ks), (j / kKStages) & 1, abort_flag)))
+          break;
+        tc_fence_after();
+        // K as the MN-major B operand: N = D (64-element groups 8 KB apart), K = 16 keys
+        const uint64_t kmn = smem_desc(sbase + L::kOffK + ks * L::kKVBytes, 8192, 1024);
+        if (elect_one()) {
+          mma_ts_bmn<idQ, 4>(tmem + kColDQ, tmem + kColDS + bb * 32, kmn, j == 0);
+          umma_commit(bar_kempty(ks));
+          umma_commit(bar_pfree(bb));
+        }
+        __syncwarp();
+      }
+      // the S_j / dP_j MMAs all completed before the last dS was written, so these commits
+      // cover every MMA of the CTA
       if (elect_one()) {
         umma_commit(bar_dq);
         umma_commit(bar_drain);
@@ -214,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- query-row threads
-    const int wg = (warp - 2) >> 2;  // row warpgroup 0 or 1
+    const int wg = (warp - 3) >> 2;  // row warpgroup 0 or 1
     const int sub = warp & 3;
     const int r = 32 * sub + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * sub) << 16);
@@ -234,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
+      const int jn = j >> 1;  // this group's n-th entry
       tc_fence_after();
       kb = (kb < 0 || kb >= s.Tk) ? 0 : kb;
       const int kv_valid = min(64, s.N - kb * 64);
@@ -245,6 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(trow + kColDP + bb * 64 + half * 32, dv);
         tmem_ld_wait(sv);
         tmem_ld_wait(dv);
+        if (half == 1) {  // S_j / dP_j are in registers: their buffer may be overwritten
+          tc_fence_before();
+          mbar_arrive(bar_sfree(bb));
+        }
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float ds[2];
@@ -257,10 +280,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[half * 16 + c / 2] = pack_f16x2(ds[0], ds[1]);
         }
       }
-      tmem_st32(trow + kColS + bb * 64, pk);
+      // dS buffer bb was last read by the dQ MMA of entry j - 2
+      if (jn >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_pfree(bb), (jn - 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st32(trow + kColDS + bb * 32, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_pfull(bb));
+      mbar_arrive(bar_pready(bb));
     }
     // ---- epilogue: dQ = scale * (dS K) accumulated over the list; each group stores half
     // of the channels of every row
