@@ -5,11 +5,13 @@
 // skipped tiles cost neither matmul nor softmax.  Here each CTA owns one query block of
 // 128 rows and walks that block's list of kept 64-token key blocks.
 //
-// Roles (192 threads, 2 CTAs per SM):
+// Roles (224 threads, 2 CTAs per SM):
 //   warp 0      TMA producer: Q once, then K_j / V_j per kept key block into NS stages
-//   warp 1      TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into a double
-//               buffered TMEM tile, O += P_j V_j with P_j read from TMEM
-//   warps 2..5  softmax: each thread owns one query row (its TMEM lane); online softmax in
+//   warp 1      TMEM owner and issuer of S_j = Q K_j^T into a double-buffered TMEM tile
+//   warp 2      issuer of O += P_j V_j with P_j read from TMEM (two issuing warps, each
+//               converged with one elect.sync lane issuing, keep the MMA queue fed while
+//               either waits on a barrier)
+//   warps 3..6  softmax: each thread owns one query row (its TMEM lane); online softmax in
 //               fp32 with exp2, P_j (fp16) written back over S_j in TMEM; epilogue O / l
 //
 // Operand types: S = Q K^T in bf16 (bf16 calls) or fp16 (fp32 calls, whose inputs arrive
@@ -23,7 +25,7 @@
 namespace sa2 {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kNumStages = 2;  // also the number of S/P buffers in TMEM (the waits rely on it)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 128;
@@ -101,9 +103,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto bar_sfull = [&](int b) { return smem_u32(&bars[1 + 4 * kNumStages + b]); };
   auto bar_pfull = [&](int b) { return smem_u32(&bars[3 + 4 * kNumStages + b]); };
   const uint32_t bar_odone = smem_u32(&bars[5 + 4 * kNumStages]);
-  const uint32_t bar_drain = smem_u32(&bars[6 + 4 * kNumStages]);
-  // 15 barriers occupy the first 120 bytes of the 256-byte barrier area
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 128);
+  const uint32_t bar_drain = smem_u32(&bars[6 + 4 * kNumStages]);   // every P V MMA completed
+  const uint32_t bar_sdrain = smem_u32(&bars[7 + 4 * kNumStages]);  // every S MMA completed
+  // 16 barriers occupy the first 128 bytes of the 256-byte barrier area
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 160);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffBar + 192);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -133,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     mbar_init(bar_odone, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_sdrain, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -179,50 +183,56 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------- MMA issuer (whole warp, one lane issues)
+    // ------------------------------------------------------------------ S_j issuer
     if (nkv > 0) {
       constexpr uint32_t idS = idesc_f32acc(128, 64, false, false, !S_F16);
-      constexpr uint32_t idO = idesc_f16_f32(128, D, false, true);
       const uint64_t qd = smem_desc(sbase + L::kOffQ, 16, 1024);
       bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag));
-      for (int j = 0; ok && j <= nkv; ++j) {
-        if (j < nkv) {
-          const int st = j % kNumStages;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_kfull(st), (j / kNumStages) & 1, abort_flag))) break;
-          // S_j overwrites the TMEM buffer whose P_{j-2} the MMA P_{j-2} V_{j-2} read: a
-          // later tcgen05.mma is not ordered after an earlier one's TMEM operand reads, so
-          // wait for that MMA to complete (its commit also releases V_{j-2}; buffer and
-          // V stage have the same index, both rings being 2 deep)
-          if (j >= 2 &&
-              !__all_sync(0xffffffffu, mbar_wait(bar_vempty(st), ((j - 2) / kNumStages) & 1, abort_flag)))
-            break;
-          tc_fence_after();
-          const uint64_t kd = smem_desc(sbase + L::kOffK + st * L::kKVBytes, 16, 1024);
-          if (elect_one()) {
-            mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + (j & 1) * 64, qd, kd);
-            umma_commit(bar_sfull(j & 1));
-            umma_commit(bar_kempty(st));
-          }
-          __syncwarp();
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int st = j % kNumStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_kfull(st), (j / kNumStages) & 1, abort_flag))) break;
+        // S_j overwrites the TMEM buffer whose P_{j-2} the MMA P_{j-2} V_{j-2} read: a
+        // later tcgen05.mma is not ordered after an earlier one's TMEM operand reads, so
+        // wait for that MMA to complete (its commit also releases V_{j-2}; buffer and
+        // V stage have the same index, both rings being 2 deep)
+        if (j >= 2 &&
+            !__all_sync(0xffffffffu, mbar_wait(bar_vempty(st), ((j - 2) / kNumStages) & 1, abort_flag)))
+          break;
+        tc_fence_after();
+        const uint64_t kd = smem_desc(sbase + L::kOffK + st * L::kKVBytes, 16, 1024);
+        if (elect_one()) {
+          mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + (j & 1) * 64, qd, kd);
+          umma_commit(bar_sfull(j & 1));
+          umma_commit(bar_kempty(st));
         }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int st = jj % kNumStages;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, abort_flag) &&
-                                           mbar_wait(bar_vfull(st), (jj / kNumStages) & 1, abort_flag)))
-            break;
-          tc_fence_after();
-          // V as the MN-major B operand: N = D (64-element groups 8 KB apart), K = 16 rows
-          const uint64_t vd = smem_desc(sbase + L::kOffV + st * L::kKVBytes, 8192, 1024);
-          if (elect_one()) {
-            mma_ts_bmn<idO, 4>(tmem + kColO, tmem + (jj & 1) * 64, vd, jj == 0);
-            umma_commit(bar_vempty(st));
-            umma_commit(bar_odone);
-          }
-          __syncwarp();
-        }
+        __syncwarp();
       }
-      // every MMA issued by this warp has completed before TMEM is released
+      // no MMA of this warp may still run when TMEM is released (matters on the abort path)
+      if (elect_one()) umma_commit(bar_sdrain);
+      __syncwarp();
+      mbar_wait(bar_sdrain, 0, abort_flag);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- P_j V_j issuer
+    if (nkv > 0) {
+      constexpr uint32_t idO = idesc_f16_f32(128, D, false, true);
+      for (int jj = 0; jj < nkv; ++jj) {
+        const int st = jj % kNumStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, abort_flag) &&
+                                         mbar_wait(bar_vfull(st), (jj / kNumStages) & 1, abort_flag)))
+          break;
+        tc_fence_after();
+        // V as the MN-major B operand: N = D (64-element groups 8 KB apart), K = 16 rows
+        const uint64_t vd = smem_desc(sbase + L::kOffV + st * L::kKVBytes, 8192, 1024);
+        if (elect_one()) {
+          mma_ts_bmn<idO, 4>(tmem + kColO, tmem + (jj & 1) * 64, vd, jj == 0);
+          umma_commit(bar_vempty(st));
+          umma_commit(bar_odone);
+        }
+        __syncwarp();
+      }
+      // the S MMAs all completed before the last P was written: this commit covers every
+      // MMA of the CTA
       if (elect_one()) umma_commit(bar_drain);
       __syncwarp();
       mbar_wait(bar_drain, 0, abort_flag);
