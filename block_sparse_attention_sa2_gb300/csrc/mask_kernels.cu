@@ -132,6 +132,70 @@ __device__ __forceinline__ Predicate count_mass(const uint32_t* keys, int Tk, ui
   return p;
 }
 
+// Keys per lane held in registers by the selection when Tk <= 32 * kRegKeys.
+constexpr int kRegKeys = 40;
+
+// The hybrid selection of one row (one warp), with the row's keys and their fixed-point
+// masses in registers: the same bisection as the shared-memory path below, without its
+// loads.  Sets keep_all when the row's mass never reaches p; otherwise the threshold t and
+// the number of entries equal to t to take.
+__device__ __forceinline__ void select_in_registers(const uint32_t* keys, int Tk, const SelectArgs& sel,
+                                                    bool& keep_all, uint32_t& t, int& take) {
+  const int lane = threadIdx.x & 31;
+  uint32_t k[kRegKeys];
+  unsigned long long mf[kRegKeys];
+  unsigned long long msum = 0;
+#pragma unroll
+  for (int i = 0; i < kRegKeys; ++i) {
+    const int j = lane + 32 * i;
+    k[i] = j < Tk ? keys[j] : 0u;
+    mf[i] = mass_fix(k[i]);
+    msum += mf[i];
+  }
+  const bool use_mass = sel.p_mode == 0;
+  if (use_mass && warp_sum_u64(msum) < sel.p_fix) {
+    keep_all = true;
+    return;
+  }
+  // largest t with count(>= t) >= K and mass(>= t) >= p; the lanes' padding keys are 0 and
+  // every tested t is >= 1, so padding is never counted
+  uint32_t lo = 0, hi = 0x3F800001u;
+  while (hi - lo > 1) {
+    const uint32_t mid = lo + (hi - lo) / 2;
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < kRegKeys; ++i) c += k[i] >= mid ? 1u : 0u;
+    bool ok = __reduce_add_sync(0xffffffffu, c) >= (uint32_t)sel.K;  // same in every lane
+    if (ok && use_mass) {
+      unsigned long long m = 0;
+#pragma unroll
+      for (int i = 0; i < kRegKeys; ++i) m += k[i] >= mid ? mf[i] : 0ull;
+      ok = warp_sum_u64(m) >= sel.p_fix;
+    }
+    if (ok)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  t = lo;
+  uint32_t c = 0;
+  unsigned long long m = 0;
+#pragma unroll
+  for (int i = 0; i < kRegKeys; ++i) {
+    c += k[i] > t ? 1u : 0u;
+    m += k[i] > t ? mf[i] : 0ull;
+  }
+  c = __reduce_add_sync(0xffffffffu, c);
+  m = warp_sum_u64(m);
+  const int r_k = sel.K - (int)c;
+  int r_m = 0;
+  if (use_mass && m < sel.p_fix) {
+    const unsigned long long vfix = mass_fix(t);
+    r_m = vfix ? (int)((sel.p_fix - m + vfix - 1) / vfix) : 0;
+  }
+  take = max(max(r_k, r_m), 0);
+}
+
 template <int RQ>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_select_kernel(const float* __restrict__ qbarT, const float* __restrict__ kbarT, ShapeArgs s, int tq_pad,
@@ -236,7 +300,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const bool keep_none = !keep_all && sel.K == 0 && sel.p_mode == 1;
     uint32_t t = 0;
     int take = 0;
-    if (!keep_all && !keep_none) {
+    if (!keep_all && !keep_none && Tk <= 32 * kRegKeys) {
+      select_in_registers(keys, Tk, sel, keep_all, t, take);
+    } else if (!keep_all && !keep_none) {
       const bool use_mass = sel.p_mode == 0;
       if (use_mass) {
         const Predicate tot = count_mass(keys, Tk, 0u, false);
