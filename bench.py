@@ -35,9 +35,11 @@ from workload import CONFIGS, make_inputs  # noqa: E402
 
 FWD_FLOPS, BWD_FLOPS = 4, 10  # per kept (query, key) pair and channel
 
-# DRAM bytes of one attn_bwd_dkdv launch from an ncu capture (profiles/); null until the
-# current kernel has been captured.
-BWD_TRAFFIC = None
+# DRAM bytes (read + write) of one attn_bwd_dkdv launch on the 40-head workload: an ncu
+# capture of the 4-head case (720.4 MB read + 140.8 MB written, profiles/) scaled by the
+# heads processed, the heads being independent.  Set to None whenever the kernel changes
+# until it has been captured again.
+BWD_TRAFFIC = (720.390912e6 + 140.769792e6) * 40 / 4
 
 
 def parse():
