@@ -11,8 +11,8 @@
 // into 4 / 2 stages), warp 1 TMEM owner and issuer of the S_j / dP_j MMAs, warp 2 issuer of
 // the dQ MMAs (each converged, one elect.sync lane issuing: two issuers keep the MMA queue
 // fed while either waits on a barrier), and two row warpgroups (warps 3..6 and 7..10) that
-// take the list entries in turn (entry j -> group j % 2, TMEM buffers j % 2), one query row
-// per thread, so that one group's exp / dS work overlaps the other's.
+// both work on every list entry (TMEM buffers j % 2), one query row per thread, group g on
+// key columns 32g .. 32g+31 of the entry, so that each entry's dS is ready in half the time.
 // Per kept key block j:
 //   S_j  = Q K_j^T     M = 128, N = 64, K = d     (A, B K-major, fp16)
 //   dP_j = dO V_j^T    M = 128, N = 64, K = d     (A, B K-major, fp16)
@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int bb = 0; bb < 2; ++bb) {
       mbar_init(bar_sfull(bb), 1);
-      mbar_init(bar_sfree(bb), 128);
-      mbar_init(bar_pready(bb), 128);
+      mbar_init(bar_sfree(bb), 256);
+      mbar_init(bar_pready(bb), 256);
       mbar_init(bar_pfree(bb), 1);
     }
     mbar_init(bar_dq, 1);
@@ -183,14 +183,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(bar_kfull(ks), (j / kKStages) & 1, abort_flag))) break;
         // buffer bb held S_{j-2} / dP_{j-2}: the row threads must have read them out
         if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_sfree(bb), ((j >> 1) - 1) & 1, abort_flag))) break;
+        // both stages present before the S_j and dP_j MMAs issue as one group
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_vfull(vs), (j / kVStages) & 1, abort_flag))) break;
         tc_fence_after();
         const uint64_t kd = smem_desc(sbase + L::kOffK + ks * L::kKVBytes, 16, 1024);
         const uint64_t vd = smem_desc(sbase + L::kOffV + vs * L::kKVBytes, 16, 1024);
-        if (elect_one()) mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qd, kd);
-        __syncwarp();
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_vfull(vs), (j / kVStages) & 1, abort_flag))) break;
-        tc_fence_after();
         if (elect_one()) {
+          mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qd, kd);
           mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColDP + bb * 64, dod, vd);
           umma_commit(bar_sfull(bb));
           umma_commit(bar_vempty(vs));
@@ -243,42 +242,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lse2 = row_valid ? rec[0] : 0.f;
     const float Dr = row_valid ? rec[64] : 0.f;
     bool ok = true;
-    const int bb = wg;  // this group's TMEM buffer
-    int next_kb = wg < nkv ? list[wg] : 0;
-    for (int j = wg; j < nkv; j += 2) {
+    // both groups take every entry j (TMEM buffers j % 2), group wg its key columns
+    // 32 wg .. 32 wg + 31
+    int next_kb = nkv > 0 ? list[0] : 0;
+    for (int j = 0; j < nkv; ++j) {
+      const int bb = j & 1, jn = j >> 1;
       int kb = next_kb;
-      if (j + 2 < nkv) next_kb = list[j + 2];
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bb), (j >> 1) & 1, abort_flag))) {
+      if (j + 1 < nkv) next_kb = list[j + 1];
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bb), jn & 1, abort_flag))) {
         ok = false;
         break;
       }
-      const int jn = j >> 1;  // this group's n-th entry
       tc_fence_after();
       kb = (kb < 0 || kb >= s.Tk) ? 0 : kb;
       const int kv_valid = min(64, s.N - kb * 64);
-      uint32_t pk[32];
+      uint32_t sv[32], dv[32], pk[16];
+      tmem_ld32(trow + kColS + bb * 64 + 32 * wg, sv);
+      tmem_ld32(trow + kColDP + bb * 64 + 32 * wg, dv);
+      tmem_ld_wait(sv);
+      tmem_ld_wait(dv);
+      // S_j / dP_j are in registers: their buffer may be overwritten
+      tc_fence_before();
+      mbar_arrive(bar_sfree(bb));
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(trow + kColS + bb * 64 + half * 32, sv);
-        tmem_ld32(trow + kColDP + bb * 64 + half * 32, dv);
-        tmem_ld_wait(sv);
-        tmem_ld_wait(dv);
-        if (half == 1) {  // S_j / dP_j are in registers: their buffer may be overwritten
-          tc_fence_before();
-          mbar_arrive(bar_sfree(bb));
+      for (int c = 0; c < 32; c += 2) {
+        float ds[2];
+#pragma unroll
+        for (int z = 0; z < 2; ++z) {
+          const bool cv = row_valid && (32 * wg + c + z) < kv_valid;
+          const float p = cv ? ex2(__uint_as_float(sv[c + z]) * a.scale_log2 - lse2) : 0.f;
+          ds[z] = p * (__uint_as_float(dv[c + z]) - Dr);
         }
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float ds[2];
-#pragma unroll
-          for (int z = 0; z < 2; ++z) {
-            const bool cv = row_valid && (half * 32 + c + z) < kv_valid;
-            const float p = cv ? ex2(__uint_as_float(sv[c + z]) * a.scale_log2 - lse2) : 0.f;
-            ds[z] = p * (__uint_as_float(dv[c + z]) - Dr);
-          }
-          pk[half * 16 + c / 2] = pack_f16x2(ds[0], ds[1]);
-        }
+        pk[c / 2] = pack_f16x2(ds[0], ds[1]);
       }
       // dS buffer bb was last read by the dQ MMA of entry j - 2
       if (jn >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_pfree(bb), (jn - 1) & 1, abort_flag))) {
@@ -286,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      tmem_st32(trow + kColDS + bb * 32, pk);
+      tmem_st16(trow + kColDS + bb * 32 + 16 * wg, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_pready(bb));
