@@ -21,8 +21,10 @@ via Hybrid Top-k+Top-p Masking and Distillation Fine-Tuning", arXiv 2602.13515):
 * abstract (shd-paper.top, fugumt.com and thelatestinai.com pages), contribution (ii):
   the sparse attention is trainable, i.e. it has a backward pass; the backward below is
   the gradient of the masked softmax attention with the mask held fixed.
+* gist.science explainer, section 2.B: the distillation loss, the squared L2 distance
+  between sparse and full-attention outputs (a toy step on one attention block).
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * pooling is the mean over the valid tokens of a block (the last block may be partial);
 * pooled scores and token scores use the scale 1/sqrt(d) (token scale overridable);
@@ -336,6 +338,32 @@ def attn_bwd(q, k, v, do, block_mask, bq, bk, scale=None):
             for t, x in zip(out, g):
                 t[b, h] = x
     return tuple(out)
+
+
+# ---------------------------------------------------------------- distillation (toy)
+
+def vd_loss(o_student, o_teacher):
+    """Velocity-distillation loss of one attention block and its gradient.
+
+    gist.science explainer, section 2.B "Geschwindigkeits-Destillation": the fine-tuning
+    loss is the squared L2 distance between the velocity predicted by the sparse model and
+    by the frozen full-attention model.  On a single attention block the block's output
+    stands in for the velocity:
+        L = sum over all elements of (O_s - O_t)^2,    dL/dO_s = 2 (O_s - O_t),
+    with the teacher O_t held fixed.  Returns (L, dL/dO_s) in float64."""
+    diff = to_f64(o_student) - to_f64(o_teacher)
+    return float(np.sum(diff * diff)), 2.0 * diff
+
+
+def distill_step(q, k, v, student_mask, teacher_mask, bq, bk, scale=None):
+    """One toy distillation step: teacher forward (full attention, or any mask), student
+    forward under the sparse mask, the loss above, and the student's backward with
+    dO = dL/dO_s.  Returns (L, dO, dQ, dK, dV) in float64."""
+    o_t, _ = attn_fwd(q, k, v, teacher_mask, bq, bk, scale)
+    o_s, _ = attn_fwd(q, k, v, student_mask, bq, bk, scale)
+    loss, do = vd_loss(o_s, o_t)
+    dq, dk, dv = attn_bwd(q, k, v, do, student_mask, bq, bk, scale)
+    return loss, do, dq, dk, dv
 
 
 # --------------------------------------------------------------------- mask comparison

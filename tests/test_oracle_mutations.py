@@ -146,3 +146,22 @@ def test_transposed_token_mask_is_caught(monkeypatch):
 def test_backward_mutation_is_caught(monkeypatch, kind):
     _patch(monkeypatch, "attn_bwd_head", _bwd_factory(kind))
     assert _fails(TA.test_backward_matches_torch_autograd_fp64, TA.test_backward_invariants)
+
+
+def _vd_loss_factory(kind):
+    def vd_loss(o_student, o_teacher):
+        diff = S.to_f64(o_student) - S.to_f64(o_teacher)
+        if kind == "no-factor-2":
+            return float(np.sum(diff * diff)), diff
+        if kind == "sign":
+            return float(np.sum(diff * diff)), -2.0 * diff
+        return float(np.sum(np.abs(diff))), 2.0 * diff  # "l1-loss"
+    return vd_loss
+
+
+@pytest.mark.parametrize("kind", ["no-factor-2", "sign", "l1-loss"])
+def test_distillation_mutation_is_caught(monkeypatch, kind):
+    from tests import test_oracle_distill as TD
+    _patch(monkeypatch, "vd_loss", _vd_loss_factory(kind))
+    assert _fails(TD.test_loss_gradient_matches_central_differences,
+                  TD.test_chain_matches_central_differences_with_teacher_frozen)
