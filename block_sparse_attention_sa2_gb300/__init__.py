@@ -17,5 +17,6 @@ from .sa2 import (  # noqa: F401
     make_shape,
     profiler_collect,
     profiler_enable,
+    vd_loss,
     workspace,
 )

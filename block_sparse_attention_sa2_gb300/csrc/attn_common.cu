@@ -218,4 +218,102 @@ cudaError_t launch_do_prep(const ShapeArgs& s, const void* dO, const void* o, co
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------- distillation loss (toy)
+//
+// gist.science explainer of SpargeAttention2, section 2.B: the fine-tuning loss is the
+// squared L2 distance between the sparse and the full-attention velocity; on one attention
+// block its output stands in for the velocity.  loss = sum (O_s - O_t)^2, dO = 2 (O_s - O_t).
+// The difference is formed as (hi_s - hi_t) + (lo_s - lo_t): both partial differences are
+// exact in fp32 for bf16 parts, so the only rounding is their sum.  Each CTA leaves its fp64
+// partial sum; one CTA adds the partials in index order, so the loss is deterministic.
+
+template <typename T>
+__device__ __forceinline__ void st8(T* p, const float* v);
+template <>
+__device__ __forceinline__ void st8<float>(float* p, const float* v) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <>
+__device__ __forceinline__ void st8<__nv_bfloat16>(__nv_bfloat16* p, const float* v) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) vd_loss_kernel(const T* __restrict__ os, const __nv_bfloat16* __restrict__ os_lo,
+                                                      const T* __restrict__ ot, const __nv_bfloat16* __restrict__ ot_lo,
+                                                      ShapeArgs s, T* __restrict__ d_o, double* __restrict__ partial) {
+  __shared__ double red[8];
+  const int per_row = s.d / 8;
+  const int64_t items = (int64_t)s.B * s.H * s.N * per_row;
+  double acc = 0.0;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < items; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / per_row;
+    const int c = (int)(i - row * per_row) * 8;
+    const int64_t bh = row / s.N;
+    const int n = (int)(row - bh * s.N);
+    const int64_t off = (bh / s.H) * s.sb + (bh % s.H) * s.sh + (int64_t)n * s.sn + c;
+    float a[8], b[8], g[8];
+    ld8<T>(os + off, a);
+    ld8<T>(ot + off, b);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) g[k] = a[k] - b[k];
+    if (os_lo && ot_lo) {
+      ld8<__nv_bfloat16>(os_lo + off, a);
+      ld8<__nv_bfloat16>(ot_lo + off, b);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) g[k] += a[k] - b[k];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      acc += (double)g[k] * (double)g[k];
+      g[k] *= 2.f;
+    }
+    st8<T>(d_o + off, g);
+  }
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < 8; ++w) t += red[w];
+    partial[blockIdx.x] = t;
+  }
+}
+
+__global__ void __launch_bounds__(256) vd_loss_sum_kernel(const double* __restrict__ partial, int n,
+                                                          double* __restrict__ loss) {
+  __shared__ double red[256];
+  double t = 0.0;
+  for (int i = threadIdx.x; i < n; i += 256) t += partial[i];
+  red[threadIdx.x] = t;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *loss = red[0];
+}
+
+size_t vd_loss_workspace_bytes() { return sizeof(double) * 152 * 8; }
+
+cudaError_t launch_vd_loss(const ShapeArgs& s, const void* os, const void* os_lo, const void* ot, const void* ot_lo,
+                           void* d_o, double* loss, double* partial, cudaStream_t st) {
+  const int blocks = grid_for((int64_t)s.B * s.H * s.N * (s.d / 8));  // <= 152 * 8 partials
+  prof_start(st, kVdLoss);
+  if (s.dtype == 0)
+    vd_loss_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(os), static_cast<const __nv_bfloat16*>(os_lo),
+        static_cast<const __nv_bfloat16*>(ot), static_cast<const __nv_bfloat16*>(ot_lo), s,
+        static_cast<__nv_bfloat16*>(d_o), partial);
+  else
+    vd_loss_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(os), nullptr,
+                                                  static_cast<const float*>(ot), nullptr, s,
+                                                  static_cast<float*>(d_o), partial);
+  vd_loss_sum_kernel<<<1, 256, 0, st>>>(partial, blocks, loss);
+  prof_stop(st, kVdLoss);
+  return cudaGetLastError();
+}
+
 }  // namespace sa2

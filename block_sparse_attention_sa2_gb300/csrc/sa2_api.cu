@@ -310,6 +310,28 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   return cuda_status(launch_attn_bwd_dq(s, mq, mk, mv, mdo, g, cs));
 }
 
+size_t sa2_vd_loss_workspace_size(const sa2_shape* shape) {
+  ShapeArgs s;
+  if (check_shape(shape, &s) != SA2_OK) return 0;
+  return vd_loss_workspace_bytes();
+}
+
+sa2_status sa2_vd_loss(const sa2_shape* shape, const void* o_s, const void* o_s_lo, const void* o_t,
+                       const void* o_t_lo, void* d_o, double* loss, void* ws, size_t ws_bytes, void* stream) {
+  ShapeArgs s;
+  sa2_status st = check_shape(shape, &s);
+  if (st != SA2_OK) return st;
+  if (!o_s || !o_t || !d_o || !loss) return SA2_ERR_INVALID_ARG;
+  if (s.dtype == SA2_BF16 && ((o_s_lo == nullptr) != (o_t_lo == nullptr))) return SA2_ERR_INVALID_ARG;
+  if (!aligned16(o_s) || !aligned16(o_t) || !aligned16(d_o) || !aligned16(o_s_lo) || !aligned16(o_t_lo) ||
+      (reinterpret_cast<uintptr_t>(loss) & 7u) || !aligned16(ws))
+    return SA2_ERR_ALIGNMENT;
+  if (!ws || ws_bytes < vd_loss_workspace_bytes()) return SA2_ERR_WORKSPACE;
+  const bool lo = s.dtype == SA2_BF16 && o_s_lo;
+  return cuda_status(launch_vd_loss(s, o_s, lo ? o_s_lo : nullptr, o_t, lo ? o_t_lo : nullptr, d_o, loss,
+                                    static_cast<double*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
 sa2_status sa2_get_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SA2_ERR_CUDA;
   unsigned* p = status_ptr();

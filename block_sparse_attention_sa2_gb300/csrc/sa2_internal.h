@@ -15,7 +15,7 @@ constexpr size_t kMaxDynSmem = 227 * 1024;
 
 // Launch profiler (profiler.cu): kernel ids and the brackets every launch wrapper calls.
 enum KernelId {
-  kPool = 0, kScoreSelect, kCsc, kToF16, kAttnFwd, kBwdPre, kAttnBwd, kAttnBwdDq, kBwdPairs, kNumKernelIds
+  kPool = 0, kScoreSelect, kCsc, kToF16, kAttnFwd, kBwdPre, kAttnBwd, kAttnBwdDq, kBwdPairs, kVdLoss, kNumKernelIds
 };
 void prof_start(cudaStream_t st, int id);
 void prof_stop(cudaStream_t st, int id);
@@ -116,5 +116,12 @@ cudaError_t launch_attn_bwd(const ShapeArgs& s, const CUtensorMap& mq, const CUt
                             const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_attn_bwd_dq(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk,
                                const CUtensorMap& mv, const CUtensorMap& mdo, const DqArgs& a, cudaStream_t st);
+
+// Toy distillation loss (attn_common.cu): loss = sum (O_s - O_t)^2 into *loss (device),
+// d_o = 2 (O_s - O_t); residuals optional (bf16 calls).  `partial` holds
+// vd_loss_workspace_bytes() of per-CTA sums.
+size_t vd_loss_workspace_bytes();
+cudaError_t launch_vd_loss(const ShapeArgs& s, const void* os, const void* os_lo, const void* ot, const void* ot_lo,
+                           void* d_o, double* loss, double* partial, cudaStream_t st);
 
 }  // namespace sa2

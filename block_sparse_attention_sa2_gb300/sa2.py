@@ -70,6 +70,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sa2_attn_fwd.argtypes = [S, P, P, P, M, F, P, P, P, P, Z, P]
     lib.sa2_attn_bwd.restype = ctypes.c_int
     lib.sa2_attn_bwd.argtypes = [S, P, P, P, P, P, P, P, M, F, P, P, P, P, Z, P]
+    lib.sa2_vd_loss_workspace_size.restype = Z
+    lib.sa2_vd_loss_workspace_size.argtypes = [S]
+    lib.sa2_vd_loss.restype = ctypes.c_int
+    lib.sa2_vd_loss.argtypes = [S, P, P, P, P, P, P, P, Z, P]
     lib.sa2_get_device_status.restype = ctypes.c_int
     lib.sa2_get_device_status.argtypes = [P]
     lib.sa2_profiler_enable.restype = None
@@ -201,6 +205,25 @@ def attn_bwd(q, k, v, o, lse, do, mask: BlockMask, bq: int = 128, bk: int = 64, 
                                             ctypes.byref(m), float(scale or 0.0), dq.data_ptr(), dk.data_ptr(),
                                             dv.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
     return dq, dk, dv
+
+
+def vd_loss(o_s: torch.Tensor, o_t: torch.Tensor, o_s_lo: Optional[torch.Tensor] = None,
+            o_t_lo: Optional[torch.Tensor] = None, d_o: Optional[torch.Tensor] = None,
+            ws: Optional[torch.Tensor] = None, stream=None):
+    """sa2_vd_loss: the toy distillation loss sum (O_s - O_t)^2 (a float64 scalar tensor on
+    the device) and d_o = 2 (O_s - O_t), ready for attn_bwd of the student."""
+    lib = load_library()
+    shp = make_shape(o_s, 128, 64)
+    if o_t.shape != o_s.shape or o_t.stride() != o_s.stride():
+        raise ValueError("o_s and o_t must have the same shape and strides")
+    d_o = torch.empty_like(o_s) if d_o is None else d_o
+    loss = torch.empty((), dtype=torch.float64, device=o_s.device)
+    if ws is None:
+        ws = workspace(lib.sa2_vd_loss_workspace_size(ctypes.byref(shp)), o_s.device)
+    _check("sa2_vd_loss", lib.sa2_vd_loss(ctypes.byref(shp), o_s.data_ptr(), _ptr(o_s_lo), o_t.data_ptr(),
+                                          _ptr(o_t_lo), d_o.data_ptr(), loss.data_ptr(), ws.data_ptr(),
+                                          ws.numel(), _stream(stream)))
+    return loss, d_o
 
 
 def device_status(stream=None) -> int:

@@ -209,6 +209,28 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
                         void* stream);
 
 /*
+ * Toy distillation step (gist.science explainer, section 2.B: the fine-tuning loss is the
+ * squared L2 distance between the velocity of the sparse model and that of the frozen
+ * full-attention model; on a single attention block the block's output stands in for the
+ * velocity).  With a teacher forward under the dense mask (k = 1) and a student forward
+ * under the hybrid mask, sa2_vd_loss gives the loss and the student's output gradient,
+ * which sa2_attn_bwd then carries to dQ, dK, dV:
+ *   loss = sum over all elements of (O_s - O_t)^2,   d_o = 2 (O_s - O_t)   (O_t held fixed)
+ *
+ *   o_s, o_t        token tensors (dtype and strides of the call): student, teacher output
+ *   o_s_lo, o_t_lo  optional residuals from sa2_attn_fwd (bf16 calls; both or neither; NULL
+ *                   for none, ignored for SA2_FP32): O is read as O + O_lo, so the difference
+ *                   of two close outputs keeps ~16 bits instead of bf16's 8
+ *   d_o             token tensor (output, same layout)
+ *   loss            device pointer to one double (output), 8-byte aligned
+ *   ws              device workspace of at least sa2_vd_loss_workspace_size(shape) bytes
+ * The sum is deterministic: per-CTA partial sums in fp64, then one ordered final sum.
+ */
+size_t sa2_vd_loss_workspace_size(const sa2_shape* shape);
+sa2_status sa2_vd_loss(const sa2_shape* shape, const void* o_s, const void* o_s_lo, const void* o_t,
+                       const void* o_t_lo, void* d_o, double* loss, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Launch profiler (instrumentation of this library; the pages have no counterpart).
  * sa2_profiler_enable(1) makes every later kernel launch of the library record a CUDA
  * event before and after it on its stream; sa2_profiler_enable(0) stops that.

@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_every_declared_function_is_exported(lib):
     names = declared_functions()
-    assert {"sa2_build_mask", "sa2_attn_fwd", "sa2_attn_bwd", "sa2_build_mask_noalloc"} <= set(names)
+    assert {"sa2_build_mask", "sa2_attn_fwd", "sa2_attn_bwd", "sa2_build_mask_noalloc", "sa2_vd_loss"} <= set(names)
     from block_sparse_attention_sa2_gb300.sa2 import LIB_PATH
     out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (sa2_\w+)", out))
@@ -125,4 +125,22 @@ def test_noalloc_rejects_oversized_shapes_on_the_host(lib):
 
 def test_profiler_size_query_needs_no_gpu(lib):
     lib.sa2_profiler_enable(0)
-    assert lib.sa2_profiler_collect(None, 0) == 9
+    assert lib.sa2_profiler_collect(None, 0) == 10
+
+
+def test_vd_loss_rejects_bad_arguments_before_any_launch(lib):
+    from block_sparse_attention_sa2_gb300 import sa2
+    good = _shape(sa2)
+    P = 256
+    lib.sa2_vd_loss.restype = ctypes.c_int
+    call = lambda sh, os=P, os_lo=None, ot_lo=None, do=P, loss=P, wsb=1 << 20: lib.sa2_vd_loss(  # noqa: E731
+        ctypes.byref(sh), ctypes.c_void_p(os), ctypes.c_void_p(os_lo), ctypes.c_void_p(P), ctypes.c_void_p(ot_lo),
+        ctypes.c_void_p(do), ctypes.c_void_p(loss), ctypes.c_void_p(P), ctypes.c_size_t(wsb), None)
+    assert lib.sa2_vd_loss_workspace_size(ctypes.byref(good)) >= 8 * 152
+    assert call(_shape(sa2, d=80)) == UNSUPPORTED
+    assert call(good, os=None) == INVALID
+    assert call(good, loss=None) == INVALID
+    assert call(good, os_lo=P) == INVALID  # one residual without the other
+    assert call(good, do=P + 8) == ALIGN
+    assert call(good, loss=P + 4) == ALIGN
+    assert call(good, wsb=8) == WORKSPACE
