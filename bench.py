@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--sparsity", type=float, default=0.95,
                     help="calibrated target block sparsity of the config (0 = dense)")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-qblocks", type=int, default=4, help="query blocks of the oracle sample")
     ap.add_argument("--heads", type=int, default=0,
@@ -248,11 +248,13 @@ def run_native(a, rank, world):
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
 
-    def step(src):
+    def step(src, out=None):
+        out = out or {"o": o, "dq": dq, "dk": dk, "dv": dv}
         sa2.build_mask(src["q"], src["k"], topk, topp, bq=cfg.bq, bk=cfg.bk, out=bm, ws=ws_m)
-        sa2.attn_fwd(src["q"], src["k"], src["v"], bm, bq=cfg.bq, bk=cfg.bk, o=o, lse=lse, o_lo=o_lo, ws=ws_f)
-        sa2.attn_bwd(src["q"], src["k"], src["v"], o, lse, src["do"], bm, bq=cfg.bq, bk=cfg.bk, o_lo=o_lo,
-                     dq=dq, dk=dk, dv=dv, ws=ws_b)
+        sa2.attn_fwd(src["q"], src["k"], src["v"], bm, bq=cfg.bq, bk=cfg.bk, o=out["o"], lse=lse, o_lo=o_lo,
+                     ws=ws_f)
+        sa2.attn_bwd(src["q"], src["k"], src["v"], out["o"], lse, src["do"], bm, bq=cfg.bq, bk=cfg.bk,
+                     o_lo=o_lo, dq=out["dq"], dk=out["dk"], dv=out["dv"], ws=ws_b)
 
     for _ in range(a.warmup):
         step(d)
@@ -292,10 +294,17 @@ def run_native(a, rank, world):
     ms_max = reduce_max_over_ranks(ev0.elapsed_time(ev1), dev)
     clk = clocks.stop() if rank == 0 else None
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  Every step uploads its
+    # inputs from pinned host memory and reads all four results back; the uploads of step
+    # i+1 and the read-back of step i-1 run on their own streams while step i computes
+    # (inputs and outputs double-buffered on the device, ordered by events).
     e2e_steps = max(1, a.e2e_steps)
-    hout = {n: torch.empty_like(host["q"]).pin_memory() for n in ("o", "dq", "dk", "dv")}
-    dst = {t: torch.empty_like(d[t]) for t in d}
+    outs = ("o", "dq", "dk", "dv")
+    hout = {n: torch.empty_like(host["q"]).pin_memory() for n in outs}
+    dins = [{t: torch.empty_like(d[t]) for t in d} for _ in range(2)]
+    douts = [{n: torch.empty_like(d["q"]) for n in outs} for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "used", "done", "read")}
     h2d = sum(host[t].numel() * host[t].element_size() for t in host)
     d2h = sum(hout[n].numel() * hout[n].element_size() for n in hout)
     torch.cuda.synchronize()
@@ -303,12 +312,28 @@ def run_native(a, rank, world):
         torch.distributed.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        for t in host:
-            dst[t].copy_(host[t], non_blocking=True)
-        step(dst)
-        for n, src_t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
-            hout[n].copy_(src_t, non_blocking=True)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(e2e_steps):
+        b = i & 1
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev["used"][b])  # step i-2 is done with this input buffer
+            for t in host:
+                dins[b][t].copy_(host[t], non_blocking=True)
+            ev["in"][b].record(s_in)
+        stream.wait_event(ev["in"][b])
+        if i >= 2:
+            stream.wait_event(ev["read"][b])  # the read-back of step i-2 has left this buffer
+        step(dins[b], douts[b])
+        ev["used"][b].record(stream)
+        ev["done"][b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["done"][b])
+            for n in outs:
+                hout[n].copy_(douts[b][n], non_blocking=True)
+            ev["read"][b].record(s_out)
+    stream.wait_stream(s_out)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1), dev) / e2e_steps
