@@ -146,74 +146,70 @@ __global__ void __launch_bounds__(256) do_prep_kernel(const T* __restrict__ dO, 
                                                       const float* __restrict__ lse, ShapeArgs s,
                                                       __half* __restrict__ dO16, float* __restrict__ stats,
                                                       unsigned* status) {
-  const int per_row = s.d / 8;  // threads per token: 16 or 8, a power of two within a warp
-  const int64_t rows = (int64_t)s.B * s.H * s.N;
-  const int64_t items = rows * per_row;
+  // grid: x = b*H + h, y over the tokens of one head (per_row threads of 8 channels each);
+  // a warp covers whole tokens (per_row = 16 or 8 divides 32), so the shuffles below stay
+  // inside a token and every lane takes part in them
+  const int shift = s.d == 128 ? 4 : 3;  // log2(per_row)
+  const int per_row = 1 << shift;
+  const int bh = blockIdx.x;
+  const int b = bh / s.H, h = bh - b * s.H;
   const int Tsub = s.Tq * (s.bq / 64);
+  const int idx = blockIdx.y * blockDim.x + threadIdx.x;
+  const int n = idx >> shift;
+  const int c = (idx & (per_row - 1)) * 8;
+  const bool live = n < s.N;
   bool bad = false;
-  // warps walk whole groups of 32 items (2 or 4 tokens), so the loop and the shuffles below
-  // are uniform across each warp
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int lane = threadIdx.x & 31;
-  for (int64_t wbase = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) - lane; wbase < items; wbase += stride) {
-    const int64_t i = wbase + lane;
-    const bool live = i < items;
-    float acc = 0.f;
-    int64_t row = 0, bh = 0;
-    int n = 0;
-    if (live) {
-      row = i / per_row;
-      const int c = (int)(i - row * per_row) * 8;
-      bh = row / s.N;
-      n = (int)(row - bh * s.N);
-      const int64_t off = (bh / s.H) * s.sb + (bh % s.H) * s.sh + (int64_t)n * s.sn + c;
-      float g[8], ov[8];
-      ld8<T>(dO + off, g);
-      ld8<T>(o + off, ov);
-      if (o_lo) {
-        float lo[8];
-        ld8<__nv_bfloat16>(o_lo + off, lo);
+  float acc = 0.f;
+  if (live) {
+    const int64_t off = (int64_t)b * s.sb + (int64_t)h * s.sh + (int64_t)n * s.sn + c;
+    float g[8], ov[8];
+    ld8<T>(dO + off, g);
+    ld8<T>(o + off, ov);
+    if (o_lo) {
+      float lo[8];
+      ld8<__nv_bfloat16>(o_lo + off, lo);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ov[k] += lo[k];
-      }
-      const uint4 h = to_f16x8(g, bad);
-      *reinterpret_cast<uint4*>(dO16 + row * s.d + c) = h;
-      const __half* hh = reinterpret_cast<const __half*>(&h);
+      for (int k = 0; k < 8; ++k) ov[k] += lo[k];
+    }
+    const uint4 hv = to_f16x8(g, bad);
+    *reinterpret_cast<uint4*>(dO16 + ((int64_t)bh * s.N + n) * s.d + c) = hv;
+    const __half* hh = reinterpret_cast<const __half*>(&hv);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc += __half2float(hh[k]) * ov[k];
-    }
-    for (int w = per_row / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-    if (live && (lane & (per_row - 1)) == 0) {
-      float* rec = stats + ((int64_t)bh * Tsub + (n >> 6)) * 128 + (n & 63);
-      rec[0] = lse[row] * 1.4426950408889634f;
-      rec[64] = acc;
-    }
+    for (int k = 0; k < 8; ++k) acc += __half2float(hh[k]) * ov[k];
+  }
+  for (int w = per_row / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+  if (live && c == 0) {
+    float* rec = stats + ((int64_t)bh * Tsub + (n >> 6)) * 128 + (n & 63);
+    rec[0] = lse[(int64_t)bh * s.N + n] * 1.4426950408889634f;
+    rec[64] = acc;
   }
   // rows of the last sub-tiles past N: +inf makes their P exactly 0
-  const int pad = Tsub * 64 - s.N;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)s.B * s.H * pad; i += stride) {
-    const int64_t bh = i / pad;
-    const int n = s.N + (int)(i - bh * pad);
-    float* rec = stats + ((int64_t)bh * Tsub + (n >> 6)) * 128 + (n & 63);
-    rec[0] = __int_as_float(0x7f800000);
-    rec[64] = 0.f;
+  if (blockIdx.y == 0) {
+    const int pad = Tsub * 64 - s.N;
+    for (int i = threadIdx.x; i < pad; i += blockDim.x) {
+      const int np = s.N + i;
+      float* rec = stats + ((int64_t)bh * Tsub + (np >> 6)) * 128 + (np & 63);
+      rec[0] = __int_as_float(0x7f800000);
+      rec[64] = 0.f;
+    }
   }
   if (bad) report_error(status, kDevErrRange);
 }
 
 cudaError_t launch_do_prep(const ShapeArgs& s, const void* dO, const void* o, const void* o_lo, const float* lse,
                            __half* dO16, float* stats, unsigned* status, cudaStream_t st) {
-  const int64_t items = (int64_t)s.B * s.H * s.N * (s.d / 8);
-  const int blocks = grid_for(items);
+  const int64_t per_head = (int64_t)s.N * (s.d / 8);
+  // y <= 491520 tokens x 16 / 256 = 30720 blocks, within the 65535 limit of gridDim.y
+  const dim3 grid((unsigned)(s.B * s.H), (unsigned)((per_head + 255) / 256));
   prof_start(st, kBwdPre);
   if (s.dtype == 0)
-    do_prep_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(dO),
-                                                          static_cast<const __nv_bfloat16*>(o),
-                                                          static_cast<const __nv_bfloat16*>(o_lo), lse, s, dO16,
-                                                          stats, status);
+    do_prep_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(dO),
+                                                        static_cast<const __nv_bfloat16*>(o),
+                                                        static_cast<const __nv_bfloat16*>(o_lo), lse, s, dO16,
+                                                        stats, status);
   else
-    do_prep_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(dO), static_cast<const float*>(o),
-                                                  nullptr, lse, s, dO16, stats, status);
+    do_prep_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(dO), static_cast<const float*>(o),
+                                                nullptr, lse, s, dO16, stats, status);
   prof_stop(st, kBwdPre);
   return cudaGetLastError();
 }
