@@ -39,7 +39,7 @@ FWD_FLOPS, BWD_FLOPS = 4, 10  # per kept (query, key) pair and channel
 # capture of the 4-head case (720.4 MB read + 140.8 MB written, profiles/) scaled by the
 # heads processed, the heads being independent.  Set to None whenever the kernel changes
 # until it has been captured again.
-BWD_TRAFFIC = (720.390912e6 + 140.769792e6) * 40 / 4
+BWD_TRAFFIC = (720.492032e6 + 140.880896e6) * 40 / 4
 
 
 def parse():
