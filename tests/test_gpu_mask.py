@@ -67,6 +67,16 @@ def test_mask_ragged_small_cases(sa2, N, d, bq, dtype):
         _compare(sa2, cfg, x, topk, topp)
 
 
+@pytest.mark.parametrize("Tk", [1400, 7680])
+def test_mask_long_rows(sa2, Tk):
+    """Rows of more than 1280 key blocks take the scoring kernel's shared-memory selection
+    path (shorter rows keep their keys in registers); 7680 key blocks is the longest row the
+    builder accepts (N = 491520 tokens)."""
+    cfg, x = small_case(f"long-rows-{Tk}", 1, 1, Tk * 64, 64, "bf16", 128, 64, seed=51, tensors=("q", "k"))
+    assert cfg.Tk == Tk
+    _compare(sa2, cfg, x, 0.02, 0.5)
+
+
 def test_mask_failure_probe_sweep(sa2):
     """Mask-failure probe (flat heads 0-3, sink heads 4-7): Top-k-only, Top-p-only, hybrid."""
     cfg = CONFIGS[1]

@@ -202,7 +202,8 @@ def make_inputs(cfg: WorkloadConfig, seed: int = 0,
 
 
 def small_case(name: str, B: int, H: int, N: int, d: int, dtype: str, bq: int, bk: int,
-               seed: int = 0, sink: bool = True) -> Tuple[WorkloadConfig, Dict[str, np.ndarray]]:
+               seed: int = 0, sink: bool = True,
+               tensors: Tuple[str, ...] = ("q", "k", "v", "do")) -> Tuple[WorkloadConfig, Dict[str, np.ndarray]]:
     """A small ragged case (N need not be a multiple of the blocks) for parity tests.
 
     The grid is 1 x 1 x N, so the positional term varies along the token index only."""
@@ -211,4 +212,4 @@ def small_case(name: str, B: int, H: int, N: int, d: int, dtype: str, bq: int, b
                          pos_sigma=(0.0, 0.0, 1.0 / max(bk, 1)),
                          sink_blocks=(0,) if sink else (), sink_s=8.0 if sink else 0.0,
                          sink_a=1.0 if sink else 0.0)
-    return cfg, make_inputs(cfg, seed=seed)
+    return cfg, make_inputs(cfg, tensors=tensors, seed=seed)
