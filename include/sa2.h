@@ -18,8 +18,9 @@
  * - Pointers are device pointers unless stated otherwise; every device pointer must be
  *   16-byte aligned and every stride * element size a multiple of 16 bytes.
  * - The caller owns every buffer, including the workspaces (sizes from the *_workspace_size
- *   queries).  The library allocates no device memory; it keeps one device status word and
- *   a few bytes of per-device set-up state.
+ *   queries).  The library allocates no device memory; it keeps one device status word, a
+ *   few bytes of per-device set-up state, and the static scratch array of
+ *   sa2_build_mask_noalloc (SA2_NOALLOC_SCRATCH_BYTES, part of the loaded module).
  * - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
  *   Argument errors are returned before anything is launched.  Errors raised by a kernel
  *   on the device (a bounded wait that timed out, a block index out of range) are recorded
