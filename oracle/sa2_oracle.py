@@ -259,18 +259,43 @@ def attn_bwd_head(q, k, v, do, block_mask, bq, bk, scale=None):
     return dQ, dK, dV
 
 
+def _kept_keys(block_mask_row: np.ndarray, N: int, bk: int) -> np.ndarray:
+    """Token indices of the key blocks one query block keeps (ascending)."""
+    blocks = np.nonzero(block_mask_row)[0]
+    if blocks.size == 0:
+        return np.zeros(0, dtype=np.int64)
+    return np.concatenate([np.arange(j * bk, min(N, (j + 1) * bk)) for j in blocks])
+
+
+def _row_block_grads(q, k, v, do, keys, rows, scale):
+    """Softmax, D and dS of the query rows of one query block over its kept keys only.
+
+    Entries of dropped blocks have P = 0 in the masked softmax (gist.science explainer,
+    section 2.C: skipped tiles are not computed), so restricting each row to its kept keys
+    gives the same P, O, D and dS as masking the full row.  Returns (P, dS) over ``keys``."""
+    s = (q[rows] @ k[keys].T) * scale
+    P, _ = _masked_softmax_rows(s, np.ones_like(s, dtype=bool))
+    o = P @ v[keys]
+    D = (do[rows] * o).sum(axis=1)
+    dS = P * (do[rows] @ v[keys].T - D[:, None])
+    return P, dS
+
+
 def attn_bwd_dq_rows(q, k, v, do, block_mask, bq, bk, rows, scale=None):
-    """dQ of the listed query rows only (same definition as ``attn_bwd_head``)."""
+    """dQ of the listed query rows only (same definition as ``attn_bwd_head``), each row
+    computed over the key blocks its query block keeps."""
     N, d = k.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     rows = np.asarray(rows)
-    allowed = token_mask(block_mask, N, bq, bk, rows)
-    P, _ = _masked_softmax_rows((q[rows] @ k.T) * scale, allowed)
-    o = P @ v
-    dP = do[rows] @ v.T
-    D = (do[rows] * o).sum(axis=1)
-    dS = P * (dP - D[:, None])
-    return scale * (dS @ k)
+    dQ = np.zeros((rows.size, d))
+    for i in np.unique(rows // bq):
+        sel = np.nonzero(rows // bq == i)[0]
+        keys = _kept_keys(block_mask[i], N, bk)
+        if keys.size == 0:
+            continue  # a row that keeps nothing has zero gradients
+        _, dS = _row_block_grads(q, k, v, do, keys, rows[sel], scale)
+        dQ[sel] = scale * (dS @ k[keys])
+    return dQ
 
 
 def attn_bwd_rows(q, k, v, do, block_mask, bq, bk, rows, scale=None):
@@ -290,28 +315,25 @@ def attn_bwd_rows(q, k, v, do, block_mask, bq, bk, rows, scale=None):
 
 
 def attn_bwd_dkdv_cols(q, k, v, do, block_mask, bq, bk, cols, scale=None):
-    """dK and dV of the listed key tokens only.  Every query row that keeps one of these
-    keys is recomputed in full (its softmax needs the whole row)."""
+    """dK and dV of the listed key tokens only: the sum over every query block that keeps
+    one of these keys, each block's rows computed over the key blocks it keeps."""
     N, d = k.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     cols = np.asarray(cols)
-    col_blocks = np.unique(cols // bk)
-    q_blocks = np.nonzero(block_mask[:, col_blocks].any(axis=1))[0]
-    rows = np.concatenate([np.arange(i * bq, min(N, (i + 1) * bq)) for i in q_blocks]) \
-        if q_blocks.size else np.zeros(0, dtype=np.int64)
     dK = np.zeros((cols.size, d))
     dV = np.zeros((cols.size, d))
-    if rows.size == 0:
-        return dK, dV
-    allowed = token_mask(block_mask, N, bq, bk, rows)
-    P, _ = _masked_softmax_rows((q[rows] @ k.T) * scale, allowed)
-    o = P @ v
-    D = (do[rows] * o).sum(axis=1)
-    Pc = P[:, cols]  # [R, C]
-    dPc = do[rows] @ v[cols].T
-    dSc = Pc * (dPc - D[:, None])
-    dV = Pc.T @ do[rows]
-    dK = scale * (dSc.T @ q[rows])
+    col_blocks = np.unique(cols // bk)
+    for i in np.nonzero(block_mask[:, col_blocks].any(axis=1))[0]:
+        rows = np.arange(i * bq, min(N, (i + 1) * bq))
+        keys = _kept_keys(block_mask[i], N, bk)
+        P, dS = _row_block_grads(q, k, v, do, keys, rows, scale)
+        pos = np.searchsorted(keys, cols)  # where each listed key sits among the kept ones
+        hit = (pos < keys.size) & (keys[np.minimum(pos, keys.size - 1)] == cols)
+        if not hit.any():
+            continue
+        Pc, dSc = P[:, pos[hit]], dS[:, pos[hit]]
+        dV[hit] += Pc.T @ do[rows]
+        dK[hit] += scale * (dSc.T @ q[rows])
     return dK, dV
 
 

@@ -137,3 +137,15 @@ def test_bwd_full_size_wan_shapes_sampled(sa2, ci):
                 mask[0, h, i, max(0, 2 * i - 3): 2 * i + 5] = 1
     rows = np.concatenate([np.arange(0, 64), np.arange(cfg.N // 2, cfg.N // 2 + 32), np.arange(cfg.N - 64, cfg.N)])
     _sampled_check(sa2, cfg, x, mask, heads, rows, [0, cfg.Tk // 2, cfg.Tk - 1])
+
+
+def test_bwd_longest_sequence_sampled(sa2):
+    """The longest sequence the library accepts (N = 491520 tokens: 3840 query blocks, 7680
+    key blocks), d = 64, with a Top-k-only mask of 39 blocks per row: long lists, the largest
+    pair-union bitmaps and 64-bit offsets.  Sampled query rows, and two key blocks away from
+    the sink (whose column holds every row), recomputed by the oracle."""
+    cfg, x = small_case("longest", 1, 1, 7680 * 64, 64, "bf16", 128, 64, seed=53)
+    mask = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, 0.005, 0.0)["mask"]
+    assert int(mask[0, 0].sum(axis=1).max()) == 39
+    rows = np.concatenate([np.arange(0, 64), np.arange(cfg.N // 2, cfg.N // 2 + 32), np.arange(cfg.N - 64, cfg.N)])
+    _sampled_check(sa2, cfg, x, mask, [(0, 0)], rows, [cfg.Tk // 2, cfg.Tk - 1])

@@ -169,6 +169,19 @@ def test_row_and_column_sampled_versions_equal_the_full_computation():
     dk_c, dv_c = O.attn_bwd_dkdv_cols(q, k, v, do, mask, 16, 8, cols)
     np.testing.assert_allclose(dk_c, dk[cols], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(dv_c, dv[cols], rtol=1e-12, atol=1e-13)
+    # a query block that keeps nothing and a key block kept by nobody
+    m2 = mask.copy()
+    m2[1, :] = 0
+    m2[:, 2] = 0
+    dq2, dk2, dv2 = O.attn_bwd_head(q, k, v, do, m2, 16, 8)
+    np.testing.assert_allclose(O.attn_bwd_dq_rows(q, k, v, do, m2, 16, 8, rows), dq2[rows],
+                               rtol=1e-12, atol=1e-13)
+    assert not O.attn_bwd_dq_rows(q, k, v, do, m2, 16, 8, np.arange(16, 32)).any()
+    cols2 = np.array([0, 16, 23, 40])  # key block 2 (tokens 16..23) is kept by nobody
+    dk_c2, dv_c2 = O.attn_bwd_dkdv_cols(q, k, v, do, m2, 16, 8, cols2)
+    np.testing.assert_allclose(dk_c2, dk2[cols2], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dv_c2, dv2[cols2], rtol=1e-12, atol=1e-13)
+    assert not dk_c2[1:3].any() and not dv_c2[1:3].any()
 
 
 def test_row_partition_of_the_backward_adds_up():
