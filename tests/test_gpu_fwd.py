@@ -136,6 +136,18 @@ def test_fwd_full_size_wan_shapes_sampled_rows(sa2, ci):
         _check_head(f"{cfg.name} h{h}", o[b, h, rows], lse[b, h, rows], ro, rlse)
 
 
+def test_fwd_longest_sequence_sampled_rows(sa2):
+    """The longest sequence the library accepts (N = 491520 tokens, 7680 key blocks), d = 64,
+    Top-k-only mask of 39 blocks per row; sampled rows (first, middle, last blocks)."""
+    cfg, x = small_case("longest", 1, 1, 7680 * 64, 64, "bf16", 128, 64, seed=53, tensors=("q", "k", "v"))
+    mask = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, 0.005, 0.0)["mask"]
+    o, lse = _run_fwd(sa2, cfg, x, mask)
+    rows = np.concatenate([np.arange(0, 64), np.arange(cfg.N // 2, cfg.N // 2 + 64), np.arange(cfg.N - 100, cfg.N)])
+    ro, rlse = O.attn_fwd_head(O.to_f64(x["q"][0, 0]), O.to_f64(x["k"][0, 0]), O.to_f64(x["v"][0, 0]),
+                               mask[0, 0], cfg.bq, cfg.bk, rows=rows)
+    _check_head("longest", o[0, 0, rows], lse[0, 0, rows], ro, rlse)
+
+
 def test_fwd_end_to_end_from_gpu_mask(sa2):
     """GPU mask -> GPU forward, against the oracle on the oracle's mask (rows whose masks
     agree; the masks differ at most in near-threshold entries)."""
