@@ -35,11 +35,20 @@ from workload import CONFIGS, make_inputs  # noqa: E402
 
 FWD_FLOPS, BWD_FLOPS = 4, 10  # per kept (query, key) pair and channel
 
-# DRAM bytes (read + write) of one attn_bwd_dkdv launch on the 40-head workload: an ncu
-# capture of the 4-head case (720.4 MB read + 140.8 MB written, profiles/) scaled by the
-# heads processed, the heads being independent.  Set to None whenever the kernel changes
-# until it has been captured again.
-BWD_TRAFFIC = (720.492032e6 + 140.880896e6) * 40 / 4
+# DRAM bytes (read + write) of one attn_bwd_dkdv launch per head of the Wan2.1-14B-720p
+# workload at its calibrated 95 % sparsity: an ncu capture of the 4-head case (720.4 MB read
+# + 140.8 MB written, profiles/) divided by its heads, the heads being independent.  Set to
+# None whenever the kernel changes until it has been captured again.
+BWD_TRAFFIC_PER_HEAD = (720.492032e6 + 140.880896e6) / 4
+BWD_TRAFFIC_WORKLOAD = ("wan2.1-14b-720p", 0.95)
+
+
+def dkdv_traffic(cfg, sparsity: float):
+    """Captured DRAM bytes of one dK/dV launch, scaled to the heads processed; None for a
+    workload other than the captured one."""
+    if BWD_TRAFFIC_PER_HEAD is None or (cfg.name, sparsity) != BWD_TRAFFIC_WORKLOAD:
+        return None
+    return BWD_TRAFFIC_PER_HEAD * cfg.B * cfg.H
 
 
 def parse():
@@ -354,7 +363,7 @@ def run_native(a, rank, world):
         achieved = algo[dom] / ((m / c) * 1e-3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": BWD_TRAFFIC if dom == "attn_bwd_dkdv" else None,
+                "frac": achieved / peak, "traffic": dkdv_traffic(cfg, a.sparsity) if dom == "attn_bwd_dkdv" else None,
                 "peak_source": f"{peaks['source']} bf16 dense, sustained (fp16 MMAs: same nominal rate)",
                 "algorithmic_flops_per_launch": algo[dom]}
     else:
