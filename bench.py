@@ -39,7 +39,7 @@ FWD_FLOPS, BWD_FLOPS = 4, 10  # per kept (query, key) pair and channel
 # workload at its calibrated 95 % sparsity: an ncu capture of the 4-head case (720.4 MB read
 # + 140.8 MB written, profiles/) divided by its heads, the heads being independent.  Set to
 # None whenever the kernel changes until it has been captured again.
-BWD_TRAFFIC_PER_HEAD = (720.492032e6 + 140.880896e6) / 4
+BWD_TRAFFIC_PER_HEAD = None
 BWD_TRAFFIC_WORKLOAD = ("wan2.1-14b-720p", 0.95)
 
 

@@ -35,6 +35,13 @@
 // query columns 0-31 of the sub-tile, warps 7-10 columns 32-63), then the dK / dV
 // epilogue.
 //
+// The CTAs are persistent, one per SM, and take key-block pairs from a counter until none
+// is left.  The producer publishes each pair in a two-slot ring in shared memory that every
+// role reads; all barrier phases count sub-tiles and pairs over the CTA's whole run.  So the
+// set-up (barriers, TMEM allocation) is paid once per SM, the next pair's K and V load as
+// soon as the current pair's S^T / dP^T MMAs have completed, and its first S^T / dP^T
+// MMAs run while the element-wise warps store the current pair's dK and dV.
+//
 // All operands are fp16: the call's Q, K, V, dO arrive as fp16 copies (exact for bf16
 // inputs within the fp16 range) and P, dS are written as fp16, which keeps 11 significant
 // bits of P and dS against bf16's 8.
@@ -48,6 +55,7 @@ namespace sa2 {
 namespace {
 
 constexpr int kThreads = 352;
+constexpr int kItemReaders = 10;  // warps reading the item slot: 1, 2 and the 8 element-wise warps
 constexpr int kStages = 4;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns
@@ -130,36 +138,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  const uint32_t bar_kv = smem_u32(&bars[0]);
+  const uint32_t bar_kv = smem_u32(&bars[0]);  // K, V of the current pair landed
   auto bar_full = [&](int st) { return smem_u32(&bars[1 + st]); };
   auto bar_empty = [&](int st) { return smem_u32(&bars[5 + st]); };
   const uint32_t bar_sfull = smem_u32(&bars[9]);   // S^T, dP^T of the current sub-tile in TMEM
   const uint32_t bar_sfree = smem_u32(&bars[10]);  // ... and read out by the element-wise warps
   auto bar_pready = [&](int b) { return smem_u32(&bars[11 + b]); };  // P^T, dS^T buffer b written
   auto bar_pfree = [&](int b) { return smem_u32(&bars[13 + b]); };   // MMAs reading buffer b done
-  const uint32_t bar_drain = smem_u32(&bars[15]);   // every dV / dK MMA completed
-  const uint32_t bar_sdrain = smem_u32(&bars[16]);  // every S^T / dP^T MMA completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 160);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 192);
+  const uint32_t bar_drain = smem_u32(&bars[15]);   // every dV / dK MMA of the pair completed
+  const uint32_t bar_sdrain = smem_u32(&bars[16]);  // every S^T / dP^T MMA of the CTA completed
+  const uint32_t bar_kvfree = smem_u32(&bars[17]);  // every S^T / dP^T MMA of the pair completed
+  const uint32_t bar_gdrain = smem_u32(&bars[18]);  // every dV / dK MMA of the CTA completed
+  auto bar_item_full = [&](int i) { return smem_u32(&bars[19 + i]); };  // item slot i written
+  auto bar_item_free = [&](int i) { return smem_u32(&bars[21 + i]); };  // ... and read by every role
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 224);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 232);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + kOffBar + 240);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // pair-major order: the pairs holding the first key blocks of every head (where
-  // attention sinks, and so the longest lists, usually sit) start first
+  // Work items are key-block pairs in pair-major order (item x: pair m = x / BH of head
+  // x % BH), so the pairs holding the first key blocks of every head, where attention sinks
+  // and so the longest lists usually sit, start first.  Each CTA stays resident and takes
+  // items from a counter: its first is blockIdx.x, the next gridDim.x + (counter value).
   const int BH = s.B * s.H;
   const int Tp = (s.Tk + 1) >> 1;
-  const int m = blockIdx.x / BH;
-  const int bh = blockIdx.x % BH;
-  const int b = bh / s.H, h = bh % s.H;
-  const int64_t pid = (int64_t)bh * Tp + m;
-  int nu = a.pair_cnt[pid];
-  if (nu < 0 || nu > s.Tq) {
-    if (tid == 0) report_error(a.status, kDevErrBounds);
-    nu = nu < 0 ? 0 : s.Tq;
-  }
-  const uint32_t* list = a.pair_idx + pid * s.Tq;
+  const int num_items = BH * Tp;
   const int sub_shift = s.bq == 128 ? 1 : 0;  // 64-row sub-tiles per query block: 2 or 1
-  const int nsub = nu << sub_shift;
   const int Tsub = s.Tq << sub_shift;
+  // union length of item x, clamped to [0, Tq] (the producer reports a bad value)
+  auto item_len = [&](int x, bool report) {
+    const int m = x / BH, bh = x - m * BH;
+    int nu = a.pair_cnt[(int64_t)bh * Tp + m];
+    if (nu < 0 || nu > s.Tq) {
+      if (report) report_error(a.status, kDevErrBounds);
+      nu = nu < 0 ? 0 : s.Tq;
+    }
+    return nu;
+  };
+  // a consumer warp takes item n from its slot and hands the slot back; -1 ends the loop
+  auto take_item = [&](int n, bool& ok) {
+    const int slot = n & 1;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar_item_full(slot), (n >> 1) & 1, abort_flag))) {
+      ok = false;
+      return -1;
+    }
+    const int x = item_slot[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_item_free(slot));
+    return x;
+  };
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -173,9 +200,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_pready(i), 256);
       mbar_init(bar_pfree(i), 1);
+      mbar_init(bar_item_full(i), 1);
+      mbar_init(bar_item_free(i), kItemReaders);
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_sdrain, 1);
+    mbar_init(bar_kvfree, 1);
+    mbar_init(bar_gdrain, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -187,52 +218,87 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Barrier phases count sub-tiles (U, W) and pairs with a non-empty list (kvn, an) over
+  // all items of the CTA, so every ring runs on across item boundaries.
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (nsub > 0) {
-      if (lane == 0) {
-        tma_prefetch_map(&mq);
-        tma_prefetch_map(&mdo);
-        mbar_arrive_expect_tx(bar_kv, 65536);
-        for (int p = 0; p < 2; ++p)
-          for (int r = 0; r < 2; ++r) {
-            tma_load_4d(sbase + kOffK + p * 16384 + r * 8192, &mk, bar_kv, p * 64, m * 128 + r * 64, h, b);
-            tma_load_4d(sbase + kOffV + p * 16384 + r * 8192, &mv, bar_kv, p * 64, m * 128 + r * 64, h, b);
-          }
+    if (lane == 0) {
+      tma_prefetch_map(&mq);
+      tma_prefetch_map(&mdo);
+      tma_prefetch_map(&mk);
+      tma_prefetch_map(&mv);
+    }
+    bool ok = true;
+    uint32_t U = 0, kvn = 0;
+    int x = blockIdx.x;
+    for (int n = 0; ok; ++n) {
+      const int slot = n & 1;
+      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_item_free(slot), ((n >> 1) - 1) & 1, abort_flag))) {
+        ok = false;
+        break;
       }
-      uint32_t chunk = 0;  // list entries t0 + lane of the current 32-entry chunk
-      bool ok = true;
-      for (int u = 0; u < nsub; ++u) {
-        const int t = u >> sub_shift, hh = u & sub_shift;
-        if ((t & 31) == 0 && hh == 0) chunk = t + lane < nu ? list[t + lane] : 0u;
-        int qi = (int)(__shfl_sync(0xffffffffu, chunk, t & 31) & 0x3FFFFFFFu);
-        if (qi >= s.Tq) {
-          if (lane == 0) report_error(a.status, kDevErrBounds);
-          qi = 0;
-        }
-        const int st = u & (kStages - 1);
-        if (u >= kStages && !__all_sync(0xffffffffu, mbar_wait(bar_empty(st), ((u >> 2) - 1) & 1, abort_flag))) {
+      const bool done = x >= num_items;
+      int xn = 0;
+      if (lane == 0) {
+        item_slot[slot] = done ? -1 : x;
+        mbar_arrive(bar_item_full(slot));
+        if (!done) xn = (int)gridDim.x + atomicAdd(a.work_ctr, 1);  // the item after this one
+      }
+      if (done) break;
+      const int nu = item_len(x, lane == 0);
+      const int nsub = nu << sub_shift;
+      if (nsub > 0) {
+        const int m = x / BH, bh = x - m * BH, b = bh / s.H, h = bh - b * s.H;
+        const uint32_t* list = a.pair_idx + ((int64_t)bh * Tp + m) * s.Tq;
+        // K, V of the previous pair are free once its S^T / dP^T MMAs completed
+        if (kvn >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_kvfree, (kvn - 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
         if (lane == 0) {
-          const uint32_t stg = sbase + kOffStage + st * kStageBytes;
-          const int row = (qi << sub_shift) + hh;  // 64-row sub-tile index within the head
-          mbar_arrive_expect_tx(bar_full(st), kStageTx);
-          for (int p = 0; p < 2; ++p) {
-            tma_load_4d(stg + kStageQ + p * 8192, &mq, bar_full(st), p * 64, row * 64, h, b);
-            tma_load_4d(stg + kStageDO + p * 8192, &mdo, bar_full(st), p * 64, row * 64, h, b);
-          }
-          bulk_load(stg + kStageStats, a.stats + ((int64_t)bh * Tsub + row) * 128, 512, bar_full(st));
+          mbar_arrive_expect_tx(bar_kv, 65536);
+          for (int p = 0; p < 2; ++p)
+            for (int r = 0; r < 2; ++r) {
+              tma_load_4d(sbase + kOffK + p * 16384 + r * 8192, &mk, bar_kv, p * 64, m * 128 + r * 64, h, b);
+              tma_load_4d(sbase + kOffV + p * 16384 + r * 8192, &mv, bar_kv, p * 64, m * 128 + r * 64, h, b);
+            }
         }
-        __syncwarp();
+        ++kvn;
+        uint32_t chunk = 0;  // list entries t0 + lane of the current 32-entry chunk
+        for (int u = 0; u < nsub; ++u, ++U) {
+          const int t = u >> sub_shift, hh = u & sub_shift;
+          if ((t & 31) == 0 && hh == 0) chunk = t + lane < nu ? list[t + lane] : 0u;
+          int qi = (int)(__shfl_sync(0xffffffffu, chunk, t & 31) & 0x3FFFFFFFu);
+          if (qi >= s.Tq) {
+            if (lane == 0) report_error(a.status, kDevErrBounds);
+            qi = 0;
+          }
+          const int st = U & (kStages - 1);
+          if (U >= kStages &&
+              !__all_sync(0xffffffffu, mbar_wait(bar_empty(st), ((U >> 2) - 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const uint32_t stg = sbase + kOffStage + st * kStageBytes;
+            const int row = (qi << sub_shift) + hh;  // 64-row sub-tile index within the head
+            mbar_arrive_expect_tx(bar_full(st), kStageTx);
+            for (int p = 0; p < 2; ++p) {
+              tma_load_4d(stg + kStageQ + p * 8192, &mq, bar_full(st), p * 64, row * 64, h, b);
+              tma_load_4d(stg + kStageDO + p * 8192, &mdo, bar_full(st), p * 64, row * 64, h, b);
+            }
+            bulk_load(stg + kStageStats, a.stats + ((int64_t)bh * Tsub + row) * 128, 512, bar_full(st));
+          }
+          __syncwarp();
+        }
       }
-      // no copy may still be in flight when the CTA exits
-      if (ok && lane == 0) {
-        const int first = nsub > kStages ? nsub - kStages : 0;
-        for (int u = first; u < nsub; ++u) mbar_wait(bar_full(u & (kStages - 1)), (u >> 2) & 1, abort_flag);
-        mbar_wait(bar_kv, 0, abort_flag);
-      }
+      x = __shfl_sync(0xffffffffu, xn, 0);
+    }
+    // no copy may still be in flight when the CTA exits
+    if (ok && lane == 0) {
+      for (uint32_t v = U > kStages ? U - kStages : 0; v < U; ++v)
+        mbar_wait(bar_full(v & (kStages - 1)), (v >> 2) & 1, abort_flag);
+      if (kvn > 0) mbar_wait(bar_kv, (kvn - 1) & 1, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- S^T, dP^T issuer (warp 1)
@@ -240,15 +306,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // while the MMA queue is full, so a single issuer that also waits on barriers between
     // its groups lets the tensor pipe drain; with S/dP and dV/dK issued by two warps, one
     // of them is always queued behind the other's MMAs.
-    if (nsub > 0) {
-      constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
-      const uint64_t kd = smem_desc(sbase + kOffK, 16, 1024), vd = smem_desc(sbase + kOffV, 16, 1024);
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar_kv, 0, abort_flag));
-      for (int u = 0; ok && u < nsub; ++u) {
-        const int st = u & (kStages - 1);
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (u >> 2) & 1, abort_flag))) break;
-        // S^T / dP^T of sub-tile u - 1 must have been read out of TMEM
-        if (u >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_sfree, (u - 1) & 1, abort_flag))) break;
+    constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
+    const uint64_t kd = smem_desc(sbase + kOffK, 16, 1024), vd = smem_desc(sbase + kOffV, 16, 1024);
+    bool ok = true;
+    uint32_t U = 0, kvn = 0;
+    for (int n = 0; ok; ++n) {
+      const int x = take_item(n, ok);
+      if (x < 0) break;
+      const int nsub = item_len(x, false) << sub_shift;
+      if (nsub == 0) continue;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_kv, kvn & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      ++kvn;
+      for (int u = 0; u < nsub; ++u, ++U) {
+        const int st = U & (kStages - 1);
+        // the stage landed, and S^T / dP^T of sub-tile U - 1 were read out of TMEM
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (U >> 2) & 1, abort_flag) &&
+                                         (U == 0 || mbar_wait(bar_sfree, (U - 1) & 1, abort_flag)))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t stg = sbase + kOffStage + st * kStageBytes;
         const uint64_t qd = smem_desc(stg + kStageQ, 16, 1024), dod = smem_desc(stg + kStageDO, 16, 1024);
@@ -259,21 +338,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      // no MMA of this warp may still run when TMEM is released (matters on the abort path)
-      if (elect_one()) umma_commit(bar_sdrain);
+      if (!ok) break;
+      if (elect_one()) umma_commit(bar_kvfree);
       __syncwarp();
-      mbar_wait(bar_sdrain, 0, abort_flag);
     }
+    // no MMA of this warp may still run when TMEM is released (matters on the abort path)
+    if (elect_one()) umma_commit(bar_sdrain);
+    __syncwarp();
+    mbar_wait(bar_sdrain, 0, abort_flag);
   } else if (warp == 2) {
     // --------------------------------------------------------- dV, dK issuer (warp 2)
-    if (nsub > 0) {
-      constexpr uint32_t idG = idesc_f16_f32(128, 128, false, true);
-      for (int w = 0; w < nsub; ++w) {
-        const int st = w & (kStages - 1), bb = w & 1;
-        // P^T / dS^T of sub-tile w written (the stage's load completed long before)
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (w >> 1) & 1, abort_flag) &&
-                                         mbar_wait(bar_full(st), (w >> 2) & 1, abort_flag)))
+    constexpr uint32_t idG = idesc_f16_f32(128, 128, false, true);
+    bool ok = true;
+    uint32_t W = 0;
+    for (int n = 0; ok; ++n) {
+      const int x = take_item(n, ok);
+      if (x < 0) break;
+      const int nsub = item_len(x, false) << sub_shift;
+      for (int w = 0; w < nsub; ++w, ++W) {
+        const int st = W & (kStages - 1), bb = W & 1;
+        // P^T / dS^T of sub-tile W written (the stage's load completed long before).  For
+        // the first sub-tile of a pair this also orders the overwrite of the dV, dK
+        // accumulators after the previous pair's epilogue: every element-wise thread read
+        // them out before it wrote this P^T / dS^T.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (W >> 1) & 1, abort_flag) &&
+                                         mbar_wait(bar_full(st), (W >> 2) & 1, abort_flag))) {
+          ok = false;
           break;
+        }
         tc_fence_after();
         const uint32_t stg = sbase + kOffStage + st * kStageBytes;
         // B = dO_w / Q_w read MN-major: 16 query rows (2048 B) per k-step, channel panels
@@ -287,105 +379,125 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      // the S^T / dP^T MMAs all completed before the last P^T was written, so this commit
-      // covers every MMA of the CTA
-      if (elect_one()) umma_commit(bar_drain);
+      if (!ok) break;
+      // the pair's S^T / dP^T MMAs all completed before its last P^T was written, so this
+      // commit covers every MMA of the pair
+      if (nsub > 0 && elect_one()) umma_commit(bar_drain);
       __syncwarp();
-      mbar_wait(bar_drain, 0, abort_flag);
     }
+    if (elect_one()) umma_commit(bar_gdrain);
+    __syncwarp();
+    mbar_wait(bar_gdrain, 0, abort_flag);
   } else {
     // ------------------------------------------------------------- element-wise warps
     const int q4 = warp & 3;          // TMEM lane quarter
     const int g = (warp - 3) >> 2;    // query columns 32g .. 32g+31 of each sub-tile
     const int r = 32 * q4 + lane;     // key row of the pair
     const int half = r >> 6;          // 0: key block 2m, 1: key block 2m+1
-    const int key = m * 128 + r;
-    const bool key_valid = key < s.N;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+    const int c0 = 64 * g;            // epilogue: channels 64g .. 64g+63 of the key row
     bool ok = true;
-    uint32_t e_next = nu > 0 ? list[0] : 0u;
-    uint32_t e = 0;
-    for (int u = 0; u < nsub; ++u) {
-      const int t = u >> sub_shift;
-      if ((u & sub_shift) == 0) {
-        e = e_next;
-        e_next = t + 1 < nu ? list[t + 1] : 0u;
-      }
-      const bool keep = ((e >> (30 + half)) & 1u) != 0;  // same for the whole warp
-      const int st = u & (kStages - 1), bb = u & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull, u & 1, abort_flag) &&
-                                       mbar_wait(bar_full(st), (u >> 2) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sv[32], dv[32];
-      tmem_ld32(trow + kColS + 32 * g, sv);
-      tmem_ld32(trow + kColDP + 32 * g, dv);
-      const float4* l4 = reinterpret_cast<const float4*>(smem + kOffStage + st * kStageBytes + kStageStats) + 8 * g;
-      const float4* d4 = l4 + 16;
-      tmem_ld_wait(sv);
-      tmem_ld_wait(dv);
-      tc_fence_before();
-      mbar_arrive(bar_sfree);
-      uint32_t pw[16], dw[16];
-      if (keep) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 L = l4[j], D = d4[j];
-          const float lv[4] = {L.x, L.y, L.z, L.w}, Dv[4] = {D.x, D.y, D.z, D.w};
-          float pv[4], ds[4];
-#pragma unroll
-          for (int e4 = 0; e4 < 4; ++e4) {
-            const int c = 4 * j + e4;
-            const float p = key_valid ? ex2(fmaf(__uint_as_float(sv[c]), a.scale_log2, -lv[e4])) : 0.f;
-            pv[e4] = p;
-            ds[e4] = p * (__uint_as_float(dv[c]) - Dv[e4]);
-          }
-          pw[2 * j] = pack_f16x2(pv[0], pv[1]);
-          pw[2 * j + 1] = pack_f16x2(pv[2], pv[3]);
-          dw[2 * j] = pack_f16x2(ds[0], ds[1]);
-          dw[2 * j + 1] = pack_f16x2(ds[2], ds[3]);
+    uint32_t U = 0, an = 0;
+    for (int n = 0; ok; ++n) {
+      const int x = take_item(n, ok);
+      if (x < 0) break;
+      const int nu = item_len(x, false);
+      const int nsub = nu << sub_shift;
+      const int m = x / BH, bh = x - m * BH, b = bh / s.H, h = bh - b * s.H;
+      const uint32_t* list = a.pair_idx + ((int64_t)bh * Tp + m) * s.Tq;
+      const int key = m * 128 + r;
+      const bool key_valid = key < s.N;
+      uint32_t e_next = nu > 0 ? list[0] : 0u;
+      uint32_t e = 0;
+      for (int u = 0; u < nsub; ++u, ++U) {
+        const int t = u >> sub_shift;
+        if ((u & sub_shift) == 0) {
+          e = e_next;
+          e_next = t + 1 < nu ? list[t + 1] : 0u;
         }
-      } else {
+        const bool keep = ((e >> (30 + half)) & 1u) != 0;  // same for the whole warp
+        const int st = U & (kStages - 1), bb = U & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull, U & 1, abort_flag) &&
+                                         mbar_wait(bar_full(st), (U >> 2) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[32], dv[32];
+        tmem_ld32(trow + kColS + 32 * g, sv);
+        tmem_ld32(trow + kColDP + 32 * g, dv);
+        const float4* l4 =
+            reinterpret_cast<const float4*>(smem + kOffStage + st * kStageBytes + kStageStats) + 8 * g;
+        const float4* d4 = l4 + 16;
+        tmem_ld_wait(sv);
+        tmem_ld_wait(dv);
+        tc_fence_before();
+        mbar_arrive(bar_sfree);
+        uint32_t pw[16], dw[16];
+        if (keep) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) pw[j] = dw[j] = 0u;
+          for (int j = 0; j < 8; ++j) {
+            const float4 L = l4[j], D = d4[j];
+            const float lv[4] = {L.x, L.y, L.z, L.w}, Dv[4] = {D.x, D.y, D.z, D.w};
+            float pv[4], ds[4];
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+              const int c = 4 * j + e4;
+              const float p = key_valid ? ex2(fmaf(__uint_as_float(sv[c]), a.scale_log2, -lv[e4])) : 0.f;
+              pv[e4] = p;
+              ds[e4] = p * (__uint_as_float(dv[c]) - Dv[e4]);
+            }
+            pw[2 * j] = pack_f16x2(pv[0], pv[1]);
+            pw[2 * j + 1] = pack_f16x2(pv[2], pv[3]);
+            dw[2 * j] = pack_f16x2(ds[0], ds[1]);
+            dw[2 * j + 1] = pack_f16x2(ds[2], ds[3]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pw[j] = dw[j] = 0u;
+        }
+        // buffer bb was last read by the dV / dK MMAs of sub-tile U - 2
+        if (U >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_pfree(bb), ((U >> 1) - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st16(trow + kColP + bb * 32 + 16 * g, pw);
+        tmem_st16(trow + kColDS + bb * 32 + 16 * g, dw);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_pready(bb));
       }
-      // buffer bb was last read by the dV / dK MMAs of sub-tile u - 2
-      if (u >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_pfree(bb), ((u >> 1) - 1) & 1, abort_flag))) {
+      if (!ok) break;
+      // ---- dK, dV of the pair: thread = key row, 64 channels 64g .. 64g+63
+      GT* dkp = reinterpret_cast<GT*>(a.dk) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + (int64_t)key * a.g_sn + c0;
+      GT* dvp = reinterpret_cast<GT*>(a.dv) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + (int64_t)key * a.g_sn + c0;
+      const bool store = key_valid && c0 < s.d;
+      if (nsub == 0) {
+        if (store) {
+          zero_row64<GT>(dkp);
+          zero_row64<GT>(dvp);
+        }
+        continue;
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_drain, an & 1, abort_flag))) {
         ok = false;
         break;
       }
+      ++an;
       tc_fence_after();
-      tmem_st16(trow + kColP + bb * 32 + 16 * g, pw);
-      tmem_st16(trow + kColDS + bb * 32 + 16 * g, dw);
-      tmem_st_wait();
+      uint32_t xv[32], yv[32];
+      tmem_ld32(trow + kColDK + c0, xv);
+      tmem_ld32(trow + kColDK + c0 + 32, yv);
+      tmem_ld_wait(xv);
+      tmem_ld_wait(yv);
+      if (store) store_row64<GT>(dkp, xv, yv, a.scale);
+      tmem_ld32(trow + kColDV + c0, xv);
+      tmem_ld32(trow + kColDV + c0 + 32, yv);
+      tmem_ld_wait(xv);
+      tmem_ld_wait(yv);
       tc_fence_before();
-      mbar_arrive(bar_pready(bb));
-    }
-    // ---- dK, dV of the pair: thread = key row, 64 channels 64g .. 64g+63
-    const int c0 = 64 * g;
-    GT* dkp = reinterpret_cast<GT*>(a.dk) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + (int64_t)key * a.g_sn + c0;
-    GT* dvp = reinterpret_cast<GT*>(a.dv) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + (int64_t)key * a.g_sn + c0;
-    const bool store = key_valid && c0 < s.d;
-    if (nsub == 0) {
-      if (store) {
-        zero_row64<GT>(dkp);
-        zero_row64<GT>(dvp);
-      }
-    } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar_drain, 0, abort_flag))) {
-      tc_fence_after();
-      uint32_t x[32], y[32];
-      tmem_ld32(trow + kColDK + c0, x);
-      tmem_ld32(trow + kColDK + c0 + 32, y);
-      tmem_ld_wait(x);
-      tmem_ld_wait(y);
-      if (store) store_row64<GT>(dkp, x, y, a.scale);
-      tmem_ld32(trow + kColDV + c0, x);
-      tmem_ld32(trow + kColDV + c0 + 32, y);
-      tmem_ld_wait(x);
-      tmem_ld_wait(y);
-      if (store) store_row64<GT>(dvp, x, y, 1.f);
+      if (store) store_row64<GT>(dvp, xv, yv, 1.f);
     }
   }
   tc_fence_before();
@@ -407,9 +519,12 @@ __global__ void __launch_bounds__(32 * kUnionWarps) pair_union_kernel(const int3
                                                                      const int32_t* __restrict__ col_idx, ShapeArgs s,
                                                                      int32_t* __restrict__ pair_cnt,
                                                                      uint32_t* __restrict__ pair_idx,
+                                                                     int* __restrict__ work_ctr,
                                                                      unsigned* status) {
   __shared__ uint32_t bits[kUnionWarps][2][kMaxTqWords];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the work counters of the two persistent backward kernels that run after this pass
+  if (blockIdx.x == 0 && threadIdx.x < kBwdWorkCounters) work_ctr[threadIdx.x] = 0;
   const int Tp = (s.Tk + 1) >> 1;
   const int64_t pid = (int64_t)blockIdx.x * kUnionWarps + warp;
   if (pid >= (int64_t)s.B * s.H * Tp) return;  // whole warps only; no block-wide barrier below
@@ -470,15 +585,20 @@ cudaError_t launch_bwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtens
   const long long pairs = (long long)s.B * s.H * ((s.Tk + 1) / 2);
   prof_start(st, kBwdPairs);
   pair_union_kernel<<<(unsigned)((pairs + kUnionWarps - 1) / kUnionWarps), 32 * kUnionWarps, 0, st>>>(
-      a.col_cnt, a.col_idx, s, a.pair_cnt, a.pair_idx, a.status);
+      a.col_cnt, a.col_idx, s, a.pair_cnt, a.pair_idx, a.work_ctr, a.status);
   prof_stop(st, kBwdPairs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   auto kern = attn_bwd_dkdv_kernel<GT>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long grid = pairs < sms ? pairs : sms;  // persistent: one CTA per SM
   prof_start(st, kAttnBwd);
-  kern<<<(unsigned)pairs, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, s, a);
+  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, s, a);
   prof_stop(st, kAttnBwd);
   return cudaGetLastError();
 }
@@ -489,7 +609,7 @@ size_t bwd_pair_entries(const ShapeArgs& s) { return (size_t)s.B * s.H * ((s.Tk 
 
 cudaError_t launch_attn_bwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                             const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st) {
-  if (s.Tq > 32 * kMaxTqWords) return cudaErrorInvalidValue;
+  if (s.Tq > 32 * kMaxTqWords || (long long)s.B * s.H * ((s.Tk + 1) / 2) > INT32_MAX) return cudaErrorInvalidValue;
   return s.dtype == 0 ? launch_bwd_t<__nv_bfloat16>(s, mq, mk, mv, mdo, a, st)
                       : launch_bwd_t<float>(s, mq, mk, mv, mdo, a, st);
 }

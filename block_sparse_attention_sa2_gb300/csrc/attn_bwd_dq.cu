@@ -7,8 +7,8 @@
 // walks that block's list of kept key blocks -- the forward's traversal -- so dQ
 // accumulates in TMEM over the whole list and is written once: no cross-CTA reduction.
 //
-// Roles (352 threads, 1 CTA per SM): warp 0 TMA (Q and dO once, K_j / V_j per kept block
-// into 4 / 2 stages), warp 1 TMEM owner and issuer of the S_j / dP_j MMAs, warp 2 issuer of
+// Roles (352 threads, 1 CTA per SM): warp 0 TMA (Q and dO once per query block, K_j / V_j
+// per kept block into 4 / 2 stages), warp 1 TMEM owner and issuer of the S_j / dP_j MMAs, warp 2 issuer of
 // the dQ MMAs (each converged, one elect.sync lane issuing: two issuers keep the MMA queue
 // fed while either waits on a barrier), and two row warpgroups (warps 3..6 and 7..10) that
 // both work on every list entry (TMEM buffers j % 2), one query row per thread, group g on
@@ -23,12 +23,20 @@
 // 384 (d columns).  S_j / dP_j may overwrite their buffers as soon as the row threads have
 // read S_{j-2} / dP_{j-2} out; only the row threads wait for dQ_{j-2} to complete before
 // writing dS_j, so the tensor pipe never drains to let an MMA overwrite an operand.
+//
+// The CTAs are persistent, one per SM, and take query blocks from a counter until none is
+// left.  The producer publishes each block in a two-slot ring in shared memory that every
+// role reads; the K / V rings and the TMEM buffers run on across blocks.  So the set-up is
+// paid once per SM, the next block's K_j / V_j stream in behind the current block's, its
+// Q and dO load as soon as the current block's S_j / dP_j MMAs have completed, and its
+// first S_j / dP_j MMAs run while the row threads store the current block's dQ.
 #include "sa2_internal.h"
 
 namespace sa2 {
 namespace {
 
 constexpr int kThreads = 352;
+constexpr int kItemReaders = 10;  // warps reading the item slot: 1, 2 and the 8 row warps
 // K_j feeds S_j and, after the softmax, dQ += dS_j K_j, so its ring is deep; V_j only feeds
 // dP_j and is released right after it
 constexpr int kKStages = 4;
@@ -46,7 +54,7 @@ struct DqSmem {
   static constexpr int kOffK = kOffDO + kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kKVBytes;
   static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
-  static constexpr int kBytes = kOffBar + 256 + 1024;
+  static constexpr int kBytes = kOffBar + 512 + 1024;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -82,7 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-  const uint32_t bar_q = smem_u32(&bars[0]);
+  const uint32_t bar_q = smem_u32(&bars[0]);  // Q, dO of the current query block landed
   auto bar_kfull = [&](int st) { return smem_u32(&bars[1 + st]); };
   auto bar_kempty = [&](int st) { return smem_u32(&bars[5 + st]); };
   auto bar_vfull = [&](int st) { return smem_u32(&bars[9 + st]); };
@@ -91,24 +99,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_sfree = [&](int b) { return smem_u32(&bars[15 + b]); };   // ... read out by the rows
   auto bar_pready = [&](int b) { return smem_u32(&bars[17 + b]); };  // dS_j written
   auto bar_pfree = [&](int b) { return smem_u32(&bars[19 + b]); };   // dQ MMA reading dS_j done
-  const uint32_t bar_dq = smem_u32(&bars[21]);
-  const uint32_t bar_drain = smem_u32(&bars[22]);
-  const uint32_t bar_sdrain = smem_u32(&bars[23]);
-  // 24 barriers occupy the first 192 bytes of the 256-byte barrier area
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 224);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffBar + 240);
+  const uint32_t bar_dq = smem_u32(&bars[21]);      // every dQ MMA of the query block completed
+  const uint32_t bar_gdrain = smem_u32(&bars[22]);  // every dQ MMA of the CTA completed
+  const uint32_t bar_sdrain = smem_u32(&bars[23]);  // every S_j / dP_j MMA of the CTA completed
+  const uint32_t bar_qfree = smem_u32(&bars[24]);   // every S_j / dP_j MMA of the query block completed
+  auto bar_item_full = [&](int i) { return smem_u32(&bars[25 + i]); };  // item slot i written
+  auto bar_item_free = [&](int i) { return smem_u32(&bars[27 + i]); };  // ... and read by every role
+  // 29 barriers occupy the first 232 bytes of the 512-byte barrier area
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 384);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffBar + 392);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kOffBar + 400);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x / s.Tq;
-  const int qi = blockIdx.x % s.Tq;
-  const int b = bh / s.H, h = bh % s.H;
-  const int64_t rowid = (int64_t)bh * s.Tq + qi;
-  int nkv = a.row_cnt[rowid];
-  if (nkv < 0 || nkv > s.Tk) {
-    if (tid == 0) report_error(a.status, kDevErrBounds);
-    nkv = nkv < 0 ? 0 : s.Tk;
-  }
-  const int32_t* list = a.row_idx + rowid * s.Tk;
+  // Work items are query blocks (item x: block x % Tq of head x / Tq).  Each CTA stays
+  // resident and takes items from a counter: its first is blockIdx.x, the next
+  // gridDim.x + (counter value).
+  const int num_items = s.B * s.H * s.Tq;
+  // list length of item x, clamped to [0, Tk] (the producer reports a bad value)
+  auto item_len = [&](int x, bool report) {
+    int nkv = a.row_cnt[x];
+    if (nkv < 0 || nkv > s.Tk) {
+      if (report) report_error(a.status, kDevErrBounds);
+      nkv = nkv < 0 ? 0 : s.Tk;
+    }
+    return nkv;
+  };
+  // a consumer warp takes item n from its slot and hands the slot back; -1 ends the loop
+  auto take_item = [&](int n, bool& ok) {
+    const int slot = n & 1;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar_item_full(slot), (n >> 1) & 1, abort_flag))) {
+      ok = false;
+      return -1;
+    }
+    const int x = item_slot[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_item_free(slot));
+    return x;
+  };
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -126,10 +153,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_sfree(bb), 256);
       mbar_init(bar_pready(bb), 256);
       mbar_init(bar_pfree(bb), 1);
+      mbar_init(bar_item_full(bb), 1);
+      mbar_init(bar_item_free(bb), kItemReaders);
     }
     mbar_init(bar_dq, 1);
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_gdrain, 1);
     mbar_init(bar_sdrain, 1);
+    mbar_init(bar_qfree, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -141,50 +171,107 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Barrier phases count list entries (J) and query blocks with a non-empty list (qn, an)
+  // over all items of the CTA, so every ring runs on across item boundaries.
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0 && nkv > 0) {
+    if (lane == 0) {
+      tma_prefetch_map(&mq);
+      tma_prefetch_map(&mdo);
       tma_prefetch_map(&mk);
       tma_prefetch_map(&mv);
-      mbar_arrive_expect_tx(bar_q, 2 * L::kQBytes);
-      for (int p = 0; p < L::kPanels; ++p) {
-        tma_load_4d(sbase + L::kOffQ + p * 16384, &mq, bar_q, p * 64, qi * s.bq, h, b);
-        tma_load_4d(sbase + L::kOffDO + p * 16384, &mdo, bar_q, p * 64, qi * s.bq, h, b);
-      }
-      for (int j = 0; j < nkv; ++j) {
-        const int ks = j % kKStages, vs = j % kVStages;
-        int kb = list[j];
-        if (kb < 0 || kb >= s.Tk) {
-          report_error(a.status, kDevErrBounds);
-          kb = 0;
+      bool ok = true;
+      uint32_t J = 0, qn = 0;
+      int x = blockIdx.x;
+      for (int n = 0; ok; ++n) {
+        const int slot = n & 1;
+        if (n >= 2 && !mbar_wait(bar_item_free(slot), ((n >> 1) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
         }
-        if (j >= kKStages && !mbar_wait(bar_kempty(ks), ((j / kKStages) - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(bar_kfull(ks), L::kKVBytes);
-        for (int p = 0; p < L::kPanels; ++p)
-          tma_load_4d(sbase + L::kOffK + ks * L::kKVBytes + p * 8192, &mk, bar_kfull(ks), p * 64, kb * 64, h, b);
-        if (j >= kVStages && !mbar_wait(bar_vempty(vs), ((j / kVStages) - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(bar_vfull(vs), L::kKVBytes);
-        for (int p = 0; p < L::kPanels; ++p)
-          tma_load_4d(sbase + L::kOffV + vs * L::kKVBytes + p * 8192, &mv, bar_vfull(vs), p * 64, kb * 64, h, b);
+        const bool done = x >= num_items;
+        item_slot[slot] = done ? -1 : x;
+        mbar_arrive(bar_item_full(slot));
+        if (done) break;
+        const int xn = (int)gridDim.x + atomicAdd(a.work_ctr, 1);  // the item after this one
+        const int nkv = item_len(x, true);
+        if (nkv > 0) {
+          const int bh = x / s.Tq, qi = x - bh * s.Tq, b = bh / s.H, h = bh - b * s.H;
+          const int32_t* list = a.row_idx + (int64_t)x * s.Tk;
+          // Q, dO of the previous query block are free once its S_j / dP_j MMAs completed
+          if (qn >= 1 && !mbar_wait(bar_qfree, (qn - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ++qn;
+          mbar_arrive_expect_tx(bar_q, 2 * L::kQBytes);
+          for (int p = 0; p < L::kPanels; ++p) {
+            tma_load_4d(sbase + L::kOffQ + p * 16384, &mq, bar_q, p * 64, qi * s.bq, h, b);
+            tma_load_4d(sbase + L::kOffDO + p * 16384, &mdo, bar_q, p * 64, qi * s.bq, h, b);
+          }
+          for (int j = 0; j < nkv; ++j, ++J) {
+            const int ks = J % kKStages, vs = J % kVStages;
+            int kb = list[j];
+            if (kb < 0 || kb >= s.Tk) {
+              report_error(a.status, kDevErrBounds);
+              kb = 0;
+            }
+            if (J >= kKStages && !mbar_wait(bar_kempty(ks), ((J / kKStages) - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar_kfull(ks), L::kKVBytes);
+            for (int p = 0; p < L::kPanels; ++p)
+              tma_load_4d(sbase + L::kOffK + ks * L::kKVBytes + p * 8192, &mk, bar_kfull(ks), p * 64, kb * 64, h,
+                          b);
+            if (J >= kVStages && !mbar_wait(bar_vempty(vs), ((J / kVStages) - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar_vfull(vs), L::kKVBytes);
+            for (int p = 0; p < L::kPanels; ++p)
+              tma_load_4d(sbase + L::kOffV + vs * L::kKVBytes + p * 8192, &mv, bar_vfull(vs), p * 64, kb * 64, h,
+                          b);
+          }
+        }
+        x = xn;
       }
-      const int kfirst = nkv > kKStages ? nkv - kKStages : 0;
-      for (int j = kfirst; j < nkv; ++j) mbar_wait(bar_kfull(j % kKStages), (j / kKStages) & 1, abort_flag);
-      const int vfirst = nkv > kVStages ? nkv - kVStages : 0;
-      for (int j = vfirst; j < nkv; ++j) mbar_wait(bar_vfull(j % kVStages), (j / kVStages) & 1, abort_flag);
+      // no copy may still be in flight when the CTA exits
+      if (ok) {
+        for (uint32_t v = J > kKStages ? J - kKStages : 0; v < J; ++v)
+          mbar_wait(bar_kfull(v % kKStages), (v / kKStages) & 1, abort_flag);
+        for (uint32_t v = J > kVStages ? J - kVStages : 0; v < J; ++v)
+          mbar_wait(bar_vfull(v % kVStages), (v / kVStages) & 1, abort_flag);
+        if (qn > 0) mbar_wait(bar_q, (qn - 1) & 1, abort_flag);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ S_j, dP_j issuer
-    if (nkv > 0) {
-      constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
-      const uint64_t qd = smem_desc(sbase + L::kOffQ, 16, 1024), dod = smem_desc(sbase + L::kOffDO, 16, 1024);
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag));
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int ks = j % kKStages, vs = j % kVStages, bb = j & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_kfull(ks), (j / kKStages) & 1, abort_flag))) break;
-        // buffer bb held S_{j-2} / dP_{j-2}: the row threads must have read them out
-        if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_sfree(bb), ((j >> 1) - 1) & 1, abort_flag))) break;
-        // both stages present before the S_j and dP_j MMAs issue as one group
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_vfull(vs), (j / kVStages) & 1, abort_flag))) break;
+    constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
+    const uint64_t qd = smem_desc(sbase + L::kOffQ, 16, 1024), dod = smem_desc(sbase + L::kOffDO, 16, 1024);
+    bool ok = true;
+    uint32_t J = 0, qn = 0;
+    for (int n = 0; ok; ++n) {
+      const int x = take_item(n, ok);
+      if (x < 0) break;
+      const int nkv = item_len(x, false);
+      if (nkv == 0) continue;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_q, qn & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      ++qn;
+      for (int j = 0; j < nkv; ++j, ++J) {
+        const int ks = J % kKStages, vs = J % kVStages, bb = J & 1;
+        // K_j and V_j present, and buffer bb (S_{j-2} / dP_{j-2}) read out by the row
+        // threads, before the S_j and dP_j MMAs issue as one group
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(bar_kfull(ks), (J / kKStages) & 1, abort_flag) &&
+                            (J < 2 || mbar_wait(bar_sfree(bb), ((J >> 1) - 1) & 1, abort_flag)) &&
+                            mbar_wait(bar_vfull(vs), (J / kVStages) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint64_t kd = smem_desc(sbase + L::kOffK + ks * L::kKVBytes, 16, 1024);
         const uint64_t vd = smem_desc(sbase + L::kOffV + vs * L::kKVBytes, 16, 1024);
@@ -196,20 +283,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      // no MMA of this warp may still run when TMEM is released (matters on the abort path)
-      if (elect_one()) umma_commit(bar_sdrain);
+      if (!ok) break;
+      if (elect_one()) umma_commit(bar_qfree);
       __syncwarp();
-      mbar_wait(bar_sdrain, 0, abort_flag);
     }
+    // no MMA of this warp may still run when TMEM is released (matters on the abort path)
+    if (elect_one()) umma_commit(bar_sdrain);
+    __syncwarp();
+    mbar_wait(bar_sdrain, 0, abort_flag);
   } else if (warp == 2) {
     // ------------------------------------------------------------------ dQ issuer
-    if (nkv > 0) {
-      constexpr uint32_t idQ = idesc_f16_f32(128, D, false, true);
-      for (int j = 0; j < nkv; ++j) {
-        const int ks = j % kKStages, bb = j & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (j >> 1) & 1, abort_flag) &&
-                                         mbar_wait(bar_kfull(ks), (j / kKStages) & 1, abort_flag)))
+    constexpr uint32_t idQ = idesc_f16_f32(128, D, false, true);
+    bool ok = true;
+    uint32_t J = 0;
+    for (int n = 0; ok; ++n) {
+      const int x = take_item(n, ok);
+      if (x < 0) break;
+      const int nkv = item_len(x, false);
+      for (int j = 0; j < nkv; ++j, ++J) {
+        const int ks = J % kKStages, bb = J & 1;
+        // dS_j written.  For the first entry of a query block this also orders the
+        // overwrite of the dQ accumulator after the previous block's epilogue: every row
+        // thread read dQ out before it wrote this dS.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (J >> 1) & 1, abort_flag) &&
+                                         mbar_wait(bar_kfull(ks), (J / kKStages) & 1, abort_flag))) {
+          ok = false;
           break;
+        }
         tc_fence_after();
         // K as the MN-major B operand: N = D (64-element groups 8 KB apart), K = 16 keys
         const uint64_t kmn = smem_desc(sbase + L::kOffK + ks * L::kKVBytes, 8192, 1024);
@@ -220,84 +320,99 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      // the S_j / dP_j MMAs all completed before the last dS was written, so these commits
-      // cover every MMA of the CTA
-      if (elect_one()) {
-        umma_commit(bar_dq);
-        umma_commit(bar_drain);
-      }
+      if (!ok) break;
+      // the block's S_j / dP_j MMAs all completed before its last dS was written, so this
+      // commit covers every MMA of the block
+      if (nkv > 0 && elect_one()) umma_commit(bar_dq);
       __syncwarp();
-      mbar_wait(bar_drain, 0, abort_flag);
     }
+    if (elect_one()) umma_commit(bar_gdrain);
+    __syncwarp();
+    mbar_wait(bar_gdrain, 0, abort_flag);
   } else {
     // -------------------------------------------------------------- query-row threads
     const int wg = (warp - 3) >> 2;  // row warpgroup 0 or 1
     const int sub = warp & 3;
     const int r = 32 * sub + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * sub) << 16);
-    const int64_t tok = (int64_t)qi * s.bq + r;
-    const bool row_valid = r < s.bq && tok < s.N;
-    // statistics record of this row: 64-row sub-tile (qi * bq + r) / 64 of the head
-    const float* rec = a.stats + ((int64_t)bh * (s.Tq * (s.bq / 64)) + ((qi * s.bq + r) >> 6)) * 128 + (r & 63);
-    const float lse2 = row_valid ? rec[0] : 0.f;
-    const float Dr = row_valid ? rec[64] : 0.f;
-    bool ok = true;
-    // both groups take every entry j (TMEM buffers j % 2), group wg its key columns
-    // 32 wg .. 32 wg + 31
-    int next_kb = nkv > 0 ? list[0] : 0;
-    for (int j = 0; j < nkv; ++j) {
-      const int bb = j & 1, jn = j >> 1;
-      int kb = next_kb;
-      if (j + 1 < nkv) next_kb = list[j + 1];
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bb), jn & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      kb = (kb < 0 || kb >= s.Tk) ? 0 : kb;
-      const int kv_valid = min(64, s.N - kb * 64);
-      uint32_t sv[32], dv[32], pk[16];
-      tmem_ld32(trow + kColS + bb * 64 + 32 * wg, sv);
-      tmem_ld32(trow + kColDP + bb * 64 + 32 * wg, dv);
-      tmem_ld_wait(sv);
-      tmem_ld_wait(dv);
-      // S_j / dP_j are in registers: their buffer may be overwritten
-      tc_fence_before();
-      mbar_arrive(bar_sfree(bb));
-#pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float ds[2];
-#pragma unroll
-        for (int z = 0; z < 2; ++z) {
-          const bool cv = row_valid && (32 * wg + c + z) < kv_valid;
-          const float p = cv ? ex2(__uint_as_float(sv[c + z]) * a.scale_log2 - lse2) : 0.f;
-          ds[z] = p * (__uint_as_float(dv[c + z]) - Dr);
-        }
-        pk[c / 2] = pack_f16x2(ds[0], ds[1]);
-      }
-      // dS buffer bb was last read by the dQ MMA of entry j - 2
-      if (jn >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_pfree(bb), (jn - 1) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st16(trow + kColDS + bb * 32 + 16 * wg, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar_pready(bb));
-    }
-    // ---- epilogue: dQ = scale * (dS K) accumulated over the list; each group stores half
-    // of the channels of every row
-    OutT* dqrow = reinterpret_cast<OutT*>(a.dq) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + tok * a.g_sn;
     const int c_begin = wg * (D / 2), c_end = c_begin + D / 2;
-    if (nkv == 0) {
-      if (row_valid) {
-        float z[32];
+    bool ok = true;
+    uint32_t J = 0, an = 0;
+    for (int n = 0; ok; ++n) {
+      const int x = take_item(n, ok);
+      if (x < 0) break;
+      const int nkv = item_len(x, false);
+      const int bh = x / s.Tq, qi = x - bh * s.Tq, b = bh / s.H, h = bh - b * s.H;
+      const int32_t* list = a.row_idx + (int64_t)x * s.Tk;
+      const int64_t tok = (int64_t)qi * s.bq + r;
+      const bool row_valid = r < s.bq && tok < s.N;
+      // statistics record of this row: 64-row sub-tile (qi * bq + r) / 64 of the head
+      const float* rec =
+          a.stats + ((int64_t)bh * (s.Tq * (s.bq / 64)) + ((qi * s.bq + r) >> 6)) * 128 + (r & 63);
+      const float lse2 = row_valid && nkv > 0 ? rec[0] : 0.f;
+      const float Dr = row_valid && nkv > 0 ? rec[64] : 0.f;
+      // both groups take every entry j (TMEM buffers J % 2), group wg its key columns
+      // 32 wg .. 32 wg + 31
+      int next_kb = nkv > 0 ? list[0] : 0;
+      for (int j = 0; j < nkv; ++j, ++J) {
+        const int bb = J & 1, jn = J >> 1;
+        int kb = next_kb;
+        if (j + 1 < nkv) next_kb = list[j + 1];
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bb), jn & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        kb = (kb < 0 || kb >= s.Tk) ? 0 : kb;
+        const int kv_valid = min(64, s.N - kb * 64);
+        uint32_t sv[32], dv[32], pk[16];
+        tmem_ld32(trow + kColS + bb * 64 + 32 * wg, sv);
+        tmem_ld32(trow + kColDP + bb * 64 + 32 * wg, dv);
+        tmem_ld_wait(sv);
+        tmem_ld_wait(dv);
+        // S_j / dP_j are in registers: their buffer may be overwritten
+        tc_fence_before();
+        mbar_arrive(bar_sfree(bb));
 #pragma unroll
-        for (int c = 0; c < 32; ++c) z[c] = 0.f;
-        for (int c0 = c_begin; c0 < c_end; c0 += 32) store_chunk<OutT>(dqrow + c0, z);
+        for (int c = 0; c < 32; c += 2) {
+          float ds[2];
+#pragma unroll
+          for (int z = 0; z < 2; ++z) {
+            const bool cv = row_valid && (32 * wg + c + z) < kv_valid;
+            const float p = cv ? ex2(__uint_as_float(sv[c + z]) * a.scale_log2 - lse2) : 0.f;
+            ds[z] = p * (__uint_as_float(dv[c + z]) - Dr);
+          }
+          pk[c / 2] = pack_f16x2(ds[0], ds[1]);
+        }
+        // dS buffer bb was last read by the dQ MMA of entry J - 2
+        if (jn >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_pfree(bb), (jn - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st16(trow + kColDS + bb * 32 + 16 * wg, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_pready(bb));
       }
-    } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar_dq, 0, abort_flag))) {
+      if (!ok) break;
+      // ---- epilogue: dQ = scale * (dS K) accumulated over the list; each group stores
+      // half of the channels of every row
+      OutT* dqrow = reinterpret_cast<OutT*>(a.dq) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + tok * a.g_sn;
+      if (nkv == 0) {
+        if (row_valid) {
+          float z[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) z[c] = 0.f;
+          for (int c0 = c_begin; c0 < c_end; c0 += 32) store_chunk<OutT>(dqrow + c0, z);
+        }
+        continue;
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, an & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      ++an;
       tc_fence_after();
 #pragma unroll 1
       for (int c0 = c_begin; c0 < c_end; c0 += 32) {
@@ -309,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(o[c]) * a.scale;
         if (row_valid) store_chunk<OutT>(dqrow + c0, v);
       }
+      tc_fence_before();
     }
   }
   tc_fence_before();
@@ -327,8 +443,14 @@ cudaError_t launch_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMa
   auto kern = attn_bwd_dq_kernel<D, OutT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long items = (long long)s.B * s.H * s.Tq;
+  const long long grid = items < sms ? items : sms;  // persistent: one CTA per SM
   prof_start(st, kAttnBwdDq);
-  kern<<<(unsigned)((long long)s.B * s.H * s.Tq), kThreads, smem, st>>>(mq, mk, mv, mdo, s, a);
+  kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, mdo, s, a);
   prof_stop(st, kAttnBwdDq);
   return cudaGetLastError();
 }
@@ -337,6 +459,7 @@ cudaError_t launch_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMa
 
 cudaError_t launch_attn_bwd_dq(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk,
                                const CUtensorMap& mv, const CUtensorMap& mdo, const DqArgs& a, cudaStream_t st) {
+  if ((long long)s.B * s.H * s.Tq > INT32_MAX) return cudaErrorInvalidValue;
   if (s.d == 128)
     return s.dtype == 0 ? launch_t<128, __nv_bfloat16>(s, mq, mk, mv, mdo, a, st)
                         : launch_t<128, float>(s, mq, mk, mv, mdo, a, st);

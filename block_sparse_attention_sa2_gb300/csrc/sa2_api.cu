@@ -96,7 +96,7 @@ FwdWs fwd_ws(const ShapeArgs& s) {
 // Backward workspace: per-row statistics, the pair-union lists of the dK / dV kernel, and
 // fp16 copies of Q, K, V, dO.
 struct BwdWs {
-  size_t stats, pair_cnt, pair_idx, q16, k16, v16, do16, total;
+  size_t stats, pair_cnt, pair_idx, q16, k16, v16, do16, ctr, total;
 };
 BwdWs bwd_ws(const ShapeArgs& s) {
   BwdWs w{};
@@ -108,7 +108,8 @@ BwdWs bwd_ws(const ShapeArgs& s) {
   w.k16 = w.q16 + t;
   w.v16 = w.k16 + t;
   w.do16 = w.v16 + t;
-  w.total = w.do16 + t;
+  w.ctr = w.do16 + t;
+  w.total = w.ctr + align_up(sizeof(int) * kBwdWorkCounters);
   return w;
 }
 
@@ -286,6 +287,7 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   a.col_idx = mask->col_idx;
   a.pair_cnt = reinterpret_cast<int32_t*>(wsb + w.pair_cnt);
   a.pair_idx = reinterpret_cast<uint32_t*>(wsb + w.pair_idx);
+  a.work_ctr = reinterpret_cast<int*>(wsb + w.ctr);
   a.stats = stats;
   a.dk = dk;
   a.dv = dv;
@@ -300,6 +302,7 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   g.row_cnt = mask->row_cnt;
   g.row_idx = mask->row_idx;
   g.stats = stats;
+  g.work_ctr = a.work_ctr + 1;
   g.dq = dq;
   g.g_sb = s.sb;
   g.g_sh = s.sh;

@@ -86,6 +86,8 @@ struct BwdArgs {
   uint32_t* pair_idx;      // [B*H, ceil(Tk/2), Tq] union entries: q block | bit 30 kept by
                            // block 2m | bit 31 kept by block 2m+1 (workspace)
   const float* stats;      // per-row statistics, layout above
+  int* work_ctr;           // [kBwdWorkCounters] item counters of the persistent kernels
+                           // (workspace; zeroed by the pair-union pass)
   void* dk;
   void* dv;
   int64_t g_sb, g_sh, g_sn;  // strides of dk / dv (dtype of the call)
@@ -98,6 +100,7 @@ struct DqArgs {
   const int32_t* row_cnt;
   const int32_t* row_idx;
   const float* stats;
+  int* work_ctr;  // item counter of the persistent kernel (workspace; zeroed by the pair-union pass)
   void* dq;
   int64_t g_sb, g_sh, g_sn;
   float scale;
@@ -107,6 +110,7 @@ struct DqArgs {
 
 // Entries of BwdArgs::pair_idx.
 size_t bwd_pair_entries(const ShapeArgs& s);
+constexpr int kBwdWorkCounters = 2;  // dK/dV kernel, dQ kernel
 
 // dO -> fp16 copy, D = rowsum(dO * (O + O_lo)) and log2(e) * LSE into the per-row
 // statistics, in one pass (attn_common.cu).
