@@ -178,8 +178,9 @@ sa2_status sa2_attn_fwd(const sa2_shape* shape, const void* q, const void* k, co
 /*
  * Bytes of device workspace sa2_attn_bwd needs: per-row statistics (log2(e) * LSE and
  * D = rowsum(dO * O), padded to whole 64-row query sub-tiles), the merged column lists of
- * each pair of adjacent key blocks ([B, H, ceil(Tk/2), Tq] uint32 plus their lengths), and
- * fp16 copies of q, k, v and dO.
+ * each pair of adjacent key blocks ([B, H, ceil(Tk/2), Tq] uint32 plus their lengths),
+ * fp16 copies of q, k, v and dO, and the work counters of the two persistent backward
+ * kernels (reset by the call itself).
  */
 size_t sa2_bwd_workspace_size(const sa2_shape* shape);
 
