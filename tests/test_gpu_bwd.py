@@ -89,6 +89,32 @@ def test_bwd_random_masks_empty_rows_unused_keys_and_scale(sa2):
     _full_check(sa2, cfg, x, mask, scale=0.05)
 
 
+@pytest.mark.parametrize("d,bq", [(64, 128), (128, 64)])
+def test_bwd_many_items_per_persistent_cta(sa2, d, bq):
+    """The dK/dV and dQ kernels keep one CTA per SM and take key-block pairs / query blocks
+    from a counter.  48 short heads give 480 pairs and 480 or 912 query blocks, several per
+    CTA, so barrier phases run across items.  Empty items sit between full ones: a head
+    keeping nothing, a whole unused key-block pair, a query block keeping nothing, and a
+    dense head with long lists.  Every gradient element is checked, and a second call must
+    repeat the first bit for bit (the counter is reset per call, and each item is computed
+    by one CTA whatever the assignment)."""
+    cfg, x = small_case(f"many-items-d{d}-bq{bq}", 2, 24, 1200, d, "bf16", bq, 64, seed=61)
+    assert cfg.B * cfg.H * ((cfg.Tk + 1) // 2) == 480 and cfg.B * cfg.H * cfg.Tq >= 480
+    rng = np.random.default_rng(17)
+    mask = (rng.random((cfg.B, cfg.H, cfg.Tq, cfg.Tk)) < 0.2).astype(np.uint8)
+    mask[0, 3] = 0              # a head keeping nothing
+    mask[1, 5, :, 4:6] = 0      # key-block pair 2 unused: an empty dK/dV item
+    mask[0, 7, 3] = 0           # a query block keeping nothing: an empty dQ item
+    mask[1, 11] = 1             # a dense head: the longest lists
+    g = _full_check(sa2, cfg, x, mask)
+    assert not g[0][0, 3].any() and not g[1][0, 3].any() and not g[2][0, 3].any()
+    assert not g[1][1, 5, 4 * 64:6 * 64].any() and not g[2][1, 5, 4 * 64:6 * 64].any()
+    assert not g[0][0, 7, 3 * bq:4 * bq].any()
+    g2 = _run(sa2, cfg, x, mask)
+    for a, b in zip(g, g2):
+        assert np.array_equal(a, b)
+
+
 def test_bwd_gradient_invariants_on_gpu(sa2):
     """Every row of dS sums to zero and every row of P to one: the keys' dK sum to ~0 and
     the keys' dV sum to the queries' dO (rows that keep something)."""
