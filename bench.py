@@ -2,7 +2,8 @@
 
 One step = the whole hot path over one batch of synthetic input: the hybrid Top-k + Top-p
 block mask (sa2_build_mask), the block-sparse forward (sa2_attn_fwd) and the backward
-(sa2_attn_bwd), on a Wan2.1-14B-720p-shaped attention layer (B=1, H=40, N=75600 tokens of
+(sa2_attn_bwd_with_fwd_ws: sa2_attn_bwd taking the forward's fp16 copy of V), on a
+Wan2.1-14B-720p-shaped attention layer (B=1, H=40, N=75600 tokens of
 a 21x45x80 latent, d=128, bf16, 128x64 blocks) at the calibrated 95 % block sparsity.
 
 Metric: kept-tile TFLOP/s of forward + backward (4 + 10 flops per kept query-key pair per
@@ -263,7 +264,7 @@ def run_native(a, rank, world):
         sa2.attn_fwd(src["q"], src["k"], src["v"], bm, bq=cfg.bq, bk=cfg.bk, o=out["o"], lse=lse, o_lo=o_lo,
                      ws=ws_f)
         sa2.attn_bwd(src["q"], src["k"], src["v"], out["o"], lse, src["do"], bm, bq=cfg.bq, bk=cfg.bk,
-                     o_lo=o_lo, dq=out["dq"], dk=out["dk"], dv=out["dv"], ws=ws_b)
+                     o_lo=o_lo, dq=out["dq"], dk=out["dk"], dv=out["dv"], ws=ws_b, fwd_ws=ws_f)
 
     for _ in range(a.warmup):
         step(d)
@@ -385,7 +386,7 @@ def run_native(a, rank, world):
                                f"blocks {cfg.bq}x{cfg.bk}",
                    "block_sparsity": sparsity, "topk": topk, "topp": topp, "seed": 0,
                    "l2": "inputs larger than L2 (Q,K,V,dO = %.1f GB per step); no flush" % (4 * B * H * N * D * 2 / 1e9),
-                   "step": "sa2_build_mask + sa2_attn_fwd + sa2_attn_bwd", "parallelism": f"replicas x{world}"},
+                   "step": "sa2_build_mask + sa2_attn_fwd + sa2_attn_bwd_with_fwd_ws (the forward's fp16 copy of V reused)", "parallelism": f"replicas x{world}"},
         "kept_tflop_per_step": flops_step / 1e12,
         "dense_equiv_tflops": world * (FWD_FLOPS + BWD_FLOPS) * D * float(N) * N * B * H * a.steps / (ms_max * 1e-3) / 1e12,
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "mask_ms": mask_ms,

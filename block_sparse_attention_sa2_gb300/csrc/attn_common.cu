@@ -92,8 +92,20 @@ __global__ void __launch_bounds__(256) to_f16_kernel(const T* __restrict__ src, 
                                                      unsigned* status) {
   const int64_t items = (int64_t)s.B * s.H * s.N * s.d / 8;
   const int per_row = s.d / 8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   bool bad = false;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < items; i += (int64_t)gridDim.x * blockDim.x) {
+  int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (CONTIG) {
+    // four 16-byte loads in flight per thread before the first store
+    for (; i0 + 3 * stride < items; i0 += 4 * stride) {
+      float v[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ld8<T>(src + (i0 + u * stride) * 8, v[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(dst + (i0 + u * stride) * 8) = to_f16x8(v[u], bad);
+    }
+  }
+  for (int64_t i = i0; i < items; i += stride) {
     const int64_t e = i * 8;
     int64_t off = e;
     if (!CONTIG) {

@@ -196,16 +196,27 @@ __device__ __forceinline__ void select_in_registers(const uint32_t* keys, int Tk
   take = max(max(r_k, r_m), 0);
 }
 
-template <int RQ>
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// RQ query blocks per CTA; NBUF k-bar chunk buffers (2: the next chunk streams in while the
+// current one is used).
+template <int RQ, int NBUF>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_select_kernel(const float* __restrict__ qbarT, const float* __restrict__ kbarT, ShapeArgs s, int tq_pad,
                         int tk_pad, SelectArgs sel, MaskOut out) {
   extern __shared__ __align__(16) float smem[];
   const int Tk = s.Tk;
   const int Tk_pad = tk_pad;  // multiple of kKeyChunk; pooled keys past Tk are never read back
-  float* qs = smem;                  // [d][RQ]
-  float* ks = qs + s.d * RQ;         // [d][kKeyChunk]
-  float* S = ks + s.d * kKeyChunk;   // [RQ][Tk_pad]
+  float* qs = smem;                    // [d][RQ]
+  float* ks = qs + s.d * RQ;           // NBUF x [d][kKeyChunk]
+  float* S = ks + NBUF * s.d * kKeyChunk;  // [RQ][Tk_pad]
   const int bh = blockIdx.y;
   const int i0 = blockIdx.x * RQ;
   const int nrow = min(RQ, s.Tq - i0);
@@ -220,35 +231,42 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   }
   // ---- pooled scores S[r][j] = (q-bar_r . k-bar_j) / sqrt(d), fp32 FMA in channel order
   constexpr int RPT = RQ / 4;  // rows per thread
-  const int tr = tid / 64, tj = tid % 64;
+  const int tr = tid / 64, tj = tid % 64;  // keys 2 tj, 2 tj + 1 of each chunk
   const float* kbase = kbarT + (int64_t)bh * s.d * Tk_pad;
-  for (int j0 = 0; j0 < Tk; j0 += kKeyChunk) {
-    __syncthreads();
-    // the chunk is d x 128 floats = d*32 float4: d/8 per thread, all loads in flight at once
-    for (int base = 0; base < s.d * 32; base += kScoreThreads * 16) {
-      float4 v[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int idx = base + u * kScoreThreads + tid;
-        if (idx < s.d * 32) {
-          const int c = idx >> 5, j4 = idx & 31;
-          v[u] = *reinterpret_cast<const float4*>(kbase + (int64_t)c * Tk_pad + j0 + 4 * j4);
-        }
+  const int nchunks = (Tk + kKeyChunk - 1) / kKeyChunk;
+  // chunk ci (d x 128 floats = d*32 float4, d/8 per thread) into buffer ci % NBUF
+  auto fetch = [&](int ci) {
+    float* dst = ks + (ci % NBUF) * s.d * kKeyChunk;
+    const int j0 = ci * kKeyChunk;
+    for (int idx = tid; idx < s.d * 32; idx += kScoreThreads) {
+      const int c = idx >> 5, j4 = idx & 31;
+      cp_async16(dst + 4 * idx, kbase + (int64_t)c * Tk_pad + j0 + 4 * j4);
+    }
+    cp_async_commit();
+  };
+  if (NBUF == 2) fetch(0);
+  for (int ci = 0; ci < nchunks; ++ci) {
+    const int j0 = ci * kKeyChunk;
+    if (NBUF == 2) {
+      // buffer (ci + 1) % 2 was last read by chunk ci - 1, which every thread has finished
+      if (ci + 1 < nchunks) {
+        fetch(ci + 1);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
       }
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int idx = base + u * kScoreThreads + tid;
-        if (idx < s.d * 32) reinterpret_cast<float4*>(ks)[idx] = v[u];
-      }
+    } else {
+      fetch(ci);
+      cp_async_wait<0>();
     }
     __syncthreads();
+    const float* kc = ks + (ci % NBUF) * s.d * kKeyChunk;
     float acc[RPT][2];
 #pragma unroll
     for (int a = 0; a < RPT; ++a) acc[a][0] = acc[a][1] = 0.f;
 #pragma unroll 4
     for (int c = 0; c < s.d; ++c) {
-      const float k0 = ks[c * kKeyChunk + tj];
-      const float k1 = ks[c * kKeyChunk + tj + 64];
+      const float2 kk = *reinterpret_cast<const float2*>(kc + c * kKeyChunk + 2 * tj);
       float qv[RPT];
       if constexpr (RPT == 4) {
         const float4 t = *reinterpret_cast<const float4*>(qs + c * RQ + tr * 4);
@@ -261,15 +279,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
 #pragma unroll
       for (int a = 0; a < RPT; ++a) {
-        acc[a][0] = fmaf(qv[a], k0, acc[a][0]);
-        acc[a][1] = fmaf(qv[a], k1, acc[a][1]);
+        acc[a][0] = fmaf(qv[a], kk.x, acc[a][0]);
+        acc[a][1] = fmaf(qv[a], kk.y, acc[a][1]);
       }
     }
 #pragma unroll
-    for (int a = 0; a < RPT; ++a) {
-      S[(tr * RPT + a) * Tk_pad + j0 + tj] = acc[a][0] * sel.inv_sqrt_d;
-      S[(tr * RPT + a) * Tk_pad + j0 + tj + 64] = acc[a][1] * sel.inv_sqrt_d;
-    }
+    for (int a = 0; a < RPT; ++a)
+      *reinterpret_cast<float2*>(S + (tr * RPT + a) * Tk_pad + j0 + 2 * tj) =
+          make_float2(acc[a][0] * sel.inv_sqrt_d, acc[a][1] * sel.inv_sqrt_d);
+    // every thread is done with this chunk's buffer before it is refilled
+    __syncthreads();
   }
   __syncthreads();
 
@@ -402,29 +421,40 @@ size_t mask_pooled_bytes(const ShapeArgs& s, size_t* kbar_offset) {
   return q + k;
 }
 
-static size_t score_smem_bytes(int rq, int Tk, int d) {
-  return sizeof(float) * ((size_t)d * rq + (size_t)d * kKeyChunk + (size_t)rq * mask_tk_pad(Tk));
+static size_t score_smem_bytes(int rq, int nbuf, int Tk, int d) {
+  return sizeof(float) * ((size_t)d * rq + (size_t)nbuf * d * kKeyChunk + (size_t)rq * mask_tk_pad(Tk));
 }
 
 int score_rows_per_cta(int Tk, int d) {
   for (int rq : {16, 8, 4})
-    if (score_smem_bytes(rq, Tk, d) <= kMaxDynSmem) return rq;
+    if (score_smem_bytes(rq, 1, Tk, d) <= kMaxDynSmem) return rq;
   return 0;
+}
+
+// chunk buffers for rq rows per CTA: two when they fit beside the score rows
+static int score_chunk_buffers(int rq, int Tk, int d) {
+  return score_smem_bytes(rq, 2, Tk, d) <= kMaxDynSmem ? 2 : 1;
+}
+
+template <int RQ, int NBUF>
+static cudaError_t launch_score(const float* qbarT, const float* kbarT, const ShapeArgs& s, const SelectArgs& sel,
+                                const MaskOut& out, cudaStream_t st) {
+  const size_t smem = score_smem_bytes(RQ, NBUF, s.Tk, s.d);
+  auto kern = score_select_kernel<RQ, NBUF>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((s.Tq + RQ - 1) / RQ, s.B * s.H);
+  prof_start(st, kScoreSelect);
+  kern<<<grid, kScoreThreads, smem, st>>>(qbarT, kbarT, s, mask_tq_pad(s.Tq), mask_tk_pad(s.Tk), sel, out);
+  prof_stop(st, kScoreSelect);
+  return cudaGetLastError();
 }
 
 template <int RQ>
 static cudaError_t launch_score(const float* qbarT, const float* kbarT, const ShapeArgs& s, const SelectArgs& sel,
                                 const MaskOut& out, cudaStream_t st) {
-  const size_t smem = score_smem_bytes(RQ, s.Tk, s.d);
-  cudaError_t e = cudaFuncSetAttribute(score_select_kernel<RQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((s.Tq + RQ - 1) / RQ, s.B * s.H);
-  prof_start(st, kScoreSelect);
-  score_select_kernel<RQ><<<grid, kScoreThreads, smem, st>>>(qbarT, kbarT, s, mask_tq_pad(s.Tq),
-                                                              mask_tk_pad(s.Tk), sel, out);
-  prof_stop(st, kScoreSelect);
-  return cudaGetLastError();
+  return score_chunk_buffers(RQ, s.Tk, s.d) == 2 ? launch_score<RQ, 2>(qbarT, kbarT, s, sel, out, st)
+                                                 : launch_score<RQ, 1>(qbarT, kbarT, s, sel, out, st);
 }
 
 cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, const SelectArgs& sel,

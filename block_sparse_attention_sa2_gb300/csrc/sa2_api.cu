@@ -246,9 +246,14 @@ size_t sa2_bwd_workspace_size(const sa2_shape* shape) {
   return bwd_ws(s).total;
 }
 
-sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, const void* v, const void* o,
-                        const void* o_lo, const float* lse, const void* dO, const sa2_blockmask* mask,
-                        float softmax_scale, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+
+// The backward; fwd_workspace, when not null, is the (already validated) workspace of the
+// forward call on the same q, k, v, whose fp16 copies replace the conversions here.
+sa2_status attn_bwd_impl(const sa2_shape* shape, const void* q, const void* k, const void* v, const void* o,
+                         const void* o_lo, const float* lse, const void* dO, const sa2_blockmask* mask,
+                         float softmax_scale, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                         const void* fwd_workspace, void* stream) {
   ShapeArgs s;
   sa2_status st = check_shape(shape, &s);
   if (st != SA2_OK) return st;
@@ -270,8 +275,21 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   __half* c16[4] = {reinterpret_cast<__half*>(wsb + w.q16), reinterpret_cast<__half*>(wsb + w.k16),
                     reinterpret_cast<__half*>(wsb + w.v16), reinterpret_cast<__half*>(wsb + w.do16)};
   const void* src[3] = {q, k, v};
+  bool copied[3] = {false, false, false};
+  if (fwd_workspace) {
+    // the forward's fp16 copies: v always, q and k for fp32 inputs
+    const FwdWs fw = fwd_ws(s);
+    const uint8_t* fb = static_cast<const uint8_t*>(fwd_workspace);
+    c16[2] = reinterpret_cast<__half*>(const_cast<uint8_t*>(fb + fw.v16));
+    copied[2] = true;
+    if (s.dtype == SA2_FP32) {
+      c16[0] = reinterpret_cast<__half*>(const_cast<uint8_t*>(fb + fw.q16));
+      c16[1] = reinterpret_cast<__half*>(const_cast<uint8_t*>(fb + fw.k16));
+      copied[0] = copied[1] = true;
+    }
+  }
   for (int i = 0; i < 3; ++i)
-    if (launch_to_f16(src[i], s, c16[i], status, cs) != cudaSuccess) return SA2_ERR_CUDA;
+    if (!copied[i] && launch_to_f16(src[i], s, c16[i], status, cs) != cudaSuccess) return SA2_ERR_CUDA;
   // fp16 dO, and D = rowsum(dO * O) from that same fp16 dO, in one pass
   if (launch_do_prep(s, dO, o, s.dtype == SA2_BF16 ? o_lo : nullptr, lse, c16[3], stats, status, cs) !=
       cudaSuccess)
@@ -311,6 +329,30 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
   g.scale_log2 = a.scale_log2;
   g.status = status;
   return cuda_status(launch_attn_bwd_dq(s, mq, mk, mv, mdo, g, cs));
+}
+
+}  // namespace
+
+sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, const void* v, const void* o,
+                        const void* o_lo, const float* lse, const void* dO, const sa2_blockmask* mask,
+                        float softmax_scale, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+  return attn_bwd_impl(shape, q, k, v, o, o_lo, lse, dO, mask, softmax_scale, dq, dk, dv, ws, ws_bytes, nullptr,
+                       stream);
+}
+
+sa2_status sa2_attn_bwd_with_fwd_ws(const sa2_shape* shape, const void* q, const void* k, const void* v,
+                                    const void* o, const void* o_lo, const float* lse, const void* dO,
+                                    const sa2_blockmask* mask, float softmax_scale, void* dq, void* dk, void* dv,
+                                    void* ws, size_t ws_bytes, const void* fwd_workspace,
+                                    size_t fwd_workspace_bytes, void* stream) {
+  ShapeArgs s;
+  sa2_status st = check_shape(shape, &s);
+  if (st != SA2_OK) return st;
+  if (!fwd_workspace) return SA2_ERR_INVALID_ARG;
+  if (!aligned16(fwd_workspace)) return SA2_ERR_ALIGNMENT;
+  if (fwd_workspace_bytes < fwd_ws(s).total) return SA2_ERR_WORKSPACE;
+  return attn_bwd_impl(shape, q, k, v, o, o_lo, lse, dO, mask, softmax_scale, dq, dk, dv, ws, ws_bytes,
+                       fwd_workspace, stream);
 }
 
 size_t sa2_vd_loss_workspace_size(const sa2_shape* shape) {

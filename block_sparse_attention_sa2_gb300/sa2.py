@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sa2_attn_fwd.argtypes = [S, P, P, P, M, F, P, P, P, P, Z, P]
     lib.sa2_attn_bwd.restype = ctypes.c_int
     lib.sa2_attn_bwd.argtypes = [S, P, P, P, P, P, P, P, M, F, P, P, P, P, Z, P]
+    lib.sa2_attn_bwd_with_fwd_ws.restype = ctypes.c_int
+    lib.sa2_attn_bwd_with_fwd_ws.argtypes = [S, P, P, P, P, P, P, P, M, F, P, P, P, P, Z, P, Z, P]
     lib.sa2_vd_loss_workspace_size.restype = Z
     lib.sa2_vd_loss_workspace_size.argtypes = [S]
     lib.sa2_vd_loss.restype = ctypes.c_int
@@ -190,8 +192,12 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: BlockMask,
 
 def attn_bwd(q, k, v, o, lse, do, mask: BlockMask, bq: int = 128, bk: int = 64, scale: Optional[float] = None,
              o_lo: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None, ws: Optional[torch.Tensor] = None,
-             stream=None):
-    """sa2_attn_bwd: gradients (dQ, dK, dV) of the block-sparse attention, mask fixed."""
+             fwd_ws: Optional[torch.Tensor] = None, stream=None):
+    """sa2_attn_bwd: gradients (dQ, dK, dV) of the block-sparse attention, mask fixed.
+
+    ``fwd_ws``: the ``ws`` tensor given to the attn_fwd call on these q, k, v (untouched
+    since); its fp16 copies are used instead of converting again
+    (sa2_attn_bwd_with_fwd_ws)."""
     lib = load_library()
     shp = make_shape(q, bq, bk)
     dq = torch.empty_like(q) if dq is None else dq
@@ -200,10 +206,14 @@ def attn_bwd(q, k, v, o, lse, do, mask: BlockMask, bq: int = 128, bk: int = 64, 
     if ws is None:
         ws = workspace(lib.sa2_bwd_workspace_size(ctypes.byref(shp)), q.device)
     m = mask.struct()
-    _check("sa2_attn_bwd", lib.sa2_attn_bwd(ctypes.byref(shp), q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                            o.data_ptr(), _ptr(o_lo), lse.data_ptr(), do.data_ptr(),
-                                            ctypes.byref(m), float(scale or 0.0), dq.data_ptr(), dk.data_ptr(),
-                                            dv.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+    args = (ctypes.byref(shp), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _ptr(o_lo), lse.data_ptr(),
+            do.data_ptr(), ctypes.byref(m), float(scale or 0.0), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+            ws.data_ptr(), ws.numel())
+    if fwd_ws is None:
+        _check("sa2_attn_bwd", lib.sa2_attn_bwd(*args, _stream(stream)))
+    else:
+        _check("sa2_attn_bwd_with_fwd_ws",
+               lib.sa2_attn_bwd_with_fwd_ws(*args, fwd_ws.data_ptr(), fwd_ws.numel(), _stream(stream)))
     return dq, dk, dv
 
 

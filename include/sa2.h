@@ -211,6 +211,27 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
                         void* stream);
 
 /*
+ * sa2_attn_bwd_with_fwd_ws -- sa2_attn_bwd that takes the fp16 copies the forward already
+ * made instead of converting again: the copy of v, and for SA2_FP32 inputs those of q and
+ * k, which sa2_attn_fwd leaves in its workspace.  The result is the same, bit for bit.
+ *
+ *   fwd_ws, fwd_ws_bytes  the workspace of the sa2_attn_fwd call on the same shape, q, k
+ *                         and v (the call that produced o, o_lo and lse), ordered before
+ *                         this call on the device and not written since; at least
+ *                         sa2_fwd_workspace_size(shape) bytes, 16-byte aligned.  Only read.
+ *   other arguments       as for sa2_attn_bwd.
+ * Errors as for sa2_attn_bwd, and: fwd_ws NULL -> SA2_ERR_INVALID_ARG, misaligned ->
+ * SA2_ERR_ALIGNMENT, too small -> SA2_ERR_WORKSPACE, all before any launch.  A workspace
+ * that does not hold the forward's copies of these q, k, v is not detected: the gradients
+ * are then those of the tensors it holds.
+ */
+sa2_status sa2_attn_bwd_with_fwd_ws(const sa2_shape* shape, const void* q, const void* k, const void* v,
+                                    const void* o, const void* o_lo, const float* lse, const void* dO,
+                                    const sa2_blockmask* mask, float softmax_scale, void* dq, void* dk, void* dv,
+                                    void* ws, size_t ws_bytes, const void* fwd_ws, size_t fwd_ws_bytes,
+                                    void* stream);
+
+/*
  * Toy distillation step (gist.science explainer, section 2.B: the fine-tuning loss is the
  * squared L2 distance between the velocity of the sparse model and that of the frozen
  * full-attention model; on a single attention block the block's output stands in for the

@@ -115,6 +115,27 @@ def test_bwd_many_items_per_persistent_cta(sa2, d, bq):
         assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_bwd_with_forward_workspace_is_bit_identical(sa2, dtype):
+    """sa2_attn_bwd_with_fwd_ws takes the forward's fp16 copy of v (and of q, k for fp32
+    inputs) instead of converting again: the gradients must equal sa2_attn_bwd's bit for bit."""
+    cfg, x = small_case(f"fwd-ws-{dtype}", 1, 3, 1500, 128, dtype, 128, 64, seed=67)
+    mask = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, 0.2, 0.6)["mask"]
+    q, k, v, do = (to_device(x[t]) for t in ("q", "k", "v", "do"))
+    bm = blockmask_from_oracle(mask)
+    lib = sa2.load_library()
+    import ctypes
+    shp = sa2.make_shape(q, cfg.bq, cfg.bk)
+    ws_f = sa2.workspace(lib.sa2_fwd_workspace_size(ctypes.byref(shp)), q.device)
+    o_lo = torch.empty_like(q) if q.dtype == torch.bfloat16 else None
+    o, lse = sa2.attn_fwd(q, k, v, bm, bq=cfg.bq, bk=cfg.bk, o_lo=o_lo, ws=ws_f)
+    plain = sa2.attn_bwd(q, k, v, o, lse, do, bm, bq=cfg.bq, bk=cfg.bk, o_lo=o_lo)
+    reused = sa2.attn_bwd(q, k, v, o, lse, do, bm, bq=cfg.bq, bk=cfg.bk, o_lo=o_lo, fwd_ws=ws_f)
+    sa2.check_device()
+    for name, a, b in zip(("dQ", "dK", "dV"), plain, reused):
+        assert torch.equal(a, b), name
+
+
 def test_bwd_gradient_invariants_on_gpu(sa2):
     """Every row of dS sums to zero and every row of P to one: the keys' dK sum to ~0 and
     the keys' dV sum to the queries' dO (rows that keep something)."""

@@ -29,7 +29,8 @@ def declared_functions():
 
 def test_every_declared_function_is_exported(lib):
     names = declared_functions()
-    assert {"sa2_build_mask", "sa2_attn_fwd", "sa2_attn_bwd", "sa2_build_mask_noalloc", "sa2_vd_loss"} <= set(names)
+    assert {"sa2_build_mask", "sa2_attn_fwd", "sa2_attn_bwd", "sa2_attn_bwd_with_fwd_ws", "sa2_build_mask_noalloc",
+            "sa2_vd_loss"} <= set(names)
     from block_sparse_attention_sa2_gb300.sa2 import LIB_PATH
     out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (sa2_\w+)", out))
@@ -109,6 +110,14 @@ def test_arguments_are_rejected_before_any_launch(lib):
     assert bwd(good, wsb=1024) == WORKSPACE
     assert lib.sa2_attn_bwd(ctypes.byref(good), P, P, P, P, None, P, P, ctypes.byref(M(16, 16, None, 16, 16, None)),
                             0.0, P, P, P, P, 1 << 40, None) == INVALID
+    # backward taking the forward's workspace
+    bwdf = lambda sh, fws=P, fwsb=1 << 40, wsb=1 << 40: lib.sa2_attn_bwd_with_fwd_ws(  # noqa: E731
+        ctypes.byref(sh), P, P, P, P, None, P, P, ctypes.byref(m), 0.0, P, P, P, P, wsb, fws, fwsb, None)
+    assert bwdf(_shape(sa2, bq=32)) == UNSUPPORTED
+    assert bwdf(good, fws=None) == INVALID
+    assert bwdf(good, fws=P + 8) == ALIGN
+    assert bwdf(good, fwsb=lib.sa2_fwd_workspace_size(ctypes.byref(good)) - 1) == WORKSPACE
+    assert bwdf(good, wsb=1024) == WORKSPACE
 
 
 def test_noalloc_rejects_oversized_shapes_on_the_host(lib):
