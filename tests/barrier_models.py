@@ -1,0 +1,547 @@
+"""Executable models of the barrier protocols of the persistent backward kernels.
+
+attn_bwd_dkdv_kernel and attn_bwd_dq_kernel run one CTA per SM.  Each CTA takes work items
+(key-block pairs, query blocks) from a counter.  Every warp role waits on mbarriers whose
+phases count sub-tiles and items over the CTA's whole run.  These models restate each role's
+sequence of waits, arrivals, copies and MMA commits as a Python generator.  A randomised
+scheduler then interleaves the roles with the asynchronous engines:
+- the TMA, whose copies complete in any order;
+- the tensor pipe, with one in-order queue per issuing warp, whose commits arrive when that
+  warp's earlier MMAs are done.
+
+A run checks three things:
+- it ends (no deadlock);
+- every parity wait passes exactly at its intended phase, never two phases late (a parity wait
+  cannot tell phase k from phase k + 2);
+- no copy or MMA overwrites a shared-memory stage, the K/V or Q/dO buffer, or a TMEM region
+  (S, dP, P, dS, accumulators) before all its readers are done, and no reader sees the wrong
+  contents.
+
+`drop` names waits to leave out, so a test can check that the model catches each missing one.
+"""
+import random
+
+
+class ProtocolError(Exception):
+    pass
+
+
+def check(cond, msg):
+    if not cond:
+        raise ProtocolError(msg)
+
+
+class Bar:
+    """An mbarrier: `count` arrivals plus the expected transaction bytes complete a phase."""
+
+    def __init__(self, name, count):
+        self.name, self.count, self.pend, self.tx, self.comp = name, count, count, 0, 0
+
+    def arrive(self):
+        self.pend -= 1
+        check(self.pend >= 0, f"{self.name}: more arrivals than its count")
+        self._complete()
+
+    def expect_tx(self, nbytes):
+        self.tx += nbytes
+        self.arrive()
+
+    def complete_tx(self, nbytes):
+        self.tx -= nbytes
+        self._complete()
+
+    def _complete(self):
+        if self.pend == 0 and self.tx == 0:
+            self.comp += 1
+            self.pend = self.count
+
+
+class Model:
+    """Shared scheduler: actors are (name, cta, generator) yielding ("wait", bar, phase) or
+    ("step",); subclasses define the CTA state, the engines' completions and the roles."""
+
+    def __init__(self, seed, ncta, items, drop=()):
+        self.rng = random.Random(seed)
+        self.items, self.ncta, self.drop = items, ncta, set(drop)
+        self.counter = 0
+        self.tma = []
+        self.processed = []
+        self.ctas = [self.make_cta(c) for c in range(ncta)]
+        self.actors = []
+        for c in self.ctas:
+            self.actors += self.roles(c)
+
+    def fetch_next(self):
+        x = self.ncta + self.counter
+        self.counter += 1
+        return x
+
+    def take(self, c, n):
+        slot = n & 1
+        yield ("wait", c.item_full[slot], n >> 1)
+        x = c.slot[slot]
+        c.item_free[slot].arrive()
+        return x
+
+    def publish(self, c, n):
+        """The producer's side of the two-slot item ring: waits until slot n % 2 is free and
+        returns it."""
+        slot = n & 1
+        if n >= 2:
+            yield ("wait", c.item_free[slot], (n >> 1) - 1)
+        return slot
+
+    def run(self):
+        pending = {id(a): self._advance(a, None) for a in self.actors}
+        while True:
+            choices = []
+            for a in self.actors:
+                p = pending[id(a)]
+                if p is not None and (p[0] == "step" or p[1].comp >= p[2] + 1):
+                    choices.append(("actor", a))
+            choices += [("tma", i) for i in range(len(self.tma))]
+            choices += [("mma", (c, w)) for c in self.ctas for w in (1, 2) if c.mmaq[w]]
+            if not choices:
+                stuck = [(a[0], a[1].cid, p[1].name, p[2], p[1].comp) for a in self.actors
+                         for p in [pending[id(a)]] if p is not None]
+                check(not stuck, f"deadlock: {stuck[:6]}")
+                return
+            kind, v = self.rng.choice(choices)
+            if kind == "actor":
+                p = pending[id(v)]
+                if p[0] == "wait":
+                    check(p[1].comp == p[2] + 1,
+                          f"{v[0]} cta{v[1].cid}: {p[1].name} wait for phase {p[2]} passes at {p[1].comp}")
+                pending[id(v)] = self._advance(v, True)
+            elif kind == "tma":
+                self.complete_tma(self.tma.pop(v))
+            else:
+                c, w = v
+                self.complete_mma(c, c.mmaq[w].pop(0))
+            for a in self.actors:
+                p = pending[id(a)]
+                if p is not None and p[0] == "wait":
+                    check(p[1].comp <= p[2] + 1,
+                          f"{a[0]} cta{a[1].cid}: {p[1].name} two phases past phase {p[2]}")
+
+    @staticmethod
+    def _advance(actor, value):
+        try:
+            return actor[2].send(value) if value is not None else next(actor[2])
+        except StopIteration:
+            return None
+
+
+NE = 8  # element-wise (dK/dV) or row (dQ) warps
+ALL = frozenset(range(NE))
+
+
+class DkdvModel(Model):
+    """attn_bwd_dkdv_kernel: items are key-block pairs of `items[x]` 64-row query sub-tiles."""
+
+    STAGES = 4
+
+    def make_cta(self, cid):
+        c = type("CTA", (), {})()
+        c.cid = cid
+        c.kv, c.sfull, c.sfree = Bar("kv", 1), Bar("sfull", 1), Bar("sfree", NE)
+        c.full = [Bar(f"full{i}", 1) for i in range(self.STAGES)]
+        c.empty = [Bar(f"empty{i}", 1) for i in range(self.STAGES)]
+        c.pready = [Bar(f"pready{i}", NE) for i in range(2)]
+        c.pfree = [Bar(f"pfree{i}", 1) for i in range(2)]
+        c.drain, c.sdrain, c.kvfree, c.gdrain = Bar("drain", 1), Bar("sdrain", 1), Bar("kvfree", 1), Bar("gdrain", 1)
+        c.item_full = [Bar(f"item_full{i}", 1) for i in range(2)]
+        c.item_free = [Bar(f"item_free{i}", 2 + NE) for i in range(2)]
+        c.slot = [None, None]
+        c.stage = [None] * self.STAGES
+        c.stage_readers = [set() for _ in range(self.STAGES)]
+        c.kv_tag, c.kv_readers = None, 0
+        c.S, c.S_read, c.DP = None, set(), None
+        c.P, c.P_readers = [dict(), dict()], [0, 0]
+        c.acc, c.acc_read, c.acc_inflight = None, set(ALL), 0
+        c.mmaq = {1: [], 2: []}
+        return c
+
+    def roles(self, c):
+        return ([("producer", c, self.producer(c)), ("s_issuer", c, self.s_issuer(c)),
+                 ("g_issuer", c, self.g_issuer(c))] + [(f"ew{g}", c, self.elementwise(c, g)) for g in range(NE)])
+
+    def complete_tma(self, job):
+        c, kind, arg = job
+        if kind == "stage":
+            st, U = arg
+            check(not c.stage_readers[st], f"stage {st} overwritten while read by {c.stage_readers[st]}")
+            c.stage[st] = U
+            c.stage_readers[st] = {"S", "DP", "DV", "DK"} | {f"ew{g}" for g in range(NE)}
+            c.full[st].complete_tx(1)
+        else:
+            check(c.kv_readers == 0, "K/V overwritten while S/dP MMAs read them")
+            c.kv_tag = arg
+            c.kv.complete_tx(1)
+
+    def complete_mma(self, c, op):
+        kind = op[0]
+        if kind == "commit":
+            op[1].arrive()
+        elif kind in ("S", "DP"):
+            _, U, st, kvk = op
+            check(c.stage[st] == U and c.kv_tag == kvk, f"{kind}({U}): operands changed before completion")
+            c.stage_readers[st].discard(kind)
+            c.kv_readers -= 1
+            if kind == "S":
+                check(c.S is None or c.S_read >= ALL, f"S({U}) overwrote S({c.S}) before it was read")
+                c.S, c.S_read = U, set()
+            else:
+                c.DP = U
+        else:
+            _, W, st, bb, item, w = op
+            check(c.stage[st] == W and all(c.P[bb].get(g) == W for g in range(NE)),
+                  f"{kind}({W}): operands changed before completion")
+            c.stage_readers[st].discard(kind)
+            c.P_readers[bb] -= 1
+            if kind == "DV":
+                if w == 0:
+                    check(c.acc_read >= ALL, f"item {item}: accumulators overwritten before the epilogue read them")
+                else:
+                    check(c.acc == (item, w - 1), f"item {item}: accumulation chain broken at {w}")
+                c.acc, c.acc_read = (item, w), set()
+            c.acc_inflight -= 1
+
+    def producer(self, c):
+        U = kvn = n = 0
+        x = c.cid
+        while True:
+            slot = yield from self.publish(c, n)
+            done = x >= len(self.items)
+            c.slot[slot] = -1 if done else x
+            c.item_full[slot].arrive()
+            if done:
+                break
+            xn = self.fetch_next()
+            yield ("step",)
+            nsub = self.items[x]
+            if nsub > 0:
+                if kvn >= 1 and "kvfree" not in self.drop:
+                    yield ("wait", c.kvfree, kvn - 1)
+                check(c.kv_readers == 0, "K/V load issued while S/dP MMAs read them")
+                c.kv.expect_tx(1)
+                self.tma.append((c, "kv", (x, kvn)))
+                kvn += 1
+                for _ in range(nsub):
+                    st = U % self.STAGES
+                    if U >= self.STAGES and "empty" not in self.drop:
+                        yield ("wait", c.empty[st], U // self.STAGES - 1)
+                    check(not c.stage_readers[st], f"stage {st} load issued while read by {c.stage_readers[st]}")
+                    c.full[st].expect_tx(1)
+                    self.tma.append((c, "stage", (st, U)))
+                    U += 1
+                    yield ("step",)
+            x = xn
+            n += 1
+        for v in range(max(0, U - self.STAGES), U):
+            yield ("wait", c.full[v % self.STAGES], v // self.STAGES)
+        if kvn > 0:
+            yield ("wait", c.kv, kvn - 1)
+
+    def s_issuer(self, c):
+        U = kvn = n = 0
+        while True:
+            x = yield from self.take(c, n)
+            n += 1
+            if x < 0:
+                break
+            nsub = self.items[x]
+            if nsub == 0:
+                continue
+            yield ("wait", c.kv, kvn)
+            kvk = (x, kvn)
+            kvn += 1
+            for _ in range(nsub):
+                st = U % self.STAGES
+                yield ("wait", c.full[st], U // self.STAGES)
+                if U >= 1 and "sfree" not in self.drop:
+                    yield ("wait", c.sfree, U - 1)
+                check(c.stage[st] == U and c.kv_tag == kvk, f"S({U}) issued on the wrong operands")
+                c.mmaq[1] += [("S", U, st, kvk), ("DP", U, st, kvk), ("commit", c.sfull)]
+                c.kv_readers += 2
+                U += 1
+                yield ("step",)
+            c.mmaq[1].append(("commit", c.kvfree))
+        c.mmaq[1].append(("commit", c.sdrain))
+        yield ("wait", c.sdrain, 0)
+
+    def g_issuer(self, c):
+        W = n = 0
+        while True:
+            x = yield from self.take(c, n)
+            n += 1
+            if x < 0:
+                break
+            nsub = self.items[x]
+            for w in range(nsub):
+                st, bb = W % self.STAGES, W & 1
+                yield ("wait", c.pready[bb], W >> 1)
+                yield ("wait", c.full[st], W // self.STAGES)
+                check(all(c.P[bb].get(g) == W for g in range(NE)), f"dV/dK({W}) issued before P/dS were written")
+                c.mmaq[2] += [("DV", W, st, bb, x, w), ("DK", W, st, bb, x, w), ("commit", c.empty[st]),
+                              ("commit", c.pfree[bb])]
+                c.P_readers[bb] += 2
+                c.acc_inflight += 2
+                W += 1
+                yield ("step",)
+            if nsub > 0:
+                c.mmaq[2].append(("commit", c.drain))
+        c.mmaq[2].append(("commit", c.gdrain))
+        yield ("wait", c.gdrain, 0)
+
+    def elementwise(self, c, g):
+        U = an = n = 0
+        while True:
+            x = yield from self.take(c, n)
+            n += 1
+            if x < 0:
+                break
+            nsub = self.items[x]
+            for _ in range(nsub):
+                st, bb = U % self.STAGES, U & 1
+                yield ("wait", c.sfull, U)
+                yield ("wait", c.full[st], U // self.STAGES)
+                check(c.S == U and c.DP == U, f"ew{g}: reads S({U}) while TMEM holds S({c.S})")
+                check(c.stage[st] == U, f"ew{g}: statistics of sub-tile {U} replaced")
+                c.S_read.add(g)
+                c.stage_readers[st].discard(f"ew{g}")
+                c.sfree.arrive()
+                yield ("step",)
+                if U >= 2 and "pfree" not in self.drop:
+                    yield ("wait", c.pfree[bb], (U >> 1) - 1)
+                check(c.P_readers[bb] == 0, f"ew{g}: P/dS buffer {bb} written while MMAs read it")
+                c.P[bb][g] = U
+                c.pready[bb].arrive()
+                U += 1
+                yield ("step",)
+            if nsub == 0:
+                continue
+            if "drain" not in self.drop:
+                yield ("wait", c.drain, an)
+            an += 1
+            check(c.acc == (x, nsub - 1) and c.acc_inflight == 0, f"ew{g}: epilogue of item {x} sees {c.acc}")
+            c.acc_read.add(g)
+            if g == 0:
+                self.processed.append(x)
+            yield ("step",)
+
+
+class DqModel(Model):
+    """attn_bwd_dq_kernel: items are query blocks with `items[x]` kept key blocks."""
+
+    KST, VST = 4, 2
+
+    def make_cta(self, cid):
+        c = type("CTA", (), {})()
+        c.cid = cid
+        c.q = Bar("q", 1)
+        c.kfull = [Bar(f"kfull{i}", 1) for i in range(self.KST)]
+        c.kempty = [Bar(f"kempty{i}", 1) for i in range(self.KST)]
+        c.vfull = [Bar(f"vfull{i}", 1) for i in range(self.VST)]
+        c.vempty = [Bar(f"vempty{i}", 1) for i in range(self.VST)]
+        c.sfull = [Bar(f"sfull{i}", 1) for i in range(2)]
+        c.sfree = [Bar(f"sfree{i}", NE) for i in range(2)]
+        c.pready = [Bar(f"pready{i}", NE) for i in range(2)]
+        c.pfree = [Bar(f"pfree{i}", 1) for i in range(2)]
+        c.dq, c.gdrain, c.sdrain, c.qfree = Bar("dq", 1), Bar("gdrain", 1), Bar("sdrain", 1), Bar("qfree", 1)
+        c.item_full = [Bar(f"item_full{i}", 1) for i in range(2)]
+        c.item_free = [Bar(f"item_free{i}", 2 + NE) for i in range(2)]
+        c.slot = [None, None]
+        c.qtag, c.q_readers = None, 0
+        c.ktag, c.k_readers = [None] * self.KST, [0] * self.KST
+        c.vtag, c.v_readers = [None] * self.VST, [0] * self.VST
+        c.S, c.S_read = [None, None], [set(ALL), set(ALL)]
+        c.DS, c.DS_readers = [dict(), dict()], [0, 0]
+        c.acc, c.acc_read, c.acc_inflight = None, set(ALL), 0
+        c.mmaq = {1: [], 2: []}
+        return c
+
+    def roles(self, c):
+        return ([("producer", c, self.producer(c)), ("s_issuer", c, self.s_issuer(c)),
+                 ("dq_issuer", c, self.dq_issuer(c))] + [(f"row{g}", c, self.rows(c, g)) for g in range(NE)])
+
+    def complete_tma(self, job):
+        c, kind, idx, tag = job
+        if kind == "q":
+            check(c.q_readers == 0, "Q/dO overwritten while S/dP MMAs read them")
+            c.qtag = tag
+            c.q.complete_tx(1)
+        elif kind == "k":
+            check(c.k_readers[idx] == 0, f"K stage {idx} overwritten while read")
+            c.ktag[idx] = tag
+            c.kfull[idx].complete_tx(1)
+        else:
+            check(c.v_readers[idx] == 0, f"V stage {idx} overwritten while read")
+            c.vtag[idx] = tag
+            c.vfull[idx].complete_tx(1)
+
+    def complete_mma(self, c, op):
+        if op[0] == "commit":
+            op[1].arrive()
+        elif op[0] == "S":
+            _, J, ks, vs, bb, qk = op
+            check(c.qtag == qk and c.ktag[ks] == J and c.vtag[vs] == J, f"S/dP({J}): operands changed")
+            check(c.S_read[bb] >= ALL, f"S({J}) overwrote buffer {bb} before it was read")
+            c.S[bb], c.S_read[bb] = J, set()
+            c.q_readers -= 1
+            c.k_readers[ks] -= 1
+            c.v_readers[vs] -= 1
+        else:
+            _, J, ks, bb, item, j = op
+            check(c.ktag[ks] == J and all(c.DS[bb].get(g) == J for g in range(NE)), f"dQ({J}): operands changed")
+            if j == 0:
+                check(c.acc_read >= ALL, f"item {item}: dQ overwritten before the epilogue read it")
+            else:
+                check(c.acc == (item, j - 1), f"item {item}: accumulation chain broken at {j}")
+            c.acc, c.acc_read = (item, j), set()
+            c.k_readers[ks] -= 1
+            c.DS_readers[bb] -= 1
+            c.acc_inflight -= 1
+
+    def producer(self, c):
+        J = qn = n = 0
+        x = c.cid
+        while True:
+            slot = yield from self.publish(c, n)
+            done = x >= len(self.items)
+            c.slot[slot] = -1 if done else x
+            c.item_full[slot].arrive()
+            if done:
+                break
+            xn = self.fetch_next()
+            nkv = self.items[x]
+            if nkv > 0:
+                if qn >= 1 and "qfree" not in self.drop:
+                    yield ("wait", c.qfree, qn - 1)
+                check(c.q_readers == 0, "Q/dO load issued while S/dP MMAs read them")
+                c.q.expect_tx(1)
+                self.tma.append((c, "q", 0, qn))
+                qn += 1
+                for _ in range(nkv):
+                    ks, vs = J % self.KST, J % self.VST
+                    if J >= self.KST and "kempty" not in self.drop:
+                        yield ("wait", c.kempty[ks], J // self.KST - 1)
+                    c.kfull[ks].expect_tx(1)
+                    self.tma.append((c, "k", ks, J))
+                    if J >= self.VST and "vempty" not in self.drop:
+                        yield ("wait", c.vempty[vs], J // self.VST - 1)
+                    c.vfull[vs].expect_tx(1)
+                    self.tma.append((c, "v", vs, J))
+                    J += 1
+                    yield ("step",)
+            x = xn
+            n += 1
+        for v in range(max(0, J - self.KST), J):
+            yield ("wait", c.kfull[v % self.KST], v // self.KST)
+        for v in range(max(0, J - self.VST), J):
+            yield ("wait", c.vfull[v % self.VST], v // self.VST)
+        if qn > 0:
+            yield ("wait", c.q, qn - 1)
+
+    def s_issuer(self, c):
+        J = qn = n = 0
+        while True:
+            x = yield from self.take(c, n)
+            n += 1
+            if x < 0:
+                break
+            nkv = self.items[x]
+            if nkv == 0:
+                continue
+            yield ("wait", c.q, qn)
+            qk = qn
+            qn += 1
+            for _ in range(nkv):
+                ks, vs, bb = J % self.KST, J % self.VST, J & 1
+                yield ("wait", c.kfull[ks], J // self.KST)
+                if J >= 2 and "sfree" not in self.drop:
+                    yield ("wait", c.sfree[bb], (J >> 1) - 1)
+                yield ("wait", c.vfull[vs], J // self.VST)
+                check(c.qtag == qk and c.ktag[ks] == J and c.vtag[vs] == J, f"S({J}) issued on the wrong operands")
+                c.mmaq[1] += [("S", J, ks, vs, bb, qk), ("commit", c.sfull[bb]), ("commit", c.vempty[vs])]
+                c.q_readers += 1
+                c.k_readers[ks] += 1
+                c.v_readers[vs] += 1
+                J += 1
+                yield ("step",)
+            c.mmaq[1].append(("commit", c.qfree))
+        c.mmaq[1].append(("commit", c.sdrain))
+        yield ("wait", c.sdrain, 0)
+
+    def dq_issuer(self, c):
+        J = n = 0
+        while True:
+            x = yield from self.take(c, n)
+            n += 1
+            if x < 0:
+                break
+            nkv = self.items[x]
+            for j in range(nkv):
+                ks, bb = J % self.KST, J & 1
+                yield ("wait", c.pready[bb], J >> 1)
+                yield ("wait", c.kfull[ks], J // self.KST)
+                check(all(c.DS[bb].get(g) == J for g in range(NE)), f"dQ({J}) issued before dS was written")
+                c.mmaq[2] += [("DQ", J, ks, bb, x, j), ("commit", c.kempty[ks]), ("commit", c.pfree[bb])]
+                c.k_readers[ks] += 1
+                c.DS_readers[bb] += 1
+                c.acc_inflight += 1
+                J += 1
+                yield ("step",)
+            if nkv > 0:
+                c.mmaq[2].append(("commit", c.dq))
+        c.mmaq[2].append(("commit", c.gdrain))
+        yield ("wait", c.gdrain, 0)
+
+    def rows(self, c, g):
+        J = an = n = 0
+        while True:
+            x = yield from self.take(c, n)
+            n += 1
+            if x < 0:
+                break
+            nkv = self.items[x]
+            for _ in range(nkv):
+                bb, jn = J & 1, J >> 1
+                yield ("wait", c.sfull[bb], jn)
+                check(c.S[bb] == J, f"row{g}: reads S({J}) while buffer {bb} holds S({c.S[bb]})")
+                c.S_read[bb].add(g)
+                c.sfree[bb].arrive()
+                yield ("step",)
+                if jn >= 1 and "pfree" not in self.drop:
+                    yield ("wait", c.pfree[bb], jn - 1)
+                check(c.DS_readers[bb] == 0, f"row{g}: dS buffer {bb} written while the dQ MMA reads it")
+                c.DS[bb][g] = J
+                c.pready[bb].arrive()
+                J += 1
+                yield ("step",)
+            if nkv == 0:
+                continue
+            if "dq" not in self.drop:
+                yield ("wait", c.dq, an)
+            an += 1
+            check(c.acc == (x, nkv - 1) and c.acc_inflight == 0, f"row{g}: epilogue of item {x} sees {c.acc}")
+            c.acc_read.add(g)
+            if g == 0:
+                self.processed.append(x)
+            yield ("step",)
+
+
+def run_trials(model_cls, trials, drop=(), seed0=0):
+    """Random item lists (with empty items) on 1-3 CTAs; returns the first error, or None."""
+    for t in range(seed0, seed0 + trials):
+        rng = random.Random(t)
+        nitems = rng.randint(1, 12)
+        items = [rng.choice([0, 0, 1, 2, 3, 4, 5, 8]) for _ in range(nitems)]
+        model = model_cls(t, rng.randint(1, min(3, nitems)), items, drop)
+        try:
+            model.run()
+            want = sorted(x for x in range(nitems) if items[x] > 0)
+            check(sorted(model.processed) == want, f"items processed {sorted(model.processed)}, want {want}")
+        except ProtocolError as e:
+            return f"trial {t}, items {items}: {e}"
+    return None

@@ -1,0 +1,25 @@
+"""The barrier protocols of the persistent backward kernels, run as executable models on the
+CPU (tests/barrier_models.py): random interleavings of the warp roles, the copies and the
+MMAs over random item lists with empty items and several CTAs on one counter must end, pass
+every parity wait at its intended phase and never overwrite data before its readers are done.
+Each model must also catch every wait that is taken out of it."""
+import pytest
+
+from tests.barrier_models import DkdvModel, DqModel, run_trials
+
+TRIALS = 150
+
+
+@pytest.mark.parametrize("model", [DkdvModel, DqModel], ids=["dkdv", "dq"])
+def test_protocol_holds_on_random_schedules(model):
+    err = run_trials(model, TRIALS)
+    assert err is None, err
+
+
+@pytest.mark.parametrize("model,wait", [
+    (DkdvModel, "kvfree"), (DkdvModel, "empty"), (DkdvModel, "sfree"), (DkdvModel, "pfree"), (DkdvModel, "drain"),
+    (DqModel, "qfree"), (DqModel, "kempty"), (DqModel, "vempty"), (DqModel, "sfree"), (DqModel, "pfree"),
+    (DqModel, "dq"),
+])
+def test_model_catches_a_missing_wait(model, wait):
+    assert run_trials(model, TRIALS, drop={wait}) is not None, f"{model.__name__} without {wait} passed"
