@@ -531,6 +531,169 @@ class DqModel(Model):
             yield ("step",)
 
 
+class FwdModel(Model):
+    """attn_fwd_kernel (one query block per CTA, not persistent): `items` holds one entry, the
+    length of the block's list.  K and V stream through 2-deep rings; S_j lands in TMEM buffer
+    j % 2 and the softmax warps write P_j over it in place; O accumulates in TMEM and is
+    rescaled by the softmax warps when a row maximum grows (a random choice per warp here)."""
+
+    STAGES = 2
+    NW = 4  # softmax warps
+
+    def make_cta(self, cid):
+        c = type("CTA", (), {})()
+        c.cid = cid
+        c.q = Bar("q", 1)
+        c.kfull = [Bar(f"kfull{i}", 1) for i in range(self.STAGES)]
+        c.vfull = [Bar(f"vfull{i}", 1) for i in range(self.STAGES)]
+        c.kempty = [Bar(f"kempty{i}", 1) for i in range(self.STAGES)]
+        c.vempty = [Bar(f"vempty{i}", 1) for i in range(self.STAGES)]
+        c.sfull = [Bar(f"sfull{i}", 1) for i in range(2)]
+        c.pfull = [Bar(f"pfull{i}", self.NW) for i in range(2)]
+        c.odone, c.drain, c.sdrain = Bar("odone", 1), Bar("drain", 1), Bar("sdrain", 1)
+        c.ktag, c.k_readers = [None] * self.STAGES, [0] * self.STAGES
+        c.vtag, c.v_readers = [None] * self.STAGES, [0] * self.STAGES
+        c.qtag = None
+        # TMEM buffer b: ("S", j) after the S MMA, ("P", j, warps written) after the softmax
+        c.buf, c.buf_readers = [None, None], [0, 0]
+        c.S_read = [set(range(self.NW)), set(range(self.NW))]
+        c.o_count, c.o_inflight = 0, 0  # P V products accumulated into O; P V MMAs in flight
+        c.mmaq = {1: [], 2: []}
+        return c
+
+    def roles(self, c):
+        return ([("producer", c, self.producer(c)), ("s_issuer", c, self.s_issuer(c)),
+                 ("pv_issuer", c, self.pv_issuer(c))] + [(f"sm{w}", c, self.softmax(c, w)) for w in range(self.NW)])
+
+    def complete_tma(self, job):
+        c, kind, idx, tag = job
+        if kind == "q":
+            c.qtag = tag
+            c.q.complete_tx(1)
+        elif kind == "k":
+            check(c.k_readers[idx] == 0, f"K stage {idx} overwritten while read")
+            c.ktag[idx] = tag
+            c.kfull[idx].complete_tx(1)
+        else:
+            check(c.v_readers[idx] == 0, f"V stage {idx} overwritten while read")
+            c.vtag[idx] = tag
+            c.vfull[idx].complete_tx(1)
+
+    def complete_mma(self, c, op):
+        if op[0] == "commit":
+            op[1].arrive()
+        elif op[0] == "S":
+            _, j, st, b = op
+            check(c.qtag == 0 and c.ktag[st] == j, f"S({j}): operands changed")
+            check(c.buf_readers[b] == 0, f"S({j}) overwrote buffer {b} while P V read it")
+            check(c.buf[b] is None or c.S_read[b] >= set(range(self.NW)) and c.buf[b][0] == "P",
+                  f"S({j}) overwrote buffer {b} before its P was formed and used")
+            c.buf[b], c.S_read[b] = ("S", j), set()
+            c.k_readers[st] -= 1
+        else:
+            _, j, st, b = op
+            check(c.vtag[st] == j and c.buf[b] == ("P", j, frozenset(range(self.NW))),
+                  f"PV({j}): operands changed before completion")
+            check(c.o_count == j, f"PV({j}) accumulated out of order")
+            c.o_count += 1
+            c.v_readers[st] -= 1
+            c.buf_readers[b] -= 1
+            c.o_inflight -= 1
+
+    def producer(self, c):
+        nkv = self.items[0]
+        c.q.expect_tx(1)
+        self.tma.append((c, "q", 0, 0))
+        for j in range(nkv):
+            st = j % self.STAGES
+            if j >= self.STAGES and "kempty" not in self.drop:
+                yield ("wait", c.kempty[st], j // self.STAGES - 1)
+            check(c.k_readers[st] == 0, "K load issued while read")
+            c.kfull[st].expect_tx(1)
+            self.tma.append((c, "k", st, j))
+            if j >= self.STAGES and "vempty" not in self.drop:
+                yield ("wait", c.vempty[st], j // self.STAGES - 1)
+            check(c.v_readers[st] == 0, "V load issued while read")
+            c.vfull[st].expect_tx(1)
+            self.tma.append((c, "v", st, j))
+            yield ("step",)
+        for j in range(max(0, nkv - self.STAGES), nkv):
+            yield ("wait", c.vfull[j % self.STAGES], j // self.STAGES)
+            yield ("wait", c.kfull[j % self.STAGES], j // self.STAGES)
+
+    def s_issuer(self, c):
+        nkv = self.items[0]
+        if nkv == 0:
+            return
+        yield ("wait", c.q, 0)
+        for j in range(nkv):
+            st, b = j % self.STAGES, j & 1
+            yield ("wait", c.kfull[st], j // self.STAGES)
+            # P_{j-2} V_{j-2} read buffer b: it must have completed (same index as the V stage)
+            if j >= 2 and "s_over_p" not in self.drop:
+                yield ("wait", c.vempty[st], (j - 2) // self.STAGES)
+            c.mmaq[1] += [("S", j, st, b), ("commit", c.sfull[b]), ("commit", c.kempty[st])]
+            c.k_readers[st] += 1
+            yield ("step",)
+        c.mmaq[1].append(("commit", c.sdrain))
+        yield ("wait", c.sdrain, 0)
+
+    def pv_issuer(self, c):
+        nkv = self.items[0]
+        if nkv == 0:
+            return
+        for j in range(nkv):
+            st, b = j % self.STAGES, j & 1
+            yield ("wait", c.pfull[b], j >> 1)
+            yield ("wait", c.vfull[st], j // self.STAGES)
+            check(c.buf[b] == ("P", j, frozenset(range(self.NW))), f"PV({j}) issued before P_{j} was written")
+            c.mmaq[2] += [("PV", j, st, b), ("commit", c.vempty[st]), ("commit", c.odone)]
+            c.v_readers[st] += 1
+            c.buf_readers[b] += 1
+            c.o_inflight += 1
+            yield ("step",)
+        c.mmaq[2].append(("commit", c.drain))
+        yield ("wait", c.drain, 0)
+
+    def softmax(self, c, w):
+        nkv = self.items[0]
+        for j in range(nkv):
+            b = j & 1
+            yield ("wait", c.sfull[b], j >> 1)
+            check(c.buf[b] is not None and c.buf[b][:2] in (("S", j), ("P", j)), f"sm{w}: reads S({j}) from {c.buf[b]}")
+            c.S_read[b].add(w)
+            if j > 0 and self.rng.random() < 0.3:
+                # rescale O: every earlier P V product must be in it and none in flight
+                if "odone" not in self.drop:
+                    yield ("wait", c.odone, j - 1)
+                check(c.o_count == j and c.o_inflight == 0, f"sm{w}: rescales O with {c.o_count} of {j} products")
+            yield ("step",)
+            check(c.buf_readers[b] == 0, f"sm{w}: writes P({j}) while P V reads buffer {b}")
+            prev = c.buf[b][2] if c.buf[b][0] == "P" else frozenset()
+            c.buf[b] = ("P", j, prev | {w})
+            c.pfull[b].arrive()
+            yield ("step",)
+        if nkv > 0:
+            yield ("wait", c.drain, 0)
+            check(c.o_count == nkv and c.o_inflight == 0, f"sm{w}: epilogue sees {c.o_count} of {nkv} products")
+            if w == 0:
+                self.processed.append(0)
+
+
+def run_forward_trials(trials, drop=(), seed0=0):
+    """Random list lengths (including 0) on one CTA; returns the first error, or None."""
+    for t in range(seed0, seed0 + trials):
+        rng = random.Random(t)
+        nkv = rng.choice([0, 1, 2, 3, 4, 5, 7, 10])
+        model = FwdModel(t, 1, [nkv], drop)
+        try:
+            model.run()
+            check(model.processed == ([0] if nkv > 0 else []), "epilogue not reached")
+        except ProtocolError as e:
+            return f"trial {t}, list length {nkv}: {e}"
+    return None
+
+
 def run_trials(model_cls, trials, drop=(), seed0=0):
     """Random item lists (with empty items) on 1-3 CTAs; returns the first error, or None."""
     for t in range(seed0, seed0 + trials):

@@ -1,11 +1,12 @@
-"""The barrier protocols of the persistent backward kernels, run as executable models on the
-CPU (tests/barrier_models.py): random interleavings of the warp roles, the copies and the
-MMAs over random item lists with empty items and several CTAs on one counter must end, pass
-every parity wait at its intended phase and never overwrite data before its readers are done.
-Each model must also catch every wait that is taken out of it."""
+"""The barrier protocols of the attention kernels, run as executable models on the CPU
+(tests/barrier_models.py).  The models cover the persistent dK/dV and dQ kernels, with random
+item lists that include empty items and several CTAs on one counter, and the forward.  Random
+interleavings of the warp roles, the copies and the MMAs must end, pass every parity wait at its
+intended phase and never overwrite data before its readers are done.  Each model must also
+catch every wait that is taken out of it."""
 import pytest
 
-from tests.barrier_models import DkdvModel, DqModel, run_trials
+from tests.barrier_models import DkdvModel, DqModel, run_forward_trials, run_trials
 
 TRIALS = 150
 
@@ -23,3 +24,13 @@ def test_protocol_holds_on_random_schedules(model):
 ])
 def test_model_catches_a_missing_wait(model, wait):
     assert run_trials(model, TRIALS, drop={wait}) is not None, f"{model.__name__} without {wait} passed"
+
+
+def test_forward_protocol_holds_on_random_schedules():
+    err = run_forward_trials(TRIALS)
+    assert err is None, err
+
+
+@pytest.mark.parametrize("wait", ["kempty", "vempty", "s_over_p", "odone"])
+def test_forward_model_catches_a_missing_wait(wait):
+    assert run_forward_trials(TRIALS, drop={wait}) is not None, f"forward without {wait} passed"
