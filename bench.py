@@ -61,7 +61,8 @@ def parse():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--sparsity", type=float, default=0.95,
                     help="calibrated target block sparsity of the config (0 = dense)")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=0,
+                    help="steps of the end-to-end leg (0: the same as --steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-qblocks", type=int, default=4, help="query blocks of the oracle sample")
     ap.add_argument("--heads", type=int, default=0,
@@ -69,6 +70,8 @@ def parse():
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if a.steps < 1 or a.e2e_steps < 0:
+        ap.error("--steps must be >= 1 and --e2e-steps >= 0")
     return a
 
 
@@ -308,7 +311,9 @@ def run_native(a, rank, world):
     # inputs from pinned host memory and reads all four results back; the uploads of step
     # i+1 and the read-back of step i-1 run on their own streams while step i computes
     # (inputs and outputs double-buffered on the device, ordered by events).
-    e2e_steps = max(1, a.e2e_steps)
+    # as many steps as the device-timed leg, so that the first upload and the last read-back,
+    # which no compute can hide, weigh as they do in a run of that length
+    e2e_steps = a.e2e_steps if a.e2e_steps > 0 else a.steps
     outs = ("o", "dq", "dk", "dv")
     hout = {n: torch.empty_like(host["q"]).pin_memory() for n in outs}
     dins = [{t: torch.empty_like(d[t]) for t in d} for _ in range(2)]
