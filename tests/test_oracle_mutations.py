@@ -165,3 +165,48 @@ def test_distillation_mutation_is_caught(monkeypatch, kind):
     _patch(monkeypatch, "vd_loss", _vd_loss_factory(kind))
     assert _fails(TD.test_loss_gradient_matches_central_differences,
                   TD.test_chain_matches_central_differences_with_teacher_frozen)
+
+
+# ---- the sampled backward variants (full-size parity checks recompute chosen rows / keys)
+
+def _kept_keys_ignoring_mask(block_mask_row, N, bk):
+    return np.arange(N)
+
+
+def _row_block_grads_without_D(q, k, v, do, keys, rows, scale):
+    s = (q[rows] @ k[keys].T) * scale
+    P, _ = S._masked_softmax_rows(s, np.ones_like(s, dtype=bool))
+    return P, P * (do[rows] @ v[keys].T)
+
+
+def _row_block_grads_unscaled(q, k, v, do, keys, rows, scale):
+    s = q[rows] @ k[keys].T
+    P, _ = S._masked_softmax_rows(s, np.ones_like(s, dtype=bool))
+    o = P @ v[keys]
+    D = (do[rows] * o).sum(axis=1)
+    return P, P * (do[rows] @ v[keys].T - D[:, None])
+
+
+@pytest.mark.parametrize("name,fn", [
+    ("_kept_keys", _kept_keys_ignoring_mask),
+    ("_row_block_grads", _row_block_grads_without_D),
+    ("_row_block_grads", _row_block_grads_unscaled),
+])
+def test_sampled_backward_mutation_is_caught(monkeypatch, name, fn):
+    monkeypatch.setattr(S, name, fn)
+    assert _fails(TA.test_row_and_column_sampled_versions_equal_the_full_computation)
+
+
+def _bwd_rows_without_D(q, k, v, do, block_mask, bq, bk, rows, scale=None):
+    N, d = k.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rows = np.asarray(rows)
+    allowed = S.token_mask(block_mask, N, bq, bk, rows)
+    P, _ = S._masked_softmax_rows((q[rows] @ k.T) * scale, allowed)
+    dS = P * (do[rows] @ v.T)
+    return scale * (dS @ k), scale * (dS.T @ q[rows]), P.T @ do[rows]
+
+
+def test_row_partition_mutation_is_caught(monkeypatch):
+    _patch(monkeypatch, "attn_bwd_rows", _bwd_rows_without_D)
+    assert _fails(TA.test_row_partition_of_the_backward_adds_up)
