@@ -8,8 +8,9 @@
 // computed over kept tiles only (gist.science explainer, section 2.C: skipped tiles cost
 // nothing).
 //
-// Each CTA owns a pair of adjacent key blocks (2m, 2m+1: 128 keys) and walks the union of
-// their two column lists (built by pair_union_kernel below) in sub-tiles of 64 query rows.
+// A work item is a pair of adjacent key blocks (2m, 2m+1: 128 keys); the CTA that takes it
+// walks the union of their two column lists (built by pair_union_kernel below) in sub-tiles
+// of 64 query rows and writes the pair's dK, dV once.
 // The products are formed transposed, keys along the 128 TMEM lanes:
 //   S^T  = K Q_u^T    M = 128 keys, N = 64 queries, K = d   (A, B from shared memory)
 //   dP^T = V dO_u^T   M = 128, N = 64, K = d

@@ -3,13 +3,14 @@
 // dQ = scale * dS K with dS = P * (dP - D), P = exp(s - LSE), dP = dO V^T: the gradient of
 // the block-sparse forward with respect to Q (the abstract of SpargeAttention2, arXiv
 // 2602.13515, contribution (ii): trainable sparse attention; gist.science explainer,
-// section 2.C: whole tiles kept or skipped).  Each CTA owns one query block of 128 rows and
-// walks that block's list of kept key blocks -- the forward's traversal -- so dQ
-// accumulates in TMEM over the whole list and is written once: no cross-CTA reduction.
+// section 2.C: whole tiles kept or skipped).  A work item is one query block of 128 rows;
+// the CTA that takes it walks that block's list of kept key blocks -- the forward's
+// traversal -- so dQ accumulates in TMEM over the whole list and is written once: no
+// cross-CTA reduction.
 //
 // Roles (352 threads, 1 CTA per SM): warp 0 TMA (Q and dO once per query block, K_j / V_j
-// per kept block into 4 / 2 stages), warp 1 TMEM owner and issuer of the S_j / dP_j MMAs, warp 2 issuer of
-// the dQ MMAs (each converged, one elect.sync lane issuing: two issuers keep the MMA queue
+// per kept block into 4 / 2 stages), warp 1 TMEM owner and issuer of the S_j / dP_j MMAs,
+// warp 2 issuer of the dQ MMAs (each converged, one elect.sync lane issuing: two issuers keep the MMA queue
 // fed while either waits on a barrier), and two row warpgroups (warps 3..6 and 7..10) that
 // both work on every list entry (TMEM buffers j % 2), one query row per thread, group g on
 // key columns 32g .. 32g+31 of the entry, so that each entry's dS is ready in half the time.
