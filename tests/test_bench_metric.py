@@ -1,0 +1,31 @@
+"""The benchmark's work count: the kept (query, key) token pairs behind every TFLOP/s figure
+equal, for ragged shapes, the number of allowed entries of the oracle's token-level mask
+(gist.science explainer, section 2.C: tiles are kept or skipped whole, and tokens past N do
+not exist)."""
+import os
+import sys
+
+import numpy as np
+import pytest
+
+import oracle as O
+from workload.gen import WorkloadConfig
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+@pytest.mark.parametrize("N,bq,bk", [(1000, 128, 64), (777, 64, 64), (130, 128, 64), (1, 128, 64), (4096, 128, 64)])
+def test_kept_pairs_count_the_token_mask(N, bq, bk):
+    cfg = WorkloadConfig(index=200, name="count", B=2, H=3, grid=(1, 1, N), d=64, dtype="bf16", bq=bq, bk=bk)
+    rng = np.random.default_rng(N)
+    mask = (rng.random((cfg.B, cfg.H, cfg.Tq, cfg.Tk)) < 0.3).astype(np.uint8)
+    mask[0, 0, -1, -1] = 1  # the ragged corner tile
+    want = sum(int(O.token_mask(mask[b, h], N, bq, bk).sum()) for b in range(cfg.B) for h in range(cfg.H))
+    assert bench.kept_pairs(cfg, mask) == want
+
+
+def test_dense_mask_counts_every_pair():
+    cfg = WorkloadConfig(index=201, name="dense", B=1, H=2, grid=(1, 1, 1000), d=64, dtype="bf16", bq=128, bk=64)
+    mask = np.ones((1, 2, cfg.Tq, cfg.Tk), dtype=np.uint8)
+    assert bench.kept_pairs(cfg, mask) == 2 * 1000 * 1000
