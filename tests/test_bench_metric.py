@@ -29,3 +29,15 @@ def test_dense_mask_counts_every_pair():
     cfg = WorkloadConfig(index=201, name="dense", B=1, H=2, grid=(1, 1, 1000), d=64, dtype="bf16", bq=128, bk=64)
     mask = np.ones((1, 2, cfg.Tq, cfg.Tk), dtype=np.uint8)
     assert bench.kept_pairs(cfg, mask) == 2 * 1000 * 1000
+
+
+def test_dkdv_traffic_is_reported_only_for_the_captured_workload():
+    import dataclasses
+    from workload import CONFIGS
+    wan14 = CONFIGS[3]
+    full = bench.dkdv_traffic(wan14, 0.95)
+    assert full is not None and full > 0
+    four = bench.dkdv_traffic(dataclasses.replace(wan14, H=4), 0.95)
+    assert four == pytest.approx(full * 4 / wan14.H)  # heads are independent and equal in work
+    assert bench.dkdv_traffic(wan14, 0.9) is None
+    assert bench.dkdv_traffic(CONFIGS[2], 0.95) is None
