@@ -2,9 +2,8 @@
 trainable block-sparse attention, behind the C ABI of include/sa2.h.
 
 The Python surface is a thin ctypes binding (``sa2.py``); the library is built in-tree by
-``build_lib.build()``.
+``build_lib.build()``.  Mask diagnostics, off the attention path, are in ``diagnostics``.
 """
-from .diagnostics import head_histograms, mask_diagnostics  # noqa: F401
 from .sa2 import (  # noqa: F401
     BlockMask,
     Sa2Error,
