@@ -221,6 +221,57 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(sm)}
 
 
+# ------------------------------------------------------------------- roofline accounting
+
+MASK_KERNELS = ("pool", "score_select", "csc")
+# Per kept (query, key) pair and channel, the algorithmic flops each attention kernel is
+# credited with: the forward's two GEMMs (S, P V); the dK/dV kernel's S, dP, dV, dK; the dQ
+# kernel's dQ GEMM only -- its recomputed S and dP are not algorithmic work.
+KERNEL_FLOPS = {"attn_fwd": 4, "attn_bwd_dkdv": 8, "attn_bwd_dq": 2}
+
+
+def phase_rooflines(prof, steps, pairs, d, peak_tflops):
+    """Per-phase time and fraction of the bf16 peak, each phase with everything it launches.
+
+    forward  = attn_fwd + its fp16 copy of V (one of the step's three to_f16 launches);
+    backward = attn_bwd_dkdv + attn_bwd_dq + bwd_preprocess + bwd_pair_union + the fp16
+               copies of Q and K (two of the three to_f16 launches);
+    algorithmic work 4 d (forward) and 10 d (backward) flops per kept pair."""
+    def ms(name, share=1.0):
+        return prof.get(name, (0, 0.0))[1] * share / steps
+
+    conv = prof.get("to_f16", (0, 0.0))
+    per_conv = conv[1] / conv[0] if conv[0] else 0.0  # the three copies are the same size
+    fwd_ms = ms("attn_fwd") + per_conv * (conv[0] / steps / 3.0 if conv[0] else 0.0)
+    bwd_ms = (ms("attn_bwd_dkdv") + ms("attn_bwd_dq") + ms("bwd_preprocess") + ms("bwd_pair_union")
+              + per_conv * (2.0 * conv[0] / steps / 3.0 if conv[0] else 0.0))
+    out = {}
+    for name, t, f in (("forward", fwd_ms, FWD_FLOPS), ("backward", bwd_ms, BWD_FLOPS)):
+        tf = f * d * pairs / (t * 1e-3) / 1e12 if t > 0 else None
+        out[name] = {"ms": t, "algorithmic_tflop": f * d * pairs / 1e12, "tflops": tf,
+                     "frac_of_bf16_burst": tf / peak_tflops if tf else None}
+    return out
+
+
+def dominant_roofline(prof, pairs, d, peaks):
+    """The `roofline` object of the kernel with the largest device time: algorithmic flops of
+    one launch (KERNEL_FLOPS x kept pairs) over its average launch time, against the measured
+    dense bf16 peak as a burst (the kernels run in steps of tens of milliseconds at full clock;
+    fp16 MMAs have the same nominal rate); the sustained figure is given beside it."""
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
+    c, m = prof[dom]
+    if dom in KERNEL_FLOPS and c > 0 and m > 0:
+        algo = KERNEL_FLOPS[dom] * d * pairs
+        achieved = algo / ((m / c) * 1e-3) / 1e12
+        return {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "peak_source": f"{peaks['source']} dense bf16, burst (fp16 MMAs: same nominal rate)",
+                "algorithmic_flops_per_launch": algo}
+    return {"kernel": dom, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": None, "traffic": None}
+
+
 # ---------------------------------------------------------------------------- native
 
 def run_native(a, rank, world):
@@ -360,28 +411,17 @@ def run_native(a, rank, world):
     value = world * flops_step * a.steps / (ms_max * 1e-3) / 1e12
     kernels = {n: {"launches": c, "ms_per_launch": (m / c if c else 0.0), "total_ms": m} for n, (c, m) in prof.items()}
     launches = sum(c for c, _ in prof.values())
-    dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
-    # algorithmic flops of each attention kernel over kept tiles: the forward's 2 GEMMs, the
-    # dK/dV kernel's 4 (S, dP, dV^T, dK^T), the dQ kernel's 3 (S, dP, dQ)
-    algo = {"attn_fwd": FWD_FLOPS * D * pairs, "attn_bwd_dkdv": 8 * D * pairs, "attn_bwd_dq": 6 * D * pairs}
-    c, m = prof[dom]
-    if dom in algo and c > 0 and m > 0:
-        achieved = algo[dom] / ((m / c) * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": dkdv_traffic(cfg, a.sparsity) if dom == "attn_bwd_dkdv" else None,
-                "peak_source": f"{peaks['source']} bf16 dense, sustained (fp16 MMAs: same nominal rate)",
-                "algorithmic_flops_per_launch": algo[dom]}
-    else:
-        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": None, "traffic": None}
+    ph = phase_rooflines(prof, a.steps, pairs, D, peaks["bf16_tflops"])
+    roof = dominant_roofline(prof, pairs, D, peaks)
+    if roof.get("kernel") == "attn_bwd_dkdv":
+        roof["traffic"] = dkdv_traffic(cfg, a.sparsity)
     # mask builder against HBM: it reads Q and K once and writes the mask and lists
     qk_bytes = 2 * B * H * N * D * 2
     out_bytes = B * H * cfg.Tq * cfg.Tk + 4 * 2 * float(bm.row_cnt.sum().item()) + 4 * B * H * (cfg.Tq + cfg.Tk)
-    mask_ms = sum(prof[k][1] for k in ("pool", "score_select", "csc")) / a.steps
+    mask_ms = sum(prof[k][1] for k in MASK_KERNELS if k in prof) / a.steps
     mask_gbs = (qk_bytes + out_bytes) / (mask_ms * 1e-3) / 1e9 if mask_ms > 0 else None
-    fwd_ms = (prof["attn_fwd"][1]) / a.steps
-    bwd_ms = (prof["attn_bwd_dkdv"][1] + prof["attn_bwd_dq"][1]) / a.steps
+    fwd_ms, bwd_ms = ph["forward"]["ms"], ph["backward"]["ms"]
+    step_frac = flops_step / (ms_max / a.steps * 1e-3) / 1e12 / peaks["bf16_tflops"]
     line = {
         "metric": metric_name(a.sparsity), "metric_detail": METRIC_DETAIL,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
@@ -395,8 +435,9 @@ def run_native(a, rank, world):
         "kept_tflop_per_step": flops_step / 1e12,
         "dense_equiv_tflops": world * (FWD_FLOPS + BWD_FLOPS) * D * float(N) * N * B * H * a.steps / (ms_max * 1e-3) / 1e12,
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "mask_ms": mask_ms,
-        "fwd_tflops": FWD_FLOPS * D * pairs / (fwd_ms * 1e-3) / 1e12 if fwd_ms > 0 else None,
-        "bwd_tflops": BWD_FLOPS * D * pairs / (bwd_ms * 1e-3) / 1e12 if bwd_ms > 0 else None,
+        "fwd_tflops": ph["forward"]["tflops"], "bwd_tflops": ph["backward"]["tflops"],
+        "phases": ph,
+        "step_frac_of_bf16_burst": step_frac,
         "mask_builder": {"ms": mask_ms, "achieved_gbs": mask_gbs, "peak_gbs": peaks["hbm_gbs"],
                          "frac": mask_gbs / peaks["hbm_gbs"] if mask_gbs else None, "bytes": qk_bytes + out_bytes},
         "roofline": roof,

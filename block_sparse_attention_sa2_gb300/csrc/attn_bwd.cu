@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 224);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 232);
   volatile int* item_slot = reinterpret_cast<volatile int*>(smem + kOffBar + 240);
+  const WaitCtl wc{abort_flag, s.wait_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Work items are key-block pairs in pair-major order (item x: pair m = x / BH of head
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a consumer warp takes item n from its slot and hands the slot back; -1 ends the loop
   auto take_item = [&](int n, bool& ok) {
     const int slot = n & 1;
-    if (!__all_sync(0xffffffffu, mbar_wait(bar_item_full(slot), (n >> 1) & 1, abort_flag))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(bar_item_full(slot), (n >> 1) & 1, wc))) {
       ok = false;
       return -1;
     }
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int x = blockIdx.x;
     for (int n = 0; ok; ++n) {
       const int slot = n & 1;
-      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_item_free(slot), ((n >> 1) - 1) & 1, abort_flag))) {
+      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_item_free(slot), ((n >> 1) - 1) & 1, wc))) {
         ok = false;
         break;
       }
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = x / BH, bh = x - m * BH, b = bh / s.H, h = bh - b * s.H;
         const uint32_t* list = a.pair_idx + ((int64_t)bh * Tp + m) * s.Tq;
         // K, V of the previous pair are free once its S^T / dP^T MMAs completed
-        if (kvn >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_kvfree, (kvn - 1) & 1, abort_flag))) {
+        if (kvn >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_kvfree, (kvn - 1) & 1, wc))) {
           ok = false;
           break;
         }
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int st = U & (kStages - 1);
           if (U >= kStages &&
-              !__all_sync(0xffffffffu, mbar_wait(bar_empty(st), ((U >> 2) - 1) & 1, abort_flag))) {
+              !__all_sync(0xffffffffu, mbar_wait(bar_empty(st), ((U >> 2) - 1) & 1, wc))) {
             ok = false;
             break;
           }
@@ -295,11 +296,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       x = __shfl_sync(0xffffffffu, xn, 0);
     }
-    // no copy may still be in flight when the CTA exits
-    if (ok && lane == 0) {
+    // No copy may still be in flight when the CTA exits, whether the loop ran to its end or
+    // gave up: U and kvn count the loads issued, so drain the last load of each stage and the
+    // last K / V load (each is its barrier's latest phase).
+    if (lane == 0) {
       for (uint32_t v = U > kStages ? U - kStages : 0; v < U; ++v)
-        mbar_wait(bar_full(v & (kStages - 1)), (v >> 2) & 1, abort_flag);
-      if (kvn > 0) mbar_wait(bar_kv, (kvn - 1) & 1, abort_flag);
+        mbar_drain(bar_full(v & (kStages - 1)), (v >> 2) & 1, abort_flag);
+      if (kvn > 0) mbar_drain(bar_kv, (kvn - 1) & 1, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- S^T, dP^T issuer (warp 1)
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (x < 0) break;
       const int nsub = item_len(x, false) << sub_shift;
       if (nsub == 0) continue;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_kv, kvn & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_kv, kvn & 1, wc))) {
         ok = false;
         break;
       }
@@ -324,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < nsub; ++u, ++U) {
         const int st = U & (kStages - 1);
         // the stage landed, and S^T / dP^T of sub-tile U - 1 were read out of TMEM
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (U >> 2) & 1, abort_flag) &&
-                                         (U == 0 || mbar_wait(bar_sfree, (U - 1) & 1, abort_flag)))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (U >> 2) & 1, wc) &&
+                                         (U == 0 || mbar_wait(bar_sfree, (U - 1) & 1, wc)))) {
           ok = false;
           break;
         }
@@ -343,10 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one()) umma_commit(bar_kvfree);
       __syncwarp();
     }
-    // no MMA of this warp may still run when TMEM is released (matters on the abort path)
+    // no MMA of this warp may still run when TMEM is released, on the abort path too
     if (elect_one()) umma_commit(bar_sdrain);
     __syncwarp();
-    mbar_wait(bar_sdrain, 0, abort_flag);
+    mbar_drain(bar_sdrain, 0, abort_flag);
   } else if (warp == 2) {
     // --------------------------------------------------------- dV, dK issuer (warp 2)
     constexpr uint32_t idG = idesc_f16_f32(128, 128, false, true);
@@ -362,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the first sub-tile of a pair this also orders the overwrite of the dV, dK
         // accumulators after the previous pair's epilogue: every element-wise thread read
         // them out before it wrote this P^T / dS^T.
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (W >> 1) & 1, abort_flag) &&
-                                         mbar_wait(bar_full(st), (W >> 2) & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (W >> 1) & 1, wc) &&
+                                         mbar_wait(bar_full(st), (W >> 2) & 1, wc))) {
           ok = false;
           break;
         }
@@ -388,9 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (elect_one()) umma_commit(bar_gdrain);
     __syncwarp();
-    mbar_wait(bar_gdrain, 0, abort_flag);
+    mbar_drain(bar_gdrain, 0, abort_flag);
   } else {
     // ------------------------------------------------------------- element-wise warps
+    if (s.stall_ns && blockIdx.x == 0) stall_for(s.stall_ns);  // failure-path test hook
     const int q4 = warp & 3;          // TMEM lane quarter
     const int g = (warp - 3) >> 2;    // query columns 32g .. 32g+31 of each sub-tile
     const int r = 32 * q4 + lane;     // key row of the pair
@@ -418,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool keep = ((e >> (30 + half)) & 1u) != 0;  // same for the whole warp
         const int st = U & (kStages - 1), bb = U & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull, U & 1, abort_flag) &&
-                                         mbar_wait(bar_full(st), (U >> 2) & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull, U & 1, wc) &&
+                                         mbar_wait(bar_full(st), (U >> 2) & 1, wc))) {
           ok = false;
           break;
         }
@@ -458,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) pw[j] = dw[j] = 0u;
         }
         // buffer bb was last read by the dV / dK MMAs of sub-tile U - 2
-        if (U >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_pfree(bb), ((U >> 1) - 1) & 1, abort_flag))) {
+        if (U >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar_pfree(bb), ((U >> 1) - 1) & 1, wc))) {
           ok = false;
           break;
         }
@@ -481,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_drain, an & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_drain, an & 1, wc))) {
         ok = false;
         break;
       }

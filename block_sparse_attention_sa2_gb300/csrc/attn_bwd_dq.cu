@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 384);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffBar + 392);
   volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kOffBar + 400);
+  const WaitCtl wc{abort_flag, s.wait_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Work items are query blocks (item x: block x % Tq of head x / Tq).  Each CTA stays
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a consumer warp takes item n from its slot and hands the slot back; -1 ends the loop
   auto take_item = [&](int n, bool& ok) {
     const int slot = n & 1;
-    if (!__all_sync(0xffffffffu, mbar_wait(bar_item_full(slot), (n >> 1) & 1, abort_flag))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(bar_item_full(slot), (n >> 1) & 1, wc))) {
       ok = false;
       return -1;
     }
@@ -183,10 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&mv);
       bool ok = true;
       uint32_t J = 0, qn = 0;
+      uint32_t nk = 0, nv = 0;  // K and V loads issued (J can lag one of them on the abort path)
       int x = blockIdx.x;
       for (int n = 0; ok; ++n) {
         const int slot = n & 1;
-        if (n >= 2 && !mbar_wait(bar_item_free(slot), ((n >> 1) - 1) & 1, abort_flag)) {
+        if (n >= 2 && !mbar_wait(bar_item_free(slot), ((n >> 1) - 1) & 1, wc)) {
           ok = false;
           break;
         }
@@ -200,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int bh = x / s.Tq, qi = x - bh * s.Tq, b = bh / s.H, h = bh - b * s.H;
           const int32_t* list = a.row_idx + (int64_t)x * s.Tk;
           // Q, dO of the previous query block are free once its S_j / dP_j MMAs completed
-          if (qn >= 1 && !mbar_wait(bar_qfree, (qn - 1) & 1, abort_flag)) {
+          if (qn >= 1 && !mbar_wait(bar_qfree, (qn - 1) & 1, wc)) {
             ok = false;
             break;
           }
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               report_error(a.status, kDevErrBounds);
               kb = 0;
             }
-            if (J >= kKStages && !mbar_wait(bar_kempty(ks), ((J / kKStages) - 1) & 1, abort_flag)) {
+            if (J >= kKStages && !mbar_wait(bar_kempty(ks), ((J / kKStages) - 1) & 1, wc)) {
               ok = false;
               break;
             }
@@ -225,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int p = 0; p < L::kPanels; ++p)
               tma_load_4d(sbase + L::kOffK + ks * L::kKVBytes + p * 8192, &mk, bar_kfull(ks), p * 64, kb * 64, h,
                           b);
-            if (J >= kVStages && !mbar_wait(bar_vempty(vs), ((J / kVStages) - 1) & 1, abort_flag)) {
+            ++nk;
+            if (J >= kVStages && !mbar_wait(bar_vempty(vs), ((J / kVStages) - 1) & 1, wc)) {
               ok = false;
               break;
             }
@@ -233,18 +236,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int p = 0; p < L::kPanels; ++p)
               tma_load_4d(sbase + L::kOffV + vs * L::kKVBytes + p * 8192, &mv, bar_vfull(vs), p * 64, kb * 64, h,
                           b);
+            ++nv;
           }
         }
         x = xn;
       }
-      // no copy may still be in flight when the CTA exits
-      if (ok) {
-        for (uint32_t v = J > kKStages ? J - kKStages : 0; v < J; ++v)
-          mbar_wait(bar_kfull(v % kKStages), (v / kKStages) & 1, abort_flag);
-        for (uint32_t v = J > kVStages ? J - kVStages : 0; v < J; ++v)
-          mbar_wait(bar_vfull(v % kVStages), (v / kVStages) & 1, abort_flag);
-        if (qn > 0) mbar_wait(bar_q, (qn - 1) & 1, abort_flag);
-      }
+      // No copy may still be in flight when the CTA exits, whether the loop ran to its end or
+      // gave up: drain the last load of each stage and the last Q / dO load (each is its
+      // barrier's latest phase).
+      for (uint32_t v = nk > kKStages ? nk - kKStages : 0; v < nk; ++v)
+        mbar_drain(bar_kfull(v % kKStages), (v / kKStages) & 1, abort_flag);
+      for (uint32_t v = nv > kVStages ? nv - kVStages : 0; v < nv; ++v)
+        mbar_drain(bar_vfull(v % kVStages), (v / kVStages) & 1, abort_flag);
+      if (qn > 0) mbar_drain(bar_q, (qn - 1) & 1, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ S_j, dP_j issuer
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (x < 0) break;
       const int nkv = item_len(x, false);
       if (nkv == 0) continue;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_q, qn & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_q, qn & 1, wc))) {
         ok = false;
         break;
       }
@@ -267,9 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K_j and V_j present, and buffer bb (S_{j-2} / dP_{j-2}) read out by the row
         // threads, before the S_j and dP_j MMAs issue as one group
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(bar_kfull(ks), (J / kKStages) & 1, abort_flag) &&
-                            (J < 2 || mbar_wait(bar_sfree(bb), ((J >> 1) - 1) & 1, abort_flag)) &&
-                            mbar_wait(bar_vfull(vs), (J / kVStages) & 1, abort_flag))) {
+                        mbar_wait(bar_kfull(ks), (J / kKStages) & 1, wc) &&
+                            (J < 2 || mbar_wait(bar_sfree(bb), ((J >> 1) - 1) & 1, wc)) &&
+                            mbar_wait(bar_vfull(vs), (J / kVStages) & 1, wc))) {
           ok = false;
           break;
         }
@@ -288,10 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one()) umma_commit(bar_qfree);
       __syncwarp();
     }
-    // no MMA of this warp may still run when TMEM is released (matters on the abort path)
+    // no MMA of this warp may still run when TMEM is released, on the abort path too
     if (elect_one()) umma_commit(bar_sdrain);
     __syncwarp();
-    mbar_wait(bar_sdrain, 0, abort_flag);
+    mbar_drain(bar_sdrain, 0, abort_flag);
   } else if (warp == 2) {
     // ------------------------------------------------------------------ dQ issuer
     constexpr uint32_t idQ = idesc_f16_f32(128, D, false, true);
@@ -306,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dS_j written.  For the first entry of a query block this also orders the
         // overwrite of the dQ accumulator after the previous block's epilogue: every row
         // thread read dQ out before it wrote this dS.
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (J >> 1) & 1, abort_flag) &&
-                                         mbar_wait(bar_kfull(ks), (J / kKStages) & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (J >> 1) & 1, wc) &&
+                                         mbar_wait(bar_kfull(ks), (J / kKStages) & 1, wc))) {
           ok = false;
           break;
         }
@@ -329,9 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (elect_one()) umma_commit(bar_gdrain);
     __syncwarp();
-    mbar_wait(bar_gdrain, 0, abort_flag);
+    mbar_drain(bar_gdrain, 0, abort_flag);
   } else {
     // -------------------------------------------------------------- query-row threads
+    if (s.stall_ns && blockIdx.x == 0) stall_for(s.stall_ns);  // failure-path test hook
     const int wg = (warp - 3) >> 2;  // row warpgroup 0 or 1
     const int sub = warp & 3;
     const int r = 32 * sub + lane;
@@ -359,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bb = J & 1, jn = J >> 1;
         int kb = next_kb;
         if (j + 1 < nkv) next_kb = list[j + 1];
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bb), jn & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bb), jn & 1, wc))) {
           ok = false;
           break;
         }
@@ -386,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[c / 2] = pack_f16x2(ds[0], ds[1]);
         }
         // dS buffer bb was last read by the dQ MMA of entry J - 2
-        if (jn >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_pfree(bb), (jn - 1) & 1, abort_flag))) {
+        if (jn >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar_pfree(bb), (jn - 1) & 1, wc))) {
           ok = false;
           break;
         }
@@ -409,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, an & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, an & 1, wc))) {
         ok = false;
         break;
       }

@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // 16 barriers occupy the first 128 bytes of the 256-byte barrier area
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 160);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffBar + 192);
+  const WaitCtl wc{abort_flag, s.wait_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x / s.Tq;
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_arrive_expect_tx(bar_q, L::kQBytes);
       for (int p = 0; p < L::kPanels; ++p)
         tma_load_4d(sbase + L::kOffQ + p * 16384, &mq, bar_q, p * 64, qi * s.bq, h, b);
+      int nk = 0, nv = 0;  // K and V loads issued
       for (int j = 0; j < nkv; ++j) {
         const int st = j % kNumStages;
         const uint32_t ph = ((j / kNumStages) - 1) & 1;
@@ -165,38 +167,40 @@ __global__ void __launch_bounds__(kThreads, 2)
           report_error(a.status, kDevErrBounds);
           kb = 0;
         }
-        if (j >= kNumStages && !mbar_wait(bar_kempty(st), ph, abort_flag)) break;
+        if (j >= kNumStages && !mbar_wait(bar_kempty(st), ph, wc)) break;
         mbar_arrive_expect_tx(bar_kfull(st), L::kKVBytes);
         for (int p = 0; p < L::kPanels; ++p)
           tma_load_4d(sbase + L::kOffK + st * L::kKVBytes + p * 8192, &mk, bar_kfull(st), p * 64, kb * 64, h, b);
-        if (j >= kNumStages && !mbar_wait(bar_vempty(st), ph, abort_flag)) break;
+        ++nk;
+        if (j >= kNumStages && !mbar_wait(bar_vempty(st), ph, wc)) break;
         mbar_arrive_expect_tx(bar_vfull(st), L::kKVBytes);
         for (int p = 0; p < L::kPanels; ++p)
           tma_load_4d(sbase + L::kOffV + st * L::kKVBytes + p * 8192, &mv, bar_vfull(st), p * 64, kb * 64, h, b);
+        ++nv;
       }
-      // wait for the loads still in flight before the CTA may exit
-      const int first = nkv > kNumStages ? nkv - kNumStages : 0;
-      for (int j = first; j < nkv; ++j) {
-        const int st = j % kNumStages;
-        mbar_wait(bar_vfull(st), (j / kNumStages) & 1, abort_flag);
-        mbar_wait(bar_kfull(st), (j / kNumStages) & 1, abort_flag);
-      }
+      // No copy may still be in flight when the CTA exits, whether the loop ran to its end or
+      // gave up: drain Q and the last load of each stage (each is that stage's latest phase).
+      mbar_drain(bar_q, 0, abort_flag);
+      for (int j = nk > kNumStages ? nk - kNumStages : 0; j < nk; ++j)
+        mbar_drain(bar_kfull(j % kNumStages), (j / kNumStages) & 1, abort_flag);
+      for (int j = nv > kNumStages ? nv - kNumStages : 0; j < nv; ++j)
+        mbar_drain(bar_vfull(j % kNumStages), (j / kNumStages) & 1, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ S_j issuer
     if (nkv > 0) {
       constexpr uint32_t idS = idesc_f32acc(128, 64, false, false, !S_F16);
       const uint64_t qd = smem_desc(sbase + L::kOffQ, 16, 1024);
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag));
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wc));
       for (int j = 0; ok && j < nkv; ++j) {
         const int st = j % kNumStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_kfull(st), (j / kNumStages) & 1, abort_flag))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_kfull(st), (j / kNumStages) & 1, wc))) break;
         // S_j overwrites the TMEM buffer whose P_{j-2} the MMA P_{j-2} V_{j-2} read: a
         // later tcgen05.mma is not ordered after an earlier one's TMEM operand reads, so
         // wait for that MMA to complete (its commit also releases V_{j-2}; buffer and
         // V stage have the same index, both rings being 2 deep)
         if (j >= 2 &&
-            !__all_sync(0xffffffffu, mbar_wait(bar_vempty(st), ((j - 2) / kNumStages) & 1, abort_flag)))
+            !__all_sync(0xffffffffu, mbar_wait(bar_vempty(st), ((j - 2) / kNumStages) & 1, wc)))
           break;
         tc_fence_after();
         const uint64_t kd = smem_desc(sbase + L::kOffK + st * L::kKVBytes, 16, 1024);
@@ -207,10 +211,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncwarp();
       }
-      // no MMA of this warp may still run when TMEM is released (matters on the abort path)
+      // no MMA of this warp may still run when TMEM is released, on the abort path too
       if (elect_one()) umma_commit(bar_sdrain);
       __syncwarp();
-      mbar_wait(bar_sdrain, 0, abort_flag);
+      mbar_drain(bar_sdrain, 0, abort_flag);
     }
   } else if (warp == 2) {
     // ---------------------------------------------------------------- P_j V_j issuer
@@ -218,8 +222,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       constexpr uint32_t idO = idesc_f16_f32(128, D, false, true);
       for (int jj = 0; jj < nkv; ++jj) {
         const int st = jj % kNumStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, abort_flag) &&
-                                         mbar_wait(bar_vfull(st), (jj / kNumStages) & 1, abort_flag)))
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, wc) &&
+                                         mbar_wait(bar_vfull(st), (jj / kNumStages) & 1, wc)))
           break;
         tc_fence_after();
         // V as the MN-major B operand: N = D (64-element groups 8 KB apart), K = 16 rows
@@ -235,10 +239,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       // MMA of the CTA
       if (elect_one()) umma_commit(bar_drain);
       __syncwarp();
-      mbar_wait(bar_drain, 0, abort_flag);
+      mbar_drain(bar_drain, 0, abort_flag);
     }
   } else {
     // ------------------------------------------------------------------ softmax rows
+    if (s.stall_ns && blockIdx.x == 0) stall_for(s.stall_ns);  // failure-path test hook
     const int sub = warp & 3;  // TMEM lane quarter this warp may access
     const int r = 32 * sub + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * sub) << 16);
@@ -251,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int bsel = j & 1;
       int kb = next_kb;
       if (j + 1 < nkv) next_kb = list[j + 1];
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bsel), (j >> 1) & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(bsel), (j >> 1) & 1, wc))) {
         ok = false;
         break;
       }
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const float alpha = need ? ex2(m_used - mx) : 1.f;
           // S_j was issued only after P_{j-2} V_{j-2} completed, so o_done is at most one
           // phase behind j - 1 here and the parity wait is exact
-          if (!__all_sync(0xffffffffu, mbar_wait(bar_odone, (j - 1) & 1, abort_flag))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_odone, (j - 1) & 1, wc))) {
             ok = false;
             break;
           }
@@ -337,10 +342,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         a.lse[(int64_t)bh * s.N + tok] = -INFINITY;
       }
-    } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar_drain, 0, abort_flag))) {
+    } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar_drain, 0, wc) && !*abort_flag)) {
       // bar_drain completes once, after the last MMA.  (A parity wait on o_done is only
       // valid while that barrier is at most one phase behind the awaited phase; here the
-      // last two P V MMAs may both still be pending.)
+      // last two P V MMAs may both still be pending.)  On the abort path the P V issuer
+      // completes it after fewer products: the flag is up then, and nothing is written.
       tc_fence_after();
       const float inv_l = 1.f / l;
 #pragma unroll 1

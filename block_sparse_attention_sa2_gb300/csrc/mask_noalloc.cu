@@ -46,43 +46,22 @@ void* scratch_for_current_device(cudaError_t* err) {
   return g_scratch_ptr[dev];
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" sa2_status sa2_build_mask_noalloc(const sa2_shape* shape, const void* q, const void* k, float topk,
                                              float topp, const sa2_blockmask* out, void* stream) {
-  if (!shape || !q || !k || !out || !out->row_cnt || !out->row_idx || !out->col_cnt || !out->col_idx || !out->mask)
-    return SA2_ERR_INVALID_ARG;
-  const sa2_shape& x = *shape;
-  if (x.B < 1 || x.H < 1 || x.N < 1 || x.reserved != 0) return SA2_ERR_INVALID_ARG;
-  if (x.dtype != SA2_BF16 && x.dtype != SA2_FP32) return SA2_ERR_UNSUPPORTED;
-  if (x.d != 64 && x.d != 128) return SA2_ERR_UNSUPPORTED;
-  if ((x.bq != 64 && x.bq != 128) || x.bk != 64) return SA2_ERR_UNSUPPORTED;
-  const int64_t esz = x.dtype == SA2_BF16 ? 2 : 4;
-  if (x.stride_n < x.d || x.stride_h < 1 || x.stride_b < 1) return SA2_ERR_INVALID_ARG;
-  if ((x.stride_n * esz) % 16 || (x.stride_h * esz) % 16 || (x.stride_b * esz) % 16) return SA2_ERR_ALIGNMENT;
-  if (!std::isfinite(topk) || !std::isfinite(topp) || topk < 0.f || topk > 1.f || topp < 0.f || topp > 1.f)
-    return SA2_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(out->row_cnt) || !aligned16(out->row_idx) ||
-      !aligned16(out->col_cnt) || !aligned16(out->col_idx) || !aligned16(out->mask) ||
-      (out->pooled_p && !aligned16(out->pooled_p)))
-    return SA2_ERR_ALIGNMENT;
-
+  // the same validation as sa2_build_mask, then the size check of the static scratch
   ShapeArgs s;
-  s.B = x.B;
-  s.H = x.H;
-  s.N = x.N;
-  s.d = x.d;
-  s.bq = x.bq;
-  s.bk = x.bk;
-  s.Tq = (x.N + x.bq - 1) / x.bq;
-  s.Tk = (x.N + x.bk - 1) / x.bk;
-  s.dtype = x.dtype;
-  s.sb = x.stride_b;
-  s.sh = x.stride_h;
-  s.sn = x.stride_n;
-  if (s.Tk > 7680 || score_rows_per_cta(s.Tk, s.d) == 0) return SA2_ERR_UNSUPPORTED;
+  sa2_status st = check_shape(shape, &s);
+  if (st != SA2_OK) return st;
+  if (!q || !k || !out || !out->row_cnt || !out->row_idx || !out->col_cnt || !out->col_idx || !out->mask)
+    return SA2_ERR_INVALID_ARG;
+  SelectArgs sel;
+  st = make_select_args(s, topk, topp, &sel);
+  if (st != SA2_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(out->row_cnt) || !aligned16(out->row_idx) ||
+      !aligned16(out->col_cnt) || !aligned16(out->col_idx) || !aligned16(out->mask) || !aligned16(out->pooled_p))
+    return SA2_ERR_ALIGNMENT;
 
   // pooled queries then pooled keys, fp32, as the builder lays them out
   if (mask_pooled_bytes(s, nullptr) > (size_t)SA2_NOALLOC_SCRATCH_BYTES) return SA2_ERR_WORKSPACE;
@@ -91,20 +70,6 @@ extern "C" sa2_status sa2_build_mask_noalloc(const sa2_shape* shape, const void*
   unsigned char* scratch = static_cast<unsigned char*>(scratch_for_current_device(&err));
   if (!scratch) return SA2_ERR_CUDA;
 
-  SelectArgs sel;
-  const double Kd = std::ceil((double)topk * s.Tk - 1e-9);
-  sel.K = (int)std::fmin(std::fmax(Kd, 0.0), (double)s.Tk);
-  if (topp <= 0.f) {
-    sel.p_mode = 1;
-    sel.p_fix = 0;
-  } else if (topp >= 1.f) {
-    sel.p_mode = 2;
-    sel.p_fix = 0;
-  } else {
-    sel.p_mode = 0;
-    sel.p_fix = (unsigned long long)std::ldexp((double)topp, 60);
-  }
-  sel.inv_sqrt_d = (float)(1.0 / std::sqrt((double)s.d));
   MaskOut mo;
   mo.row_cnt = out->row_cnt;
   mo.row_idx = out->row_idx;

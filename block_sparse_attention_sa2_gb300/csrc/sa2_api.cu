@@ -2,6 +2,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/sa2.h"
@@ -31,9 +32,16 @@ unsigned* status_ptr() {
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Limits of the attention kernels' bounded waits, set by sa2_debug_set_wait_limit (0: the
+// default limit, no stall).
+std::atomic<unsigned long long> g_wait_limit_ns{0}, g_stall_ns{0};
+
+}  // namespace
+
+namespace sa2 {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Validates a shape and fills the derived block counts.
 sa2_status check_shape(const sa2_shape* shape, ShapeArgs* s) {
   if (!shape) return SA2_ERR_INVALID_ARG;
   const sa2_shape& x = *shape;
@@ -56,10 +64,36 @@ sa2_status check_shape(const sa2_shape* shape, ShapeArgs* s) {
   s->sb = x.stride_b;
   s->sh = x.stride_h;
   s->sn = x.stride_n;
+  const unsigned long long w = g_wait_limit_ns.load(std::memory_order_relaxed);
+  s->wait_ns = w ? w : kWaitLimitNs;
+  s->stall_ns = g_stall_ns.load(std::memory_order_relaxed);
   if (s->Tk > 7680 || score_rows_per_cta(s->Tk, s->d) == 0) return SA2_ERR_UNSUPPORTED;
   if ((int64_t)s->B * s->H * s->Tq >= (int64_t)1 << 31) return SA2_ERR_UNSUPPORTED;
   return SA2_OK;
 }
+
+sa2_status make_select_args(const ShapeArgs& s, float topk, float topp, SelectArgs* sel) {
+  if (!std::isfinite(topk) || !std::isfinite(topp) || topk < 0.f || topk > 1.f || topp < 0.f || topp > 1.f)
+    return SA2_ERR_INVALID_ARG;
+  const double Kd = std::ceil((double)topk * s.Tk - 1e-9);
+  sel->K = (int)std::fmin(std::fmax(Kd, 0.0), (double)s.Tk);
+  if (topp <= 0.f) {
+    sel->p_mode = 1;
+    sel->p_fix = 0;
+  } else if (topp >= 1.f) {
+    sel->p_mode = 2;
+    sel->p_fix = 0;
+  } else {
+    sel->p_mode = 0;
+    sel->p_fix = (unsigned long long)std::ldexp((double)topp, 60);
+  }
+  sel->inv_sqrt_d = (float)(1.0 / std::sqrt((double)s.d));
+  return SA2_OK;
+}
+
+}  // namespace sa2
+
+namespace {
 
 size_t token_elems(const ShapeArgs& s) { return (size_t)s.B * s.H * s.N * s.d; }
 
@@ -156,28 +190,15 @@ sa2_status sa2_build_mask(const sa2_shape* shape, const void* q, const void* k, 
   if (st != SA2_OK) return st;
   if (!q || !k || !out || !out->row_cnt || !out->row_idx || !out->col_cnt || !out->col_idx)
     return SA2_ERR_INVALID_ARG;
-  if (!std::isfinite(topk) || !std::isfinite(topp) || topk < 0.f || topk > 1.f || topp < 0.f || topp > 1.f)
-    return SA2_ERR_INVALID_ARG;
+  SelectArgs sel;
+  st = make_select_args(s, topk, topp, &sel);
+  if (st != SA2_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(out->row_cnt) || !aligned16(out->row_idx) ||
       !aligned16(out->col_cnt) || !aligned16(out->col_idx) || (out->mask && !aligned16(out->mask)) ||
       (out->pooled_p && !aligned16(out->pooled_p)) || !aligned16(ws))
     return SA2_ERR_ALIGNMENT;
   const MaskWs w = mask_ws(s);
   if (!ws || ws_bytes < w.total) return SA2_ERR_WORKSPACE;
-  SelectArgs sel;
-  const double Kd = std::ceil((double)topk * s.Tk - 1e-9);
-  sel.K = (int)std::fmin(std::fmax(Kd, 0.0), (double)s.Tk);
-  if (topp <= 0.f) {
-    sel.p_mode = 1;
-    sel.p_fix = 0;
-  } else if (topp >= 1.f) {
-    sel.p_mode = 2;
-    sel.p_fix = 0;
-  } else {
-    sel.p_mode = 0;
-    sel.p_fix = (unsigned long long)std::ldexp((double)topp, 60);
-  }
-  sel.inv_sqrt_d = (float)(1.0 / std::sqrt((double)s.d));
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   MaskOut mo;
   mo.row_cnt = out->row_cnt;
@@ -375,6 +396,11 @@ sa2_status sa2_vd_loss(const sa2_shape* shape, const void* o_s, const void* o_s_
   const bool lo = s.dtype == SA2_BF16 && o_s_lo;
   return cuda_status(launch_vd_loss(s, o_s, lo ? o_s_lo : nullptr, o_t, lo ? o_t_lo : nullptr, d_o, loss,
                                     static_cast<double*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+void sa2_debug_set_wait_limit(unsigned long long limit_ns, unsigned long long stall_ns) {
+  g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+  g_stall_ns.store(stall_ns, std::memory_order_relaxed);
 }
 
 sa2_status sa2_get_device_status(void* stream) {

@@ -16,8 +16,9 @@ constexpr unsigned kDevErrTimeout = 6u;
 constexpr unsigned kDevErrBounds = 7u;
 constexpr unsigned kDevErrRange = 8u;
 
-// A wait on an mbarrier gives up after this many nanoseconds of %globaltimer; legitimate
-// waits in these kernels last microseconds.
+// Default limit of a wait on an mbarrier, in nanoseconds of %globaltimer; legitimate waits
+// in these kernels last microseconds.  The limit of the waits that make progress can be
+// lowered at run time (ShapeArgs::wait_ns); the drains below always use this one.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -65,22 +66,55 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Returns false, and raises the
-// CTA's abort flag, once kWaitLimitNs have passed; returns false at once when another
-// thread of the CTA has already raised the flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// What a CTA's waits share: its abort flag (in shared memory) and the time limit of its
+// waits that make progress.
+struct WaitCtl {
+  volatile int* abort;
+  unsigned long long limit_ns;
+};
+
+// A wait that makes progress: returns true once the phase with the given parity has
+// completed.  Returns false, and raises the CTA's abort flag, once limit_ns have passed;
+// returns false at once when another thread of the CTA has already raised the flag (the
+// phase is tested first, so a completed phase is always seen).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
+    if (*w.abort) return false;
+    if (global_timer_ns() - t0 > w.limit_ns) {
+      *w.abort = 1;
+      return false;
+    }
+  }
+}
+
+// A drain: waits for a copy or an MMA this CTA has already issued to complete, so that no
+// asynchronous operation still writes its shared memory when it exits, or reads or writes
+// tensor memory when it is freed.  It ignores the abort flag -- an issued operation
+// completes by itself -- and gives up only after kWaitLimitNs, raising the flag.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
       return false;
     }
   }
+}
+
+// Test hook of the failure path: the calling warps sleep for stall_ns (bounded, in steps of
+// at most 1 ms), so that waits of other warps on them expire when the wait limit is lower.
+__device__ __forceinline__ void stall_for(unsigned long long stall_ns) {
+  const unsigned long long t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < stall_ns) __nanosleep(1000000u);
 }
 
 // ------------------------------------------------------------------------------- TMA

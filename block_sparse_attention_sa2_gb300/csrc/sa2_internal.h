@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include "../../include/sa2.h"
 #include "sa2_device.cuh"
 
 namespace sa2 {
@@ -20,11 +21,19 @@ enum KernelId {
 void prof_start(cudaStream_t st, int id);
 void prof_stop(cudaStream_t st, int id);
 
-// Shape of one call, with the derived block counts.  Strides are in elements.
+// Shape of one call, with the derived block counts.  Strides are in elements.  wait_ns is
+// the time limit of the attention kernels' bounded waits; stall_ns (0 in normal use) makes
+// the row warps of their first CTA sleep that long before they start, so that a test of the
+// failure path can make a wait expire (sa2_debug_set_wait_limit).
 struct ShapeArgs {
   int B, H, N, d, bq, bk, Tq, Tk, dtype;
   int64_t sb, sh, sn;
+  unsigned long long wait_ns, stall_ns;
 };
+
+// Validates a shape and fills the derived block counts and the wait settings (sa2_api.cu).
+sa2_status check_shape(const sa2_shape* shape, ShapeArgs* s);
+bool aligned16(const void* p);
 
 // Selection parameters of the hybrid mask, prepared on the host.
 struct SelectArgs {
@@ -33,6 +42,9 @@ struct SelectArgs {
   unsigned long long p_fix;   // floor(p * 2^60), used when p_mode == 0
   float inv_sqrt_d;           // 1/sqrt(d) rounded to fp32
 };
+
+// Validates k and p of a mask call and prepares the selection parameters (sa2_api.cu).
+sa2_status make_select_args(const ShapeArgs& s, float topk, float topp, SelectArgs* sel);
 
 struct MaskOut {
   int32_t* row_cnt;

@@ -78,6 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sa2_vd_loss.argtypes = [S, P, P, P, P, P, P, P, Z, P]
     lib.sa2_get_device_status.restype = ctypes.c_int
     lib.sa2_get_device_status.argtypes = [P]
+    lib.sa2_debug_set_wait_limit.restype = None
+    lib.sa2_debug_set_wait_limit.argtypes = [ctypes.c_ulonglong, ctypes.c_ulonglong]
     lib.sa2_profiler_enable.restype = None
     lib.sa2_profiler_enable.argtypes = [ctypes.c_int]
     lib.sa2_profiler_collect.restype = ctypes.c_int
@@ -255,6 +257,12 @@ def profiler_collect() -> dict:
     if got < 0:
         raise Sa2Error("sa2_profiler_collect", 5)
     return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(got)}
+
+
+def debug_set_wait_limit(limit_ns: int = 0, stall_ns: int = 0):
+    """sa2_debug_set_wait_limit: test hook of the failure path (limit of the attention
+    kernels' bounded waits, 0 = default; stall of their first CTA's row warps)."""
+    load_library().sa2_debug_set_wait_limit(int(limit_ns), int(stall_ns))
 
 
 def check_device(stream=None):

@@ -274,10 +274,28 @@ int sa2_profiler_collect(sa2_kernel_time* out, int max_entries);
 
 /*
  * Synchronizes `stream`, then returns and clears the device status word of the current
- * device: SA2_OK, SA2_ERR_TIMEOUT or SA2_ERR_DEVICE_BOUNDS (or SA2_ERR_CUDA when the
- * synchronization itself fails).
+ * device: SA2_OK, or the first error a kernel recorded since the last call --
+ * SA2_ERR_TIMEOUT (a bounded wait gave up), SA2_ERR_DEVICE_BOUNDS (a block list held an
+ * index or count out of range; the kernel clamped it and went on) or SA2_ERR_RANGE (an
+ * attention input beyond the fp16 range was saturated) -- or SA2_ERR_CUDA when the
+ * synchronization itself fails.
  */
 sa2_status sa2_get_device_status(void* stream);
+
+/*
+ * Test hook of the failure path (the pages have no counterpart).  Every wait inside the
+ * attention kernels is bounded in time; when one expires, its CTA raises an abort flag,
+ * every role leaves its loop, the copies and MMAs already issued are drained, tensor memory
+ * is freed and sa2_get_device_status reports SA2_ERR_TIMEOUT.  This call lets a test make
+ * that happen on purpose:
+ *   limit_ns  limit of the waits of the attention calls made after it (0 restores the
+ *             default of 2 s);
+ *   stall_ns  the row warps of the first CTA of each attention kernel sleep this long before
+ *             they start (0: no stall), so that waits on them expire when limit_ns is shorter.
+ * Both apply to the calls made after it, from any thread; not for production use.  The
+ * drains of the abort path keep their own 2 s bound.
+ */
+void sa2_debug_set_wait_limit(unsigned long long limit_ns, unsigned long long stall_ns);
 
 #ifdef __cplusplus
 }

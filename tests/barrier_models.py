@@ -18,12 +18,24 @@ A run checks three things:
   contents.
 
 `drop` names waits to leave out, so a test can check that the model catches each missing one.
+
+Abort runs (`expire=True`) model the failure path.  A wait that makes progress may expire at
+any moment: the CTA's abort flag goes up and the wait returns False.  Once the flag is up,
+every such wait that has not completed returns False, and each role leaves its loops the way
+the kernel does.  Drain waits ignore the flag and only pass when their phase completes.  When
+the last role of a CTA finishes, which is where the kernel frees tensor memory and exits, no
+copy and no MMA of that CTA may still be in flight, and no drain may wait for something never
+issued (a deadlock).
 """
 import random
 
 
 class ProtocolError(Exception):
     pass
+
+
+class Aborted(Exception):
+    """A wait returned False: the role leaves its loops (the kernel's `ok = false; break`)."""
 
 
 def check(cond, msg):
@@ -60,9 +72,10 @@ class Model:
     """Shared scheduler: actors are (name, cta, generator) yielding ("wait", bar, phase) or
     ("step",); subclasses define the CTA state, the engines' completions and the roles."""
 
-    def __init__(self, seed, ncta, items, drop=()):
+    def __init__(self, seed, ncta, items, drop=(), expire=False):
         self.rng = random.Random(seed)
         self.items, self.ncta, self.drop = items, ncta, set(drop)
+        self.expire = expire
         self.counter = 0
         self.tma = []
         self.processed = []
@@ -76,9 +89,21 @@ class Model:
         self.counter += 1
         return x
 
+    @staticmethod
+    def wait(bar, phase):
+        """A wait that makes progress; raises Aborted when it returns False."""
+        ok = yield ("wait", bar, phase)
+        if not ok:
+            raise Aborted()
+
+    @staticmethod
+    def drain(bar, phase):
+        """A drain: passes only once the phase has completed, abort flag or not."""
+        yield ("drain", bar, phase)
+
     def take(self, c, n):
         slot = n & 1
-        yield ("wait", c.item_full[slot], n >> 1)
+        yield from self.wait(c.item_full[slot], n >> 1)
         x = c.slot[slot]
         c.item_free[slot].arrive()
         return x
@@ -88,31 +113,62 @@ class Model:
         returns it."""
         slot = n & 1
         if n >= 2:
-            yield ("wait", c.item_free[slot], (n >> 1) - 1)
+            yield from self.wait(c.item_free[slot], (n >> 1) - 1)
         return slot
 
+    def mma_drain(self, c, bar):
+        """An issuing warp waits for its own MMAs before tensor memory may be freed: a drain,
+        or -- with "abort_mma_drain" dropped -- a wait that gives up once the flag is up."""
+        if "abort_mma_drain" in self.drop:
+            yield ("wait", bar, 0)
+        else:
+            yield from self.drain(bar, 0)
+
+    def check_exit(self, c):
+        """The last role of CTA c finished: tensor memory is freed and the CTA exits."""
+        check(not any(j[0] is c for j in self.tma), f"cta{c.cid} exits with copies in flight")
+        check(not c.mmaq[1] and not c.mmaq[2], f"cta{c.cid} frees tensor memory with MMAs in flight")
+
     def run(self):
+        for c in self.ctas:
+            c.abort = False
         pending = {id(a): self._advance(a, None) for a in self.actors}
+        live = {c.cid: sum(1 for a in self.actors if a[1] is c and pending[id(a)] is not None) for c in self.ctas}
+        for c in self.ctas:
+            if live[c.cid] == 0:
+                self.check_exit(c)
         while True:
             choices = []
             for a in self.actors:
                 p = pending[id(a)]
-                if p is not None and (p[0] == "step" or p[1].comp >= p[2] + 1):
-                    choices.append(("actor", a))
-            choices += [("tma", i) for i in range(len(self.tma))]
-            choices += [("mma", (c, w)) for c in self.ctas for w in (1, 2) if c.mmaq[w]]
+                if p is None:
+                    continue
+                if p[0] == "step" or p[1].comp >= p[2] + 1:
+                    choices.append(("actor", a, True))
+                elif p[0] == "wait" and a[1].abort:
+                    choices.append(("actor", a, False))  # the flag is up: the wait gives up
+                elif p[0] == "wait" and self.expire and self.rng.random() < 0.02:
+                    choices.append(("expire", a, False))  # the wait's time limit runs out
+            choices += [("tma", i, None) for i in range(len(self.tma))]
+            choices += [("mma", (c, w), None) for c in self.ctas for w in (1, 2) if c.mmaq[w]]
             if not choices:
                 stuck = [(a[0], a[1].cid, p[1].name, p[2], p[1].comp) for a in self.actors
                          for p in [pending[id(a)]] if p is not None]
                 check(not stuck, f"deadlock: {stuck[:6]}")
                 return
-            kind, v = self.rng.choice(choices)
-            if kind == "actor":
+            kind, v, ok = self.rng.choice(choices)
+            if kind in ("actor", "expire"):
                 p = pending[id(v)]
-                if p[0] == "wait":
+                if kind == "expire":
+                    v[1].abort = True
+                if p[0] != "step" and ok:
                     check(p[1].comp == p[2] + 1,
                           f"{v[0]} cta{v[1].cid}: {p[1].name} wait for phase {p[2]} passes at {p[1].comp}")
-                pending[id(v)] = self._advance(v, True)
+                pending[id(v)] = self._advance(v, ok)
+                if pending[id(v)] is None:
+                    live[v[1].cid] -= 1
+                    if live[v[1].cid] == 0:
+                        self.check_exit(v[1])
             elif kind == "tma":
                 self.complete_tma(self.tma.pop(v))
             else:
@@ -120,7 +176,7 @@ class Model:
                 self.complete_mma(c, c.mmaq[w].pop(0))
             for a in self.actors:
                 p = pending[id(a)]
-                if p is not None and p[0] == "wait":
+                if p is not None and p[0] != "step":
                     check(p[1].comp <= p[2] + 1,
                           f"{a[0]} cta{a[1].cid}: {p[1].name} two phases past phase {p[2]}")
 
@@ -210,126 +266,136 @@ class DkdvModel(Model):
     def producer(self, c):
         U = kvn = n = 0
         x = c.cid
-        while True:
-            slot = yield from self.publish(c, n)
-            done = x >= len(self.items)
-            c.slot[slot] = -1 if done else x
-            c.item_full[slot].arrive()
-            if done:
-                break
-            xn = self.fetch_next()
-            yield ("step",)
-            nsub = self.items[x]
-            if nsub > 0:
-                if kvn >= 1 and "kvfree" not in self.drop:
-                    yield ("wait", c.kvfree, kvn - 1)
-                check(c.kv_readers == 0, "K/V load issued while S/dP MMAs read them")
-                c.kv.expect_tx(1)
-                self.tma.append((c, "kv", (x, kvn)))
+        try:
+            while True:
+                slot = yield from self.publish(c, n)
+                done = x >= len(self.items)
+                c.slot[slot] = -1 if done else x
+                c.item_full[slot].arrive()
+                if done:
+                    break
+                xn = self.fetch_next()
+                yield ("step",)
+                nsub = self.items[x]
+                if nsub > 0:
+                    if kvn >= 1 and "kvfree" not in self.drop:
+                        yield from self.wait(c.kvfree, kvn - 1)
+                    check(c.kv_readers == 0, "K/V load issued while S/dP MMAs read them")
+                    c.kv.expect_tx(1)
+                    self.tma.append((c, "kv", (x, kvn)))
+                    kvn += 1
+                    for _ in range(nsub):
+                        st = U % self.STAGES
+                        if U >= self.STAGES and "empty" not in self.drop:
+                            yield from self.wait(c.empty[st], U // self.STAGES - 1)
+                        check(not c.stage_readers[st], f"stage {st} load issued while read by {c.stage_readers[st]}")
+                        c.full[st].expect_tx(1)
+                        self.tma.append((c, "stage", (st, U)))
+                        U += 1
+                        yield ("step",)
+                x = xn
+                n += 1
+        except Aborted:
+            if "abort_drain" in self.drop:
+                return  # drains skipped on the abort path
+        # U and kvn count the loads issued: drain the last one of each stage and the K / V load
+        for v in range(max(0, U - self.STAGES), U):
+            yield from self.drain(c.full[v % self.STAGES], v // self.STAGES)
+        if kvn > 0:
+            yield from self.drain(c.kv, kvn - 1)
+    def s_issuer(self, c):
+        U = kvn = n = 0
+        try:
+            while True:
+                x = yield from self.take(c, n)
+                n += 1
+                if x < 0:
+                    break
+                nsub = self.items[x]
+                if nsub == 0:
+                    continue
+                yield from self.wait(c.kv, kvn)
+                kvk = (x, kvn)
                 kvn += 1
                 for _ in range(nsub):
                     st = U % self.STAGES
-                    if U >= self.STAGES and "empty" not in self.drop:
-                        yield ("wait", c.empty[st], U // self.STAGES - 1)
-                    check(not c.stage_readers[st], f"stage {st} load issued while read by {c.stage_readers[st]}")
-                    c.full[st].expect_tx(1)
-                    self.tma.append((c, "stage", (st, U)))
+                    yield from self.wait(c.full[st], U // self.STAGES)
+                    if U >= 1 and "sfree" not in self.drop:
+                        yield from self.wait(c.sfree, U - 1)
+                    check(c.stage[st] == U and c.kv_tag == kvk, f"S({U}) issued on the wrong operands")
+                    c.mmaq[1] += [("S", U, st, kvk), ("DP", U, st, kvk), ("commit", c.sfull)]
+                    c.kv_readers += 2
                     U += 1
                     yield ("step",)
-            x = xn
-            n += 1
-        for v in range(max(0, U - self.STAGES), U):
-            yield ("wait", c.full[v % self.STAGES], v // self.STAGES)
-        if kvn > 0:
-            yield ("wait", c.kv, kvn - 1)
-
-    def s_issuer(self, c):
-        U = kvn = n = 0
-        while True:
-            x = yield from self.take(c, n)
-            n += 1
-            if x < 0:
-                break
-            nsub = self.items[x]
-            if nsub == 0:
-                continue
-            yield ("wait", c.kv, kvn)
-            kvk = (x, kvn)
-            kvn += 1
-            for _ in range(nsub):
-                st = U % self.STAGES
-                yield ("wait", c.full[st], U // self.STAGES)
-                if U >= 1 and "sfree" not in self.drop:
-                    yield ("wait", c.sfree, U - 1)
-                check(c.stage[st] == U and c.kv_tag == kvk, f"S({U}) issued on the wrong operands")
-                c.mmaq[1] += [("S", U, st, kvk), ("DP", U, st, kvk), ("commit", c.sfull)]
-                c.kv_readers += 2
-                U += 1
-                yield ("step",)
-            c.mmaq[1].append(("commit", c.kvfree))
+                c.mmaq[1].append(("commit", c.kvfree))
+        except Aborted:
+            pass
         c.mmaq[1].append(("commit", c.sdrain))
-        yield ("wait", c.sdrain, 0)
-
+        yield from self.mma_drain(c, c.sdrain)
     def g_issuer(self, c):
         W = n = 0
-        while True:
-            x = yield from self.take(c, n)
-            n += 1
-            if x < 0:
-                break
-            nsub = self.items[x]
-            for w in range(nsub):
-                st, bb = W % self.STAGES, W & 1
-                yield ("wait", c.pready[bb], W >> 1)
-                yield ("wait", c.full[st], W // self.STAGES)
-                check(all(c.P[bb].get(g) == W for g in range(NE)), f"dV/dK({W}) issued before P/dS were written")
-                c.mmaq[2] += [("DV", W, st, bb, x, w), ("DK", W, st, bb, x, w), ("commit", c.empty[st]),
-                              ("commit", c.pfree[bb])]
-                c.P_readers[bb] += 2
-                c.acc_inflight += 2
-                W += 1
-                yield ("step",)
-            if nsub > 0:
-                c.mmaq[2].append(("commit", c.drain))
+        try:
+            while True:
+                x = yield from self.take(c, n)
+                n += 1
+                if x < 0:
+                    break
+                nsub = self.items[x]
+                for w in range(nsub):
+                    st, bb = W % self.STAGES, W & 1
+                    yield from self.wait(c.pready[bb], W >> 1)
+                    yield from self.wait(c.full[st], W // self.STAGES)
+                    check(all(c.P[bb].get(g) == W for g in range(NE)), f"dV/dK({W}) issued before P/dS were written")
+                    c.mmaq[2] += [("DV", W, st, bb, x, w), ("DK", W, st, bb, x, w), ("commit", c.empty[st]),
+                                  ("commit", c.pfree[bb])]
+                    c.P_readers[bb] += 2
+                    c.acc_inflight += 2
+                    W += 1
+                    yield ("step",)
+                if nsub > 0:
+                    c.mmaq[2].append(("commit", c.drain))
+        except Aborted:
+            pass
         c.mmaq[2].append(("commit", c.gdrain))
-        yield ("wait", c.gdrain, 0)
-
+        yield from self.mma_drain(c, c.gdrain)
     def elementwise(self, c, g):
         U = an = n = 0
-        while True:
-            x = yield from self.take(c, n)
-            n += 1
-            if x < 0:
-                break
-            nsub = self.items[x]
-            for _ in range(nsub):
-                st, bb = U % self.STAGES, U & 1
-                yield ("wait", c.sfull, U)
-                yield ("wait", c.full[st], U // self.STAGES)
-                check(c.S == U and c.DP == U, f"ew{g}: reads S({U}) while TMEM holds S({c.S})")
-                check(c.stage[st] == U, f"ew{g}: statistics of sub-tile {U} replaced")
-                c.S_read.add(g)
-                c.stage_readers[st].discard(f"ew{g}")
-                c.sfree.arrive()
+        try:
+            while True:
+                x = yield from self.take(c, n)
+                n += 1
+                if x < 0:
+                    break
+                nsub = self.items[x]
+                for _ in range(nsub):
+                    st, bb = U % self.STAGES, U & 1
+                    yield from self.wait(c.sfull, U)
+                    yield from self.wait(c.full[st], U // self.STAGES)
+                    check(c.S == U and c.DP == U, f"ew{g}: reads S({U}) while TMEM holds S({c.S})")
+                    check(c.stage[st] == U, f"ew{g}: statistics of sub-tile {U} replaced")
+                    c.S_read.add(g)
+                    c.stage_readers[st].discard(f"ew{g}")
+                    c.sfree.arrive()
+                    yield ("step",)
+                    if U >= 2 and "pfree" not in self.drop:
+                        yield from self.wait(c.pfree[bb], (U >> 1) - 1)
+                    check(c.P_readers[bb] == 0, f"ew{g}: P/dS buffer {bb} written while MMAs read it")
+                    c.P[bb][g] = U
+                    c.pready[bb].arrive()
+                    U += 1
+                    yield ("step",)
+                if nsub == 0:
+                    continue
+                if "drain" not in self.drop:
+                    yield from self.wait(c.drain, an)
+                an += 1
+                check(c.acc == (x, nsub - 1) and c.acc_inflight == 0, f"ew{g}: epilogue of item {x} sees {c.acc}")
+                c.acc_read.add(g)
+                if g == 0:
+                    self.processed.append(x)
                 yield ("step",)
-                if U >= 2 and "pfree" not in self.drop:
-                    yield ("wait", c.pfree[bb], (U >> 1) - 1)
-                check(c.P_readers[bb] == 0, f"ew{g}: P/dS buffer {bb} written while MMAs read it")
-                c.P[bb][g] = U
-                c.pready[bb].arrive()
-                U += 1
-                yield ("step",)
-            if nsub == 0:
-                continue
-            if "drain" not in self.drop:
-                yield ("wait", c.drain, an)
-            an += 1
-            check(c.acc == (x, nsub - 1) and c.acc_inflight == 0, f"ew{g}: epilogue of item {x} sees {c.acc}")
-            c.acc_read.add(g)
-            if g == 0:
-                self.processed.append(x)
-            yield ("step",)
-
+        except Aborted:
+            pass
 
 class DqModel(Model):
     """attn_bwd_dq_kernel: items are query blocks with `items[x]` kept key blocks."""
@@ -405,131 +471,143 @@ class DqModel(Model):
 
     def producer(self, c):
         J = qn = n = 0
+        nk = nv = 0  # K and V loads issued (J lags one of them when a V wait gives up)
         x = c.cid
-        while True:
-            slot = yield from self.publish(c, n)
-            done = x >= len(self.items)
-            c.slot[slot] = -1 if done else x
-            c.item_full[slot].arrive()
-            if done:
-                break
-            xn = self.fetch_next()
-            nkv = self.items[x]
-            if nkv > 0:
-                if qn >= 1 and "qfree" not in self.drop:
-                    yield ("wait", c.qfree, qn - 1)
-                check(c.q_readers == 0, "Q/dO load issued while S/dP MMAs read them")
-                c.q.expect_tx(1)
-                self.tma.append((c, "q", 0, qn))
-                qn += 1
-                for _ in range(nkv):
-                    ks, vs = J % self.KST, J % self.VST
-                    if J >= self.KST and "kempty" not in self.drop:
-                        yield ("wait", c.kempty[ks], J // self.KST - 1)
-                    c.kfull[ks].expect_tx(1)
-                    self.tma.append((c, "k", ks, J))
-                    if J >= self.VST and "vempty" not in self.drop:
-                        yield ("wait", c.vempty[vs], J // self.VST - 1)
-                    c.vfull[vs].expect_tx(1)
-                    self.tma.append((c, "v", vs, J))
-                    J += 1
-                    yield ("step",)
-            x = xn
-            n += 1
-        for v in range(max(0, J - self.KST), J):
-            yield ("wait", c.kfull[v % self.KST], v // self.KST)
-        for v in range(max(0, J - self.VST), J):
-            yield ("wait", c.vfull[v % self.VST], v // self.VST)
+        try:
+            while True:
+                slot = yield from self.publish(c, n)
+                done = x >= len(self.items)
+                c.slot[slot] = -1 if done else x
+                c.item_full[slot].arrive()
+                if done:
+                    break
+                xn = self.fetch_next()
+                nkv = self.items[x]
+                if nkv > 0:
+                    if qn >= 1 and "qfree" not in self.drop:
+                        yield from self.wait(c.qfree, qn - 1)
+                    check(c.q_readers == 0, "Q/dO load issued while S/dP MMAs read them")
+                    c.q.expect_tx(1)
+                    self.tma.append((c, "q", 0, qn))
+                    qn += 1
+                    for _ in range(nkv):
+                        ks, vs = J % self.KST, J % self.VST
+                        if J >= self.KST and "kempty" not in self.drop:
+                            yield from self.wait(c.kempty[ks], J // self.KST - 1)
+                        c.kfull[ks].expect_tx(1)
+                        self.tma.append((c, "k", ks, J))
+                        nk += 1
+                        if J >= self.VST and "vempty" not in self.drop:
+                            yield from self.wait(c.vempty[vs], J // self.VST - 1)
+                        c.vfull[vs].expect_tx(1)
+                        self.tma.append((c, "v", vs, J))
+                        nv += 1
+                        J += 1
+                        yield ("step",)
+                x = xn
+                n += 1
+        except Aborted:
+            if "abort_drain" in self.drop:
+                return
+        for v in range(max(0, nk - self.KST), nk):
+            yield from self.drain(c.kfull[v % self.KST], v // self.KST)
+        for v in range(max(0, nv - self.VST), nv):
+            yield from self.drain(c.vfull[v % self.VST], v // self.VST)
         if qn > 0:
-            yield ("wait", c.q, qn - 1)
-
+            yield from self.drain(c.q, qn - 1)
     def s_issuer(self, c):
         J = qn = n = 0
-        while True:
-            x = yield from self.take(c, n)
-            n += 1
-            if x < 0:
-                break
-            nkv = self.items[x]
-            if nkv == 0:
-                continue
-            yield ("wait", c.q, qn)
-            qk = qn
-            qn += 1
-            for _ in range(nkv):
-                ks, vs, bb = J % self.KST, J % self.VST, J & 1
-                yield ("wait", c.kfull[ks], J // self.KST)
-                if J >= 2 and "sfree" not in self.drop:
-                    yield ("wait", c.sfree[bb], (J >> 1) - 1)
-                yield ("wait", c.vfull[vs], J // self.VST)
-                check(c.qtag == qk and c.ktag[ks] == J and c.vtag[vs] == J, f"S({J}) issued on the wrong operands")
-                c.mmaq[1] += [("S", J, ks, vs, bb, qk), ("commit", c.sfull[bb]), ("commit", c.vempty[vs])]
-                c.q_readers += 1
-                c.k_readers[ks] += 1
-                c.v_readers[vs] += 1
-                J += 1
-                yield ("step",)
-            c.mmaq[1].append(("commit", c.qfree))
+        try:
+            while True:
+                x = yield from self.take(c, n)
+                n += 1
+                if x < 0:
+                    break
+                nkv = self.items[x]
+                if nkv == 0:
+                    continue
+                yield from self.wait(c.q, qn)
+                qk = qn
+                qn += 1
+                for _ in range(nkv):
+                    ks, vs, bb = J % self.KST, J % self.VST, J & 1
+                    yield from self.wait(c.kfull[ks], J // self.KST)
+                    if J >= 2 and "sfree" not in self.drop:
+                        yield from self.wait(c.sfree[bb], (J >> 1) - 1)
+                    yield from self.wait(c.vfull[vs], J // self.VST)
+                    check(c.qtag == qk and c.ktag[ks] == J and c.vtag[vs] == J, f"S({J}) issued on the wrong operands")
+                    c.mmaq[1] += [("S", J, ks, vs, bb, qk), ("commit", c.sfull[bb]), ("commit", c.vempty[vs])]
+                    c.q_readers += 1
+                    c.k_readers[ks] += 1
+                    c.v_readers[vs] += 1
+                    J += 1
+                    yield ("step",)
+                c.mmaq[1].append(("commit", c.qfree))
+        except Aborted:
+            pass
         c.mmaq[1].append(("commit", c.sdrain))
-        yield ("wait", c.sdrain, 0)
-
+        yield from self.mma_drain(c, c.sdrain)
     def dq_issuer(self, c):
         J = n = 0
-        while True:
-            x = yield from self.take(c, n)
-            n += 1
-            if x < 0:
-                break
-            nkv = self.items[x]
-            for j in range(nkv):
-                ks, bb = J % self.KST, J & 1
-                yield ("wait", c.pready[bb], J >> 1)
-                yield ("wait", c.kfull[ks], J // self.KST)
-                check(all(c.DS[bb].get(g) == J for g in range(NE)), f"dQ({J}) issued before dS was written")
-                c.mmaq[2] += [("DQ", J, ks, bb, x, j), ("commit", c.kempty[ks]), ("commit", c.pfree[bb])]
-                c.k_readers[ks] += 1
-                c.DS_readers[bb] += 1
-                c.acc_inflight += 1
-                J += 1
-                yield ("step",)
-            if nkv > 0:
-                c.mmaq[2].append(("commit", c.dq))
+        try:
+            while True:
+                x = yield from self.take(c, n)
+                n += 1
+                if x < 0:
+                    break
+                nkv = self.items[x]
+                for j in range(nkv):
+                    ks, bb = J % self.KST, J & 1
+                    yield from self.wait(c.pready[bb], J >> 1)
+                    yield from self.wait(c.kfull[ks], J // self.KST)
+                    check(all(c.DS[bb].get(g) == J for g in range(NE)), f"dQ({J}) issued before dS was written")
+                    c.mmaq[2] += [("DQ", J, ks, bb, x, j), ("commit", c.kempty[ks]), ("commit", c.pfree[bb])]
+                    c.k_readers[ks] += 1
+                    c.DS_readers[bb] += 1
+                    c.acc_inflight += 1
+                    J += 1
+                    yield ("step",)
+                if nkv > 0:
+                    c.mmaq[2].append(("commit", c.dq))
+        except Aborted:
+            pass
         c.mmaq[2].append(("commit", c.gdrain))
-        yield ("wait", c.gdrain, 0)
-
+        yield from self.mma_drain(c, c.gdrain)
     def rows(self, c, g):
         J = an = n = 0
-        while True:
-            x = yield from self.take(c, n)
-            n += 1
-            if x < 0:
-                break
-            nkv = self.items[x]
-            for _ in range(nkv):
-                bb, jn = J & 1, J >> 1
-                yield ("wait", c.sfull[bb], jn)
-                check(c.S[bb] == J, f"row{g}: reads S({J}) while buffer {bb} holds S({c.S[bb]})")
-                c.S_read[bb].add(g)
-                c.sfree[bb].arrive()
+        try:
+            while True:
+                x = yield from self.take(c, n)
+                n += 1
+                if x < 0:
+                    break
+                nkv = self.items[x]
+                for _ in range(nkv):
+                    bb, jn = J & 1, J >> 1
+                    yield from self.wait(c.sfull[bb], jn)
+                    check(c.S[bb] == J, f"row{g}: reads S({J}) while buffer {bb} holds S({c.S[bb]})")
+                    c.S_read[bb].add(g)
+                    c.sfree[bb].arrive()
+                    yield ("step",)
+                    if jn >= 1 and "pfree" not in self.drop:
+                        yield from self.wait(c.pfree[bb], jn - 1)
+                    check(c.DS_readers[bb] == 0, f"row{g}: dS buffer {bb} written while the dQ MMA reads it")
+                    c.DS[bb][g] = J
+                    c.pready[bb].arrive()
+                    J += 1
+                    yield ("step",)
+                if nkv == 0:
+                    continue
+                if "dq" not in self.drop:
+                    yield from self.wait(c.dq, an)
+                an += 1
+                check(c.acc == (x, nkv - 1) and c.acc_inflight == 0, f"row{g}: epilogue of item {x} sees {c.acc}")
+                c.acc_read.add(g)
+                if g == 0:
+                    self.processed.append(x)
                 yield ("step",)
-                if jn >= 1 and "pfree" not in self.drop:
-                    yield ("wait", c.pfree[bb], jn - 1)
-                check(c.DS_readers[bb] == 0, f"row{g}: dS buffer {bb} written while the dQ MMA reads it")
-                c.DS[bb][g] = J
-                c.pready[bb].arrive()
-                J += 1
-                yield ("step",)
-            if nkv == 0:
-                continue
-            if "dq" not in self.drop:
-                yield ("wait", c.dq, an)
-            an += 1
-            check(c.acc == (x, nkv - 1) and c.acc_inflight == 0, f"row{g}: epilogue of item {x} sees {c.acc}")
-            c.acc_read.add(g)
-            if g == 0:
-                self.processed.append(x)
-            yield ("step",)
-
+        except Aborted:
+            pass
 
 class FwdModel(Model):
     """attn_fwd_kernel (one query block per CTA, not persistent): `items` holds one entry, the
@@ -602,109 +680,132 @@ class FwdModel(Model):
 
     def producer(self, c):
         nkv = self.items[0]
+        if nkv == 0:
+            return
         c.q.expect_tx(1)
         self.tma.append((c, "q", 0, 0))
-        for j in range(nkv):
-            st = j % self.STAGES
-            if j >= self.STAGES and "kempty" not in self.drop:
-                yield ("wait", c.kempty[st], j // self.STAGES - 1)
-            check(c.k_readers[st] == 0, "K load issued while read")
-            c.kfull[st].expect_tx(1)
-            self.tma.append((c, "k", st, j))
-            if j >= self.STAGES and "vempty" not in self.drop:
-                yield ("wait", c.vempty[st], j // self.STAGES - 1)
-            check(c.v_readers[st] == 0, "V load issued while read")
-            c.vfull[st].expect_tx(1)
-            self.tma.append((c, "v", st, j))
-            yield ("step",)
-        for j in range(max(0, nkv - self.STAGES), nkv):
-            yield ("wait", c.vfull[j % self.STAGES], j // self.STAGES)
-            yield ("wait", c.kfull[j % self.STAGES], j // self.STAGES)
-
+        nk = nv = 0  # K and V loads issued
+        try:
+            for j in range(nkv):
+                st = j % self.STAGES
+                if j >= self.STAGES and "kempty" not in self.drop:
+                    yield from self.wait(c.kempty[st], j // self.STAGES - 1)
+                check(c.k_readers[st] == 0, "K load issued while read")
+                c.kfull[st].expect_tx(1)
+                self.tma.append((c, "k", st, j))
+                nk += 1
+                if j >= self.STAGES and "vempty" not in self.drop:
+                    yield from self.wait(c.vempty[st], j // self.STAGES - 1)
+                check(c.v_readers[st] == 0, "V load issued while read")
+                c.vfull[st].expect_tx(1)
+                self.tma.append((c, "v", st, j))
+                nv += 1
+                yield ("step",)
+        except Aborted:
+            if "abort_drain" in self.drop:
+                return
+        yield from self.drain(c.q, 0)
+        for j in range(max(0, nk - self.STAGES), nk):
+            yield from self.drain(c.kfull[j % self.STAGES], j // self.STAGES)
+        for j in range(max(0, nv - self.STAGES), nv):
+            yield from self.drain(c.vfull[j % self.STAGES], j // self.STAGES)
     def s_issuer(self, c):
         nkv = self.items[0]
         if nkv == 0:
             return
-        yield ("wait", c.q, 0)
-        for j in range(nkv):
-            st, b = j % self.STAGES, j & 1
-            yield ("wait", c.kfull[st], j // self.STAGES)
-            # P_{j-2} V_{j-2} read buffer b: it must have completed (same index as the V stage)
-            if j >= 2 and "s_over_p" not in self.drop:
-                yield ("wait", c.vempty[st], (j - 2) // self.STAGES)
-            c.mmaq[1] += [("S", j, st, b), ("commit", c.sfull[b]), ("commit", c.kempty[st])]
-            c.k_readers[st] += 1
-            yield ("step",)
+        try:
+            yield from self.wait(c.q, 0)
+            for j in range(nkv):
+                st, b = j % self.STAGES, j & 1
+                yield from self.wait(c.kfull[st], j // self.STAGES)
+                # P_{j-2} V_{j-2} read buffer b: it must have completed (same index as the V stage)
+                if j >= 2 and "s_over_p" not in self.drop:
+                    yield from self.wait(c.vempty[st], (j - 2) // self.STAGES)
+                c.mmaq[1] += [("S", j, st, b), ("commit", c.sfull[b]), ("commit", c.kempty[st])]
+                c.k_readers[st] += 1
+                yield ("step",)
+        except Aborted:
+            pass
         c.mmaq[1].append(("commit", c.sdrain))
-        yield ("wait", c.sdrain, 0)
-
+        yield from self.mma_drain(c, c.sdrain)
     def pv_issuer(self, c):
         nkv = self.items[0]
         if nkv == 0:
             return
-        for j in range(nkv):
-            st, b = j % self.STAGES, j & 1
-            yield ("wait", c.pfull[b], j >> 1)
-            yield ("wait", c.vfull[st], j // self.STAGES)
-            check(c.buf[b] == ("P", j, frozenset(range(self.NW))), f"PV({j}) issued before P_{j} was written")
-            c.mmaq[2] += [("PV", j, st, b), ("commit", c.vempty[st]), ("commit", c.odone)]
-            c.v_readers[st] += 1
-            c.buf_readers[b] += 1
-            c.o_inflight += 1
-            yield ("step",)
+        try:
+            for j in range(nkv):
+                st, b = j % self.STAGES, j & 1
+                yield from self.wait(c.pfull[b], j >> 1)
+                yield from self.wait(c.vfull[st], j // self.STAGES)
+                check(c.buf[b] == ("P", j, frozenset(range(self.NW))), f"PV({j}) issued before P_{j} was written")
+                c.mmaq[2] += [("PV", j, st, b), ("commit", c.vempty[st]), ("commit", c.odone)]
+                c.v_readers[st] += 1
+                c.buf_readers[b] += 1
+                c.o_inflight += 1
+                yield ("step",)
+        except Aborted:
+            pass
         c.mmaq[2].append(("commit", c.drain))
-        yield ("wait", c.drain, 0)
-
+        yield from self.mma_drain(c, c.drain)
     def softmax(self, c, w):
         nkv = self.items[0]
-        for j in range(nkv):
-            b = j & 1
-            yield ("wait", c.sfull[b], j >> 1)
-            check(c.buf[b] is not None and c.buf[b][:2] in (("S", j), ("P", j)), f"sm{w}: reads S({j}) from {c.buf[b]}")
-            c.S_read[b].add(w)
-            if j > 0 and self.rng.random() < 0.3:
-                # rescale O: every earlier P V product must be in it and none in flight
-                if "odone" not in self.drop:
-                    yield ("wait", c.odone, j - 1)
-                check(c.o_count == j and c.o_inflight == 0, f"sm{w}: rescales O with {c.o_count} of {j} products")
-            yield ("step",)
-            check(c.buf_readers[b] == 0, f"sm{w}: writes P({j}) while P V reads buffer {b}")
-            prev = c.buf[b][2] if c.buf[b][0] == "P" else frozenset()
-            c.buf[b] = ("P", j, prev | {w})
-            c.pfull[b].arrive()
-            yield ("step",)
-        if nkv > 0:
-            yield ("wait", c.drain, 0)
-            check(c.o_count == nkv and c.o_inflight == 0, f"sm{w}: epilogue sees {c.o_count} of {nkv} products")
-            if w == 0:
-                self.processed.append(0)
+        try:
+            for j in range(nkv):
+                b = j & 1
+                yield from self.wait(c.sfull[b], j >> 1)
+                check(c.buf[b] is not None and c.buf[b][:2] in (("S", j), ("P", j)),
+                      f"sm{w}: reads S({j}) from {c.buf[b]}")
+                c.S_read[b].add(w)
+                if j > 0 and self.rng.random() < 0.3:
+                    # rescale O: every earlier P V product must be in it and none in flight
+                    if "odone" not in self.drop:
+                        yield from self.wait(c.odone, j - 1)
+                    check(c.o_count == j and c.o_inflight == 0, f"sm{w}: rescales O with {c.o_count} of {j} products")
+                yield ("step",)
+                check(c.buf_readers[b] == 0, f"sm{w}: writes P({j}) while P V reads buffer {b}")
+                prev = c.buf[b][2] if c.buf[b][0] == "P" else frozenset()
+                c.buf[b] = ("P", j, prev | {w})
+                c.pfull[b].arrive()
+                yield ("step",)
+            if nkv > 0:
+                yield from self.wait(c.drain, 0)
+                if c.abort:  # the P V issuer gave up and completed `drain` early: no epilogue
+                    raise Aborted()
+                check(c.o_count == nkv and c.o_inflight == 0, f"sm{w}: epilogue sees {c.o_count} of {nkv} products")
+                if w == 0:
+                    self.processed.append(0)
+        except Aborted:
+            pass
 
-
-def run_forward_trials(trials, drop=(), seed0=0):
-    """Random list lengths (including 0) on one CTA; returns the first error, or None."""
+def run_forward_trials(trials, drop=(), seed0=0, expire=False):
+    """Random list lengths (including 0) on one CTA; returns the first error, or None.  With
+    `expire`, waits expire at random (the abort path) and the epilogue is not required."""
     for t in range(seed0, seed0 + trials):
         rng = random.Random(t)
         nkv = rng.choice([0, 1, 2, 3, 4, 5, 7, 10])
-        model = FwdModel(t, 1, [nkv], drop)
+        model = FwdModel(t, 1, [nkv], drop, expire)
         try:
             model.run()
-            check(model.processed == ([0] if nkv > 0 else []), "epilogue not reached")
+            if not expire:
+                check(model.processed == ([0] if nkv > 0 else []), "epilogue not reached")
         except ProtocolError as e:
             return f"trial {t}, list length {nkv}: {e}"
     return None
 
 
-def run_trials(model_cls, trials, drop=(), seed0=0):
-    """Random item lists (with empty items) on 1-3 CTAs; returns the first error, or None."""
+def run_trials(model_cls, trials, drop=(), seed0=0, expire=False):
+    """Random item lists (with empty items) on 1-3 CTAs; returns the first error, or None.
+    With `expire`, waits expire at random (the abort path) and items may stay unfinished."""
     for t in range(seed0, seed0 + trials):
         rng = random.Random(t)
         nitems = rng.randint(1, 12)
         items = [rng.choice([0, 0, 1, 2, 3, 4, 5, 8]) for _ in range(nitems)]
-        model = model_cls(t, rng.randint(1, min(3, nitems)), items, drop)
+        model = model_cls(t, rng.randint(1, min(3, nitems)), items, drop, expire)
         try:
             model.run()
-            want = sorted(x for x in range(nitems) if items[x] > 0)
-            check(sorted(model.processed) == want, f"items processed {sorted(model.processed)}, want {want}")
+            if not expire:
+                want = sorted(x for x in range(nitems) if items[x] > 0)
+                check(sorted(model.processed) == want, f"items processed {sorted(model.processed)}, want {want}")
         except ProtocolError as e:
             return f"trial {t}, items {items}: {e}"
     return None

@@ -34,3 +34,28 @@ def test_forward_protocol_holds_on_random_schedules():
 @pytest.mark.parametrize("wait", ["kempty", "vempty", "s_over_p", "odone"])
 def test_forward_model_catches_a_missing_wait(wait):
     assert run_forward_trials(TRIALS, drop={wait}) is not None, f"forward without {wait} passed"
+
+
+@pytest.mark.parametrize("model", [DkdvModel, DqModel], ids=["dkdv", "dq"])
+def test_abort_path_leaves_nothing_in_flight(model):
+    """Waits expire at random: every role leaves its loops, and when the CTA frees its tensor
+    memory and exits no copy or MMA is still in flight (and no drain waits forever)."""
+    err = run_trials(model, 2 * TRIALS, expire=True)
+    assert err is None, err
+
+
+def test_forward_abort_path_leaves_nothing_in_flight():
+    err = run_forward_trials(2 * TRIALS, expire=True)
+    assert err is None, err
+
+
+@pytest.mark.parametrize("model", [DkdvModel, DqModel, "fwd"], ids=["dkdv", "dq", "fwd"])
+@pytest.mark.parametrize("skipped", ["abort_drain", "abort_mma_drain"])
+def test_model_catches_a_drain_skipped_on_abort(model, skipped):
+    """Without the producer's drain of its issued copies, or with the issuers' drains giving
+    up once the abort flag is up, some CTA exits with work in flight."""
+    if model == "fwd":
+        err = run_forward_trials(2 * TRIALS, drop={skipped}, expire=True)
+    else:
+        err = run_trials(model, 2 * TRIALS, drop={skipped}, expire=True)
+    assert err is not None, f"{model} without {skipped} passed"

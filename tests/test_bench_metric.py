@@ -41,3 +41,23 @@ def test_dkdv_traffic_is_reported_only_for_the_captured_workload():
     assert four == pytest.approx(full * 4 / wan14.H)  # heads are independent and equal in work
     assert bench.dkdv_traffic(wan14, 0.9) is None
     assert bench.dkdv_traffic(CONFIGS[2], 0.95) is None
+
+
+def test_roofline_accounting_credits_only_algorithmic_work():
+    """The dQ kernel is credited with its dQ GEMM only (2 d per kept pair), the dK/dV kernel with
+    S, dP, dV, dK (8 d): together the backward's 10 d.  Fractions use the burst bf16 peak, and
+    each phase's time includes its conversions and preprocessing."""
+    pairs, d, steps = 1.0e9, 128, 2
+    prof = {"attn_fwd": (2, 4.0), "attn_bwd_dkdv": (2, 10.0), "attn_bwd_dq": (2, 6.0), "to_f16": (6, 1.5),
+            "bwd_preprocess": (2, 1.0), "bwd_pair_union": (2, 0.2), "pool": (2, 0.6)}
+    peaks = {"bf16_tflops": 1000.0, "bf16_tflops_sustained": 800.0, "hbm_gbs": 7000.0, "source": "test"}
+    ph = bench.phase_rooflines(prof, steps, pairs, d, peaks["bf16_tflops"])
+    assert ph["forward"]["ms"] == pytest.approx(2.0 + 0.25)
+    assert ph["backward"]["ms"] == pytest.approx(5.0 + 3.0 + 0.5 + 0.1 + 0.5)
+    assert ph["backward"]["algorithmic_tflop"] == pytest.approx(10 * d * pairs / 1e12)
+    assert ph["backward"]["frac_of_bf16_burst"] == pytest.approx(10 * d * pairs / (9.1e-3) / 1e12 / 1000.0)
+    roof = bench.dominant_roofline(prof, pairs, d, peaks)
+    assert roof["kernel"] == "attn_bwd_dkdv" and roof["peak"] == 1000.0
+    assert roof["achieved"] == pytest.approx(8 * d * pairs / 5e-3 / 1e12)
+    dq_only = {"attn_bwd_dq": (1, 3.0)}
+    assert bench.dominant_roofline(dq_only, pairs, d, peaks)["achieved"] == pytest.approx(2 * d * pairs / 3e-3 / 1e12)

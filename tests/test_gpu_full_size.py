@@ -1,0 +1,83 @@
+"""GPU parity at the full sizes of the Wan-shaped workloads, on the masks the benchmark
+times: the GPU builds the calibrated hybrid mask of every head, the forward and the backward
+run on it exactly as in the benchmark (the backward reusing the forward's workspace), and
+the oracle -- run on that same GPU mask -- recomputes sampled query rows (O, LSE, dQ) and key
+blocks (dK, dV: the two sink blocks, a middle one and the ragged last one) of several heads.
+
+Workloads: the Wan2.1-1.3B-480p shape (B=1, H=12, N=32760, d=128) and the Wan2.1-14B-720p
+shape (H=40, N=75600) at 95 % block sparsity, and the sparsity sweep on the 1.3B-480p shape
+(80, 90, 95, 97 % and the dense k = 1 point; thelatestinai.com page, Tables 4-5 give the
+95 % context).  The mask of the sampled heads is also compared with the oracle's."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+from tests.gpu_util import compare_masks, run_step_on_own_mask, sample_rows, sampled_attention_parity, to_device
+from workload import CONFIGS, make_inputs
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def sa2():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_sparse_attention_sa2_gb300 as m
+    m.load_library()
+    return m
+
+
+_cache = {}
+
+
+def _inputs(ci):
+    if ci not in _cache:
+        _cache.clear()
+        cfg = CONFIGS[ci]
+        x = make_inputs(cfg, threads=16)
+        _cache[ci] = (cfg, x, {t: to_device(x[t]) for t in x})
+    return _cache[ci]
+
+
+def _params(ci, target):
+    if target == 0.0:
+        return 1.0, 1.0
+    cal = json.load(open(os.path.join(GOLDEN, "calibration.json")))[str(ci)]["targets"][f"{target:.2f}"]
+    return cal["k"], cal["p"]
+
+
+def _check(sa2, ci, target, heads, dkdv_heads=None):
+    cfg, x, dev = _inputs(ci)
+    topk, topp = _params(ci, target)
+    bm, got = run_step_on_own_mask(sa2, cfg, dev, topk, topp)
+    kept = bm.row_cnt.sum().item() / (cfg.B * cfg.H * cfg.Tq * cfg.Tk)
+    assert abs((1.0 - kept) - target) < 2e-3, f"block sparsity {1 - kept:.4f}, target {target}"
+    label = f"{cfg.name} @{round(100 * target)}%"
+    ref = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, topk, topp, heads=heads)
+    compare_masks(bm, ref, heads, topk, topp, label)
+    mask = bm.mask.cpu().numpy()
+    sampled_attention_parity(cfg, x, mask, got, heads, sample_rows(cfg), [0, 1, cfg.Tk // 2, cfg.Tk - 1], label,
+                             dkdv_heads=dkdv_heads)
+
+
+@pytest.mark.parametrize("ci", [2, 3])
+def test_wan_shapes_at_95_percent_on_the_gpu_mask(sa2, ci):
+    cfg = CONFIGS[ci]
+    heads = [(0, 0), (0, cfg.H // 3), (0, (2 * cfg.H) // 3), (0, cfg.H - 1)]
+    _check(sa2, ci, 0.95, heads)
+
+
+@pytest.mark.parametrize("target", [0.80, 0.90, 0.95, 0.97])
+def test_sparsity_sweep_points(sa2, target):
+    _check(sa2, 4, target, [(0, 0), (0, 4), (0, 8), (0, 11)])
+
+
+def test_sparsity_sweep_dense_point(sa2):
+    """k = 1: every block kept, the dense reference point of the sweep.  dK / dV of a key
+    block then depend on every query row, so the oracle recomputes them on one head."""
+    _check(sa2, 4, 0.0, [(0, 0), (0, 11)], dkdv_heads=[(0, 11)])

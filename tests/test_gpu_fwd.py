@@ -112,30 +112,6 @@ def test_fwd_mask_probe_config_sampled_rows(sa2):
             _check_head(f"probe h{h}", o[0, h, rows], lse[0, h, rows], ro, rlse)
 
 
-@pytest.mark.parametrize("ci", [2, 3])
-def test_fwd_full_size_wan_shapes_sampled_rows(sa2, ci):
-    """Full size, in the launch configuration the benchmark times; sampled rows of a few
-    heads are recomputed by the oracle one by one (every block row type: first, middle,
-    ragged last)."""
-    cfg = CONFIGS[ci]
-    cal = json.load(open(os.path.join(GOLDEN, "calibration.json")))[str(ci)]["targets"]["0.95"]
-    x = make_inputs(cfg, tensors=("q", "k", "v"), threads=16)
-    heads = [(0, 1), (0, cfg.H - 1)]
-    ref = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, cal["k"], cal["p"], heads=heads)
-    mask = ref["mask"].copy()
-    # heads the oracle did not build keep a dense diagonal band, so every CTA has work
-    for h in range(cfg.H):
-        if (0, h) not in heads:
-            for i in range(cfg.Tq):
-                mask[0, h, i, max(0, 2 * i - 3): 2 * i + 5] = 1
-    o, lse = _run_fwd(sa2, cfg, x, mask)
-    rows = np.concatenate([np.arange(0, 64), np.arange(cfg.N // 2, cfg.N // 2 + 64), np.arange(cfg.N - 100, cfg.N)])
-    for (b, h) in heads + [(0, 0)]:
-        ro, rlse = O.attn_fwd_head(O.to_f64(x["q"][b, h]), O.to_f64(x["k"][b, h]), O.to_f64(x["v"][b, h]),
-                                   mask[b, h], cfg.bq, cfg.bk, rows=rows)
-        _check_head(f"{cfg.name} h{h}", o[b, h, rows], lse[b, h, rows], ro, rlse)
-
-
 def test_fwd_longest_sequence_sampled_rows(sa2):
     """The longest sequence the library accepts (N = 491520 tokens, 7680 key blocks), d = 64,
     Top-k-only mask of 39 blocks per row; sampled rows (first, middle, last blocks)."""

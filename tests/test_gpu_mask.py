@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from tests.gpu_util import NEAR_THRESHOLD, check_lists_consistent, to_device
+from tests.gpu_util import check_lists_consistent, compare_masks, to_device
 from workload import CONFIGS, make_inputs
 from workload.gen import small_case
 
@@ -29,28 +29,23 @@ def sa2():
     return m
 
 
-def _compare(sa2, cfg, x, topk, topp, heads=None, log=None, check_lists=True):
+def _compare(sa2, cfg, x, topk, topp, heads=None, log=None, check_lists=True, label=None):
+    """Builds the mask on the GPU and compares it with the oracle's on `heads` (all by
+    default): P-bar, the entries (near-threshold ones exempt and logged), and every row as
+    the hybrid selection of the GPU's own P-bar.  Returns (mask, oracle result, exempt)."""
     torch = pytest.importorskip("torch")
     q, k = to_device(x["q"]), to_device(x["k"])
     bm = sa2.build_mask(q, k, topk, topp, bq=cfg.bq, bk=cfg.bk, want_pooled=True)
     sa2.check_device()
     torch.cuda.synchronize()
-    gmask = bm.mask.cpu().numpy()
-    gP = bm.pooled_p.cpu().numpy()
     ref = O.build_mask(x["q"], x["k"], cfg.bq, cfg.bk, topk, topp, heads=heads)
     todo = heads or [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
-    n_exempt = 0
-    for (b, h) in todo:
-        P = ref["P"][b, h]
-        assert np.abs(gP[b, h] - P).max() <= 5e-6, "pooled probabilities differ beyond fp32 accuracy"
-        exempt, bad = O.compare_mask_head(P, ref["sel"][(b, h)], gmask[b, h], NEAR_THRESHOLD)
-        assert not bad, f"head {(b, h)}: mask entries differ away from the threshold: {bad[:5]}"
-        n_exempt += len(exempt)
-        if log is not None and exempt:
-            log.extend([(b, h) + e for e in exempt])
+    exempt = compare_masks(bm, ref, todo, topk, topp, label or f"{cfg.name} k={topk} p={topp}")
+    if log is not None:
+        log.extend(exempt)
     if check_lists:
         check_lists_consistent(bm, cfg.B, cfg.H, cfg.Tq, cfg.Tk)
-    return bm, ref, n_exempt
+    return bm, ref, exempt
 
 
 def test_mask_tiny_fp32_config(sa2):
@@ -95,27 +90,30 @@ def test_mask_failure_probe_sweep(sa2):
         flat = cnt["topp"][:4].mean()
         assert abs(flat - topp * cfg.Tk) <= 0.1 * topp * cfg.Tk + 1  # flat heads keep about p*Tk
         assert (cnt["hybrid"] == np.maximum(cnt["topk"], cnt["topp"])).all()
-    print("exempt entries:", len(log), log[:10])
+    # every exempt entry was checked to sit at its row's threshold (compare_masks)
+    assert len(log) <= 8, f"{len(log)} exempt entries on the probe sweep: {log[:8]}"
     print(json.dumps(summary, indent=0))
 
 
 @pytest.mark.parametrize("ci", [2, 3])
 def test_mask_full_size_wan_shapes(sa2, ci):
-    """Full-size Wan-shaped workloads at the calibrated 95 % sparsity; the oracle checks a
-    few heads (P-bar, selection) and the lists are checked for internal consistency."""
+    """Full-size Wan-shaped workloads at the calibrated 95 % sparsity, in the launch
+    configuration the benchmark times: the oracle checks every head (P-bar, the entries, the
+    selection of the GPU's own P-bar) and the lists of three heads are checked entry by entry."""
     cfg = CONFIGS[ci]
     cal = json.load(open(os.path.join(GOLDEN, "calibration.json")))[str(ci)]["targets"]["0.95"]
-    heads = [(0, 0), (0, cfg.H // 2), (0, cfg.H - 1)]
+    heads = [(0, h) for h in range(cfg.H)]
     x = make_inputs(cfg, tensors=("q", "k"), threads=16)
-    bm, ref, n_exempt = _compare(sa2, cfg, x, cal["k"], cal["p"], heads=heads, check_lists=False)
+    bm, ref, exempt = _compare(sa2, cfg, x, cal["k"], cal["p"], heads=heads, check_lists=False)
+    n_exempt = len(exempt)
     kept = bm.row_cnt.sum().item() / (cfg.B * cfg.H * cfg.Tq * cfg.Tk)
     assert abs((1 - kept) - 0.95) < 0.01
-    # lists of two heads checked exhaustively
+    # lists of three heads checked entry by entry
     mask = bm.mask.cpu().numpy().astype(bool)
     rc, cc = bm.row_cnt.cpu().numpy(), bm.col_cnt.cpu().numpy()
     assert (rc == mask.sum(-1)).all() and (cc == mask.sum(-2)).all()
     ri, ci_ = bm.row_idx.cpu().numpy(), bm.col_idx.cpu().numpy()
-    for (b, h) in heads[:2]:
+    for (b, h) in (heads[0], heads[len(heads) // 2], heads[-1]):
         for i in range(cfg.Tq):
             assert (ri[b, h, i, :rc[b, h, i]] == np.nonzero(mask[b, h, i])[0]).all()
         for j in range(cfg.Tk):
