@@ -12,6 +12,7 @@ from .sa2 import (  # noqa: F401
     blocks,
     build_mask,
     check_device,
+    debug_set_wait_limit,
     device_status,
     load_library,
     make_shape,
