@@ -67,6 +67,9 @@ def parse():
     ap.add_argument("--cpu-qblocks", type=int, default=4, help="query blocks of the oracle sample")
     ap.add_argument("--heads", type=int, default=0,
                     help="heads of the workload (default: all); a smaller case for profiler captures")
+    ap.add_argument("--shard", choices=("heads", "replicas"), default="heads",
+                    help="with several ranks: split the heads of the layer over them (strong scaling, "
+                         "default) or run a whole layer on every rank (weak scaling)")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -111,6 +114,39 @@ def cpu_threads() -> int:
 
 
 # ------------------------------------------------------------------- ranks and timing
+
+def shard_range(total: int, world: int, rank: int):
+    """The contiguous share [lo, hi) of `total` independent (batch, head) items that rank
+    `rank` of `world` takes: sizes differ by at most one, the first total % world ranks take
+    the larger share.  Every (b, h) is independent through the mask, the forward and the
+    backward, so the ranks need no exchange."""
+    base, extra = divmod(total, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def reduce_sum_over_ranks(value: float, device) -> float:
+    """Sum of one scalar over the ranks (the kept work of every rank's heads)."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def local_inputs(cfg, lo: int, hi: int):
+    """The seeded inputs of the flat (batch, head) items [lo, hi) of the workload, laid out as
+    one batch of hi - lo heads (each item keeps the stream of its global (b, h))."""
+    from workload.gen import _stored, make_head
+    n = hi - lo
+    dt = np.uint16 if cfg.dtype == "bf16" else np.float32
+    out = {t: np.zeros((1, n, cfg.N, cfg.d), dtype=dt) for t in ("q", "k", "v", "do")}
+    for i, bh in enumerate(range(lo, hi)):
+        for t in out:
+            out[t][0, i] = _stored(cfg, make_head(cfg, bh // cfg.H, bh % cfg.H, t))
+    return out
+
 
 def reduce_max_over_ranks(value: float, device) -> float:
     """The slowest rank's time: every rank contributes its own and gets the maximum back
@@ -223,7 +259,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------- roofline accounting
 
-MASK_KERNELS = ("pool", "score_select", "csc")
+MASK_KERNELS = ("pool", "score_tc", "select", "csc")
 # Per kept (query, key) pair and channel, the algorithmic flops each attention kernel is
 # credited with: the forward's two GEMMs (S, P V); the dK/dV kernel's S, dP, dV, dK; the dQ
 # kernel's dQ GEMM only -- its recomputed S and dP are not algorithmic work.
@@ -291,7 +327,15 @@ def run_native(a, rank, world):
         import dataclasses
         cfg = dataclasses.replace(cfg, H=a.heads)
     topk, topp = calibration(a.config, a.sparsity)
-    x = make_inputs(cfg, threads=os.cpu_count() or 8)
+    sharded = world > 1 and a.shard == "heads"
+    cfg_job = cfg  # the whole layer (sharded runs split its heads)
+    if sharded:
+        import dataclasses
+        lo, hi = shard_range(cfg.B * cfg.H, world, rank)
+        x = local_inputs(cfg, lo, hi)
+        cfg = dataclasses.replace(cfg, B=1, H=hi - lo)
+    else:
+        x = make_inputs(cfg, threads=os.cpu_count() or 8)
 
     def pinned(arr):
         t = torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16)
@@ -328,6 +372,8 @@ def run_native(a, rank, world):
     pairs = kept_pairs(cfg, mask_np)
     sparsity = 1.0 - float(bm.row_cnt.sum().item()) / (B * H * cfg.Tq * cfg.Tk)
     flops_step = (FWD_FLOPS + BWD_FLOPS) * D * pairs
+    # the work of the whole job per step: every rank's heads (sharded), or N whole layers
+    job_flops_step = reduce_sum_over_ranks(flops_step, dev) if world > 1 else flops_step
 
     bus = None
     try:
@@ -357,6 +403,19 @@ def run_native(a, rank, world):
     sa2.check_device()
     ms_max = reduce_max_over_ranks(ev0.elapsed_time(ev1), dev)
     clk = clocks.stop() if rank == 0 else None
+
+    # ---- the mask builder timed on its own: wall time of sa2_build_mask on the stream (its
+    # pooling and its second stream's scoring / selection overlap), inputs larger than L2
+    mb_reps = max(5, a.steps)
+    torch.cuda.synchronize()
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    m0.record(stream)
+    for _ in range(mb_reps):
+        sa2.build_mask(d["q"], d["k"], topk, topp, bq=cfg.bq, bk=cfg.bk, out=bm, ws=ws_m)
+    m1.record(stream)
+    torch.cuda.synchronize()
+    mask_wall_ms = reduce_max_over_ranks(m0.elapsed_time(m1), dev) / mb_reps
+    sa2.check_device()
 
     # ---- end to end through the public API with host buffers.  Every step uploads its
     # inputs from pinned host memory and reads all four results back; the uploads of step
@@ -408,7 +467,7 @@ def run_native(a, rank, world):
     if rank != 0:
         return None
     peaks = measured_peaks()
-    value = world * flops_step * a.steps / (ms_max * 1e-3) / 1e12
+    value = job_flops_step * a.steps / (ms_max * 1e-3) / 1e12
     kernels = {n: {"launches": c, "ms_per_launch": (m / c if c else 0.0), "total_ms": m} for n, (c, m) in prof.items()}
     launches = sum(c for c, _ in prof.values())
     ph = phase_rooflines(prof, a.steps, pairs, D, peaks["bf16_tflops"])
@@ -418,30 +477,36 @@ def run_native(a, rank, world):
     # mask builder against HBM: it reads Q and K once and writes the mask and lists
     qk_bytes = 2 * B * H * N * D * 2
     out_bytes = B * H * cfg.Tq * cfg.Tk + 4 * 2 * float(bm.row_cnt.sum().item()) + 4 * B * H * (cfg.Tq + cfg.Tk)
-    mask_ms = sum(prof[k][1] for k in MASK_KERNELS if k in prof) / a.steps
+    mask_kernel_ms = sum(prof[k][1] for k in MASK_KERNELS if k in prof) / a.steps
+    mask_ms = mask_wall_ms
     mask_gbs = (qk_bytes + out_bytes) / (mask_ms * 1e-3) / 1e9 if mask_ms > 0 else None
     fwd_ms, bwd_ms = ph["forward"]["ms"], ph["backward"]["ms"]
     step_frac = flops_step / (ms_max / a.steps * 1e-3) / 1e12 / peaks["bf16_tflops"]
     line = {
         "metric": metric_name(a.sparsity), "metric_detail": METRIC_DETAIL,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
-        "ms_per_step": ms_max / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms_max / a.steps, "higher_is_better": True,
+        "scaling": "strong" if sharded else "weak", "vs_baseline": None,
         "dtype": "bf16 in/out; tcgen05 MMAs bf16 (S) and fp16 (P, dS), fp32 accumulate", "data": "synthetic",
-        "config": {"workload": f"{cfg.name} attention layer: B={B}, H={H}, N={N} (latent {'x'.join(map(str, cfg.grid))}), d={D}, bf16, "
+        "config": {"workload": f"{cfg.name} attention layer: B={cfg_job.B}, H={cfg_job.H}, N={N} (latent {'x'.join(map(str, cfg.grid))}), d={D}, bf16, "
                                f"blocks {cfg.bq}x{cfg.bk}",
                    "block_sparsity": sparsity, "topk": topk, "topp": topp, "seed": 0,
                    "l2": "inputs larger than L2 (Q,K,V,dO = %.1f GB per step); no flush" % (4 * B * H * N * D * 2 / 1e9),
-                   "step": "sa2_build_mask + sa2_attn_fwd + sa2_attn_bwd_with_fwd_ws (the forward's fp16 copy of V reused)", "parallelism": f"replicas x{world}"},
+                   "step": "sa2_build_mask + sa2_attn_fwd + sa2_attn_bwd_with_fwd_ws (the forward's fp16 copy of V reused)", "parallelism": (f"heads sharded over {world} ranks, {H} per rank (no collective)" if sharded
+                                   else f"replicas x{world}")},
         "kept_tflop_per_step": flops_step / 1e12,
-        "dense_equiv_tflops": world * (FWD_FLOPS + BWD_FLOPS) * D * float(N) * N * B * H * a.steps / (ms_max * 1e-3) / 1e12,
+        "dense_equiv_tflops": (1 if sharded else world) * (FWD_FLOPS + BWD_FLOPS) * D * float(N) * N
+                              * cfg_job.B * cfg_job.H * a.steps / (ms_max * 1e-3) / 1e12,
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "mask_ms": mask_ms,
         "fwd_tflops": ph["forward"]["tflops"], "bwd_tflops": ph["backward"]["tflops"],
         "phases": ph,
         "step_frac_of_bf16_burst": step_frac,
         "mask_builder": {"ms": mask_ms, "achieved_gbs": mask_gbs, "peak_gbs": peaks["hbm_gbs"],
-                         "frac": mask_gbs / peaks["hbm_gbs"] if mask_gbs else None, "bytes": qk_bytes + out_bytes},
+                         "frac": mask_gbs / peaks["hbm_gbs"] if mask_gbs else None, "bytes": qk_bytes + out_bytes,
+                         "timing": f"wall time of sa2_build_mask alone, mean of {mb_reps} calls (CUDA events)",
+                         "sum_of_kernel_ms_in_step": mask_kernel_ms},
         "roofline": roof,
-        "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": job_flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "kernels": kernels,

@@ -63,8 +63,8 @@ extern "C" sa2_status sa2_build_mask_noalloc(const sa2_shape* shape, const void*
       !aligned16(out->col_cnt) || !aligned16(out->col_idx) || !aligned16(out->mask) || !aligned16(out->pooled_p))
     return SA2_ERR_ALIGNMENT;
 
-  // pooled queries then pooled keys, fp32, as the builder lays them out
-  if (mask_pooled_bytes(s, nullptr) > (size_t)SA2_NOALLOC_SCRATCH_BYTES) return SA2_ERR_WORKSPACE;
+  // the pooled pairs of Q and K and the score tiles of at least one head must fit
+  if (mask_scratch_bytes(s, SA2_NOALLOC_SCRATCH_BYTES) > (size_t)SA2_NOALLOC_SCRATCH_BYTES) return SA2_ERR_WORKSPACE;
 
   cudaError_t err = cudaSuccess;
   unsigned char* scratch = static_cast<unsigned char*>(scratch_for_current_device(&err));
@@ -77,9 +77,10 @@ extern "C" sa2_status sa2_build_mask_noalloc(const sa2_shape* shape, const void*
   mo.col_idx = out->col_idx;
   mo.mask = out->mask;
   mo.pooled_p = out->pooled_p;
-  // The pooling kernel writes every pooled element whose scores are used (the scoring
-  // kernel also reads the padding past Tq / Tk, but discards what it computes from it), so
-  // nothing in the scratch has to start at zero.
-  err = launch_build_mask(s, q, k, sel, scratch, mo, static_cast<cudaStream_t>(stream));
+  mo.status = nullptr;
+  // The pooling kernel writes every pooled element the scores read (rows past Tq / Tk are
+  // read as zeros by the tensor copies and never come from the scratch), and the score
+  // tiles are written before they are read, so nothing in the scratch has to start at zero.
+  err = launch_build_mask(s, q, k, sel, scratch, SA2_NOALLOC_SCRATCH_BYTES, mo, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SA2_OK : SA2_ERR_CUDA;
 }

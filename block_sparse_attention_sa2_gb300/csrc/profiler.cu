@@ -23,9 +23,9 @@ std::vector<Record> g_open;         // started, not yet stopped (per id, at most
 std::vector<Record> g_done;         // stopped, not yet collected
 std::vector<cudaEvent_t> g_pool;    // events ready for reuse
 
-const char* kNames[kNumKernelIds] = {"pool", "score_select", "csc", "to_f16", "attn_fwd",
+const char* kNames[kNumKernelIds] = {"pool", "select", "csc", "to_f16", "attn_fwd",
                                      "bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq",
-                                     "bwd_pair_union", "vd_loss"};
+                                     "bwd_pair_union", "vd_loss", "score_tc"};
 
 cudaEvent_t take_event() {
   if (!g_pool.empty()) {

@@ -105,7 +105,7 @@ struct MaskWs {
 MaskWs mask_ws(const ShapeArgs& s) {
   MaskWs w;
   w.pooled = 0;
-  w.mask = align_up(mask_pooled_bytes(s, nullptr));
+  w.mask = align_up(mask_scratch_bytes(s, 0));
   w.total = align_up(w.mask + (size_t)s.B * s.H * s.Tq * s.Tk);
   return w;
 }
@@ -207,7 +207,8 @@ sa2_status sa2_build_mask(const sa2_shape* shape, const void* q, const void* k, 
   mo.col_idx = out->col_idx;
   mo.mask = out->mask ? out->mask : wsb + w.mask;
   mo.pooled_p = out->pooled_p;
-  return cuda_status(launch_build_mask(s, q, k, sel, wsb + w.pooled, mo, static_cast<cudaStream_t>(stream)));
+  mo.status = status_ptr();
+  return cuda_status(launch_build_mask(s, q, k, sel, wsb + w.pooled, 0, mo, static_cast<cudaStream_t>(stream)));
 }
 
 size_t sa2_fwd_workspace_size(const sa2_shape* shape) {

@@ -229,6 +229,14 @@ __device__ __forceinline__ void mma_ts_bmn(uint32_t d, uint32_t a, uint64_t b, b
   if constexpr (KK + 1 < KSTEPS) mma_ts_bmn<IDESC, KSTEPS, KK + 1>(d, a, b, fresh);
 }
 
+// TS form with B K-major (B_ROWS rows per channel panel): A from TMEM, 8 columns (16 16-bit
+// elements) per k-step; the first k-step overwrites D.
+template <uint32_t IDESC, int B_ROWS, int KSTEPS, int KK = 0>
+__device__ __forceinline__ void mma_ts_bkmajor(uint32_t d, uint32_t a, uint64_t b) {
+  umma_ts(d, a + KK * 8, b + kmajor_kstep(KK, B_ROWS), IDESC, KK > 0 ? 1u : 0u);
+  if constexpr (KK + 1 < KSTEPS) mma_ts_bkmajor<IDESC, B_ROWS, KSTEPS, KK + 1>(d, a, b);
+}
+
 // Arrive (once) on an mbarrier when every tcgen05 operation issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {

@@ -16,7 +16,8 @@ constexpr size_t kMaxDynSmem = 227 * 1024;
 
 // Launch profiler (profiler.cu): kernel ids and the brackets every launch wrapper calls.
 enum KernelId {
-  kPool = 0, kScoreSelect, kCsc, kToF16, kAttnFwd, kBwdPre, kAttnBwd, kAttnBwdDq, kBwdPairs, kVdLoss, kNumKernelIds
+  kPool = 0, kScoreSelect, kCsc, kToF16, kAttnFwd, kBwdPre, kAttnBwd, kAttnBwdDq, kBwdPairs, kVdLoss, kScoreTc,
+  kNumKernelIds
 };
 void prof_start(cudaStream_t st, int id);
 void prof_stop(cudaStream_t st, int id);
@@ -53,15 +54,18 @@ struct MaskOut {
   int32_t* col_idx;
   uint8_t* mask;      // never null here (workspace stands in when the caller passes null)
   float* pooled_p;    // may be null
+  unsigned* status;   // device status word
 };
 
 // Mask builder (mask_kernels.cu).
 int score_rows_per_cta(int Tk, int d);
-// Bytes of the pooled scratch (q-bar then k-bar, fp32, channel-major with padded pitches);
-// *kbar_offset receives the byte offset of k-bar.
-size_t mask_pooled_bytes(const ShapeArgs& s, size_t* kbar_offset);
-cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, const SelectArgs& sel, void* pooled,
-                              const MaskOut& out, cudaStream_t st);
+// Bytes of the builder's scratch: the pooled TF32 pairs of Q and K and the score tiles of
+// one chunk of heads.  budget = 0: the default chunk; otherwise the scratch of the largest
+// chunk that fits `budget` bytes (a result above budget means not even one head fits).
+size_t mask_scratch_bytes(const ShapeArgs& s, size_t budget);
+// scratch_bytes: the bytes behind `scratch` (0: mask_scratch_bytes(s, 0) of them).
+cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, const SelectArgs& sel, void* scratch,
+                              size_t scratch_bytes, const MaskOut& out, cudaStream_t st);
 
 // Tensor maps of bf16 token tensors [B, H, N, d] (attn_common.cu).
 bool make_token_map(CUtensorMap* map, const void* base, const ShapeArgs& s, int64_t sb, int64_t sh, int64_t sn,

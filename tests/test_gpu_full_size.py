@@ -81,3 +81,10 @@ def test_sparsity_sweep_dense_point(sa2):
     """k = 1: every block kept, the dense reference point of the sweep.  dK / dV of a key
     block then depend on every query row, so the oracle recomputes them on one head."""
     _check(sa2, 4, 0.0, [(0, 0), (0, 11)], dkdv_heads=[(0, 11)])
+
+
+def test_d64_wan_shape_at_95_percent_on_the_gpu_mask(sa2):
+    """The 1.3B-480p latent with 24 heads of 64 channels (the same model width): d = 64 at
+    production size, on its calibrated 95 % mask."""
+    cfg = CONFIGS[5]
+    _check(sa2, 5, 0.95, [(0, 0), (0, 8), (0, 16), (0, 23)])

@@ -130,3 +130,39 @@ def test_mask_rejects_bad_arguments(sa2):
         sa2.build_mask(q, q, 0.1, float("nan"))
     with pytest.raises(sa2.Sa2Error):
         sa2.build_mask(q, q, 0.1, 0.5, bk=32)
+
+
+def test_mask_diagnostics_on_gpu_masks(sa2):
+    """The diagnostics (per-row kept counts, kept pooled mass, per-head histograms) computed
+    on the device from masks the GPU built for the mask-probe workload: kept counts equal the
+    oracle's max(K, m) and kept masses its pooled mass over the kept blocks (rows holding a
+    logged near-threshold entry aside), and they show the failure modes of the single rules
+    (gist.science explainer, section 1; thelatestinai.com Table 6, Top-k-only / Top-p-only)."""
+    torch = pytest.importorskip("torch")
+    from block_sparse_attention_sa2_gb300.diagnostics import mask_diagnostics
+    cfg = CONFIGS[1]
+    x = make_inputs(cfg, tensors=("q", "k"))
+    k, p = 0.05, 0.9
+    K = O.topk_count(k, cfg.Tk)
+    flat, sink = slice(0, 4), slice(4, 8)
+    stats = {}
+    for mode, (kk, pp) in (("topk", (k, 0.0)), ("topp", (0.0, p)), ("hybrid", (k, p))):
+        bm, ref, exempt = _compare(sa2, cfg, x, kk, pp, label=f"diagnostics {mode}")
+        d = mask_diagnostics(bm, bins=8)
+        assert d["kept"].is_cuda and d["kept_mass"].is_cuda
+        kept, mass = d["kept"].cpu().numpy()[0], d["kept_mass"].cpu().numpy()[0]
+        for h in range(cfg.H):
+            sel = ref["sel"][(0, h)]
+            skip = {e[2] for e in exempt if e[1] == h}
+            rows = [i for i in range(cfg.Tq) if i not in skip]
+            assert (kept[h, rows] == sel.L[rows]).all(), f"{mode} head {h}: kept counts"
+            want = np.array([sel.sorted_P[i, :sel.L[i]].sum() for i in rows])
+            assert np.abs(mass[h, rows] - want).max() <= 1e-5, f"{mode} head {h}: kept mass"
+        assert (d["kept_frac_hist"].sum(-1) == cfg.Tq).all() and (d["kept_mass_hist"].sum(-1) == cfg.Tq).all()
+        stats[mode] = (torch.as_tensor(kept), torch.as_tensor(mass))
+    kept, mass = stats["topk"]
+    assert (kept == K).all() and mass[flat].median() < 0.5  # Top-k alone misses a flat row's mass
+    kept, mass = stats["topp"]
+    assert (kept[sink] == 1).all() and (mass[sink] >= p).all()  # Top-p alone: the sink block only
+    kept, mass = stats["hybrid"]
+    assert (mass[flat] >= p - 1e-6).all() and (kept[sink] >= K).all()  # the hybrid covers both

@@ -134,7 +134,7 @@ def test_noalloc_rejects_oversized_shapes_on_the_host(lib):
 
 def test_profiler_size_query_needs_no_gpu(lib):
     lib.sa2_profiler_enable(0)
-    assert lib.sa2_profiler_collect(None, 0) == 10
+    assert lib.sa2_profiler_collect(None, 0) == 11
 
 
 def test_vd_loss_rejects_bad_arguments_before_any_launch(lib):

@@ -30,11 +30,12 @@ def test_generation_is_deterministic_and_per_head():
 def test_shapes_and_dtypes_of_every_config():
     expect = {0: (1, 2, 1024, 64, 16, 16), 1: (1, 8, 8192, 128, 64, 128),
               2: (1, 12, 32760, 128, 256, 512), 3: (1, 40, 75600, 128, 591, 1182),
-              4: (1, 12, 32760, 128, 256, 512)}
+              4: (1, 12, 32760, 128, 256, 512), 5: (1, 24, 32760, 64, 256, 512)}
     for i, (B, H, N, d, Tq, Tk) in expect.items():
         c = CONFIGS[i]
         assert (c.B, c.H, c.N, c.d, c.Tq, c.Tk) == (B, H, N, d, Tq, Tk)
-    assert CONFIGS[0].dtype == "fp32" and all(CONFIGS[i].dtype == "bf16" for i in (1, 2, 3, 4))
+    assert CONFIGS[0].dtype == "fp32" and all(CONFIGS[i].dtype == "bf16" for i in (1, 2, 3, 4, 5))
+    assert CONFIGS[5].H * CONFIGS[5].d == CONFIGS[2].H * CONFIGS[2].d  # the same model width
 
 
 def _pooled(cfg, h):

@@ -98,6 +98,12 @@ CONFIGS: Dict[int, WorkloadConfig] = {
         index=4, name="wan2.1-1.3b-480p-sweep", B=1, H=12, grid=(21, 30, 52), d=128,
         dtype="bf16", bq=128, bk=64, pos_amp=1.0, pos_sigma=_WAN_SIGMA, sink_blocks=(0, 1),
         sink_s=30.0, sink_a=2.0),
+    # The same latent and model width (1536) split into 24 heads of 64 channels: the d = 64
+    # form of the Wan2.1 drop-in.
+    5: WorkloadConfig(
+        index=5, name="wan2.1-1.3b-480p-d64", B=1, H=24, grid=(21, 30, 52), d=64,
+        dtype="bf16", bq=128, bk=64, pos_amp=1.0, pos_sigma=_WAN_SIGMA, sink_blocks=(0, 1),
+        sink_s=30.0, sink_a=2.0),
 }
 
 
