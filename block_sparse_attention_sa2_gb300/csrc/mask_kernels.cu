@@ -6,18 +6,21 @@
 // whose cumulative probability reaches p).
 //
 // Four kernels:
-//   pool_kernel      persistent; streams Q and K through a ring of shared-memory stages
-//                    with TMA and writes the block means (fp32) as a TF32 pair hi + lo,
-//                    row-major [2][B*H][T][d].  The HBM-bound part of the builder.
+//   pool_kernel      persistent, one warp per 128-token chunk of Q or K: plain streaming
+//                    loads, fp32 sums in token order, and the block means written as a TF32
+//                    pair hi + lo, row-major [2][B*H][T][d].  The HBM-bound part.
 //   score_tc_kernel  pooled scores S-bar = q-bar k-bar^T / sqrt(d) of a 128-row x 256-key
 //                    tile on the tensor cores (tcgen05, kind::tf32) as the three products
 //                    hi.hi + hi.lo + lo.hi -- about fp32 accuracy -- accumulated in tensor
-//                    memory and written to a scratch tile.
-//   select_kernel    one warp per row: row softmax in fp32, the hybrid selection by a
-//                    bisection on the fp32 bit patterns of P-bar with the mass in 2^-60
-//                    fixed point, and the emit of the row list and the u8 mask.
-//   csc_kernel       transposes the u8 mask into the per-key-block lists (ascending).
-// The scores run in chunks of heads whose scratch tiles stay small enough for L2.
+//                    memory and written to a scratch row in a lane-friendly permuted order.
+//   select_kernel    one warp per row: row softmax in fp32, the hybrid selection with the
+//                    mass in 2^-60 fixed point (a warp-wide sort of each lane's largest
+//                    keys, or a bisection on the fp32 bit patterns of P-bar), and the emit
+//                    of the row list, the u8 mask and the row's kept bits.
+//   csc_kernel       transposes the kept bits into the per-key-block lists (ascending).
+// The heads run in chunks: the caller's stream pools chunk after chunk while two more
+// streams take the scores, the selection and the column lists of alternate chunks, each
+// with its own scratch buffer small enough to stay in L2.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -35,7 +38,7 @@ constexpr int kChunkTokens = 128;           // tokens per pooling chunk
 constexpr int kScoreRows = 128;             // MMA M: query blocks per tile
 constexpr int kScoreKeys = 256;             // MMA N: key blocks per tile
 constexpr int kSelectThreads = 256;
-constexpr size_t kScoreChunkBudget = 24u << 20;  // bytes of scratch tiles per head chunk
+constexpr size_t kScoreChunkBudget = 32u << 20;  // bytes of the two head-chunk buffers
 
 // ---------------------------------------------------------------------------- helpers
 
@@ -51,22 +54,6 @@ __device__ __forceinline__ float tf32_rna(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
   return __uint_as_float(r);
-}
-
-// TMA load with an L2 eviction-priority policy (evict_first for data streamed once).
-__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
-                                                 int c2, int c3, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 
 // ----------------------------------------------------------------------------- pooling
@@ -339,16 +326,26 @@ __global__ void __launch_bounds__(kScoreThreadsP, 1)
       const int kc = ti % nkc, rt = (ti / nkc) % nrt, z = ti / (nkc * nrt);
       const int row = rt * kScoreRows + 32 * q4 + lane;
       float* dst = a.sbar + ((size_t)z * a.tq_pad + row) * a.tk_pad + (size_t)kc * kScoreKeys;
+      // rows are stored permuted per 128-key chunk (key 128 c + 32 i + l at 128 c + 4 l + i),
+      // keys past Tk as -inf
 #pragma unroll 1
-      for (int c0 = 0; c0 < kScoreKeys; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(trow + tb * kScoreKeys + c0, r);
-        tmem_ld_wait(r);
+      for (int g = 0; g < kScoreKeys; g += 128) {
+        uint32_t r[4][32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          reinterpret_cast<float4*>(dst + c0)[i] =
-              make_float4(__uint_as_float(r[4 * i]) * a.inv_sqrt_d, __uint_as_float(r[4 * i + 1]) * a.inv_sqrt_d,
-                          __uint_as_float(r[4 * i + 2]) * a.inv_sqrt_d, __uint_as_float(r[4 * i + 3]) * a.inv_sqrt_d);
+        for (int i = 0; i < 4; ++i) tmem_ld32(trow + tb * kScoreKeys + g + 32 * i, r[i]);
+        tmem_ld_wait(r[0]);
+        tmem_ld_wait(r[1]);
+        tmem_ld_wait(r[2]);
+        tmem_ld_wait(r[3]);
+        const int j0 = kc * kScoreKeys + g;
+#pragma unroll
+        for (int l = 0; l < 32; ++l) {
+          float v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            v[i] = j0 + 32 * i + l < s.Tk ? __uint_as_float(r[i][l]) * a.inv_sqrt_d : -INFINITY;
+          reinterpret_cast<float4*>(dst + g)[l] = make_float4(v[0], v[1], v[2], v[3]);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -407,379 +404,491 @@ __device__ __forceinline__ Predicate count_mass(const uint32_t* keys, int Tk, ui
   return p;
 }
 
-// Keys per lane held in registers by the selection when Tk <= 32 * kRegKeys.
-constexpr int kRegKeys = 40;
+// Coarse mass floor(P * 2^31) of a key, equal to mass_fix(key) >> 29: the scaling by 2^31 is
+// exact in fp32 and the conversion rounds down.
+__device__ __forceinline__ uint32_t mass_c31(uint32_t key) {
+  return __float2uint_rd(__uint_as_float(key) * 2147483648.0f);
+}
 
-// The hybrid selection of one row (one warp) with the row's keys in registers (lane holds
-// entries lane, lane + 32, ...; padding keys are 0).  The kept set is every key > t and the
-// first `take` keys == t in index order, where t is the largest value with
-// count(>= t) >= K and mass(>= t) >= p; keep_all when the row's mass never reaches p.
-//
-// Masses are compared in 2^-60 fixed point, exactly.  Each lane keeps a coarse 32-bit mass
-// per key, c = floor(P * 2^31) = floor(P * 2^60) / 2^29 rounded down; the row's coarse sum S
-// stays below 2^32, and over n keys the exact sum lies in [S 2^29, (S + n) 2^29).  A test
-// against p is decided by that bracket unless p falls inside it; only then is the exact sum
-// formed (from the keys themselves).
-__device__ __forceinline__ bool mass_at_least(const uint32_t (&k)[kRegKeys], const uint32_t (&c31)[kRegKeys],
-                                              uint32_t t, bool strictly, uint32_t n, unsigned long long p_fix) {
-  uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
-#pragma unroll
-  for (int i = 0; i < kRegKeys; i += 4) {
-    s0 += (strictly ? k[i] > t : k[i] >= t) ? c31[i] : 0u;
-    s1 += (strictly ? k[i + 1] > t : k[i + 1] >= t) ? c31[i + 1] : 0u;
-    s2 += (strictly ? k[i + 2] > t : k[i + 2] >= t) ? c31[i + 2] : 0u;
-    s3 += (strictly ? k[i + 3] > t : k[i + 3] >= t) ? c31[i + 3] : 0u;
+// Scratch rows of scores (and, for rows in memory, of keys) are stored permuted within each
+// 128-entry chunk: entry 128 c + 32 i + l sits at position 128 c + 4 l + i, so that one
+// 16-byte load gives lane l the entries l, l + 32, l + 64, l + 96 of chunk c.  A lane then
+// holds every 32nd entry of the row (neighbouring key blocks sit in neighbouring lanes), and
+// a ballot over the lanes for a fixed i covers 32 consecutive entries.  Positions past Tk
+// hold -inf scores, hence zero keys.
+
+// The hybrid selection of one row (one warp) keeps every key > t and the first `take` keys
+// == t in index order, where t is the largest value with count(>= t) >= K and
+// mass(>= t) >= p; keep_all when the row's mass never reaches p.  Masses are compared in
+// 2^-60 fixed point, exactly.
+
+// `take` from the count and the exact mass of the keys strictly above t.
+__device__ __forceinline__ int ties_to_take(const SelectArgs& sel, uint32_t t, uint32_t cnt_gt,
+                                            unsigned long long mass_gt) {
+  const int r_k = sel.K - (int)cnt_gt;
+  int r_m = 0;
+  if (sel.p_mode == 0 && mass_gt < sel.p_fix) {
+    const unsigned long long vfix = mass_fix(t);
+    r_m = vfix ? (int)((sel.p_fix - mass_gt + vfix - 1) / vfix) : 0;
   }
-  const unsigned long long S = __reduce_add_sync(0xffffffffu, (s0 + s1) + (s2 + s3));
-  if ((S << 29) >= p_fix) return true;
-  if (((S + n) << 29) <= p_fix) return false;
-  unsigned long long m = 0;
-#pragma unroll
-  for (int i = 0; i < kRegKeys; ++i) m += (strictly ? k[i] > t : k[i] >= t) ? mass_fix(k[i]) : 0ull;
-  return warp_sum_u64(m) >= p_fix;
+  return max(max(r_k, r_m), 0);
 }
 
-__device__ __forceinline__ unsigned long long mass_exact(const uint32_t (&k)[kRegKeys], uint32_t t) {
+// Whether the n keys in memory that are >= t number at least K (when with_count) and reach
+// the mass p (when with_mass).  Each lane sums a coarse 32-bit mass per key,
+// c = floor(P * 2^31); the row's coarse sum S stays below 2^32, and over m keys the exact sum
+// lies in [S 2^29, (S + m) 2^29).  The test against p is decided by that bracket unless p
+// falls inside it; only then is the exact sum formed.
+__device__ __forceinline__ bool keys_reach(const uint32_t* keys, int n, uint32_t t, const SelectArgs& sel,
+                                           bool with_count, bool with_mass) {
+  const int lane = threadIdx.x & 31;
+  uint32_t c = 0, S = 0;
+  for (int j = lane; j < n; j += 32) {
+    const uint32_t key = keys[j];
+    const bool in = key >= t;
+    c += in ? 1u : 0u;
+    S += in ? mass_c31(key) : 0u;
+  }
+  c = __reduce_add_sync(0xffffffffu, c);
+  if (with_count && c < (uint32_t)sel.K) return false;
+  if (!with_mass) return true;
+  const unsigned long long St = __reduce_add_sync(0xffffffffu, S);
+  if ((St << 29) >= sel.p_fix) return true;
+  if (((St + c) << 29) <= sel.p_fix) return false;
   unsigned long long m = 0;
-#pragma unroll
-  for (int i = 0; i < kRegKeys; ++i) m += k[i] > t ? mass_fix(k[i]) : 0ull;
-  return warp_sum_u64(m);
+  for (int j = lane; j < n; j += 32) {
+    const uint32_t key = keys[j];
+    m += key >= t ? mass_fix(key) : 0ull;
+  }
+  return warp_sum_u64(m) >= sel.p_fix;
 }
 
-__device__ __forceinline__ void select_in_registers(const uint32_t (&k)[kRegKeys], const SelectArgs& sel,
-                                                    bool& keep_all, uint32_t& t, int& take) {
+// The selection by bisection over the fp32 bit patterns, with the row's n keys in memory
+// (shared or global; padding keys 0).  Sets keep_all when the row's mass never reaches p,
+// else t, take and n_eq (the number of keys == t, padding zeros included when t = 0).
+__device__ __forceinline__ void select_in_memory(const uint32_t* keys, int n, const SelectArgs& sel, bool& keep_all,
+                                                 uint32_t& t, int& take, int& n_eq) {
   const bool use_mass = sel.p_mode == 0;
-  uint32_t c31[kRegKeys];
-#pragma unroll
-  for (int i = 0; i < kRegKeys; ++i) c31[i] = (uint32_t)(mass_fix(k[i]) >> 29);
   // every real key is >= 1 (P > 0 after the softmax; a key of 0 is padding or an
-  // underflowed probability, whose mass is 0 as well)
-  if (use_mass && !mass_at_least(k, c31, 1u, false, 32u * kRegKeys, sel.p_fix)) {
+  // underflowed probability, whose mass is 0 as well), so every tested t is >= 1
+  if (use_mass && !keys_reach(keys, n, 1u, sel, false, true)) {
     keep_all = true;
     return;
   }
-  // every tested t is >= 1, so the padding keys (0) are never counted
   uint32_t lo = 0, hi = 0x3F800001u;
   while (hi - lo > 1) {
     const uint32_t mid = lo + (hi - lo) / 2;
-    uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
-#pragma unroll
-    for (int i = 0; i < kRegKeys; i += 4) {
-      c0 += k[i] >= mid ? 1u : 0u;
-      c1 += k[i + 1] >= mid ? 1u : 0u;
-      c2 += k[i + 2] >= mid ? 1u : 0u;
-      c3 += k[i + 3] >= mid ? 1u : 0u;
-    }
-    const uint32_t n = __reduce_add_sync(0xffffffffu, (c0 + c1) + (c2 + c3));  // same in every lane
-    bool ok = n >= (uint32_t)sel.K;
-    if (ok && use_mass) ok = mass_at_least(k, c31, mid, false, n, sel.p_fix);
-    if (ok)
+    if (keys_reach(keys, n, mid, sel, true, use_mass))
       lo = mid;
     else
       hi = mid;
   }
   t = lo;
-  uint32_t c = 0;
-#pragma unroll
-  for (int i = 0; i < kRegKeys; ++i) c += k[i] > t ? 1u : 0u;
-  c = __reduce_add_sync(0xffffffffu, c);
-  const int r_k = sel.K - (int)c;
-  int r_m = 0;
-  if (use_mass) {
-    const unsigned long long m = mass_exact(k, t);
-    if (m < sel.p_fix) {
-      const unsigned long long vfix = mass_fix(t);
-      r_m = vfix ? (int)((sel.p_fix - m + vfix - 1) / vfix) : 0;
-    }
-  }
-  take = max(max(r_k, r_m), 0);
+  const Predicate gt = count_mass(keys, n, t, true);
+  const Predicate ge = count_mass(keys, n, t, false);
+  n_eq = (int)(ge.cnt - gt.cnt);
+  take = ties_to_take(sel, t, gt.cnt, gt.mass);
 }
 
-// The same selection with the keys in memory (rows longer than 32 * kRegKeys).
-__device__ __forceinline__ void select_in_memory(const uint32_t* keys, int Tk, const SelectArgs& sel, bool& keep_all,
-                                                 uint32_t& t, int& take) {
-  const bool use_mass = sel.p_mode == 0;
-  if (use_mass) {
-    const Predicate tot = count_mass(keys, Tk, 0u, false);
-    if (tot.mass < sel.p_fix) {
-      keep_all = true;
-      return;
-    }
-  }
-  uint32_t lo = 0, hi = 0x3F800001u;
-  while (hi - lo > 1) {
-    const uint32_t mid = lo + (hi - lo) / 2;
-    const Predicate pr = count_mass(keys, Tk, mid, false);
-    const bool ok = pr.cnt >= (uint32_t)sel.K && (!use_mass || pr.mass >= sel.p_fix);
-    if (ok)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  t = lo;
-  const Predicate gt = count_mass(keys, Tk, t, true);
-  const int r_k = sel.K - (int)gt.cnt;
-  int r_m = 0;
-  if (use_mass && gt.mass < sel.p_fix) {
-    const unsigned long long vfix = mass_fix(t);
-    r_m = vfix ? (int)((sel.p_fix - gt.mass + vfix - 1) / vfix) : 0;
-  }
-  take = max(max(r_k, r_m), 0);
-}
-
-// Sorting network for the kRegKeys keys of a lane, descending: K. E. Batcher's odd-even
-// merge sort (1968) for 64 inputs, generated at compile time, keeping only the comparators
-// whose two positions are below kRegKeys (positions kRegKeys..63 would hold zeros, the
-// minimum, which no comparator moves).
-// Comparator `idx` of the network (its first or second position), or the number of
-// comparators when idx < 0; evaluated by the compiler only.
-constexpr int sort_net(int idx, bool second) {
+// Sorting network for N keys, descending: K. E. Batcher's odd-even merge sort (1968) for the
+// next power of two P2 >= N inputs, generated at compile time, keeping only the comparators
+// whose two positions are below N (positions N..P2-1 would hold zeros, the minimum, which no
+// comparator moves).  sort_net<N>(idx, second) is comparator idx's first or second position,
+// or the number of comparators when idx < 0; evaluated by the compiler only.
+template <int N>
+__host__ __device__ constexpr int sort_net(int idx, bool second) {
+  int P2 = 1;
+  while (P2 < N) P2 *= 2;
   int n = 0;
-  for (int p = 1; p < 64; p *= 2)
+  for (int p = 1; p < P2; p *= 2)
     for (int k = p; k >= 1; k /= 2)
-      for (int j = k % p; j + k < 64; j += 2 * k)
-        for (int i = 0; i < k && i + j + k < 64; ++i)
-          if ((i + j) / (2 * p) == (i + j + k) / (2 * p) && i + j + k < kRegKeys) {
+      for (int j = k % p; j + k < P2; j += 2 * k)
+        for (int i = 0; i < k && i + j + k < P2; ++i)
+          if ((i + j) / (2 * p) == (i + j + k) / (2 * p) && i + j + k < N) {
             if (n == idx) return second ? i + j + k : i + j;
             ++n;
           }
   return n;
 }
-constexpr int kSortNetSize = sort_net(-1, false);
 
-template <int C>
-__device__ __forceinline__ void sort_cmp(uint32_t (&k)[kRegKeys]) {
-  constexpr int a = sort_net(C, false), b = sort_net(C, true);
+// Comparator C of the N-key network applied to k[O .. O + N).
+template <int N, int O, int C, int L>
+__device__ __forceinline__ void sort_cmp(uint32_t (&k)[L]) {
+  constexpr int a = O + sort_net<N>(C, false), b = O + sort_net<N>(C, true);
   const uint32_t x = k[a], y = k[b];
   k[a] = max(x, y);
   k[b] = min(x, y);
 }
 
-template <int... C>
-__device__ __forceinline__ void sort_all(uint32_t (&k)[kRegKeys], std::integer_sequence<int, C...>) {
-  (sort_cmp<C>(k), ...);
+template <int N, int O, int L, int... C>
+__device__ __forceinline__ void sort_all(uint32_t (&k)[L], std::integer_sequence<int, C...>) {
+  (sort_cmp<N, O, C>(k), ...);
 }
 
-__device__ __forceinline__ void sort_desc(uint32_t (&k)[kRegKeys]) {
-  sort_all(k, std::make_integer_sequence<int, kSortNetSize>{});
+// Sorts k[O .. O + N) descending.
+template <int N, int O = 0, int L>
+__device__ __forceinline__ void sort_desc(uint32_t (&k)[L]) {
+  static_assert(O + N <= L, "slice out of range");
+  sort_all<N, O>(k, std::make_integer_sequence<int, sort_net<N>(-1, false)>{});
 }
 
-constexpr int kWalkMax = 128;  // longest walk before the bisection takes over
+template <int L, int... G>
+__device__ __forceinline__ void sort_groups8(uint32_t (&k)[L], std::integer_sequence<int, G...>) {
+  (sort_desc<8, 8 * G>(k), ...);
+}
 
-// The hybrid selection by walking the row in descending order: each lane sorts its keys and
-// parks them in shared memory (column `lane`), the warp repeatedly takes the largest head
-// (all lanes holding that value advance), and counts and masses (2^-60 fixed point, exact)
-// accumulate until count >= K and mass >= p.  The value reached is the threshold t; the
-// counts and masses of the keys strictly above it give `take` exactly as the bisection
-// does.  Returns false when the walk needs more than kWalkMax steps (the row is then
-// left to the bisection; k is sorted but its values are intact).
-__device__ __forceinline__ bool select_by_walk(uint32_t (&k)[kRegKeys], uint32_t* col, const SelectArgs& sel,
-                                               uint32_t& t, int& take) {
+// Leaves the 8 largest of the lane's KPL keys in k[0..7], descending, and returns the
+// largest of the others.  Each group of 8 is sorted; then group g is folded into group 0 by
+// comparing k[i] with the group's (7 - i)-th key: the larger of each pair are the 8 largest
+// of the 16 (in bitonic order, sorted by three half-cleaner steps), the smaller are out of
+// the running for good, and the largest of those is tracked.
+template <int KPL>
+__device__ __forceinline__ uint32_t top8_desc(uint32_t (&k)[KPL]) {
+  static_assert(KPL % 8 == 0 && KPL >= 16, "groups of 8");
+  sort_groups8(k, std::make_integer_sequence<int, KPL / 8>{});
+  uint32_t H = 0;
+#pragma unroll
+  for (int g = 1; g < KPL / 8; ++g) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t x = k[i], y = k[8 * g + 7 - i];
+      k[i] = max(x, y);
+      H = max(H, min(x, y));
+    }
+#pragma unroll
+    for (int dist = 4; dist >= 1; dist /= 2)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if ((i & dist) == 0) {
+          const uint32_t x = k[i], y = k[i + dist];
+          k[i] = max(x, y);
+          k[i + dist] = min(x, y);
+        }
+  }
+  return H;
+}
+
+// Bitonic merge across the warp: on entry every lane holds M keys in descending order in
+// k[0..M-1]; on exit the 32 M keys are in descending order lane after lane (lane 0 holds
+// the M largest).  Level m merges pairs of sorted runs of 2^m lanes: the first step
+// compares each key of the first run with its mirror image in the second (lane ^ (2^(m+1) -
+// 1), position M - 1 - r), which leaves two bitonic halves with every key of the first
+// above every key of the second; half-cleaners at lane distances 2^(m-1) .. 1 and then at
+// register distances M/2 .. 1 sort each half.
+template <int M, int N>
+__device__ __forceinline__ void warp_merge_runs(uint32_t (&k)[N], int lane) {
+#pragma unroll
+  for (int m = 0; m < 5; ++m) {
+    {
+      const bool upper = (lane >> m) & 1;
+      uint32_t o[M];
+#pragma unroll
+      for (int r = 0; r < M; ++r) o[r] = __shfl_xor_sync(0xffffffffu, k[M - 1 - r], (2 << m) - 1);
+#pragma unroll
+      for (int r = 0; r < M; ++r) k[r] = upper ? min(k[r], o[r]) : max(k[r], o[r]);
+    }
+#pragma unroll
+    for (int d = m - 1; d >= 0; --d) {
+      const bool upper = (lane >> d) & 1;
+#pragma unroll
+      for (int r = 0; r < M; ++r) {
+        const uint32_t o = __shfl_xor_sync(0xffffffffu, k[r], 1 << d);
+        k[r] = upper ? min(k[r], o) : max(k[r], o);
+      }
+    }
+#pragma unroll
+    for (int dist = M / 2; dist >= 1; dist /= 2)
+#pragma unroll
+      for (int r = 0; r < M; ++r)
+        if ((r & dist) == 0) {
+          const uint32_t x = k[r], y = k[r + dist];
+          k[r] = max(x, y);
+          k[r + dist] = min(x, y);
+        }
+  }
+}
+
+// The selection by sorting.  The M0 largest keys of every lane (or all of them when a lane
+// holds fewer) are the candidates, merged into one descending order across the warp.
+// Position e of that order has count e + 1 and the exact prefix mass of positions 0..e
+// (lane-local prefix plus a warp scan); the first position where count >= K and mass >= p
+// holds t.  That order is the row's own order for every value above H, the largest key left
+// out of the candidates, so the result is the row's whenever t > H (or no key was left
+// out).  Returns false when it is not (or when no position qualifies): a second pass with
+// more candidates, or the bisection, then decides the row.  k is clobbered.
+template <int KPL, int M0>
+__device__ __forceinline__ bool select_by_sort(uint32_t (&k)[KPL], const SelectArgs& sel, uint32_t& t, int& take,
+                                               int& n_eq) {
+  constexpr int M = KPL < M0 ? KPL : M0;
   const int lane = threadIdx.x & 31;
   const bool use_mass = sel.p_mode == 0;
-  sort_desc(k);
-#pragma unroll
-  for (int i = 0; i < kRegKeys; ++i) col[i * 32 + lane] = k[i];
-  __syncwarp();
-  int cur = 0;
-  uint32_t head = k[0];
-  uint32_t count = 0, cnt_gt = 0, val = 0xFFFFFFFFu;
-  unsigned long long mass = 0, mass_gt = 0;
-  for (int step = 0; step < kWalkMax; ++step) {
-    const uint32_t mx = __reduce_max_sync(0xffffffffu, head);
-    if (mx == 0u) return false;  // every key consumed (not reached when K <= Tk and the mass reaches p)
-    if (mx != val) {  // a new value: the keys counted so far are all above it
-      val = mx;
-      cnt_gt = count;
-      mass_gt = mass;
-    }
-    const bool adv = head == mx;  // every lane holding the value advances
-    const uint32_t n_eq = __popc(__ballot_sync(0xffffffffu, adv));
-    count += n_eq;
-    mass += (unsigned long long)n_eq * mass_fix(mx);
-    if (count >= (uint32_t)sel.K && (!use_mass || mass >= sel.p_fix)) {
-      t = mx;
-      const int r_k = sel.K - (int)cnt_gt;
-      int r_m = 0;
-      if (use_mass && mass_gt < sel.p_fix) {
-        const unsigned long long vfix = mass_fix(t);
-        r_m = vfix ? (int)((sel.p_fix - mass_gt + vfix - 1) / vfix) : 0;
-      }
-      take = max(max(r_k, r_m), 0);
-      return true;
-    }
-    // branch-free advance: every lane stays on the warp-wide reductions' path
-    const int nc = cur + (adv ? 1 : 0);
-    const uint32_t nxt = nc < kRegKeys ? col[nc * 32 + lane] : 0u;
-    head = adv ? nxt : head;
-    cur = nc;
+  uint32_t H = 0;
+  if constexpr (KPL == M) {
+    sort_desc<KPL>(k);
+  } else if constexpr (M == 8) {
+    H = __reduce_max_sync(0xffffffffu, top8_desc(k));
+  } else {
+    sort_desc<KPL>(k);
+    H = __reduce_max_sync(0xffffffffu, k[M]);
   }
-  return false;
+  warp_merge_runs<M>(k, lane);
+  unsigned long long lp[M];  // lane-local inclusive prefix masses
+  unsigned long long run = 0;
+#pragma unroll
+  for (int r = 0; r < M; ++r) {
+    run += mass_fix(k[r]);
+    lp[r] = run;
+  }
+  unsigned long long base = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long v = __shfl_up_sync(0xffffffffu, base, o);
+    if (lane >= o) base += v;
+  }
+  base -= run;  // mass of the lanes before this one
+  const int e0 = lane * M;
+  int first = M;
+#pragma unroll
+  for (int r = M - 1; r >= 0; --r) {
+    const bool ok = e0 + r + 1 >= sel.K && (!use_mass || base + lp[r] >= sel.p_fix);
+    first = ok ? r : first;
+  }
+  const unsigned found = __ballot_sync(0xffffffffu, first < M);
+  if (found == 0u) return false;
+  uint32_t tv = 0;
+#pragma unroll
+  for (int r = 0; r < M; ++r) tv = r == first ? k[r] : tv;
+  t = __shfl_sync(0xffffffffu, tv, __ffs(found) - 1);
+  if (KPL > M && t <= H) return false;
+  uint32_t c = 0, ce = 0;
+#pragma unroll
+  for (int r = 0; r < M; ++r) {
+    c += k[r] > t ? 1u : 0u;
+    ce += k[r] == t ? 1u : 0u;
+  }
+  const uint32_t cnt_gt = __reduce_add_sync(0xffffffffu, c);
+  n_eq = (int)__reduce_add_sync(0xffffffffu, ce);
+  unsigned long long mass_gt = 0;
+  if (cnt_gt > 0) {  // the prefix mass at position cnt_gt - 1
+    const int pos = (int)cnt_gt - 1, rr = pos % M;
+    unsigned long long v = 0;
+#pragma unroll
+    for (int r = 0; r < M; ++r) v = r == rr ? lp[r] : v;
+    mass_gt = __shfl_sync(0xffffffffu, base + v, pos / M);
+  }
+  take = ties_to_take(sel, t, cnt_gt, mass_gt);
+  return true;
 }
 
 struct SelArgs {
-  float* sbar;  // scratch tiles of the head chunk; rows past 32 * kRegKeys keys are
-                // overwritten in place by their P-bar bit patterns
+  float* sbar;     // permuted score rows of the head chunk; rows past 32 * kMaxKeysPerLane
+                   // keys are overwritten in place by their keys
+  uint32_t* bits;  // kept bits of the head chunk's rows, [nbh][Tq][W]
   int bh0, nbh;
   int tq_pad, tk_pad;
+  int W;           // 32-bit words per row: ceil(Tk / 32)
 };
 
-// One warp per row: softmax of the pooled scores in fp32 (exponentials by the ex2
-// instruction, one correctly rounded reciprocal of the row sum), the hybrid selection (the
-// walk, or the bisection for long walks and long rows), and the emit of the ascending kept
-// indices, the u8 mask and, when asked, P-bar.
-constexpr int kSelectWarps = kSelectThreads / 32;
-constexpr int kSelectSmem = kSelectWarps * 2 * kRegKeys * 32 * 4;  // 80 KB
-
-__global__ void __launch_bounds__(kSelectThreads, 2) select_kernel(ShapeArgs s, SelectArgs sel, SelArgs a,
-                                                                   MaskOut out) {
-  // per warp: the sorted keys of the walk, and the keys in index order for the emit
-  extern __shared__ __align__(16) uint32_t sel_smem[];
-  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  uint32_t* walk_col = sel_smem + wib * (2 * kRegKeys * 32);
-  uint32_t* row_keys = walk_col + kRegKeys * 32;
-  const long long gw = (long long)blockIdx.x * kSelectWarps + wib;
-  if (gw >= (long long)a.nbh * s.Tq) return;  // whole warps only
-  const int z = (int)(gw / s.Tq), i = (int)(gw - (long long)z * s.Tq);
-  const int Tk = s.Tk;
-  float* row = a.sbar + ((size_t)z * a.tq_pad + i) * a.tk_pad;
-  const int64_t rowid = (int64_t)(a.bh0 + z) * s.Tq + i;
-  const bool in_regs = Tk <= 32 * kRegKeys;
-
-  // row softmax
-  float mx = -INFINITY, inv = 0.f;
-  uint32_t k[kRegKeys];
-  if (in_regs) {
-    float v[kRegKeys];
-#pragma unroll
-    for (int t = 0; t < kRegKeys; ++t) {
-      const int j = lane + 32 * t;
-      v[t] = j < Tk ? row[j] : -INFINITY;
-      mx = fmaxf(mx, v[t]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int t = 0; t < kRegKeys; ++t) {
-      v[t] = lane + 32 * t < Tk ? ex2_approx((v[t] - mx) * kLog2e) : 0.f;
-      if (t & 1)
-        s1 += v[t];
-      else
-        s0 += v[t];
-    }
-    float sum = s0 + s1;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    inv = __frcp_rn(sum);
-#pragma unroll
-    for (int t = 0; t < kRegKeys; ++t) {
-      k[t] = lane + 32 * t < Tk ? __float_as_uint(v[t] * inv) : 0u;
-      row_keys[t * 32 + lane] = k[t];  // entry lane + 32 t: the emit reads these keys
-    }
-    __syncwarp();
-  } else {
-    for (int j = lane; j < Tk; j += 32) mx = fmaxf(mx, row[j]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float sum = 0.f;
-    for (int j = lane; j < Tk; j += 32) sum += ex2_approx((row[j] - mx) * kLog2e);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    inv = __frcp_rn(sum);
-    __syncwarp();
-    for (int j = lane; j < Tk; j += 32) row[j] = ex2_approx((row[j] - mx) * kLog2e) * inv;
-    __syncwarp();
-  }
-  const uint32_t* mkeys = reinterpret_cast<const uint32_t*>(row);
-
-  // selection: keep every key > t, and the first `take` keys == t (ascending index);
-  // keep_all / keep_none cover K >= Tk, p >= 1, and K = 0 with p <= 0
-  bool keep_all = sel.K >= Tk || sel.p_mode == 2;
-  const bool keep_none = !keep_all && sel.K == 0 && sel.p_mode == 1;
-  uint32_t t = 0;
-  int take = 0;
-  if (!keep_all && !keep_none) {
-    if (in_regs) {
-      // the row's mass may never reach p (rounding): then every block is kept
-      if (sel.p_mode == 0) {
-        uint32_t c31[kRegKeys];
-#pragma unroll
-        for (int q = 0; q < kRegKeys; ++q) c31[q] = (uint32_t)(mass_fix(k[q]) >> 29);
-        keep_all = !mass_at_least(k, c31, 1u, false, 32u * kRegKeys, sel.p_fix);
-      }
-      if (!keep_all && !select_by_walk(k, walk_col, sel, t, take))
-        select_in_registers(k, sel, keep_all, t, take);
-    } else {
-      select_in_memory(mkeys, Tk, sel, keep_all, t, take);
-    }
-  }
-  // emit: ascending kept indices (ballot-compacted), the u8 mask and P-bar, from the very keys
-  // the selection used (entry j = j0 + lane is key j0 / 32 of the lane)
+// Writes a row's outputs from its keys in the permuted order (one 16-byte read per lane per
+// 128-entry chunk): for each quarter i of the chunk the 32 lanes hold 32 consecutive entries,
+// so one ballot gives the kept bits of a 32-entry word and compacts the ascending kept
+// indices; the u8 mask and P-bar (when asked) are written entry by entry.
+__device__ __forceinline__ void emit_row(const uint4* keys4, int Tk, const MaskOut& out, int64_t rowid,
+                                         uint32_t* bits_row, int W, bool keep_all, bool keep_none, bool tie_order,
+                                         uint32_t t, int take) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
   int kept = 0, ties_seen = 0;
   int32_t* ridx = out.row_idx + rowid * Tk;
   uint8_t* mrow = out.mask + rowid * Tk;
   float* prow = out.pooled_p ? out.pooled_p + rowid * Tk : nullptr;
-  const unsigned lt = (1u << lane) - 1u;
-  for (int j0 = 0; j0 < Tk; j0 += 32) {
-    const int j = j0 + lane;
-    const bool valid = j < Tk;
-    const uint32_t key = !valid ? 0u : (in_regs ? row_keys[j0 + lane] : mkeys[j]);
-    bool keep;
-    if (keep_all)
-      keep = valid;
-    else if (keep_none)
-      keep = false;
-    else {
-      const bool eq = valid && key == t;
-      const unsigned eqm = __ballot_sync(0xffffffffu, eq);
-      const int tie_rank = ties_seen + __popc(eqm & lt);
-      ties_seen += __popc(eqm);
-      keep = valid && (key > t || (eq && tie_rank < take));
-    }
-    const unsigned km = __ballot_sync(0xffffffffu, keep);
-    if (keep) ridx[kept + __popc(km & lt)] = j;
-    kept += __popc(km);
-    if (valid) {
-      mrow[j] = keep ? 1 : 0;
-      if (prow) prow[j] = __uint_as_float(key);
+  const int nch = (Tk + 127) / 128;
+  for (int c = 0; c < nch; ++c) {
+    const uint4 kv = keys4[c * 32 + lane];
+    const uint32_t key[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = c * 128 + 32 * i + lane;
+      const bool valid = j < Tk;
+      bool keep;
+      if (keep_all || keep_none || !tie_order) {
+        keep = valid && (keep_all || (!keep_none && key[i] >= t));
+      } else {  // only `take` of the keys == t, in ascending index order
+        const bool eq = valid && key[i] == t;
+        const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+        keep = valid && (key[i] > t || (eq && ties_seen + __popc(eqm & lt) < take));
+        ties_seen += __popc(eqm);
+      }
+      const unsigned km = __ballot_sync(0xffffffffu, keep);
+      if (keep) ridx[kept + __popc(km & lt)] = j;
+      kept += __popc(km);
+      if (lane == 0 && 4 * c + i < W) bits_row[4 * c + i] = km;
+      if (valid) {
+        mrow[j] = keep ? 1 : 0;
+        if (prow) prow[j] = __uint_as_float(key[i]);
+      }
     }
   }
   if (lane == 0) out.row_cnt[rowid] = kept;
 }
 
-// Column lists from the u8 mask.  A CTA takes 32 consecutive key blocks of one head (lane =
-// key block) and its 8 warps split the query blocks into ranges: each warp reads its rows'
-// 32-byte segments (coalesced, 32 loads in flight), keeps the kept-bits of its lane's column
-// in shared memory, then the per-warp counts are prefix-summed and every lane writes its
-// column's query blocks in ascending order.  blockIdx.y is the head within [bh0, ...).
+// Rows of up to 32 * KPL keys: one warp per row, the warps of the grid striding over the
+// rows of the head chunk.  Row softmax in fp32 (exponentials by the ex2 instruction, one
+// correctly rounded reciprocal of the row sum), the selection by sorting (the bisection
+// where that cannot decide), and the emit from the keys parked in shared memory.
+constexpr int kSelectWarps = kSelectThreads / 32;
+constexpr int kMaxKeysPerLane = 40;
+
+template <int KPL>
+constexpr int select_smem_bytes() {
+  return kSelectWarps * KPL * 32 * 4;
+}
+
+template <int KPL>
+__global__ void __launch_bounds__(kSelectThreads, KPL >= 16 ? 3 : 4)
+    select_kernel(ShapeArgs s, SelectArgs sel, SelArgs a, MaskOut out) {
+  extern __shared__ __align__(16) uint4 sel_smem4[];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  uint4* row_keys = sel_smem4 + wib * (KPL / 4) * 32;
+  const int Tk = s.Tk;
+  const long long rows = (long long)a.nbh * s.Tq;
+  const long long nwarps = (long long)gridDim.x * kSelectWarps;
+  for (long long gw = (long long)blockIdx.x * kSelectWarps + wib; gw < rows; gw += nwarps) {
+    const int z = (int)(gw / s.Tq), i = (int)(gw - (long long)z * s.Tq);
+    const float4* row4 = reinterpret_cast<const float4*>(a.sbar + ((size_t)z * a.tq_pad + i) * a.tk_pad);
+    const int64_t rowid = (int64_t)(a.bh0 + z) * s.Tq + i;
+    uint32_t k[KPL];
+    {
+      float v[KPL];
+#pragma unroll
+      for (int c = 0; c < KPL / 4; ++c) {
+        const float4 x = row4[c * 32 + lane];
+        v[4 * c] = x.x;
+        v[4 * c + 1] = x.y;
+        v[4 * c + 2] = x.z;
+        v[4 * c + 3] = x.w;
+      }
+      float mx = v[0];
+#pragma unroll
+      for (int r = 1; r < KPL; ++r) mx = fmaxf(mx, v[r]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int r = 0; r < KPL; ++r) {
+        v[r] = ex2_approx((v[r] - mx) * kLog2e);  // -inf padding: 0
+        if (r & 1)
+          s1 += v[r];
+        else
+          s0 += v[r];
+      }
+      float sum = s0 + s1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      const float inv = __frcp_rn(sum);
+#pragma unroll
+      for (int r = 0; r < KPL; ++r) k[r] = __float_as_uint(v[r] * inv);
+#pragma unroll
+      for (int c = 0; c < KPL / 4; ++c)
+        row_keys[c * 32 + lane] = make_uint4(k[4 * c], k[4 * c + 1], k[4 * c + 2], k[4 * c + 3]);
+    }
+    __syncwarp();
+    // keep_all / keep_none cover K >= Tk, p >= 1, and K = 0 with p <= 0
+    bool keep_all = sel.K >= Tk || sel.p_mode == 2;
+    const bool keep_none = !keep_all && sel.K == 0 && sel.p_mode == 1;
+    uint32_t t = 0;
+    int take = 0, n_eq = 0;
+    if (!keep_all && !keep_none && !select_by_sort<KPL, 8>(k, sel, t, take, n_eq)) {
+      bool done = false;
+      if constexpr (KPL > 8) {  // the 16 largest keys of every lane
+#pragma unroll
+        for (int c = 0; c < KPL / 4; ++c) {
+          const uint4 x = row_keys[c * 32 + lane];
+          k[4 * c] = x.x;
+          k[4 * c + 1] = x.y;
+          k[4 * c + 2] = x.z;
+          k[4 * c + 3] = x.w;
+        }
+        done = select_by_sort<KPL, 16>(k, sel, t, take, n_eq);
+      }
+      if (!done)
+        select_in_memory(reinterpret_cast<const uint32_t*>(row_keys), 32 * KPL, sel, keep_all, t, take, n_eq);
+    }
+    emit_row(row_keys, Tk, out, rowid, a.bits + ((size_t)z * s.Tq + i) * a.W, a.W, keep_all, keep_none, take < n_eq,
+             t, take);
+    __syncwarp();
+  }
+}
+
+// Rows longer than 32 * kMaxKeysPerLane keys: the softmax overwrites the scratch row with
+// its keys (same permuted positions), the bisection runs over memory.
+__global__ void __launch_bounds__(kSelectThreads) select_mem_kernel(ShapeArgs s, SelectArgs sel, SelArgs a,
+                                                                    MaskOut out) {
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int Tk = s.Tk, n = a.tk_pad;
+  const long long rows = (long long)a.nbh * s.Tq;
+  const long long nwarps = (long long)gridDim.x * kSelectWarps;
+  for (long long gw = (long long)blockIdx.x * kSelectWarps + wib; gw < rows; gw += nwarps) {
+    const int z = (int)(gw / s.Tq), i = (int)(gw - (long long)z * s.Tq);
+    float* row = a.sbar + ((size_t)z * a.tq_pad + i) * a.tk_pad;
+    const int64_t rowid = (int64_t)(a.bh0 + z) * s.Tq + i;
+    float mx = -INFINITY;
+    for (int j = lane; j < n; j += 32) mx = fmaxf(mx, row[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sum = 0.f;
+    for (int j = lane; j < n; j += 32) sum += ex2_approx((row[j] - mx) * kLog2e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float inv = __frcp_rn(sum);
+    __syncwarp();
+    for (int j = lane; j < n; j += 32) row[j] = ex2_approx((row[j] - mx) * kLog2e) * inv;
+    __syncwarp();
+    const uint32_t* keys = reinterpret_cast<const uint32_t*>(row);
+    bool keep_all = sel.K >= Tk || sel.p_mode == 2;
+    const bool keep_none = !keep_all && sel.K == 0 && sel.p_mode == 1;
+    uint32_t t = 0;
+    int take = 0, n_eq = 0;
+    if (!keep_all && !keep_none) select_in_memory(keys, n, sel, keep_all, t, take, n_eq);
+    emit_row(reinterpret_cast<const uint4*>(row), Tk, out, rowid, a.bits + ((size_t)z * s.Tq + i) * a.W, a.W,
+             keep_all, keep_none, take < n_eq, t, take);
+    __syncwarp();
+  }
+}
+
+// Column lists from the rows' kept bits.  A CTA takes one 32-bit word of the rows (32
+// consecutive key blocks, lane = key block) of one head, and its 8 warps split the query
+// blocks into ranges: per 32 rows a warp loads one word per row (lane = row) and transposes
+// the 32 x 32 bit block with ballots, so that lane j holds its column's kept bits; the per-warp
+// counts are then prefix-summed and every lane writes its column's query blocks in ascending
+// order.  blockIdx.y is the head within the chunk.
 constexpr int kCscWarps = 8;
 constexpr int kCscMaxWords = 30;  // Tq <= 7680 (bq >= 64, N <= 7680 * 64): 960 rows per warp
 
-__global__ void __launch_bounds__(32 * kCscWarps) csc_kernel(ShapeArgs s, int bh0, const uint8_t* __restrict__ mask,
+__global__ void __launch_bounds__(32 * kCscWarps) csc_kernel(ShapeArgs s, int bh0, int W,
+                                                             const uint32_t* __restrict__ bits,
                                                              int32_t* __restrict__ col_cnt,
                                                              int32_t* __restrict__ col_idx) {
-  __shared__ uint32_t bits[kCscWarps][kCscMaxWords][32];
+  __shared__ uint32_t cbits[kCscWarps][kCscMaxWords][32];
   __shared__ int cnt[kCscWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = bh0 + blockIdx.y;
+  const int z = blockIdx.y, bh = bh0 + z;
   const int j = blockIdx.x * 32 + lane;
-  const bool col_ok = j < s.Tk;
   const int R = (s.Tq + kCscWarps - 1) / kCscWarps;  // rows per warp (<= 32 * kCscMaxWords)
   const int i0 = warp * R, i1 = min(s.Tq, i0 + R);
-  const uint8_t* m = mask + (int64_t)bh * s.Tq * s.Tk + min(j, s.Tk - 1);
+  const uint32_t* b = bits + (size_t)z * s.Tq * W + blockIdx.x;
   int c = 0;
-  for (int w = 0; w * 32 < R; ++w) {
-    uint8_t v[32];
+  for (int g = 0; g * 32 < R; ++g) {
+    const int i = i0 + g * 32 + lane;
+    const uint32_t word = i < i1 ? b[(size_t)i * W] : 0u;
+    uint32_t mine = 0;
 #pragma unroll
-    for (int b = 0; b < 32; ++b) v[b] = m[(int64_t)min(i0 + w * 32 + b, s.Tq - 1) * s.Tk];
-    uint32_t word = 0;
-#pragma unroll
-    for (int b = 0; b < 32; ++b)
-      if (v[b] && i0 + w * 32 + b < i1) word |= 1u << b;
-    if (!col_ok) word = 0;
-    bits[warp][w][lane] = word;
-    c += __popc(word);
+    for (int q = 0; q < 32; ++q) {
+      const unsigned m = __ballot_sync(0xffffffffu, (word >> q) & 1u);
+      mine = lane == q ? m : mine;
+    }
+    cbits[warp][g][lane] = mine;  // bit r: query block i0 + 32 g + r keeps key block j
+    c += __popc(mine);
   }
   cnt[warp][lane] = c;
   __syncthreads();
@@ -788,14 +897,14 @@ __global__ void __launch_bounds__(32 * kCscWarps) csc_kernel(ShapeArgs s, int bh
     if (q < warp) base += cnt[q][lane];
     total += cnt[q][lane];
   }
-  if (!col_ok) return;
-  int32_t* out = col_idx + ((int64_t)bh * s.Tk + j) * s.Tq + base;
-  for (int w = 0; w * 32 < R; ++w) {
-    uint32_t word = bits[warp][w][lane];
+  if (j >= s.Tk) return;
+  int32_t* o = col_idx + ((int64_t)bh * s.Tk + j) * s.Tq + base;
+  for (int g = 0; g * 32 < R; ++g) {
+    uint32_t word = cbits[warp][g][lane];
     while (word) {
-      const int b = __ffs(word) - 1;
+      const int q = __ffs(word) - 1;
       word &= word - 1;
-      *out++ = i0 + w * 32 + b;
+      *o++ = i0 + g * 32 + q;
     }
   }
   if (warp == 0) col_cnt[(int64_t)bh * s.Tk + j] = total;
@@ -833,31 +942,41 @@ bool make_pooled_map(CUtensorMap* map, const float* base, const ShapeArgs& s, in
 }
 
 struct MaskLayout {
-  size_t qbar, kbar, sbar, total;
-  int tq_pad, tk_pad, hc;  // padded tile extents; heads per score chunk
+  size_t qbar, kbar, sbar, bits, total;
+  size_t sbar_buf, bits_buf;  // bytes of one buffer of each
+  int tq_pad, tk_pad, hc;     // padded tile extents; heads per chunk
+  int W;                      // 32-bit words of kept bits per row
 };
 
-MaskLayout mask_layout(const ShapeArgs& s, size_t sbar_budget) {
+// The pooled pairs of all heads, then two buffers (for two head chunks in flight) of the
+// chunk's score tiles and of its rows' kept bits.  chunk_budget bounds the bytes of both
+// buffers together; a chunk holds at least one head.
+MaskLayout mask_layout(const ShapeArgs& s, size_t chunk_budget) {
   MaskLayout L;
   const size_t BH = (size_t)s.B * s.H;
   auto al = [](size_t x) { return (x + 1023) / 1024 * 1024; };
   L.tq_pad = (s.Tq + kScoreRows - 1) / kScoreRows * kScoreRows;
   L.tk_pad = (s.Tk + kScoreKeys - 1) / kScoreKeys * kScoreKeys;
-  const size_t per_head = (size_t)L.tq_pad * L.tk_pad * 4;
-  L.hc = (int)std::max<size_t>(1, std::min<size_t>(BH, sbar_budget / per_head));
+  L.W = (s.Tk + 31) / 32;
+  const size_t tile_head = (size_t)L.tq_pad * L.tk_pad * 4, bits_head = (size_t)s.Tq * L.W * 4;
+  L.hc = (int)std::max<size_t>(1, std::min<size_t>(BH, chunk_budget / (2 * (tile_head + bits_head) + 4096)));
+  L.sbar_buf = al((size_t)L.hc * tile_head);
+  L.bits_buf = al((size_t)L.hc * bits_head);
   L.qbar = 0;
   L.kbar = al(2 * BH * s.Tq * s.d * 4);
   L.sbar = L.kbar + al(2 * BH * s.Tk * s.d * 4);
-  L.total = L.sbar + al((size_t)L.hc * per_head);
+  L.bits = L.sbar + 2 * L.sbar_buf;
+  L.total = L.bits + 2 * L.bits_buf;
   return L;
 }
 
-// A second stream per device on which the scores, the selection and the column lists of a
-// chunk of heads run while the caller's stream pools the next chunk; the caller's stream
-// waits for it at the end of the call.  Set up on the first build on a device.
+// Two more streams per device, of the highest priority.  The scores, the selection and the
+// column lists of head chunk c run on stream c % 2 (with buffer c % 2) while the caller's
+// stream pools the next chunks, so that the chains of two chunks overlap; the caller's
+// stream waits for both at the end of the call.  Set up on the first build on a device.
 struct AuxStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t pooled = nullptr, done = nullptr;
+  cudaStream_t stream[2] = {nullptr, nullptr};
+  cudaEvent_t pooled = nullptr, done[2] = {nullptr, nullptr};
   cudaError_t err = cudaSuccess;
   std::mutex mu;  // one enqueue sequence at a time per device
 };
@@ -869,9 +988,15 @@ AuxStream* aux_stream(int dev) {
   if (dev < 0 || dev >= kMaxAuxDevices) return nullptr;
   std::call_once(g_aux_once[dev], [dev]() {
     AuxStream& a = g_aux[dev];
-    a.err = cudaStreamCreateWithFlags(&a.stream, cudaStreamNonBlocking);
+    // the chains are latency-bound and the pooling streams in the background: the chains'
+    // blocks go first where both wait for an SM
+    int lo = 0, hi = 0;
+    a.err = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    for (int i = 0; i < 2 && a.err == cudaSuccess; ++i) {
+      a.err = cudaStreamCreateWithPriority(&a.stream[i], cudaStreamNonBlocking, hi);
+      if (a.err == cudaSuccess) a.err = cudaEventCreateWithFlags(&a.done[i], cudaEventDisableTiming);
+    }
     if (a.err == cudaSuccess) a.err = cudaEventCreateWithFlags(&a.pooled, cudaEventDisableTiming);
-    if (a.err == cudaSuccess) a.err = cudaEventCreateWithFlags(&a.done, cudaEventDisableTiming);
   });
   return g_aux[dev].err == cudaSuccess ? &g_aux[dev] : nullptr;
 }
@@ -897,7 +1022,9 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
   uint8_t* base = static_cast<uint8_t*>(scratch);
   float* qbar = reinterpret_cast<float*>(base + L.qbar);
   float* kbar = reinterpret_cast<float*>(base + L.kbar);
-  float* sbar = reinterpret_cast<float*>(base + L.sbar);
+  float* sbar_buf[2] = {reinterpret_cast<float*>(base + L.sbar), reinterpret_cast<float*>(base + L.sbar + L.sbar_buf)};
+  uint32_t* bits_buf[2] = {reinterpret_cast<uint32_t*>(base + L.bits),
+                           reinterpret_cast<uint32_t*>(base + L.bits + L.bits_buf)};
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -910,7 +1037,33 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
     return cudaErrorInvalidValue;
   auto score = s.d == 128 ? score_tc_kernel<128> : score_tc_kernel<64>;
   e = cudaFuncSetAttribute(score, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelectSmem);
+  // the selection: keys per lane by row length, or the rows in memory
+  const void* select = nullptr;
+  int sel_smem = 0;
+  auto pick = [&](auto kernel, int bytes) {
+    select = (const void*)kernel;
+    sel_smem = bytes;
+  };
+  if (s.Tk <= 128)
+    pick(select_kernel<4>, select_smem_bytes<4>());
+  else if (s.Tk <= 256)
+    pick(select_kernel<8>, select_smem_bytes<8>());
+  else if (s.Tk <= 512)
+    pick(select_kernel<16>, select_smem_bytes<16>());
+  else if (s.Tk <= 768)
+    pick(select_kernel<24>, select_smem_bytes<24>());
+  else if (s.Tk <= 1024)
+    pick(select_kernel<32>, select_smem_bytes<32>());
+  else if (s.Tk <= 32 * kMaxKeysPerLane)
+    pick(select_kernel<kMaxKeysPerLane>, select_smem_bytes<kMaxKeysPerLane>());
+  else
+    pick(select_mem_kernel, 0);
+  // a register row reads 32 * (keys per lane) entries of its scratch row: never past tk_pad
+  if (sel_smem > 0 && sel_smem / (kSelectWarps * 4) > L.tk_pad) return cudaErrorInvalidValue;
+  if (e == cudaSuccess && sel_smem > 0)
+    e = cudaFuncSetAttribute(select, cudaFuncAttributeMaxDynamicSharedMemorySize, sel_smem);
+  int sel_occ = 0;
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sel_occ, select, kSelectThreads, sel_smem);
   if (e != cudaSuccess) return e;
   const void* pool = s.dtype == 0
                          ? (s.d == 128 ? (const void*)pool_kernel<__nv_bfloat16, 128> : (const void*)pool_kernel<__nv_bfloat16, 64>)
@@ -925,8 +1078,10 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
   std::lock_guard<std::mutex> lock(aux->mu);
   const int BH = s.B * s.H;
   const int nc = (s.N + kChunkTokens - 1) / kChunkTokens;
-  for (int bh0 = 0; bh0 < BH; bh0 += L.hc) {
+  for (int bh0 = 0, ci = 0; bh0 < BH; bh0 += L.hc, ++ci) {
     const int nbh = std::min(L.hc, BH - bh0);
+    float* sbar = sbar_buf[ci & 1];
+    uint32_t* bits = bits_buf[ci & 1];
     // ---- pooling of the chunk, on the caller's stream
     PoolArgs pa;
     pa.qbar = qbar;
@@ -954,10 +1109,10 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
     prof_stop(st, kPool);
     e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaEventRecord(aux->pooled, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux->stream, aux->pooled, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux->stream[ci & 1], aux->pooled, 0);
     if (e != cudaSuccess) return e;
     // ---- scores, selection and column lists of the chunk, on the second stream
-    cudaStream_t st2 = aux->stream;
+    cudaStream_t st2 = aux->stream[ci & 1];
     ScoreArgs sa;
     sa.sbar = sbar;
     sa.bh0 = bh0;
@@ -974,26 +1129,36 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
     if (e != cudaSuccess) return e;
     SelArgs ca;
     ca.sbar = sbar;
+    ca.bits = bits;
     ca.bh0 = bh0;
     ca.nbh = nbh;
     ca.tq_pad = L.tq_pad;
     ca.tk_pad = L.tk_pad;
+    ca.W = L.W;
     const long long rows = (long long)nbh * s.Tq;
+    const int sgrid = (int)std::min<long long>((rows + kSelectWarps - 1) / kSelectWarps,
+                                               (long long)sms * std::max(1, sel_occ));
     prof_start(st2, kScoreSelect);
-    select_kernel<<<(unsigned)((rows + kSelectWarps - 1) / kSelectWarps), kSelectThreads, kSelectSmem, st2>>>(
-        s, sel, ca, out);
+    {
+      SelectArgs sl = sel;
+      MaskOut mo = out;
+      void* args[] = {(void*)&s, (void*)&sl, (void*)&ca, (void*)&mo};
+      e = cudaLaunchKernel(select, dim3(sgrid), dim3(kSelectThreads), args, (size_t)sel_smem, st2);
+    }
     prof_stop(st2, kScoreSelect);
-    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dim3 cgrid((s.Tk + 31) / 32, nbh);
+    dim3 cgrid(L.W, nbh);
     prof_start(st2, kCsc);
-    csc_kernel<<<cgrid, 32 * kCscWarps, 0, st2>>>(s, bh0, out.mask, out.col_cnt, out.col_idx);
+    csc_kernel<<<cgrid, 32 * kCscWarps, 0, st2>>>(s, bh0, L.W, bits, out.col_cnt, out.col_idx);
     prof_stop(st2, kCsc);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  e = cudaEventRecord(aux->done, aux->stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, aux->done, 0);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+    e = cudaEventRecord(aux->done[i], aux->stream[i]);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, aux->done[i], 0);
+  }
   return e;
 }
 
