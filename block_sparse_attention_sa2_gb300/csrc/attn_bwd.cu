@@ -57,7 +57,6 @@ namespace {
 
 constexpr int kThreads = 352;
 constexpr int kItemReaders = 10;  // warps reading the item slot: 1, 2 and the 8 element-wise warps
-constexpr int kStages = 4;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns
 constexpr uint32_t kColS = 0;     // 64: S^T
@@ -67,16 +66,24 @@ constexpr uint32_t kColDS = 192;  // 2 x 32: dS^T, fp16 pairs
 constexpr uint32_t kColDV = 256;  // 128
 constexpr uint32_t kColDK = 384;  // 128
 
-// shared memory (bytes from the 1024-aligned base)
-constexpr int kOffK = 0;         // 128 key rows x 2 channel panels of 128 B (panel = 16 KB)
-constexpr int kOffV = 32768;
-constexpr int kOffStage = 65536;  // stage: Q (2 panels x 64 rows x 128 B), dO (same), stats
-constexpr int kStageQ = 0, kStageDO = 16384, kStageStats = 32768;
-constexpr int kStageBytes = 33792;
-constexpr uint32_t kStageTx = 2 * 16384 + 512;
-constexpr int kOffBar = kOffStage + kStages * kStageBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
-static_assert(kSmemBytes <= (int)kMaxDynSmem, "shared memory");
+// Shared memory (bytes from the 1024-aligned base).  SPLIT (fp32 calls): K and Q also as
+// fp16 residuals lo = fp16(x - hi) for the split product S^T = Khi Qhi^T + Khi Qlo^T +
+// Klo Qhi^T, with a 2-deep sub-tile ring to fit.
+template <bool SPLIT>
+struct DkdvSmem {
+  static constexpr int kStages = SPLIT ? 2 : 4;
+  static constexpr int kShift = SPLIT ? 1 : 2;  // log2(kStages)
+  static constexpr int kOffK = 0;               // 128 key rows x 2 channel panels of 128 B (panel = 16 KB)
+  static constexpr int kOffKlo = 32768;         // (SPLIT)
+  static constexpr int kOffV = SPLIT ? 65536 : 32768;
+  static constexpr int kOffStage = kOffV + 32768;  // stage: Q (2 panels x 64 rows x 128 B), dO (same), stats
+  static constexpr int kStageQ = 0, kStageDO = 16384, kStageStats = 32768, kStageQlo = 33792;
+  static constexpr int kStageBytes = SPLIT ? 33792 + 16384 : 33792;
+  static constexpr uint32_t kStageTx = (SPLIT ? 3 : 2) * 16384 + 512;
+  static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static_assert(kSmemBytes <= (int)kMaxDynSmem, "shared memory");
+};
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -130,11 +137,18 @@ __device__ __forceinline__ void zero_row64(GT* p) {
   for (int c = 0; c < 64 / kVec; ++c) *reinterpret_cast<uint4*>(p + kVec * c) = make_uint4(0, 0, 0, 0);
 }
 
-template <typename GT>
+template <typename GT, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+                         const __grid_constant__ CUtensorMap mql, const __grid_constant__ CUtensorMap mkl,
                          ShapeArgs s, BwdArgs a) {
+  using L = DkdvSmem<SPLIT>;
+  constexpr int kStages = L::kStages, kStShift = L::kShift;
+  constexpr int kOffK = L::kOffK, kOffKlo = L::kOffKlo, kOffV = L::kOffV, kOffStage = L::kOffStage;
+  constexpr int kStageQ = L::kStageQ, kStageDO = L::kStageDO, kStageStats = L::kStageStats, kStageQlo = L::kStageQlo;
+  constexpr int kStageBytes = L::kStageBytes, kOffBar = L::kOffBar;
+  constexpr uint32_t kStageTx = L::kStageTx;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -258,10 +272,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar_kv, 65536);
+          mbar_arrive_expect_tx(bar_kv, SPLIT ? 3 * 32768 : 65536);
           for (int p = 0; p < 2; ++p)
             for (int r = 0; r < 2; ++r) {
               tma_load_4d(sbase + kOffK + p * 16384 + r * 8192, &mk, bar_kv, p * 64, m * 128 + r * 64, h, b);
+              if constexpr (SPLIT)
+                tma_load_4d(sbase + kOffKlo + p * 16384 + r * 8192, &mkl, bar_kv, p * 64, m * 128 + r * 64, h, b);
               tma_load_4d(sbase + kOffV + p * 16384 + r * 8192, &mv, bar_kv, p * 64, m * 128 + r * 64, h, b);
             }
         }
@@ -277,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int st = U & (kStages - 1);
           if (U >= kStages &&
-              !__all_sync(0xffffffffu, mbar_wait(bar_empty(st), ((U >> 2) - 1) & 1, wc))) {
+              !__all_sync(0xffffffffu, mbar_wait(bar_empty(st), ((U >> kStShift) - 1) & 1, wc))) {
             ok = false;
             break;
           }
@@ -287,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar_full(st), kStageTx);
             for (int p = 0; p < 2; ++p) {
               tma_load_4d(stg + kStageQ + p * 8192, &mq, bar_full(st), p * 64, row * 64, h, b);
+              if constexpr (SPLIT) tma_load_4d(stg + kStageQlo + p * 8192, &mql, bar_full(st), p * 64, row * 64, h, b);
               tma_load_4d(stg + kStageDO + p * 8192, &mdo, bar_full(st), p * 64, row * 64, h, b);
             }
             bulk_load(stg + kStageStats, a.stats + ((int64_t)bh * Tsub + row) * 128, 512, bar_full(st));
@@ -301,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // last K / V load (each is its barrier's latest phase).
     if (lane == 0) {
       for (uint32_t v = U > kStages ? U - kStages : 0; v < U; ++v)
-        mbar_drain(bar_full(v & (kStages - 1)), (v >> 2) & 1, abort_flag);
+        mbar_drain(bar_full(v & (kStages - 1)), (v >> kStShift) & 1, abort_flag);
       if (kvn > 0) mbar_drain(bar_kv, (kvn - 1) & 1, abort_flag);
     }
   } else if (warp == 1) {
@@ -327,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < nsub; ++u, ++U) {
         const int st = U & (kStages - 1);
         // the stage landed, and S^T / dP^T of sub-tile U - 1 were read out of TMEM
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (U >> 2) & 1, wc) &&
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (U >> kStShift) & 1, wc) &&
                                          (U == 0 || mbar_wait(bar_sfree, (U - 1) & 1, wc)))) {
           ok = false;
           break;
@@ -337,6 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t qd = smem_desc(stg + kStageQ, 16, 1024), dod = smem_desc(stg + kStageDO, 16, 1024);
         if (elect_one()) {
           mma_ss_kmajor<idS, 128, 64, 8>(tmem + kColS, kd, qd);
+          if constexpr (SPLIT) {
+            const uint64_t kld = smem_desc(sbase + kOffKlo, 16, 1024), qld = smem_desc(stg + kStageQlo, 16, 1024);
+            mma_ss_kmajor_acc<idS, 128, 64, 8>(tmem + kColS, kd, qld);
+            mma_ss_kmajor_acc<idS, 128, 64, 8>(tmem + kColS, kld, qd);
+          }
           mma_ss_kmajor<idS, 128, 64, 8>(tmem + kColDP, vd, dod);
           umma_commit(bar_sfull);
         }
@@ -366,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // accumulators after the previous pair's epilogue: every element-wise thread read
         // them out before it wrote this P^T / dS^T.
         if (!__all_sync(0xffffffffu, mbar_wait(bar_pready(bb), (W >> 1) & 1, wc) &&
-                                         mbar_wait(bar_full(st), (W >> 2) & 1, wc))) {
+                                         mbar_wait(bar_full(st), (W >> kStShift) & 1, wc))) {
           ok = false;
           break;
         }
@@ -423,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool keep = ((e >> (30 + half)) & 1u) != 0;  // same for the whole warp
         const int st = U & (kStages - 1), bb = U & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull, U & 1, wc) &&
-                                         mbar_wait(bar_full(st), (U >> 2) & 1, wc))) {
+                                         mbar_wait(bar_full(st), (U >> kStShift) & 1, wc))) {
           ok = false;
           break;
         }
@@ -584,9 +606,11 @@ __global__ void __launch_bounds__(32 * kUnionWarps) pair_union_kernel(const int3
   if (bad) report_error(status, kDevErrBounds);
 }
 
-template <typename GT>
+template <typename GT, bool SPLIT>
 cudaError_t launch_bwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st) {
+                         const CUtensorMap& mdo, const CUtensorMap& mql, const CUtensorMap& mkl, const BwdArgs& a,
+                         cudaStream_t st) {
+  constexpr int kSmemBytes = DkdvSmem<SPLIT>::kSmemBytes;
   const long long pairs = (long long)s.B * s.H * ((s.Tk + 1) / 2);
   prof_start(st, kBwdPairs);
   pair_union_kernel<<<(unsigned)((pairs + kUnionWarps - 1) / kUnionWarps), 32 * kUnionWarps, 0, st>>>(
@@ -594,7 +618,7 @@ cudaError_t launch_bwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtens
   prof_stop(st, kBwdPairs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = attn_bwd_dkdv_kernel<GT>;
+  auto kern = attn_bwd_dkdv_kernel<GT, SPLIT>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -603,7 +627,7 @@ cudaError_t launch_bwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtens
   if (e != cudaSuccess) return e;
   const long long grid = pairs < sms ? pairs : sms;  // persistent: one CTA per SM
   prof_start(st, kAttnBwd);
-  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, s, a);
+  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, mql, mkl, s, a);
   prof_stop(st, kAttnBwd);
   return cudaGetLastError();
 }
@@ -613,10 +637,13 @@ cudaError_t launch_bwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtens
 size_t bwd_pair_entries(const ShapeArgs& s) { return (size_t)s.B * s.H * ((s.Tk + 1) / 2) * s.Tq; }
 
 cudaError_t launch_attn_bwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                            const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st) {
+                            const CUtensorMap& mdo, const CUtensorMap* mql, const CUtensorMap* mkl, const BwdArgs& a,
+                            cudaStream_t st) {
   if (s.Tq > 32 * kMaxTqWords || (long long)s.B * s.H * ((s.Tk + 1) / 2) > INT32_MAX) return cudaErrorInvalidValue;
-  return s.dtype == 0 ? launch_bwd_t<__nv_bfloat16>(s, mq, mk, mv, mdo, a, st)
-                      : launch_bwd_t<float>(s, mq, mk, mv, mdo, a, st);
+  // fp32 calls take the split S product
+  if (s.dtype != 0 && (!mql || !mkl)) return cudaErrorInvalidValue;
+  return s.dtype == 0 ? launch_bwd_t<__nv_bfloat16, false>(s, mq, mk, mv, mdo, mq, mk, a, st)
+                      : launch_bwd_t<float, true>(s, mq, mk, mv, mdo, *mql, *mkl, a, st);
 }
 
 }  // namespace sa2

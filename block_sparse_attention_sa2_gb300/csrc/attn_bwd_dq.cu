@@ -26,7 +26,7 @@
 // writing dS_j, so the tensor pipe never drains to let an MMA overwrite an operand.
 //
 // The CTAs are persistent, one per SM, and take query blocks from a counter until none is
-// left.  The producer publishes each block in a two-slot ring in shared memory that every
+// left, head by head and within a head longest list first.  The producer publishes each block in a two-slot ring in shared memory that every
 // role reads; the K / V rings and the TMEM buffers run on across blocks.  So the set-up is
 // paid once per SM, the next block's K_j / V_j stream in behind the current block's, its
 // Q and dO load as soon as the current block's S_j / dP_j MMAs have completed, and its
@@ -45,15 +45,21 @@ constexpr int kVStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 384;
 
-template <int D>
+// SPLIT (fp32 calls): Q and K also as fp16 residuals lo = fp16(x - hi) for the split S
+// product Qhi Khi^T + Qhi Klo^T + Qlo Khi^T; the K ring is then 2 deep to fit.
+template <int D, bool SPLIT>
 struct DqSmem {
+  static constexpr int kKSt = SPLIT ? 2 : kKStages;  // K ring depth
   static constexpr int kPanels = D / 64;
   static constexpr int kQBytes = 128 * 128 * kPanels;  // 128 rows x 128 B per panel
   static constexpr int kKVBytes = 64 * 128 * kPanels;
+  static constexpr int kParts = SPLIT ? 2 : 1;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffDO = kOffQ + kQBytes;
+  static constexpr int kOffQlo = kOffQ + kQBytes;
+  static constexpr int kOffDO = kOffQ + kParts * kQBytes;
   static constexpr int kOffK = kOffDO + kQBytes;
-  static constexpr int kOffV = kOffK + kKStages * kKVBytes;
+  static constexpr int kOffKlo = kOffK + kKSt * kKVBytes;
+  static constexpr int kOffV = kOffK + kParts * kKSt * kKVBytes;
   static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
   static constexpr int kBytes = kOffBar + 512 + 1024;
 };
@@ -81,12 +87,14 @@ __device__ __forceinline__ void store_chunk<float>(float* dst, const float* v) {
   for (int i = 0; i < 8; ++i) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-template <int D, typename OutT>
+template <int D, typename OutT, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                       const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo, ShapeArgs s,
+                       const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+                       const __grid_constant__ CUtensorMap mql, const __grid_constant__ CUtensorMap mkl, ShapeArgs s,
                        DqArgs a) {
-  using L = DqSmem<D>;
+  using L = DqSmem<D, SPLIT>;
+  constexpr int kKStages = L::kKSt;  // the K ring of this variant
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -113,9 +121,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{abort_flag, s.wait_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Work items are query blocks (item x: block x % Tq of head x / Tq).  Each CTA stays
-  // resident and takes items from a counter: its first is blockIdx.x, the next
-  // gridDim.x + (counter value).
+  // Work items are query blocks (block x: block x % Tq of head x / Tq), taken head by head
+  // and longest first within a head: each CTA stays resident and takes items from a counter
+  // over that order, its first being order[blockIdx.x], the next order[gridDim.x + (counter
+  // value)].
   const int num_items = s.B * s.H * s.Tq;
   // list length of item x, clamped to [0, Tk] (the producer reports a bad value)
   auto item_len = [&](int x, bool report) {
@@ -193,23 +202,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const bool done = x >= num_items;
-        item_slot[slot] = done ? -1 : x;
+        int qb = done ? -1 : a.order[x];
+        if (!done && (qb < 0 || qb >= num_items)) {
+          report_error(a.status, kDevErrBounds);
+          qb = 0;
+        }
+        item_slot[slot] = qb;
         mbar_arrive(bar_item_full(slot));
         if (done) break;
         const int xn = (int)gridDim.x + atomicAdd(a.work_ctr, 1);  // the item after this one
-        const int nkv = item_len(x, true);
+        const int nkv = item_len(qb, true);
         if (nkv > 0) {
-          const int bh = x / s.Tq, qi = x - bh * s.Tq, b = bh / s.H, h = bh - b * s.H;
-          const int32_t* list = a.row_idx + (int64_t)x * s.Tk;
+          const int bh = qb / s.Tq, qi = qb - bh * s.Tq, b = bh / s.H, h = bh - b * s.H;
+          const int32_t* list = a.row_idx + (int64_t)qb * s.Tk;
           // Q, dO of the previous query block are free once its S_j / dP_j MMAs completed
           if (qn >= 1 && !mbar_wait(bar_qfree, (qn - 1) & 1, wc)) {
             ok = false;
             break;
           }
           ++qn;
-          mbar_arrive_expect_tx(bar_q, 2 * L::kQBytes);
+          mbar_arrive_expect_tx(bar_q, (1 + L::kParts) * L::kQBytes);
           for (int p = 0; p < L::kPanels; ++p) {
             tma_load_4d(sbase + L::kOffQ + p * 16384, &mq, bar_q, p * 64, qi * s.bq, h, b);
+            if constexpr (SPLIT) tma_load_4d(sbase + L::kOffQlo + p * 16384, &mql, bar_q, p * 64, qi * s.bq, h, b);
             tma_load_4d(sbase + L::kOffDO + p * 16384, &mdo, bar_q, p * 64, qi * s.bq, h, b);
           }
           for (int j = 0; j < nkv; ++j, ++J) {
@@ -223,10 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(bar_kfull(ks), L::kKVBytes);
-            for (int p = 0; p < L::kPanels; ++p)
+            mbar_arrive_expect_tx(bar_kfull(ks), L::kParts * L::kKVBytes);
+            for (int p = 0; p < L::kPanels; ++p) {
               tma_load_4d(sbase + L::kOffK + ks * L::kKVBytes + p * 8192, &mk, bar_kfull(ks), p * 64, kb * 64, h,
                           b);
+              if constexpr (SPLIT)
+                tma_load_4d(sbase + L::kOffKlo + ks * L::kKVBytes + p * 8192, &mkl, bar_kfull(ks), p * 64, kb * 64,
+                            h, b);
+            }
             ++nk;
             if (J >= kVStages && !mbar_wait(bar_vempty(vs), ((J / kVStages) - 1) & 1, wc)) {
               ok = false;
@@ -282,6 +301,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t vd = smem_desc(sbase + L::kOffV + vs * L::kKVBytes, 16, 1024);
         if (elect_one()) {
           mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qd, kd);
+          if constexpr (SPLIT) {
+            const uint64_t kld = smem_desc(sbase + L::kOffKlo + ks * L::kKVBytes, 16, 1024);
+            const uint64_t qld = smem_desc(sbase + L::kOffQlo, 16, 1024);
+            mma_ss_kmajor_acc<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qd, kld);
+            mma_ss_kmajor_acc<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qld, kd);
+          }
           mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColDP + bb * 64, dod, vd);
           umma_commit(bar_sfull(bb));
           umma_commit(bar_vempty(vs));
@@ -385,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int z = 0; z < 2; ++z) {
             const bool cv = row_valid && (32 * wg + c + z) < kv_valid;
-            const float p = cv ? ex2(__uint_as_float(sv[c + z]) * a.scale_log2 - lse2) : 0.f;
+            const float p = cv ? ex2(fmaf(__uint_as_float(sv[c + z]), a.scale_log2, -lse2)) : 0.f;
             ds[z] = p * (__uint_as_float(dv[c + z]) - Dr);
           }
           pk[c / 2] = pack_f16x2(ds[0], ds[1]);
@@ -442,11 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, typename OutT>
+template <int D, typename OutT, bool SPLIT>
 cudaError_t launch_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                     const CUtensorMap& mdo, const DqArgs& a, cudaStream_t st) {
-  const int smem = DqSmem<D>::kBytes;
-  auto kern = attn_bwd_dq_kernel<D, OutT>;
+                     const CUtensorMap& mdo, const CUtensorMap& mql, const CUtensorMap& mkl, const DqArgs& a,
+                     cudaStream_t st) {
+  const int smem = DqSmem<D, SPLIT>::kBytes;
+  auto kern = attn_bwd_dq_kernel<D, OutT, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -456,21 +482,25 @@ cudaError_t launch_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMa
   const long long items = (long long)s.B * s.H * s.Tq;
   const long long grid = items < sms ? items : sms;  // persistent: one CTA per SM
   prof_start(st, kAttnBwdDq);
-  kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, mdo, s, a);
+  e = launch_item_order(a.row_cnt, s.B * s.H, s.Tq, s.Tk, const_cast<int32_t*>(a.order), a.work_ctr, st);
+  if (e == cudaSuccess) kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, mdo, mql, mkl, s, a);
   prof_stop(st, kAttnBwdDq);
-  return cudaGetLastError();
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_bwd_dq(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk,
-                               const CUtensorMap& mv, const CUtensorMap& mdo, const DqArgs& a, cudaStream_t st) {
+                               const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap* mql,
+                               const CUtensorMap* mkl, const DqArgs& a, cudaStream_t st) {
   if ((long long)s.B * s.H * s.Tq > INT32_MAX) return cudaErrorInvalidValue;
+  // fp32 calls take the split S product
+  if (s.dtype != 0 && (!mql || !mkl)) return cudaErrorInvalidValue;
   if (s.d == 128)
-    return s.dtype == 0 ? launch_t<128, __nv_bfloat16>(s, mq, mk, mv, mdo, a, st)
-                        : launch_t<128, float>(s, mq, mk, mv, mdo, a, st);
-  return s.dtype == 0 ? launch_t<64, __nv_bfloat16>(s, mq, mk, mv, mdo, a, st)
-                      : launch_t<64, float>(s, mq, mk, mv, mdo, a, st);
+    return s.dtype == 0 ? launch_t<128, __nv_bfloat16, false>(s, mq, mk, mv, mdo, mq, mk, a, st)
+                        : launch_t<128, float, true>(s, mq, mk, mv, mdo, *mql, *mkl, a, st);
+  return s.dtype == 0 ? launch_t<64, __nv_bfloat16, false>(s, mq, mk, mv, mdo, mq, mk, a, st)
+                      : launch_t<64, float, true>(s, mq, mk, mv, mdo, *mql, *mkl, a, st);
 }
 
 }  // namespace sa2

@@ -87,9 +87,26 @@ __device__ __forceinline__ uint4 to_f16x8(float* v, bool& bad) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// The low-order part of an fp32 -> fp16 rounding: fp16(v - hi) with hi the (saturated)
+// fp16 value just stored, so that hi + lo carries about 22 significant bits.
+__device__ __forceinline__ uint4 lo_f16x8(const float* v, uint4 hi) {
+  const uint32_t h[4] = {hi.x, hi.y, hi.z, hi.w};
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 hh = *reinterpret_cast<const __half2*>(&h[i]);
+    const float2 f = __half22float2(hh);
+    // finite even for a saturated input (whose error is reported)
+    w[i] = pack_f16x2(fminf(fmaxf(v[2 * i] - f.x, -65504.f), 65504.f),
+                      fminf(fmaxf(v[2 * i + 1] - f.y, -65504.f), 65504.f));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// fp16 copy of a token tensor (and, when dst_lo is not null, of its rounding residual)
 template <typename T, bool CONTIG>
 __global__ void __launch_bounds__(256) to_f16_kernel(const T* __restrict__ src, ShapeArgs s, __half* __restrict__ dst,
-                                                     unsigned* status) {
+                                                     __half* __restrict__ dst_lo, unsigned* status) {
   const int64_t items = (int64_t)s.B * s.H * s.N * s.d / 8;
   const int per_row = s.d / 8;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -102,7 +119,14 @@ __global__ void __launch_bounds__(256) to_f16_kernel(const T* __restrict__ src, 
 #pragma unroll
       for (int u = 0; u < 4; ++u) ld8<T>(src + (i0 + u * stride) * 8, v[u]);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(dst + (i0 + u * stride) * 8) = to_f16x8(v[u], bad);
+      for (int u = 0; u < 4; ++u) {
+        float raw[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) raw[e] = v[u][e];
+        const uint4 hi = to_f16x8(v[u], bad);
+        *reinterpret_cast<uint4*>(dst + (i0 + u * stride) * 8) = hi;
+        if (dst_lo) *reinterpret_cast<uint4*>(dst_lo + (i0 + u * stride) * 8) = lo_f16x8(raw, hi);
+      }
     }
   }
   for (int64_t i = i0; i < items; i += stride) {
@@ -115,9 +139,13 @@ __global__ void __launch_bounds__(256) to_f16_kernel(const T* __restrict__ src, 
       const int n = (int)(row - bh * s.N);
       off = (bh / s.H) * s.sb + (bh % s.H) * s.sh + (int64_t)n * s.sn + c;
     }
-    float v[8];
+    float v[8], raw[8];
     ld8<T>(src + off, v);
-    *reinterpret_cast<uint4*>(dst + e) = to_f16x8(v, bad);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) raw[u] = v[u];
+    const uint4 hi = to_f16x8(v, bad);
+    *reinterpret_cast<uint4*>(dst + e) = hi;
+    if (dst_lo) *reinterpret_cast<uint4*>(dst_lo + e) = lo_f16x8(raw, hi);
   }
   if (bad) report_error(status, kDevErrRange);
 }
@@ -128,22 +156,92 @@ static bool contiguous(const ShapeArgs& s) {
 
 static int grid_for(int64_t items) { return (int)std::min<int64_t>((items + 255) / 256, 152 * 8); }
 
-cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsigned* status, cudaStream_t st) {
+namespace {
+
+// Counting sort of each head's query blocks by descending list length, one CTA per head: a
+// histogram of Tk - length in shared memory, its exclusive scan, and a scatter through the
+// running bin offsets.  Heads stay in order, so the items in flight at any time come from one
+// or two heads and share their K / V blocks in L2.
+constexpr int kOrderThreads = 1024;
+
+__global__ void __launch_bounds__(kOrderThreads) item_order_kernel(const int32_t* __restrict__ row_cnt, int Tq,
+                                                                   int Tk, int32_t* __restrict__ order,
+                                                                   int* __restrict__ work_ctr) {
+  extern __shared__ int bins[];  // Tk + 1
+  __shared__ int warp_sum[kOrderThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t x0 = (int64_t)blockIdx.x * Tq;  // the head's first item
+  const int nb = Tk + 1;
+  for (int i = tid; i < nb; i += kOrderThreads) bins[i] = 0;
+  __syncthreads();
+  auto bin_of = [&](int i) {
+    const int n = row_cnt[x0 + i];
+    return Tk - (n < 0 ? 0 : (n > Tk ? Tk : n));
+  };
+  for (int i = tid; i < Tq; i += kOrderThreads) atomicAdd(&bins[bin_of(i)], 1);
+  __syncthreads();
+  // exclusive scan: each thread sums a contiguous run of bins, the runs are scanned across
+  // the block, then each run is rewritten as offsets
+  const int per = (nb + kOrderThreads - 1) / kOrderThreads;
+  const int b0 = min(nb, tid * per), b1 = min(nb, b0 + per);
+  int run = 0;
+  for (int i = b0; i < b1; ++i) run += bins[i];
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    warp_sum[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int base = incl - run + (warp > 0 ? warp_sum[warp - 1] : 0);
+  for (int i = b0; i < b1; ++i) {
+    const int c = bins[i];
+    bins[i] = base;
+    base += c;
+  }
+  __syncthreads();
+  for (int i = tid; i < Tq; i += kOrderThreads) order[x0 + atomicAdd(&bins[bin_of(i)], 1)] = (int32_t)(x0 + i);
+  if (blockIdx.x == 0 && tid == 0) *work_ctr = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_item_order(const int32_t* row_cnt, int heads, int Tq, int Tk, int32_t* order, int* work_ctr,
+                              cudaStream_t st) {
+  const size_t smem = (size_t)(Tk + 1) * sizeof(int);
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;  // Tk <= 12287
+  item_order_kernel<<<heads, kOrderThreads, smem, st>>>(row_cnt, Tq, Tk, order, work_ctr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsigned* status, cudaStream_t st,
+                          __half* dst_lo) {
   const int blocks = grid_for((int64_t)s.B * s.H * s.N * s.d / 8);
   const bool c = contiguous(s);
   prof_start(st, kToF16);
   if (s.dtype == 0) {
     auto p = static_cast<const __nv_bfloat16*>(src);
     if (c)
-      to_f16_kernel<__nv_bfloat16, true><<<blocks, 256, 0, st>>>(p, s, dst, status);
+      to_f16_kernel<__nv_bfloat16, true><<<blocks, 256, 0, st>>>(p, s, dst, dst_lo, status);
     else
-      to_f16_kernel<__nv_bfloat16, false><<<blocks, 256, 0, st>>>(p, s, dst, status);
+      to_f16_kernel<__nv_bfloat16, false><<<blocks, 256, 0, st>>>(p, s, dst, dst_lo, status);
   } else {
     auto p = static_cast<const float*>(src);
     if (c)
-      to_f16_kernel<float, true><<<blocks, 256, 0, st>>>(p, s, dst, status);
+      to_f16_kernel<float, true><<<blocks, 256, 0, st>>>(p, s, dst, dst_lo, status);
     else
-      to_f16_kernel<float, false><<<blocks, 256, 0, st>>>(p, s, dst, status);
+      to_f16_kernel<float, false><<<blocks, 256, 0, st>>>(p, s, dst, dst_lo, status);
   }
   prof_stop(st, kToF16);
   return cudaGetLastError();

@@ -14,9 +14,11 @@
 //   warps 3..6  softmax: each thread owns one query row (its TMEM lane); online softmax in
 //               fp32 with exp2, P_j (fp16) written back over S_j in TMEM; epilogue O / l
 //
-// Operand types: S = Q K^T in bf16 (bf16 calls) or fp16 (fp32 calls, whose inputs arrive
-// as fp16 copies); P V always in fp16 with an fp16 copy of V: P lies in [0, 1], where fp16
-// keeps 11 significant bits against bf16's 8, and bf16 V converts to fp16 exactly.
+// Operand types: S = Q K^T in bf16 (bf16 calls) or, for fp32 calls, as three fp16 products
+// of the inputs' hi = fp16(x) and lo = fp16(x - hi) parts, Qhi Khi^T + Qhi Klo^T + Qlo Khi^T
+// (about 22 bits: the fp32 scores to within ~2^-21 relative); P V always in fp16 with an
+// fp16 copy of V: P lies in [0, 1], where fp16 keeps 11 significant bits against bf16's 8,
+// and bf16 V converts to fp16 exactly.
 //
 // TMEM columns: S buffers at 0 and 64 (fp32, 64 columns each; P_j as packed fp16 pairs in
 // the first 32 columns of its S buffer), O at 128 (D columns).
@@ -31,14 +33,19 @@ constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O and l are rescaled only past 2^8
 
-template <int D>
+// SPLIT (fp32 calls): Q and K also as fp16 residuals, lo = fp16(x - hi), behind their hi
+// tiles; S = Qhi Khi^T + Qhi Klo^T + Qlo Khi^T carries ~22 bits of the fp32 inputs.
+template <int D, bool SPLIT>
 struct FwdSmem {
   static constexpr int kPanels = D / 64;
   static constexpr int kQBytes = 128 * 128 * kPanels;   // 128 rows x 128 B per panel
   static constexpr int kKVBytes = 64 * 128 * kPanels;   // 64 rows x 128 B per panel
+  static constexpr int kParts = SPLIT ? 2 : 1;          // hi (and lo) of Q and K
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + kNumStages * kKVBytes;
+  static constexpr int kOffQlo = kOffQ + kQBytes;
+  static constexpr int kOffK = kOffQ + kParts * kQBytes;
+  static constexpr int kOffKlo = kOffK + kNumStages * kKVBytes;
+  static constexpr int kOffV = kOffK + kParts * kNumStages * kKVBytes;
   static constexpr int kOffBar = kOffV + kNumStages * kKVBytes;
   // barriers, TMEM slot and alignment slack; at least 80 KB so that no more than two CTAs
   // (2 x 256 TMEM columns) share an SM
@@ -83,11 +90,12 @@ __device__ __forceinline__ void store_row_chunk<float>(float* dst, const float* 
   for (int i = 0; i < 8; ++i) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-template <int D, typename OutT, bool S_F16>
+template <int D, typename OutT, bool S_F16, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 2)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                    const __grid_constant__ CUtensorMap mv, ShapeArgs s, FwdArgs a) {
-  using L = FwdSmem<D>;
+                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mql,
+                    const __grid_constant__ CUtensorMap mkl, ShapeArgs s, FwdArgs a) {
+  using L = FwdSmem<D, SPLIT>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -155,9 +163,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       tma_prefetch_map(&mq);
       tma_prefetch_map(&mk);
       tma_prefetch_map(&mv);
-      mbar_arrive_expect_tx(bar_q, L::kQBytes);
-      for (int p = 0; p < L::kPanels; ++p)
+      if constexpr (SPLIT) {
+        tma_prefetch_map(&mql);
+        tma_prefetch_map(&mkl);
+      }
+      mbar_arrive_expect_tx(bar_q, L::kParts * L::kQBytes);
+      for (int p = 0; p < L::kPanels; ++p) {
         tma_load_4d(sbase + L::kOffQ + p * 16384, &mq, bar_q, p * 64, qi * s.bq, h, b);
+        if constexpr (SPLIT) tma_load_4d(sbase + L::kOffQlo + p * 16384, &mql, bar_q, p * 64, qi * s.bq, h, b);
+      }
       int nk = 0, nv = 0;  // K and V loads issued
       for (int j = 0; j < nkv; ++j) {
         const int st = j % kNumStages;
@@ -168,9 +182,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           kb = 0;
         }
         if (j >= kNumStages && !mbar_wait(bar_kempty(st), ph, wc)) break;
-        mbar_arrive_expect_tx(bar_kfull(st), L::kKVBytes);
-        for (int p = 0; p < L::kPanels; ++p)
+        mbar_arrive_expect_tx(bar_kfull(st), L::kParts * L::kKVBytes);
+        for (int p = 0; p < L::kPanels; ++p) {
           tma_load_4d(sbase + L::kOffK + st * L::kKVBytes + p * 8192, &mk, bar_kfull(st), p * 64, kb * 64, h, b);
+          if constexpr (SPLIT)
+            tma_load_4d(sbase + L::kOffKlo + st * L::kKVBytes + p * 8192, &mkl, bar_kfull(st), p * 64, kb * 64, h,
+                        b);
+        }
         ++nk;
         if (j >= kNumStages && !mbar_wait(bar_vempty(st), ph, wc)) break;
         mbar_arrive_expect_tx(bar_vfull(st), L::kKVBytes);
@@ -206,6 +224,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint64_t kd = smem_desc(sbase + L::kOffK + st * L::kKVBytes, 16, 1024);
         if (elect_one()) {
           mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + (j & 1) * 64, qd, kd);
+          if constexpr (SPLIT) {
+            const uint64_t kld = smem_desc(sbase + L::kOffKlo + st * L::kKVBytes, 16, 1024);
+            const uint64_t qld = smem_desc(sbase + L::kOffQlo, 16, 1024);
+            mma_ss_kmajor_acc<idS, 128, 64, D / 16>(tmem + (j & 1) * 64, qd, kld);
+            mma_ss_kmajor_acc<idS, 128, 64, D / 16>(tmem + (j & 1) * 64, qld, kd);
+          }
           umma_commit(bar_sfull(j & 1));
           umma_commit(bar_kempty(st));
         }
@@ -267,16 +291,26 @@ __global__ void __launch_bounds__(kThreads, 2)
       tmem_ld_wait(u0);
       tmem_ld_wait(u1);
       kb = (kb < 0 || kb >= s.Tk) ? 0 : kb;
-      const int valid = min(64, s.N - kb * 64);
+      // raw scores; the scale (> 0) is folded into the exponent's FMA below
       float x[64];
-      float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        x[c] = (c < valid) ? __uint_as_float(u0[c]) * a.scale_log2 : -INFINITY;
-        x[c + 32] = (c + 32 < valid) ? __uint_as_float(u1[c]) * a.scale_log2 : -INFINITY;
+        x[c] = __uint_as_float(u0[c]);
+        x[c + 32] = __uint_as_float(u1[c]);
       }
+      const int valid = min(64, s.N - kb * 64);
+      if (valid < 64) {  // the ragged last key block (the same for the whole CTA)
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
+        for (int c = 0; c < 64; ++c) x[c] = c < valid ? x[c] : -INFINITY;
+      }
+      // row maximum and (below) row sum as 8- and 4-way trees: short dependency chains
+      float m8[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) m8[c] = x[c];
+#pragma unroll
+      for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+      const float mr = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      const float mx = mr * a.scale_log2;
       if (j == 0) {
         m_used = mx;
       } else {
@@ -309,15 +343,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       uint32_t pk[32];
-      float lsum = 0.f;
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(x[2 * c] - m_used);
-        const float p1 = ex2(x[2 * c + 1] - m_used);
-        lsum += p0 + p1;
+        const float p0 = ex2(fmaf(x[2 * c], a.scale_log2, -m_used));
+        const float p1 = ex2(fmaf(x[2 * c + 1], a.scale_log2, -m_used));
+        l4[c & 3] += p0 + p1;
         pk[c] = pack_f16x2(p0, p1);
       }
-      l += lsum;
+      l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
       tmem_st32(trow + bsel * 64, pk);
       tmem_st_wait();
       tc_fence_before();
@@ -378,16 +412,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-template <int D, typename OutT, bool S_F16>
+template <int D, typename OutT, bool S_F16, bool SPLIT>
 cudaError_t launch_fwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const FwdArgs& a, cudaStream_t st) {
-  const int smem = FwdSmem<D>::kBytes;
-  auto kern = attn_fwd_kernel<D, OutT, S_F16>;
+                         const CUtensorMap& mql, const CUtensorMap& mkl, const FwdArgs& a, cudaStream_t st) {
+  const int smem = FwdSmem<D, SPLIT>::kBytes;
+  auto kern = attn_fwd_kernel<D, OutT, S_F16, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)s.B * s.H * s.Tq;
   prof_start(st, kAttnFwd);
-  kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, s, a);
+  kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, mql, mkl, s, a);
   prof_stop(st, kAttnFwd);
   return cudaGetLastError();
 }
@@ -395,13 +429,15 @@ cudaError_t launch_fwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtens
 }  // namespace
 
 cudaError_t launch_attn_fwd(const ShapeArgs& s, bool s_f16, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st) {
-  // bf16 calls: bf16 S, bf16 output; fp32 calls: fp16 S, fp32 output
+                            const CUtensorMap& mv, const CUtensorMap* mql, const CUtensorMap* mkl, const FwdArgs& a,
+                            cudaStream_t st) {
+  // bf16 calls: bf16 S, bf16 output; fp32 calls: the split fp16 S product, fp32 output
   if (!s_f16)
-    return s.d == 128 ? launch_fwd_t<128, __nv_bfloat16, false>(s, mq, mk, mv, a, st)
-                      : launch_fwd_t<64, __nv_bfloat16, false>(s, mq, mk, mv, a, st);
-  return s.d == 128 ? launch_fwd_t<128, float, true>(s, mq, mk, mv, a, st)
-                    : launch_fwd_t<64, float, true>(s, mq, mk, mv, a, st);
+    return s.d == 128 ? launch_fwd_t<128, __nv_bfloat16, false, false>(s, mq, mk, mv, mq, mk, a, st)
+                      : launch_fwd_t<64, __nv_bfloat16, false, false>(s, mq, mk, mv, mq, mk, a, st);
+  if (!mql || !mkl) return cudaErrorInvalidValue;
+  return s.d == 128 ? launch_fwd_t<128, float, true, true>(s, mq, mk, mv, *mql, *mkl, a, st)
+                    : launch_fwd_t<64, float, true, true>(s, mq, mk, mv, *mql, *mkl, a, st);
 }
 
 }  // namespace sa2

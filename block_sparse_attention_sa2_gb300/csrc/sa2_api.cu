@@ -111,8 +111,10 @@ MaskWs mask_ws(const ShapeArgs& s) {
 }
 
 // Forward workspace: fp16 copy of V (every call); fp16 copies of Q and K (fp32 calls).
+// Forward workspace: the fp16 copy of V; for fp32 calls also the fp16 copies of Q and K and
+// their fp16 residuals (the split S product).
 struct FwdWs {
-  size_t v16, q16, k16, total;
+  size_t v16, q16, k16, q16lo, k16lo, total;
 };
 FwdWs fwd_ws(const ShapeArgs& s) {
   const size_t t = align_up(2 * token_elems(s));
@@ -122,7 +124,9 @@ FwdWs fwd_ws(const ShapeArgs& s) {
   if (s.dtype == SA2_FP32) {
     w.q16 = t;
     w.k16 = 2 * t;
-    w.total = 3 * t;
+    w.q16lo = 3 * t;
+    w.k16lo = 4 * t;
+    w.total = 5 * t;
   }
   return w;
 }
@@ -130,7 +134,7 @@ FwdWs fwd_ws(const ShapeArgs& s) {
 // Backward workspace: per-row statistics, the pair-union lists of the dK / dV kernel, and
 // fp16 copies of Q, K, V, dO.
 struct BwdWs {
-  size_t stats, pair_cnt, pair_idx, q16, k16, v16, do16, ctr, total;
+  size_t stats, pair_cnt, pair_idx, q16, k16, v16, do16, ctr, order, q16lo, k16lo, total;
 };
 BwdWs bwd_ws(const ShapeArgs& s) {
   BwdWs w{};
@@ -143,7 +147,13 @@ BwdWs bwd_ws(const ShapeArgs& s) {
   w.v16 = w.k16 + t;
   w.do16 = w.v16 + t;
   w.ctr = w.do16 + t;
-  w.total = w.ctr + align_up(sizeof(int) * kBwdWorkCounters);
+  w.order = w.ctr + align_up(sizeof(int) * kBwdWorkCounters);
+  w.total = w.order + align_up(sizeof(int32_t) * (size_t)s.B * s.H * s.Tq);
+  if (s.dtype == SA2_FP32) {  // fp16 residuals of Q and K (the split S product)
+    w.q16lo = w.total;
+    w.k16lo = w.q16lo + t;
+    w.total = w.k16lo + t;
+  }
   return w;
 }
 
@@ -236,13 +246,18 @@ sa2_status sa2_attn_fwd(const sa2_shape* shape, const void* q, const void* k, co
   __half* v16 = reinterpret_cast<__half*>(wsb + w.v16);
   if (launch_to_f16(v, s, v16, status, cs) != cudaSuccess) return SA2_ERR_CUDA;
   const bool f16_inputs = s.dtype == SA2_FP32;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mql, mkl;
   if (f16_inputs) {
     __half* q16 = reinterpret_cast<__half*>(wsb + w.q16);
     __half* k16 = reinterpret_cast<__half*>(wsb + w.k16);
-    if (launch_to_f16(q, s, q16, status, cs) != cudaSuccess || launch_to_f16(k, s, k16, status, cs) != cudaSuccess)
+    __half* q16lo = reinterpret_cast<__half*>(wsb + w.q16lo);
+    __half* k16lo = reinterpret_cast<__half*>(wsb + w.k16lo);
+    if (launch_to_f16(q, s, q16, status, cs, q16lo) != cudaSuccess ||
+        launch_to_f16(k, s, k16, status, cs, k16lo) != cudaSuccess)
       return SA2_ERR_CUDA;
-    if (!copy_map(s, q16, &mq, 128) || !copy_map(s, k16, &mk, 64)) return SA2_ERR_CUDA;
+    if (!copy_map(s, q16, &mq, 128) || !copy_map(s, k16, &mk, 64) || !copy_map(s, q16lo, &mql, 128) ||
+        !copy_map(s, k16lo, &mkl, 64))
+      return SA2_ERR_CUDA;
   } else {
     if (!caller_map(s, q, &mq, 128) || !caller_map(s, k, &mk, 64)) return SA2_ERR_CUDA;
   }
@@ -259,7 +274,8 @@ sa2_status sa2_attn_fwd(const sa2_shape* shape, const void* q, const void* k, co
   a.o_sn = s.sn;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
-  return cuda_status(launch_attn_fwd(s, f16_inputs, mq, mk, mv, a, cs));
+  return cuda_status(launch_attn_fwd(s, f16_inputs, mq, mk, mv, f16_inputs ? &mql : nullptr,
+                                     f16_inputs ? &mkl : nullptr, a, cs));
 }
 
 size_t sa2_bwd_workspace_size(const sa2_shape* shape) {
@@ -296,30 +312,38 @@ sa2_status attn_bwd_impl(const sa2_shape* shape, const void* q, const void* k, c
   float* stats = reinterpret_cast<float*>(wsb + w.stats);
   __half* c16[4] = {reinterpret_cast<__half*>(wsb + w.q16), reinterpret_cast<__half*>(wsb + w.k16),
                     reinterpret_cast<__half*>(wsb + w.v16), reinterpret_cast<__half*>(wsb + w.do16)};
+  const bool split = s.dtype == SA2_FP32;  // fp32 calls: fp16 residuals of Q and K too
+  __half* lo16[3] = {split ? reinterpret_cast<__half*>(wsb + w.q16lo) : nullptr,
+                     split ? reinterpret_cast<__half*>(wsb + w.k16lo) : nullptr, nullptr};
   const void* src[3] = {q, k, v};
   bool copied[3] = {false, false, false};
   if (fwd_workspace) {
-    // the forward's fp16 copies: v always, q and k for fp32 inputs
+    // the forward's fp16 copies: v always, q and k (and their residuals) for fp32 inputs
     const FwdWs fw = fwd_ws(s);
     const uint8_t* fb = static_cast<const uint8_t*>(fwd_workspace);
     c16[2] = reinterpret_cast<__half*>(const_cast<uint8_t*>(fb + fw.v16));
     copied[2] = true;
-    if (s.dtype == SA2_FP32) {
+    if (split) {
       c16[0] = reinterpret_cast<__half*>(const_cast<uint8_t*>(fb + fw.q16));
       c16[1] = reinterpret_cast<__half*>(const_cast<uint8_t*>(fb + fw.k16));
+      lo16[0] = reinterpret_cast<__half*>(const_cast<uint8_t*>(fb + fw.q16lo));
+      lo16[1] = reinterpret_cast<__half*>(const_cast<uint8_t*>(fb + fw.k16lo));
       copied[0] = copied[1] = true;
     }
   }
   for (int i = 0; i < 3; ++i)
-    if (!copied[i] && launch_to_f16(src[i], s, c16[i], status, cs) != cudaSuccess) return SA2_ERR_CUDA;
+    if (!copied[i] && launch_to_f16(src[i], s, c16[i], status, cs, lo16[i]) != cudaSuccess) return SA2_ERR_CUDA;
   // fp16 dO, and D = rowsum(dO * O) from that same fp16 dO, in one pass
   if (launch_do_prep(s, dO, o, s.dtype == SA2_BF16 ? o_lo : nullptr, lse, c16[3], stats, status, cs) !=
       cudaSuccess)
     return SA2_ERR_CUDA;
   // the dK / dV kernel reads 64-row query sub-tiles, the dQ kernel 128-row query tiles
-  CUtensorMap mq64, mdo64, mq, mk, mv, mdo;
+  CUtensorMap mq64, mdo64, mq, mk, mv, mdo, mql64, mql, mkl;
   if (!copy_map(s, c16[0], &mq64, 64) || !copy_map(s, c16[3], &mdo64, 64) || !copy_map(s, c16[0], &mq, 128) ||
       !copy_map(s, c16[1], &mk, 64) || !copy_map(s, c16[2], &mv, 64) || !copy_map(s, c16[3], &mdo, 128))
+    return SA2_ERR_CUDA;
+  if (split && (!copy_map(s, lo16[0], &mql64, 64) || !copy_map(s, lo16[0], &mql, 128) ||
+                !copy_map(s, lo16[1], &mkl, 64)))
     return SA2_ERR_CUDA;
   const float scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / std::sqrt((double)s.d));
   BwdArgs a;
@@ -337,10 +361,13 @@ sa2_status attn_bwd_impl(const sa2_shape* shape, const void* q, const void* k, c
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
-  if (launch_attn_bwd(s, mq64, mk, mv, mdo64, a, cs) != cudaSuccess) return SA2_ERR_CUDA;
+  if (launch_attn_bwd(s, mq64, mk, mv, mdo64, split ? &mql64 : nullptr, split ? &mkl : nullptr, a, cs) !=
+      cudaSuccess)
+    return SA2_ERR_CUDA;
   DqArgs g;
   g.row_cnt = mask->row_cnt;
   g.row_idx = mask->row_idx;
+  g.order = reinterpret_cast<int32_t*>(wsb + w.order);
   g.stats = stats;
   g.work_ctr = a.work_ctr + 1;
   g.dq = dq;
@@ -350,7 +377,7 @@ sa2_status attn_bwd_impl(const sa2_shape* shape, const void* q, const void* k, c
   g.scale = scale;
   g.scale_log2 = a.scale_log2;
   g.status = status;
-  return cuda_status(launch_attn_bwd_dq(s, mq, mk, mv, mdo, g, cs));
+  return cuda_status(launch_attn_bwd_dq(s, mq, mk, mv, mdo, split ? &mql : nullptr, split ? &mkl : nullptr, g, cs));
 }
 
 }  // namespace

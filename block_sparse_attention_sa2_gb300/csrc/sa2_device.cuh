@@ -221,6 +221,12 @@ __device__ __forceinline__ void mma_ss_kmajor(uint32_t d, uint64_t a, uint64_t b
   umma_ss(d, a + kmajor_kstep(KK, A_ROWS), b + kmajor_kstep(KK, B_ROWS), IDESC, KK > 0 ? 1u : 0u);
   if constexpr (KK + 1 < KSTEPS) mma_ss_kmajor<IDESC, A_ROWS, B_ROWS, KSTEPS, KK + 1>(d, a, b);
 }
+// The same product accumulated onto D from the first k-step on.
+template <uint32_t IDESC, int A_ROWS, int B_ROWS, int KSTEPS, int KK = 0>
+__device__ __forceinline__ void mma_ss_kmajor_acc(uint32_t d, uint64_t a, uint64_t b) {
+  umma_ss(d, a + kmajor_kstep(KK, A_ROWS), b + kmajor_kstep(KK, B_ROWS), IDESC, 1u);
+  if constexpr (KK + 1 < KSTEPS) mma_ss_kmajor_acc<IDESC, A_ROWS, B_ROWS, KSTEPS, KK + 1>(d, a, b);
+}
 // TS form: A from TMEM (8 columns of fp16 pairs per k-step), B MN-major with 16 rows
 // (2048 bytes) per k-step.  The first k-step overwrites D when `fresh`, else accumulates.
 template <uint32_t IDESC, int KSTEPS, int KK = 0>

@@ -72,7 +72,16 @@ bool make_token_map(CUtensorMap* map, const void* base, const ShapeArgs& s, int6
                     int box_rows, bool f16);
 
 // Element-wise helpers (attn_common.cu).
-cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsigned* status, cudaStream_t st);
+// fp16 copy of a token tensor into contiguous [B, H, N, d]; with dst_lo, also the residual
+// fp16(x - hi) of each element (fp32 sources: hi + lo carries ~22 bits).
+cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsigned* status, cudaStream_t st,
+                          __half* dst_lo = nullptr);
+
+// The B*H*Tq query blocks head by head, each head's blocks by descending kept-list length
+// (lengths clamped to [0, Tk]; equal lengths in no fixed order), for the persistent kernels
+// that take one query block per work item; also zeroes *work_ctr.  One CTA per head.
+cudaError_t launch_item_order(const int32_t* row_cnt, int heads, int Tq, int Tk, int32_t* order, int* work_ctr,
+                              cudaStream_t st);
 
 struct FwdArgs {
   const int32_t* row_cnt;
@@ -86,9 +95,11 @@ struct FwdArgs {
 };
 
 // S = Q K^T reads bf16 Q and K (s_f16 = false, bf16 calls) or their fp16 copies (fp32
-// calls); P V always reads fp16 P and V.
+// calls; with the maps of their fp16 residuals mql, mkl, S is the split product
+// Qhi Khi^T + Qhi Klo^T + Qlo Khi^T); P V always reads fp16 P and V.
 cudaError_t launch_attn_fwd(const ShapeArgs& s, bool s_f16, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st);
+                            const CUtensorMap& mv, const CUtensorMap* mql, const CUtensorMap* mkl, const FwdArgs& a,
+                            cudaStream_t st);
 
 // Per-row statistics of the backward, one record per 64-row query sub-tile:
 // stats[(bh * Tsub + r) * 128 + i] = log2(e) * LSE of row 64 r + i (+inf past N), and
@@ -115,8 +126,9 @@ struct BwdArgs {
 struct DqArgs {
   const int32_t* row_cnt;
   const int32_t* row_idx;
+  const int32_t* order;  // query blocks, head by head, longest list first (launch_item_order)
   const float* stats;
-  int* work_ctr;  // item counter of the persistent kernel (workspace; zeroed by the pair-union pass)
+  int* work_ctr;  // item counter of the persistent kernel (workspace; zeroed by launch_item_order)
   void* dq;
   int64_t g_sb, g_sh, g_sn;
   float scale;
@@ -132,10 +144,14 @@ constexpr int kBwdWorkCounters = 2;  // dK/dV kernel, dQ kernel
 // statistics, in one pass (attn_common.cu).
 cudaError_t launch_do_prep(const ShapeArgs& s, const void* dO, const void* o, const void* o_lo, const float* lse,
                            __half* dO16, float* stats, unsigned* status, cudaStream_t st);
+// fp32 calls (dtype 1) pass the maps of the fp16 residuals of Q and K (mql, mkl): their S
+// product is split like the forward's; bf16 calls pass null.
 cudaError_t launch_attn_bwd(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                            const CUtensorMap& mdo, const BwdArgs& a, cudaStream_t st);
+                            const CUtensorMap& mdo, const CUtensorMap* mql, const CUtensorMap* mkl, const BwdArgs& a,
+                            cudaStream_t st);
 cudaError_t launch_attn_bwd_dq(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk,
-                               const CUtensorMap& mv, const CUtensorMap& mdo, const DqArgs& a, cudaStream_t st);
+                               const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap* mql,
+                               const CUtensorMap* mkl, const DqArgs& a, cudaStream_t st);
 
 // Toy distillation loss (attn_common.cu): loss = sum (O_s - O_t)^2 into *loss (device),
 // d_o = 2 (O_s - O_t); residuals optional (bf16 calls).  `partial` holds

@@ -126,8 +126,9 @@ sa2_status sa2_build_mask(const sa2_shape* shape, const void* q, const void* k, 
  * tensors, and paths where an allocation would synchronize the device.
  *
  * Same computation and outputs as sa2_build_mask, except that the builder's scratch (the
- * fp32 pooled queries and keys, B*H*d*(Tq+Tk) floats) lives in a static device array of
- * SA2_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the library
+ * pooled queries and keys as fp32 TF32 pairs, 2*B*H*d*(Tq+Tk) floats, and two buffers of the
+ * score rows and kept bits of a chunk of heads, the chunk as large as the array allows)
+ * lives in a static device array of SA2_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the library
  * holds until the process exits.  Nothing is allocated: no cudaMalloc, no cudaFree.
  *   - out->mask is required here (the u8 mask is built in place of the workspace copy).
  *   - A shape whose scratch exceeds SA2_NOALLOC_SCRATCH_BYTES is rejected with
@@ -143,8 +144,8 @@ sa2_status sa2_build_mask_noalloc(const sa2_shape* shape, const void* q, const v
                                   const sa2_blockmask* out, void* stream);
 
 /*
- * Bytes of device workspace sa2_attn_fwd needs: an fp16 copy of v, plus fp16 copies of q
- * and k for SA2_FP32 inputs.
+ * Bytes of device workspace sa2_attn_fwd needs: an fp16 copy of v, plus for SA2_FP32
+ * inputs fp16 copies of q and k and their fp16 residuals fp16(x - fp16(x)).
  */
 size_t sa2_fwd_workspace_size(const sa2_shape* shape);
 
@@ -157,9 +158,10 @@ size_t sa2_fwd_workspace_size(const sa2_shape* shape);
  *   O_a = sum over kept key tokens c of exp(s_ac - LSE_a) v_c,  s_ac = scale * q_a . k_c,
  *   LSE_a = log sum over kept c of exp(s_ac)   (natural log).
  * A query block with no kept key block gets O = 0 and LSE = -inf.
- * Arithmetic: S = Q K^T on the tensor cores in bf16 (SA2_BF16) or fp16 (SA2_FP32 inputs,
- * rounded to fp16 first), fp32 accumulation, fp32 online softmax, then P V with P and V in
- * fp16 (P lies in [0, 1]; bf16 V converts to fp16 exactly).  Attention inputs must lie
+ * Arithmetic: S = Q K^T on the tensor cores in bf16 (SA2_BF16), or for SA2_FP32 inputs as
+ * the split fp16 product Qhi Khi^T + Qhi Klo^T + Qlo Khi^T of hi = fp16(x), lo = fp16(x - hi)
+ * (about 22 bits of the fp32 inputs), fp32 accumulation, fp32 online softmax, then P V with
+ * P and V in fp16 (P lies in [0, 1]; bf16 V converts to fp16 exactly).  Attention inputs must lie
  * within the fp16 range (|x| <= 65504); larger values are saturated and reported as
  * SA2_ERR_RANGE through sa2_get_device_status.
  *
@@ -179,8 +181,9 @@ sa2_status sa2_attn_fwd(const sa2_shape* shape, const void* q, const void* k, co
  * Bytes of device workspace sa2_attn_bwd needs: per-row statistics (log2(e) * LSE and
  * D = rowsum(dO * O), padded to whole 64-row query sub-tiles), the merged column lists of
  * each pair of adjacent key blocks ([B, H, ceil(Tk/2), Tq] uint32 plus their lengths),
- * fp16 copies of q, k, v and dO, and the work counters of the two persistent backward
- * kernels (reset by the call itself).
+ * fp16 copies of q, k, v and dO (and for SA2_FP32 inputs the fp16 residuals of q and k),
+ * the work counters of the two persistent backward kernels and the order of the query
+ * blocks (reset and rebuilt by the call itself).
  */
 size_t sa2_bwd_workspace_size(const sa2_shape* shape);
 
@@ -194,8 +197,9 @@ size_t sa2_bwd_workspace_size(const sa2_shape* shape);
  * over kept tiles only.  Rows with LSE = -inf contribute nothing.
  *
  * Every product runs on the tensor cores in fp16 (q, k, v, dO converted; P and dS written
- * in fp16, which keeps 11 significant bits where the rows of dS cancel in dQ = dS K) with
- * fp32 accumulation in tensor memory: dK and dV per pair of key blocks across its query
+ * in fp16, which keeps 11 significant bits where the rows of dS cancel in dQ = dS K; for
+ * SA2_FP32 inputs the recomputed scores are the split product of the forward) with fp32
+ * accumulation in tensor memory: dK and dV per pair of key blocks across its query
  * blocks, dQ per query block across its key blocks, so no output is reduced across CTAs
  * and the result does not depend on scheduling.
  *
@@ -213,7 +217,7 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
 /*
  * sa2_attn_bwd_with_fwd_ws -- sa2_attn_bwd that takes the fp16 copies the forward already
  * made instead of converting again: the copy of v, and for SA2_FP32 inputs those of q and
- * k, which sa2_attn_fwd leaves in its workspace.  The result is the same, bit for bit.
+ * k and their residuals, which sa2_attn_fwd leaves in its workspace.  The result is the same, bit for bit.
  *
  *   fwd_ws, fwd_ws_bytes  the workspace of the sa2_attn_fwd call on the same shape, q, k
  *                         and v (the call that produced o, o_lo and lse), ordered before

@@ -4,9 +4,9 @@ The CUDA forward runs on the oracle's own block mask (handed over as compact lis
 the comparison isolates the attention.  Bar: max |d| <= 2e-2 and sum|d| / sum|ref| <= 5e-3
 on O; LSE within 2e-2 where finite, and -inf exactly where the row keeps nothing.
 
-fp32 inputs: the library computes the attention of the fp16-rounded inputs (documented in
-include/sa2.h), so the reference is the oracle on those rounded values; a looser check
-against the oracle on the exact fp32 inputs bounds what the rounding itself costs."""
+fp32 inputs are held to the same bar against the oracle on the exact fp32 inputs: the
+library forms their scores as the split fp16 product Qhi Khi^T + Qhi Klo^T + Qlo Khi^T
+(about 22 bits) and only P and V take a single fp16 rounding (include/sa2.h)."""
 import json
 import os
 
@@ -20,10 +20,6 @@ from workload.gen import small_case
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-# Against the exact fp32 inputs the fp16 staging itself moves O and LSE (relative rounding
-# of 2^-12 per input element, on scores up to ~20 and values up to ~4 in these workloads).
-FP32_INPUT_MAX_ABS = 6e-2
-FP32_INPUT_LSE_TOL = 1e-1
 
 
 @pytest.fixture(scope="module")
@@ -44,12 +40,6 @@ def _run_fwd(sa2, cfg, x, mask, scale=None):
     return to_f64(o), lse.cpu().numpy().astype(np.float64)
 
 
-def attn_inputs(x):
-    """What the attention kernels compute on: fp32 inputs rounded to fp16 (the library's
-    documented staging), bf16 inputs as they are (bf16 converts to fp16 exactly)."""
-    return {t: (a.astype(np.float16).astype(np.float32) if a.dtype == np.float32 else a) for t, a in x.items()}
-
-
 def _check_head(name, o, lse, ro, rlse, lse_tol=2e-2, **tol):
     assert_close(name + " O", o, ro, **tol)
     fin = np.isfinite(rlse)
@@ -60,17 +50,10 @@ def _check_head(name, o, lse, ro, rlse, lse_tol=2e-2, **tol):
 
 def _full_check(sa2, cfg, x, mask, scale=None):
     o, lse = _run_fwd(sa2, cfg, x, mask, scale)
-    xa = attn_inputs(x)
-    ro, rlse = O.attn_fwd(xa["q"], xa["k"], xa["v"], mask, cfg.bq, cfg.bk, scale)
+    ro, rlse = O.attn_fwd(x["q"], x["k"], x["v"], mask, cfg.bq, cfg.bk, scale)
     for b in range(cfg.B):
         for h in range(cfg.H):
             _check_head(f"{cfg.name} b{b}h{h}", o[b, h], lse[b, h], ro[b, h], rlse[b, h])
-    if cfg.dtype == "fp32":
-        eo, else_ = O.attn_fwd(x["q"], x["k"], x["v"], mask, cfg.bq, cfg.bk, scale)
-        for b in range(cfg.B):
-            for h in range(cfg.H):
-                _check_head(f"{cfg.name} b{b}h{h} vs exact fp32", o[b, h], lse[b, h], eo[b, h], else_[b, h],
-                            lse_tol=FP32_INPUT_LSE_TOL, max_abs=FP32_INPUT_MAX_ABS)
 
 
 def test_fwd_tiny_fp32_config(sa2):
