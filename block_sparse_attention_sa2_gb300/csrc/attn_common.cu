@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kOrderThreads) item_order_kernel(const int32_t
   }
   __syncthreads();
   for (int i = tid; i < Tq; i += kOrderThreads) order[x0 + atomicAdd(&bins[bin_of(i)], 1)] = (int32_t)(x0 + i);
-  if (blockIdx.x == 0 && tid == 0) *work_ctr = 0;
+  if (work_ctr && blockIdx.x == 0 && tid == 0) *work_ctr = 0;
 }
 
 }  // namespace

@@ -119,8 +119,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   const WaitCtl wc{abort_flag, s.wait_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x / s.Tq;
-  const int qi = blockIdx.x % s.Tq;
+  // CTAs launch head by head, within a head longest list first: the CTAs in flight share
+  // their heads' K / V in L2, and the last wave holds the shortest lists
+  const int x = a.order[blockIdx.x];
+  const int bh = x / s.Tq;
+  const int qi = x % s.Tq;
   const int b = bh / s.H, h = bh % s.H;
   const int64_t rowid = (int64_t)bh * s.Tq + qi;
   int nkv = a.row_cnt[rowid];
@@ -421,9 +424,10 @@ cudaError_t launch_fwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtens
   if (e != cudaSuccess) return e;
   const long long grid = (long long)s.B * s.H * s.Tq;
   prof_start(st, kAttnFwd);
-  kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, mql, mkl, s, a);
+  e = launch_item_order(a.row_cnt, s.B * s.H, s.Tq, s.Tk, a.order, nullptr, st);
+  if (e == cudaSuccess) kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, mql, mkl, s, a);
   prof_stop(st, kAttnFwd);
-  return cudaGetLastError();
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace

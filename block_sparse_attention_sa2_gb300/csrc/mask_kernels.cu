@@ -18,9 +18,9 @@
 //                    keys, or a bisection on the fp32 bit patterns of P-bar), and the emit
 //                    of the row list, the u8 mask and the row's kept bits.
 //   csc_kernel       transposes the kept bits into the per-key-block lists (ascending).
-// The heads run in chunks: the caller's stream pools chunk after chunk while two more
-// streams take the scores, the selection and the column lists of alternate chunks, each
-// with its own scratch buffer small enough to stay in L2.
+// The heads run in chunks: the caller's stream pools chunk after chunk while kChains more
+// streams take the scores, the selection and the column lists of successive chunks in turn,
+// each with its own scratch buffer small enough to stay in L2.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -38,7 +38,8 @@ constexpr int kChunkTokens = 128;           // tokens per pooling chunk
 constexpr int kScoreRows = 128;             // MMA M: query blocks per tile
 constexpr int kScoreKeys = 256;             // MMA N: key blocks per tile
 constexpr int kSelectThreads = 256;
-constexpr size_t kScoreChunkBudget = 32u << 20;  // bytes of the two head-chunk buffers
+constexpr int kChains = 2;                       // head chunks whose score / select / lists run at once
+constexpr size_t kScoreChunkBudget = 32u << 20;  // bytes of the kChains head-chunk buffers
 
 // ---------------------------------------------------------------------------- helpers
 
@@ -948,8 +949,8 @@ struct MaskLayout {
   int W;                      // 32-bit words of kept bits per row
 };
 
-// The pooled pairs of all heads, then two buffers (for two head chunks in flight) of the
-// chunk's score tiles and of its rows' kept bits.  chunk_budget bounds the bytes of both
+// The pooled pairs of all heads, then kChains buffers (one per head chunk in flight) of the
+// chunk's score tiles and of its rows' kept bits.  chunk_budget bounds the bytes of all the
 // buffers together; a chunk holds at least one head.
 MaskLayout mask_layout(const ShapeArgs& s, size_t chunk_budget) {
   MaskLayout L;
@@ -959,24 +960,25 @@ MaskLayout mask_layout(const ShapeArgs& s, size_t chunk_budget) {
   L.tk_pad = (s.Tk + kScoreKeys - 1) / kScoreKeys * kScoreKeys;
   L.W = (s.Tk + 31) / 32;
   const size_t tile_head = (size_t)L.tq_pad * L.tk_pad * 4, bits_head = (size_t)s.Tq * L.W * 4;
-  L.hc = (int)std::max<size_t>(1, std::min<size_t>(BH, chunk_budget / (2 * (tile_head + bits_head) + 4096)));
+  L.hc = (int)std::max<size_t>(1, std::min<size_t>(BH, chunk_budget / (kChains * (tile_head + bits_head) + 4096)));
   L.sbar_buf = al((size_t)L.hc * tile_head);
   L.bits_buf = al((size_t)L.hc * bits_head);
   L.qbar = 0;
   L.kbar = al(2 * BH * s.Tq * s.d * 4);
   L.sbar = L.kbar + al(2 * BH * s.Tk * s.d * 4);
-  L.bits = L.sbar + 2 * L.sbar_buf;
-  L.total = L.bits + 2 * L.bits_buf;
+  L.bits = L.sbar + kChains * L.sbar_buf;
+  L.total = L.bits + kChains * L.bits_buf;
   return L;
 }
 
-// Two more streams per device, of the highest priority.  The scores, the selection and the
-// column lists of head chunk c run on stream c % 2 (with buffer c % 2) while the caller's
-// stream pools the next chunks, so that the chains of two chunks overlap; the caller's
-// stream waits for both at the end of the call.  Set up on the first build on a device.
+// kChains more streams per device, of the highest priority.  The scores, the selection and
+// the column lists of head chunk c run on stream c % kChains (with buffer c % kChains) while
+// the caller's stream pools the next chunks, so that the chains of several chunks overlap;
+// the caller's stream waits for all of them at the end of the call.  Set up on the first
+// build on a device.
 struct AuxStream {
-  cudaStream_t stream[2] = {nullptr, nullptr};
-  cudaEvent_t pooled = nullptr, done[2] = {nullptr, nullptr};
+  cudaStream_t stream[kChains] = {};
+  cudaEvent_t pooled = nullptr, done[kChains] = {};
   cudaError_t err = cudaSuccess;
   std::mutex mu;  // one enqueue sequence at a time per device
 };
@@ -992,7 +994,7 @@ AuxStream* aux_stream(int dev) {
     // blocks go first where both wait for an SM
     int lo = 0, hi = 0;
     a.err = cudaDeviceGetStreamPriorityRange(&lo, &hi);
-    for (int i = 0; i < 2 && a.err == cudaSuccess; ++i) {
+    for (int i = 0; i < kChains && a.err == cudaSuccess; ++i) {
       a.err = cudaStreamCreateWithPriority(&a.stream[i], cudaStreamNonBlocking, hi);
       if (a.err == cudaSuccess) a.err = cudaEventCreateWithFlags(&a.done[i], cudaEventDisableTiming);
     }
@@ -1022,9 +1024,12 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
   uint8_t* base = static_cast<uint8_t*>(scratch);
   float* qbar = reinterpret_cast<float*>(base + L.qbar);
   float* kbar = reinterpret_cast<float*>(base + L.kbar);
-  float* sbar_buf[2] = {reinterpret_cast<float*>(base + L.sbar), reinterpret_cast<float*>(base + L.sbar + L.sbar_buf)};
-  uint32_t* bits_buf[2] = {reinterpret_cast<uint32_t*>(base + L.bits),
-                           reinterpret_cast<uint32_t*>(base + L.bits + L.bits_buf)};
+  float* sbar_buf[kChains];
+  uint32_t* bits_buf[kChains];
+  for (int i = 0; i < kChains; ++i) {
+    sbar_buf[i] = reinterpret_cast<float*>(base + L.sbar + i * L.sbar_buf);
+    bits_buf[i] = reinterpret_cast<uint32_t*>(base + L.bits + i * L.bits_buf);
+  }
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1080,8 +1085,9 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
   const int nc = (s.N + kChunkTokens - 1) / kChunkTokens;
   for (int bh0 = 0, ci = 0; bh0 < BH; bh0 += L.hc, ++ci) {
     const int nbh = std::min(L.hc, BH - bh0);
-    float* sbar = sbar_buf[ci & 1];
-    uint32_t* bits = bits_buf[ci & 1];
+    const int chain = ci % kChains;
+    float* sbar = sbar_buf[chain];
+    uint32_t* bits = bits_buf[chain];
     // ---- pooling of the chunk, on the caller's stream
     PoolArgs pa;
     pa.qbar = qbar;
@@ -1109,10 +1115,10 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
     prof_stop(st, kPool);
     e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaEventRecord(aux->pooled, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux->stream[ci & 1], aux->pooled, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux->stream[chain], aux->pooled, 0);
     if (e != cudaSuccess) return e;
     // ---- scores, selection and column lists of the chunk, on the second stream
-    cudaStream_t st2 = aux->stream[ci & 1];
+    cudaStream_t st2 = aux->stream[chain];
     ScoreArgs sa;
     sa.sbar = sbar;
     sa.bh0 = bh0;
@@ -1155,7 +1161,7 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+  for (int i = 0; i < kChains && e == cudaSuccess; ++i) {
     e = cudaEventRecord(aux->done[i], aux->stream[i]);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, aux->done[i], 0);
   }

@@ -112,9 +112,9 @@ MaskWs mask_ws(const ShapeArgs& s) {
 
 // Forward workspace: fp16 copy of V (every call); fp16 copies of Q and K (fp32 calls).
 // Forward workspace: the fp16 copy of V; for fp32 calls also the fp16 copies of Q and K and
-// their fp16 residuals (the split S product).
+// their fp16 residuals (the split S product); the launch order of the query blocks.
 struct FwdWs {
-  size_t v16, q16, k16, q16lo, k16lo, total;
+  size_t v16, q16, k16, q16lo, k16lo, order, total;
 };
 FwdWs fwd_ws(const ShapeArgs& s) {
   const size_t t = align_up(2 * token_elems(s));
@@ -128,6 +128,8 @@ FwdWs fwd_ws(const ShapeArgs& s) {
     w.k16lo = 4 * t;
     w.total = 5 * t;
   }
+  w.order = w.total;  // the launch order of the query blocks
+  w.total += align_up(sizeof(int32_t) * (size_t)s.B * s.H * s.Tq);
   return w;
 }
 
@@ -266,6 +268,7 @@ sa2_status sa2_attn_fwd(const sa2_shape* shape, const void* q, const void* k, co
   FwdArgs a;
   a.row_cnt = mask->row_cnt;
   a.row_idx = mask->row_idx;
+  a.order = reinterpret_cast<int32_t*>(wsb + w.order);
   a.o = o;
   a.o_lo = s.dtype == SA2_BF16 ? o_lo : nullptr;
   a.lse = lse;

@@ -79,13 +79,15 @@ cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsi
 
 // The B*H*Tq query blocks head by head, each head's blocks by descending kept-list length
 // (lengths clamped to [0, Tk]; equal lengths in no fixed order), for the persistent kernels
-// that take one query block per work item; also zeroes *work_ctr.  One CTA per head.
+// that take one query block per work item; also zeroes *work_ctr (when not null).  One CTA
+// per head.
 cudaError_t launch_item_order(const int32_t* row_cnt, int heads, int Tq, int Tk, int32_t* order, int* work_ctr,
                               cudaStream_t st);
 
 struct FwdArgs {
   const int32_t* row_cnt;
   const int32_t* row_idx;
+  int32_t* order;    // workspace: the launch order of the query blocks (launch_item_order)
   void* o;           // output, dtype of the call
   void* o_lo;        // optional bf16 residual O - bf16(O) (bf16 calls only), or null
   float* lse;        // [B, H, N]

@@ -77,8 +77,8 @@ def test_noalloc_matches_build_mask_on_two_calls_in_a_row(sa2):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(sa2):
     import torch
-    # B*H*d*(Tq+Tk)*4 bytes of pooled scratch: 1*40*128*(591+1182)*4 = 36 MB > 16 MB.  The
-    # size check runs before anything is launched, so the tensors are never read.
+    # 2*B*H*d*(Tq+Tk)*4 bytes of pooled TF32 pairs alone: 2*1*40*128*(591+1182)*4 = 73 MB > 16 MB.
+    # The size check runs before anything is launched, so the tensors are never read.
     q = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
     shp = sa2.sa2.Shape(1, 40, 75600, 128, 128, 64, 0, 0, 40 * 75600 * 128, 75600 * 128, 128)
     out = sa2.BlockMask.empty(1, 1, 1, 1, q.device)
