@@ -6,9 +6,12 @@
 // whose cumulative probability reaches p).
 //
 // Four kernels:
-//   pool_kernel      persistent, one warp per 128-token chunk of Q or K: plain streaming
-//                    loads, fp32 sums in token order, and the block means written as a TF32
-//                    pair hi + lo, row-major [2][B*H][T][d].  The HBM-bound part.
+//   pool_tc_kernel   (bf16 inputs) persistent; 128-token chunks of Q and K streamed by TMA
+//                    and summed per 64-token half on the tensor cores (D = X^T Sel with a 0/1
+//                    selector), the block means written as a TF32 pair hi + lo, row-major
+//                    [2][B*H][T][d].  The HBM-bound part.
+//   pool_kernel      (fp32 inputs) the same with one warp per chunk: plain streaming loads
+//                    and fp32 sums in token order.
 //   score_tc_kernel  pooled scores S-bar = q-bar k-bar^T / sqrt(d) of a 128-row x 256-key
 //                    tile on the tensor cores (tcgen05, kind::tf32) as the three products
 //                    hi.hi + hi.lo + lo.hi -- about fp32 accuracy -- accumulated in tensor
@@ -163,6 +166,193 @@ __global__ void __launch_bounds__(kPoolThreads, 4) pool_kernel(const T* __restri
         *reinterpret_cast<float4*>(dst + plane + e) = make_float4(lo[e], lo[e + 1], lo[e + 2], lo[e + 3]);
       }
     }
+  }
+}
+
+// ------------------------------------------------------------------- pooling on the TC
+
+// Pooling of bf16 Q and K as a product on the tensor cores.  A 128-token chunk X
+// [tokens x d channels] lands in shared memory by TMA (64-channel panels, 128-byte swizzle)
+// and is read as the MN-major A operand of D = X^T Sel: M = 128 channel rows (a d = 64 chunk
+// leaves the upper 64 rows unused), K = 128 tokens, N = 16 columns, where the selector Sel
+// (K-major, 4 KB) has column 0 = ones on tokens 0..63 and column 1 = ones on tokens
+// 64..127.  So D[c][0], D[c][1] are the sums of channel c over the two 64-token halves:
+// products by 1 are exact and the sums accumulate in fp32.  The SMs' ALUs stay free for
+// the kernels that run beside the pooling.
+// Persistent: CTA i takes the chunks i, i + gridDim.x, ... of the head chunk (Q chunks, then
+// K chunks, head by head).  Warp 0 streams them through a kPoolStages-deep ring, warp 1
+// owns tensor memory (two 16-column accumulators) and issues one 8-k-step MMA per chunk,
+// warps 2..5 read the accumulators out (thread = channel = TMEM lane), form the block means
+// (fp32, divided by the valid tokens) and store them as TF32 pairs, a warp's 32 channels as
+// one 128-byte row segment.
+constexpr int kPoolStages = 3;
+constexpr int kPoolStageBytes = 128 * 128 * 2;  // two 64-channel panels of 128 tokens x 128 B
+constexpr int kPoolSelBytes = 2 * 16 * 128;     // Sel: 16 rows x 2 panels of 64 tokens
+constexpr int kPoolTcThreads = 192;
+constexpr int kPoolTcSmem = kPoolStages * kPoolStageBytes + kPoolSelBytes + 256 + 1024;
+
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait2(uint32_t& r0, uint32_t& r1) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r0), "+r"(r1)::"memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPoolTcThreads, 1)
+    pool_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk, ShapeArgs s,
+                   PoolArgs a, unsigned* status) {
+  constexpr int kPanels = D / 64;
+  constexpr uint32_t kCols = 32;  // two accumulators of 16 columns
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t ssel = sbase + kPoolStages * kPoolStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPoolStages * kPoolStageBytes + kPoolSelBytes);
+  auto bar_full = [&](int st) { return smem_u32(&bars[st]); };
+  auto bar_empty = [&](int st) { return smem_u32(&bars[kPoolStages + st]); };
+  auto bar_acc = [&](int b) { return smem_u32(&bars[2 * kPoolStages + b]); };          // accumulator b complete
+  auto bar_accfree = [&](int b) { return smem_u32(&bars[2 * kPoolStages + 2 + b]); };  // ... read out
+  const uint32_t bar_drain = smem_u32(&bars[2 * kPoolStages + 4]);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[2 * kPoolStages + 6]);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&bars[2 * kPoolStages + 7]);
+  const WaitCtl wc{abort_flag, s.wait_ns};
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nc = (s.N + kChunkTokens - 1) / kChunkTokens;
+  const int items = a.nbh * 2 * nc;
+  // the selector: row j of panel p is 128 bytes of bf16 ones when token half p is column j
+  // (j = p for j < 2), zeros otherwise; rows of ones or zeros are swizzle-invariant
+  {
+    uint32_t* sel = reinterpret_cast<uint32_t*>(smem + kPoolStages * kPoolStageBytes);
+    for (int i = tid; i < kPoolSelBytes / 4; i += kPoolTcThreads) {
+      const int p = i / (16 * 32), row = (i / 32) % 16;
+      sel[i] = row == p ? 0x3F803F80u : 0u;
+    }
+  }
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < kPoolStages; ++i) {
+      mbar_init(bar_full(i), 1);
+      mbar_init(bar_empty(i), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_acc(b), 1);
+      mbar_init(bar_accfree(b), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(bar_drain, 1);
+    fence_barrier_init();
+  }
+  fence_proxy_async();  // the selector's generic stores, before the tensor core reads them
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&mq);
+      tma_prefetch_map(&mk);
+      uint32_t n = 0;
+      for (int x = blockIdx.x; x < items; x += gridDim.x, ++n) {
+        const int z = x / (2 * nc), r2 = x - z * 2 * nc;
+        const bool isk = r2 >= nc;
+        const int c = isk ? r2 - nc : r2;
+        const int bh = a.bh0 + z, b = bh / s.H, h = bh - b * s.H;
+        const int st = n % kPoolStages;
+        if (n >= kPoolStages && !mbar_wait(bar_empty(st), ((n / kPoolStages) - 1) & 1, wc)) break;
+        mbar_arrive_expect_tx(bar_full(st), kPanels * 16384);
+        for (int p = 0; p < kPanels; ++p)
+          tma_load_4d(sbase + st * kPoolStageBytes + p * 16384, isk ? &mk : &mq, bar_full(st), p * 64,
+                      c * kChunkTokens, h, b);
+      }
+      // no copy may still be in flight when the CTA exits
+      for (uint32_t v = n > kPoolStages ? n - kPoolStages : 0; v < n; ++v)
+        mbar_drain(bar_full(v % kPoolStages), (v / kPoolStages) & 1, abort_flag);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idP = idesc_bf16_f32(128, 16, true, false);
+    // Sel as the K-major B operand (16 rows); X as the MN-major A operand: M = 128 channels
+    // (64-channel groups 16 KB apart), 16 tokens (2048 B) per k-step
+    const uint64_t seld = smem_desc(ssel, 16, 1024);
+    uint32_t n = 0;
+    for (int x = blockIdx.x; x < items; x += gridDim.x, ++n) {
+      const int st = n % kPoolStages, ab = n & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (n / kPoolStages) & 1, wc) &&
+                                       (n < 2 || mbar_wait(bar_accfree(ab), ((n >> 1) - 1) & 1, wc))))
+        break;
+      tc_fence_after();
+      const uint64_t xd = smem_desc(sbase + st * kPoolStageBytes, 16384, 1024);
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tmem + ab * 16, xd + (uint64_t)(kk * 128), seld + kmajor_kstep(kk, 16), idP, kk > 0 ? 1u : 0u);
+        umma_commit(bar_empty(st));
+        umma_commit(bar_acc(ab));
+      }
+      __syncwarp();
+    }
+    // every MMA completed (on the abort path too) before tensor memory is freed
+    if (elect_one()) umma_commit(bar_drain);
+    __syncwarp();
+    mbar_drain(bar_drain, 0, abort_flag);
+  } else {
+    // ------------------------------------------ epilogue: thread = channel = TMEM lane
+    const int q4 = warp & 3;  // warps 2..5: lane quarters 2, 3, 0, 1
+    const int ch = 32 * q4 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+    uint32_t n = 0;
+    for (int x = blockIdx.x; x < items; x += gridDim.x, ++n) {
+      const int ab = n & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_acc(ab), (n >> 1) & 1, wc))) break;
+      tc_fence_after();
+      uint32_t u0 = 0, u1 = 0;
+      tmem_ld2(trow + ab * 16, u0, u1);
+      tmem_ld_wait2(u0, u1);
+      // accumulator ab read out: the MMA of chunk n + 2 may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_accfree(ab));
+      if (ch >= D) continue;  // (d = 64: the upper lanes hold no channel)
+      const int z = x / (2 * nc), r2 = x - z * 2 * nc;
+      const bool isk = r2 >= nc;
+      const int c = isk ? r2 - nc : r2;
+      const int bh = a.bh0 + z;
+      const int bsz = isk ? s.bk : s.bq;
+      const int nT = isk ? s.Tk : s.Tq;
+      float* out = isk ? a.kbar : a.qbar;
+      const size_t plane = (size_t)s.B * s.H * nT * s.d;
+      const float s0 = __uint_as_float(u0), s1 = __uint_as_float(u1);
+      const int nblk = bsz == 128 ? 1 : 2;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (u >= nblk) break;
+        const int blk = c * nblk + u;
+        if (blk >= nT) break;
+        const int valid = min(bsz, s.N - blk * bsz);
+        const float inv = 1.f / static_cast<float>(valid);
+        // a block of 128 tokens spans both halves of the chunk
+        const float sum = nblk == 1 ? s0 + s1 : (u == 0 ? s0 : s1);
+        const float mean = sum * inv;
+        const float hi = tf32_rna(mean);
+        float* dst = out + ((size_t)bh * nT + blk) * s.d + ch;
+        dst[0] = hi;
+        dst[plane] = tf32_rna(mean - hi);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) report_error(status, kDevErrTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
   }
 }
 
@@ -1070,12 +1260,20 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
   int sel_occ = 0;
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sel_occ, select, kSelectThreads, sel_smem);
   if (e != cudaSuccess) return e;
-  const void* pool = s.dtype == 0
-                         ? (s.d == 128 ? (const void*)pool_kernel<__nv_bfloat16, 128> : (const void*)pool_kernel<__nv_bfloat16, 64>)
-                         : (s.d == 128 ? (const void*)pool_kernel<float, 128> : (const void*)pool_kernel<float, 64>);
+  const void* pool = s.d == 128 ? (const void*)pool_kernel<float, 128> : (const void*)pool_kernel<float, 64>;
   int pool_occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&pool_occ, pool, kPoolThreads, 0);
   if (e != cudaSuccess) return e;
+  // bf16 inputs: the tensor-core pooling over token tensor maps (128-token boxes)
+  CUtensorMap mqt, mkt;
+  auto pool_tc = s.d == 128 ? pool_tc_kernel<128> : pool_tc_kernel<64>;
+  if (s.dtype == 0) {
+    if (!make_token_map(&mqt, q, s, s.sb, s.sh, s.sn, kChunkTokens, false) ||
+        !make_token_map(&mkt, k, s, s.sb, s.sh, s.sn, kChunkTokens, false))
+      return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(pool_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kPoolTcSmem);
+    if (e != cudaSuccess) return e;
+  }
   // a third of the SMs' pooling capacity per chunk: the other kernels of the previous chunk
   // run beside it
   const int pool_blocks = std::max(1, sms * std::max(1, pool_occ) / 2);
@@ -1098,12 +1296,8 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
     const int pgrid = (int)std::min<long long>((pool_warps + 7) / 8, pool_blocks);
     prof_start(st, kPool);
     if (s.dtype == 0) {
-      auto qq = static_cast<const __nv_bfloat16*>(q);
-      auto kk = static_cast<const __nv_bfloat16*>(k);
-      if (s.d == 128)
-        pool_kernel<__nv_bfloat16, 128><<<pgrid, kPoolThreads, 0, st>>>(qq, kk, s, pa);
-      else
-        pool_kernel<__nv_bfloat16, 64><<<pgrid, kPoolThreads, 0, st>>>(qq, kk, s, pa);
+      const int tgrid = (int)std::min<long long>(pool_warps, sms);
+      pool_tc<<<tgrid, kPoolTcThreads, kPoolTcSmem, st>>>(mqt, mkt, s, pa, out.status);
     } else {
       auto qq = static_cast<const float*>(q);
       auto kk = static_cast<const float*>(k);

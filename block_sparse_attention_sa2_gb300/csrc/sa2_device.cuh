@@ -31,6 +31,10 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
+// Makes this thread's generic-proxy shared-memory writes visible to the async proxy (TMA,
+// tensor core) once the threads synchronise.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ void report_error(unsigned* status, unsigned code) {
   if (status) atomicCAS(status, 0u, code);
 }
