@@ -12,7 +12,7 @@
 //                    [2][B*H][T][d].  The HBM-bound part.
 //   pool_kernel      (fp32 inputs) the same with one warp per chunk: plain streaming loads
 //                    and fp32 sums in token order.
-//   score_tc_kernel  pooled scores S-bar = q-bar k-bar^T / sqrt(d) of a 128-row x 256-key
+//   score_tc_kernel  pooled scores S-bar = q-bar k-bar^T / sqrt(d) of a 128-row x 128-key
 //                    tile on the tensor cores (tcgen05, kind::tf32) as the three products
 //                    hi.hi + hi.lo + lo.hi -- about fp32 accuracy -- accumulated in tensor
 //                    memory and written to a scratch row in a lane-friendly permuted order.
@@ -39,7 +39,8 @@ namespace {
 
 constexpr int kChunkTokens = 128;           // tokens per pooling chunk
 constexpr int kScoreRows = 128;             // MMA M: query blocks per tile
-constexpr int kScoreKeys = 256;             // MMA N: key blocks per tile
+constexpr int kScoreKeys = 128;             // MMA N: key blocks per tile
+constexpr int kRowPad = 256;                // score rows are padded to a multiple of this
 constexpr int kSelectThreads = 256;
 constexpr int kChains = 2;                       // head chunks whose score / select / lists run at once
 constexpr size_t kScoreChunkBudget = 32u << 20;  // bytes of the kChains head-chunk buffers
@@ -52,6 +53,22 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// TMA load with an L2 eviction-priority policy (evict_first for data streamed once).
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 __device__ __forceinline__ float tf32_rna(float x) {
@@ -73,6 +90,7 @@ __device__ __forceinline__ float tf32_rna(float x) {
 struct PoolArgs {
   float* qbar;  // [2][B*H][Tq][d]
   float* kbar;  // [2][B*H][Tk][d]
+  int* ctr;     // chunk counter of this launch (zeroed on the stream before it; TC pooling)
   int bh0, nbh;
 };
 constexpr int kPoolThreads = 256;
@@ -179,17 +197,20 @@ __global__ void __launch_bounds__(kPoolThreads, 4) pool_kernel(const T* __restri
 // 64..127.  So D[c][0], D[c][1] are the sums of channel c over the two 64-token halves:
 // products by 1 are exact and the sums accumulate in fp32.  The SMs' ALUs stay free for
 // the kernels that run beside the pooling.
-// Persistent: CTA i takes the chunks i, i + gridDim.x, ... of the head chunk (Q chunks, then
-// K chunks, head by head).  Warp 0 streams them through a kPoolStages-deep ring, warp 1
-// owns tensor memory (two 16-column accumulators) and issues one 8-k-step MMA per chunk,
-// warps 2..5 read the accumulators out (thread = channel = TMEM lane), form the block means
-// (fp32, divided by the valid tokens) and store them as TF32 pairs, a warp's 32 channels as
-// one 128-byte row segment.
-constexpr int kPoolStages = 3;
+// Persistent: the CTAs take the chunks of the head chunk (Q chunks, then K chunks, head by
+// head) from a counter, so a CTA that starts late (its SM busy with the kernels beside the
+// pooling) takes fewer.  Warp 0 fetches them and streams them through a kPoolStages-deep
+// ring, publishing each chunk's index in a ring of item slots that the other roles read in
+// order; warp 1 owns tensor memory (two 16-column accumulators) and issues one 8-k-step MMA
+// per chunk, warps 2..5 read the accumulators out (thread = channel = TMEM lane), form the
+// block means (fp32, divided by the valid tokens) and store them as TF32 pairs, a warp's 32
+// channels as one 128-byte row segment.
+constexpr int kPoolStages = 2;
 constexpr int kPoolStageBytes = 128 * 128 * 2;  // two 64-channel panels of 128 tokens x 128 B
 constexpr int kPoolSelBytes = 2 * 16 * 128;     // Sel: 16 rows x 2 panels of 64 tokens
 constexpr int kPoolTcThreads = 192;
-constexpr int kPoolTcSmem = kPoolStages * kPoolStageBytes + kPoolSelBytes + 256 + 1024;
+constexpr int kPoolItems = 8;  // item slots in flight (>= stages + accumulators)
+constexpr int kPoolTcSmem = kPoolStages * kPoolStageBytes + kPoolSelBytes + 512 + 1024;
 
 __device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& r0, uint32_t& r1) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(taddr));
@@ -214,13 +235,28 @@ __global__ void __launch_bounds__(kPoolTcThreads, 1)
   auto bar_acc = [&](int b) { return smem_u32(&bars[2 * kPoolStages + b]); };          // accumulator b complete
   auto bar_accfree = [&](int b) { return smem_u32(&bars[2 * kPoolStages + 2 + b]); };  // ... read out
   const uint32_t bar_drain = smem_u32(&bars[2 * kPoolStages + 4]);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[2 * kPoolStages + 6]);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(&bars[2 * kPoolStages + 7]);
+  auto bar_item_full = [&](int i) { return smem_u32(&bars[2 * kPoolStages + 5 + i]); };  // slot i written
+  auto bar_item_free = [&](int i) { return smem_u32(&bars[2 * kPoolStages + 5 + kPoolItems + i]); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[2 * kPoolStages + 5 + 2 * kPoolItems]);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&bars[2 * kPoolStages + 6 + 2 * kPoolItems]);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(&bars[2 * kPoolStages + 7 + 2 * kPoolItems]);
   const WaitCtl wc{abort_flag, s.wait_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nc = (s.N + kChunkTokens - 1) / kChunkTokens;
   const int items = a.nbh * 2 * nc;
+  // a consumer warp takes item n from its slot and hands the slot back; -1 ends the loop
+  auto take_item = [&](uint32_t n, bool& ok) {
+    const int slot = n % kPoolItems;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar_item_full(slot), (n / kPoolItems) & 1, wc))) {
+      ok = false;
+      return -1;
+    }
+    const int x = item_slot[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_item_free(slot));
+    return x;
+  };
   // the selector: row j of panel p is 128 bytes of bf16 ones when token half p is column j
   // (j = p for j < 2), zeros otherwise; rows of ones or zeros are swizzle-invariant
   {
@@ -240,6 +276,10 @@ __global__ void __launch_bounds__(kPoolTcThreads, 1)
       mbar_init(bar_acc(b), 1);
       mbar_init(bar_accfree(b), 4);  // one arrival per epilogue warp
     }
+    for (int i = 0; i < kPoolItems; ++i) {
+      mbar_init(bar_item_full(i), 1);
+      mbar_init(bar_item_free(i), 5);  // the MMA warp and the four epilogue warps
+    }
     mbar_init(bar_drain, 1);
     fence_barrier_init();
   }
@@ -258,8 +298,16 @@ __global__ void __launch_bounds__(kPoolTcThreads, 1)
     if (lane == 0) {
       tma_prefetch_map(&mq);
       tma_prefetch_map(&mk);
-      uint32_t n = 0;
-      for (int x = blockIdx.x; x < items; x += gridDim.x, ++n) {
+      const uint64_t stream_policy = policy_evict_first();
+      uint32_t n = 0, loads = 0;  // items published, chunk loads issued
+      for (bool ok = true; ok; ++n) {
+        const int slot = n % kPoolItems;
+        if (n >= kPoolItems && !mbar_wait(bar_item_free(slot), ((n / kPoolItems) - 1) & 1, wc)) break;
+        const int x = atomicAdd(a.ctr, 1);
+        const bool done = x >= items;
+        item_slot[slot] = done ? -1 : x;
+        mbar_arrive(bar_item_full(slot));
+        if (done) break;
         const int z = x / (2 * nc), r2 = x - z * 2 * nc;
         const bool isk = r2 >= nc;
         const int c = isk ? r2 - nc : r2;
@@ -267,12 +315,15 @@ __global__ void __launch_bounds__(kPoolTcThreads, 1)
         const int st = n % kPoolStages;
         if (n >= kPoolStages && !mbar_wait(bar_empty(st), ((n / kPoolStages) - 1) & 1, wc)) break;
         mbar_arrive_expect_tx(bar_full(st), kPanels * 16384);
+        // Q and K are read once: evict them first, so that the chains' score rows and kept
+        // bits stay in L2
         for (int p = 0; p < kPanels; ++p)
-          tma_load_4d(sbase + st * kPoolStageBytes + p * 16384, isk ? &mk : &mq, bar_full(st), p * 64,
-                      c * kChunkTokens, h, b);
+          tma_load_4d_hint(sbase + st * kPoolStageBytes + p * 16384, isk ? &mk : &mq, bar_full(st), p * 64,
+                           c * kChunkTokens, h, b, stream_policy);
+        ++loads;
       }
       // no copy may still be in flight when the CTA exits
-      for (uint32_t v = n > kPoolStages ? n - kPoolStages : 0; v < n; ++v)
+      for (uint32_t v = loads > kPoolStages ? loads - kPoolStages : 0; v < loads; ++v)
         mbar_drain(bar_full(v % kPoolStages), (v / kPoolStages) & 1, abort_flag);
     }
   } else if (warp == 1) {
@@ -281,8 +332,9 @@ __global__ void __launch_bounds__(kPoolTcThreads, 1)
     // Sel as the K-major B operand (16 rows); X as the MN-major A operand: M = 128 channels
     // (64-channel groups 16 KB apart), 16 tokens (2048 B) per k-step
     const uint64_t seld = smem_desc(ssel, 16, 1024);
-    uint32_t n = 0;
-    for (int x = blockIdx.x; x < items; x += gridDim.x, ++n) {
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+      if (take_item(n, ok) < 0) break;
       const int st = n % kPoolStages, ab = n & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (n / kPoolStages) & 1, wc) &&
                                        (n < 2 || mbar_wait(bar_accfree(ab), ((n >> 1) - 1) & 1, wc))))
@@ -307,8 +359,10 @@ __global__ void __launch_bounds__(kPoolTcThreads, 1)
     const int q4 = warp & 3;  // warps 2..5: lane quarters 2, 3, 0, 1
     const int ch = 32 * q4 + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-    uint32_t n = 0;
-    for (int x = blockIdx.x; x < items; x += gridDim.x, ++n) {
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+      const int x = take_item(n, ok);
+      if (x < 0) break;
       const int ab = n & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar_acc(ab), (n >> 1) & 1, wc))) break;
       tc_fence_after();
@@ -358,13 +412,14 @@ __global__ void __launch_bounds__(kPoolTcThreads, 1)
 
 // ------------------------------------------------------------------------ TC scores
 
-// One tile: 128 query blocks (TMEM lanes) x 256 key blocks (columns) of one head.  The
+// One tile: 128 query blocks (TMEM lanes) x 128 key blocks (columns) of one head.  The
 // channels arrive in panels of 32 (128 bytes, the TF32 K-major 128-byte-swizzled layout),
-// two panels in flight: per panel the hi and lo parts of both operands (96 KB).
+// two panels in flight: per panel the hi and lo parts of both operands (64 KB, so that a
+// pooling CTA fits beside the two stages on an SM).
 // S = Ahi Bhi + Ahi Blo + Alo Bhi over 8-channel k-steps; the epilogue scales by 1/sqrt(d)
 // and writes the tile rows to the scratch [chunk heads][Tq_pad][Tk_pad].
 constexpr int kAPanelBytes = kScoreRows * 128;  // 16 KB
-constexpr int kBPanelBytes = kScoreKeys * 128;  // 32 KB
+constexpr int kBPanelBytes = kScoreKeys * 128;  // 16 KB
 constexpr int kScoreStageBytes = 2 * kAPanelBytes + 2 * kBPanelBytes;
 constexpr int kScoreSmem = 2 * kScoreStageBytes + 256 + 1024;
 
@@ -394,7 +449,7 @@ struct ScoreArgs {
 
 // Persistent: CTA c takes tiles c, c + gridDim.x, ... (key chunk fastest, then row tile,
 // then head).  Warp 0 streams the panels of its tiles through a two-stage ring without
-// stopping between tiles, warp 1 owns tensor memory (two 256-column accumulators) and issues
+// stopping between tiles, warp 1 owns tensor memory (two 128-column accumulators) and issues
 // the MMAs, warps 2..5 read each finished accumulator out (thread = tile row = TMEM lane),
 // so the write-out of tile i overlaps the products of tile i + 1.
 constexpr int kScoreThreadsP = 192;
@@ -891,7 +946,7 @@ __device__ __forceinline__ void emit_row(const uint4* keys4, int Tk, const MaskO
   const unsigned lt = (1u << lane) - 1u;
   int kept = 0, ties_seen = 0;
   int32_t* ridx = out.row_idx + rowid * Tk;
-  uint8_t* mrow = out.mask + rowid * Tk;
+  uint8_t* mrow = out.mask ? out.mask + rowid * Tk : nullptr;
   float* prow = out.pooled_p ? out.pooled_p + rowid * Tk : nullptr;
   const int nch = (Tk + 127) / 128;
   for (int c = 0; c < nch; ++c) {
@@ -915,7 +970,7 @@ __device__ __forceinline__ void emit_row(const uint4* keys4, int Tk, const MaskO
       kept += __popc(km);
       if (lane == 0 && 4 * c + i < W) bits_row[4 * c + i] = km;
       if (valid) {
-        mrow[j] = keep ? 1 : 0;
+        if (mrow) mrow[j] = keep ? 1 : 0;
         if (prow) prow[j] = __uint_as_float(key[i]);
       }
     }
@@ -959,21 +1014,21 @@ __global__ void __launch_bounds__(kSelectThreads, KPL >= 16 ? 3 : 4)
         v[4 * c + 2] = x.z;
         v[4 * c + 3] = x.w;
       }
-      float mx = v[0];
+      // the row maximum and the row sum as 4-way trees (short dependency chains)
+      float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-      for (int r = 1; r < KPL; ++r) mx = fmaxf(mx, v[r]);
+      for (int r = 4; r < KPL; ++r) m4[r & 3] = fmaxf(m4[r & 3], v[r]);
+      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      float s0 = 0.f, s1 = 0.f;
+      const float mb = mx * kLog2e;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int r = 0; r < KPL; ++r) {
-        v[r] = ex2_approx((v[r] - mx) * kLog2e);  // -inf padding: 0
-        if (r & 1)
-          s1 += v[r];
-        else
-          s0 += v[r];
+        v[r] = ex2_approx(fmaf(v[r], kLog2e, -mb));  // -inf padding: 0
+        s4[r & 3] += v[r];
       }
-      float sum = s0 + s1;
+      float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       const float inv = __frcp_rn(sum);
@@ -1133,7 +1188,7 @@ bool make_pooled_map(CUtensorMap* map, const float* base, const ShapeArgs& s, in
 }
 
 struct MaskLayout {
-  size_t qbar, kbar, sbar, bits, total;
+  size_t qbar, kbar, sbar, bits, ctr, total;
   size_t sbar_buf, bits_buf;  // bytes of one buffer of each
   int tq_pad, tk_pad, hc;     // padded tile extents; heads per chunk
   int W;                      // 32-bit words of kept bits per row
@@ -1147,7 +1202,7 @@ MaskLayout mask_layout(const ShapeArgs& s, size_t chunk_budget) {
   const size_t BH = (size_t)s.B * s.H;
   auto al = [](size_t x) { return (x + 1023) / 1024 * 1024; };
   L.tq_pad = (s.Tq + kScoreRows - 1) / kScoreRows * kScoreRows;
-  L.tk_pad = (s.Tk + kScoreKeys - 1) / kScoreKeys * kScoreKeys;
+  L.tk_pad = (s.Tk + kRowPad - 1) / kRowPad * kRowPad;
   L.W = (s.Tk + 31) / 32;
   const size_t tile_head = (size_t)L.tq_pad * L.tk_pad * 4, bits_head = (size_t)s.Tq * L.W * 4;
   L.hc = (int)std::max<size_t>(1, std::min<size_t>(BH, chunk_budget / (kChains * (tile_head + bits_head) + 4096)));
@@ -1157,7 +1212,8 @@ MaskLayout mask_layout(const ShapeArgs& s, size_t chunk_budget) {
   L.kbar = al(2 * BH * s.Tq * s.d * 4);
   L.sbar = L.kbar + al(2 * BH * s.Tk * s.d * 4);
   L.bits = L.sbar + kChains * L.sbar_buf;
-  L.total = L.bits + kChains * L.bits_buf;
+  L.ctr = L.bits + kChains * L.bits_buf;  // the pooling's chunk counters, one per head chunk
+  L.total = L.ctr + al(BH * sizeof(int));
   return L;
 }
 
@@ -1212,6 +1268,7 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
   const MaskLayout L = scratch_bytes == 0 ? mask_layout(s, kScoreChunkBudget)
                                           : mask_layout(s, std::min(kScoreChunkBudget, scratch_bytes - L0.sbar));
   uint8_t* base = static_cast<uint8_t*>(scratch);
+  int* pool_ctr = reinterpret_cast<int*>(base + L.ctr);
   float* qbar = reinterpret_cast<float*>(base + L.qbar);
   float* kbar = reinterpret_cast<float*>(base + L.kbar);
   float* sbar_buf[kChains];
@@ -1280,6 +1337,10 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
 
   std::lock_guard<std::mutex> lock(aux->mu);
   const int BH = s.B * s.H;
+  if (s.dtype == 0) {
+    e = cudaMemsetAsync(pool_ctr, 0, (size_t)((BH + L.hc - 1) / L.hc) * sizeof(int), st);
+    if (e != cudaSuccess) return e;
+  }
   const int nc = (s.N + kChunkTokens - 1) / kChunkTokens;
   for (int bh0 = 0, ci = 0; bh0 < BH; bh0 += L.hc, ++ci) {
     const int nbh = std::min(L.hc, BH - bh0);
@@ -1292,6 +1353,7 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
     pa.kbar = kbar;
     pa.bh0 = bh0;
     pa.nbh = nbh;
+    pa.ctr = pool_ctr + ci;
     const long long pool_warps = (long long)nbh * 2 * nc;
     const int pgrid = (int)std::min<long long>((pool_warps + 7) / 8, pool_blocks);
     prof_start(st, kPool);

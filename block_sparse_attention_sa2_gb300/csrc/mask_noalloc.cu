@@ -54,7 +54,7 @@ extern "C" sa2_status sa2_build_mask_noalloc(const sa2_shape* shape, const void*
   ShapeArgs s;
   sa2_status st = check_shape(shape, &s);
   if (st != SA2_OK) return st;
-  if (!q || !k || !out || !out->row_cnt || !out->row_idx || !out->col_cnt || !out->col_idx || !out->mask)
+  if (!q || !k || !out || !out->row_cnt || !out->row_idx || !out->col_cnt || !out->col_idx)
     return SA2_ERR_INVALID_ARG;
   SelectArgs sel;
   st = make_select_args(s, topk, topp, &sel);

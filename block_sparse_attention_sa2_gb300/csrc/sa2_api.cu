@@ -99,18 +99,17 @@ size_t token_elems(const ShapeArgs& s) { return (size_t)s.B * s.H * s.N * s.d; }
 
 sa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SA2_OK : SA2_ERR_CUDA; }
 
+// Mask workspace: the builder's scratch (pooled pairs, the chunk buffers).
 struct MaskWs {
-  size_t pooled, mask, total;
+  size_t pooled, total;
 };
 MaskWs mask_ws(const ShapeArgs& s) {
   MaskWs w;
   w.pooled = 0;
-  w.mask = align_up(mask_scratch_bytes(s, 0));
-  w.total = align_up(w.mask + (size_t)s.B * s.H * s.Tq * s.Tk);
+  w.total = align_up(mask_scratch_bytes(s, 0));
   return w;
 }
 
-// Forward workspace: fp16 copy of V (every call); fp16 copies of Q and K (fp32 calls).
 // Forward workspace: the fp16 copy of V; for fp32 calls also the fp16 copies of Q and K and
 // their fp16 residuals (the split S product); the launch order of the query blocks.
 struct FwdWs {
@@ -217,7 +216,7 @@ sa2_status sa2_build_mask(const sa2_shape* shape, const void* q, const void* k, 
   mo.row_idx = out->row_idx;
   mo.col_cnt = out->col_cnt;
   mo.col_idx = out->col_idx;
-  mo.mask = out->mask ? out->mask : wsb + w.mask;
+  mo.mask = out->mask;  // null: not written
   mo.pooled_p = out->pooled_p;
   mo.status = status_ptr();
   return cuda_status(launch_build_mask(s, q, k, sel, wsb + w.pooled, 0, mo, static_cast<cudaStream_t>(stream)));

@@ -52,7 +52,7 @@ struct MaskOut {
   int32_t* row_idx;
   int32_t* col_cnt;
   int32_t* col_idx;
-  uint8_t* mask;      // never null here (workspace stands in when the caller passes null)
+  uint8_t* mask;      // may be null (not written)
   float* pooled_p;    // may be null
   unsigned* status;   // device status word
 };

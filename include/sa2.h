@@ -88,8 +88,9 @@ int sa2_version(void);
 const char* sa2_status_string(sa2_status status);
 
 /*
- * Bytes of device workspace sa2_build_mask needs for this shape (the fp32 pooled queries
- * and keys).  Returns 0 for an invalid shape.
+ * Bytes of device workspace sa2_build_mask needs for this shape (the pooled queries and
+ * keys as fp32 TF32 pairs, and two buffers of the score rows and kept bits of a chunk of
+ * heads).  Returns 0 for an invalid shape.
  */
 size_t sa2_mask_workspace_size(const sa2_shape* shape);
 
@@ -130,7 +131,6 @@ sa2_status sa2_build_mask(const sa2_shape* shape, const void* q, const void* k, 
  * score rows and kept bits of a chunk of heads, the chunk as large as the array allows)
  * lives in a static device array of SA2_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the library
  * holds until the process exits.  Nothing is allocated: no cudaMalloc, no cudaFree.
- *   - out->mask is required here (the u8 mask is built in place of the workspace copy).
  *   - A shape whose scratch exceeds SA2_NOALLOC_SCRATCH_BYTES is rejected with
  *     SA2_ERR_WORKSPACE before anything is launched.
  *   - The first call on a device looks up the array's device address on that device (the

@@ -72,6 +72,8 @@ class Model:
     """Shared scheduler: actors are (name, cta, generator) yielding ("wait", bar, phase) or
     ("step",); subclasses define the CTA state, the engines' completions and the roles."""
 
+    SKIPS_EMPTY = True  # items with an empty list produce no epilogue
+
     def __init__(self, seed, ncta, items, drop=(), expire=False):
         self.rng = random.Random(seed)
         self.items, self.ncta, self.drop = items, ncta, set(drop)
@@ -793,6 +795,130 @@ def run_forward_trials(trials, drop=(), seed0=0, expire=False):
     return None
 
 
+class PoolModel(Model):
+    """pool_tc_kernel (mask builder): items are 128-token chunks taken by every CTA's producer
+    from one counter (`items[x]` is unused: every chunk is one load and one MMA).  The chunks
+    stream through a 2-deep stage ring; each chunk's index goes to a ring of 8 item slots read
+    by the MMA warp and the four epilogue warps; the MMA of chunk n writes accumulator n % 2,
+    which the epilogue warps read out before the MMA of chunk n + 2 may overwrite it."""
+
+    STAGES, SLOTS, NW = 2, 8, 4
+    SKIPS_EMPTY = False  # every chunk is pooled
+
+    def make_cta(self, cid):
+        c = type("CTA", (), {})()
+        c.cid = cid
+        c.full = [Bar(f"full{i}", 1) for i in range(self.STAGES)]
+        c.empty = [Bar(f"empty{i}", 1) for i in range(self.STAGES)]
+        c.acc = [Bar(f"acc{i}", 1) for i in range(2)]
+        c.accfree = [Bar(f"accfree{i}", self.NW) for i in range(2)]
+        c.drain = Bar("drain", 1)
+        c.item_full = [Bar(f"item_full{i}", 1) for i in range(self.SLOTS)]
+        c.item_free = [Bar(f"item_free{i}", 1 + self.NW) for i in range(self.SLOTS)]
+        c.slot, c.slot_reads = [None] * self.SLOTS, [1 + self.NW] * self.SLOTS
+        c.stage, c.stage_readers = [None] * self.STAGES, [0] * self.STAGES
+        c.accv, c.acc_read = [None, None], [set(range(self.NW)), set(range(self.NW))]
+        c.mmaq = {1: [], 2: []}
+        return c
+
+    def roles(self, c):
+        return ([("producer", c, self.producer(c)), ("mma", c, self.mma(c))] +
+                [(f"epi{w}", c, self.epilogue(c, w)) for w in range(self.NW)])
+
+    def take(self, c, n):
+        slot = n % self.SLOTS
+        yield from self.wait(c.item_full[slot], n // self.SLOTS)
+        x = c.slot[slot]
+        c.slot_reads[slot] += 1
+        c.item_free[slot].arrive()
+        return x
+
+    def complete_tma(self, job):
+        c, kind, st, x = job
+        check(c.stage_readers[st] == 0, f"stage {st} overwritten while the MMA reads it")
+        c.stage[st] = x
+        c.full[st].complete_tx(1)
+
+    def complete_mma(self, c, op):
+        if op[0] == "commit":
+            op[1].arrive()
+            return
+        _, n, st, ab, x = op
+        check(c.stage[st] == x, f"MMA of chunk {x}: stage {st} holds {c.stage[st]}")
+        check(c.acc_read[ab] >= set(range(self.NW)), f"accumulator {ab} overwritten before it was read out")
+        c.accv[ab], c.acc_read[ab] = x, set()
+        c.stage_readers[st] -= 1
+
+    def producer(self, c):
+        n = loads = 0
+        try:
+            while True:
+                slot = n % self.SLOTS
+                if n >= self.SLOTS and "item_free" not in self.drop:
+                    yield from self.wait(c.item_free[slot], n // self.SLOTS - 1)
+                x = self.counter
+                self.counter += 1
+                done = x >= len(self.items)
+                check(c.slot_reads[slot] == 1 + self.NW, f"item slot {slot} overwritten before every role read it")
+                c.slot[slot], c.slot_reads[slot] = (-1 if done else x), 0
+                c.item_full[slot].arrive()
+                if done:
+                    break
+                st = n % self.STAGES
+                if n >= self.STAGES and "empty" not in self.drop:
+                    yield from self.wait(c.empty[st], n // self.STAGES - 1)
+                c.full[st].expect_tx(1)
+                self.tma.append((c, "x", st, x))
+                loads += 1
+                n += 1
+                yield ("step",)
+        except Aborted:
+            if "abort_drain" in self.drop:
+                return
+        for v in range(max(0, loads - self.STAGES), loads):
+            yield from self.drain(c.full[v % self.STAGES], v // self.STAGES)
+
+    def mma(self, c):
+        n = 0
+        try:
+            while True:
+                x = yield from self.take(c, n)
+                if x < 0:
+                    break
+                st, ab = n % self.STAGES, n & 1
+                yield from self.wait(c.full[st], n // self.STAGES)
+                if n >= 2 and "accfree" not in self.drop:
+                    yield from self.wait(c.accfree[ab], (n >> 1) - 1)
+                check(c.stage[st] == x, f"MMA of chunk {x} issued on stage {st} holding {c.stage[st]}")
+                c.mmaq[1] += [("MMA", n, st, ab, x), ("commit", c.empty[st]), ("commit", c.acc[ab])]
+                c.stage_readers[st] += 1
+                n += 1
+                yield ("step",)
+        except Aborted:
+            pass
+        c.mmaq[1].append(("commit", c.drain))
+        yield from self.mma_drain(c, c.drain)
+
+    def epilogue(self, c, w):
+        n = 0
+        try:
+            while True:
+                x = yield from self.take(c, n)
+                if x < 0:
+                    break
+                ab = n & 1
+                yield from self.wait(c.acc[ab], n >> 1)
+                check(c.accv[ab] == x, f"epi{w}: accumulator {ab} holds chunk {c.accv[ab]}, not {x}")
+                c.acc_read[ab].add(w)
+                c.accfree[ab].arrive()
+                if w == 0:
+                    self.processed.append(x)
+                n += 1
+                yield ("step",)
+        except Aborted:
+            pass
+
+
 def run_trials(model_cls, trials, drop=(), seed0=0, expire=False):
     """Random item lists (with empty items) on 1-3 CTAs; returns the first error, or None.
     With `expire`, waits expire at random (the abort path) and items may stay unfinished."""
@@ -804,7 +930,7 @@ def run_trials(model_cls, trials, drop=(), seed0=0, expire=False):
         try:
             model.run()
             if not expire:
-                want = sorted(x for x in range(nitems) if items[x] > 0)
+                want = sorted(x for x in range(nitems) if items[x] > 0 or not model_cls.SKIPS_EMPTY)
                 check(sorted(model.processed) == want, f"items processed {sorted(model.processed)}, want {want}")
         except ProtocolError as e:
             return f"trial {t}, items {items}: {e}"

@@ -121,6 +121,31 @@ def test_mask_full_size_wan_shapes(sa2, ci):
     print(f"config {ci}: sparsity {1 - kept:.4f}, exempt {n_exempt}")
 
 
+def test_mask_lists_without_the_optional_outputs(sa2):
+    """The u8 mask and P-bar are optional outputs: without them the lists (which the column
+    lists build from the rows' kept bits, not from the u8 mask) are the same, bit for bit."""
+    import torch
+    cfg = CONFIGS[1]
+    x = make_inputs(cfg, tensors=("q", "k"))
+    q, k = to_device(x["q"]), to_device(x["k"])
+    full = sa2.build_mask(q, k, 0.05, 0.9, bq=cfg.bq, bk=cfg.bk, want_pooled=True)
+    bare = sa2.build_mask(q, k, 0.05, 0.9, bq=cfg.bq, bk=cfg.bk, want_mask=False, want_pooled=False)
+    sa2.check_device()
+    torch.cuda.synchronize()
+    assert bare.mask is None and bare.pooled_p is None
+    for name in ("row_cnt", "col_cnt"):
+        assert torch.equal(getattr(full, name), getattr(bare, name)), name
+    rc, cc = full.row_cnt.cpu().numpy(), full.col_cnt.cpu().numpy()
+    ri, ci = full.row_idx.cpu().numpy(), full.col_idx.cpu().numpy()
+    bri, bci = bare.row_idx.cpu().numpy(), bare.col_idx.cpu().numpy()
+    for b in range(cfg.B):
+        for h in range(cfg.H):
+            for i in range(cfg.Tq):
+                assert (ri[b, h, i, :rc[b, h, i]] == bri[b, h, i, :rc[b, h, i]]).all()
+            for j in range(cfg.Tk):
+                assert (ci[b, h, j, :cc[b, h, j]] == bci[b, h, j, :cc[b, h, j]]).all()
+
+
 def test_mask_rejects_bad_arguments(sa2):
     torch = pytest.importorskip("torch")
     q = torch.zeros((1, 1, 128, 128), dtype=torch.bfloat16, device="cuda")

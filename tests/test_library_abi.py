@@ -127,9 +127,10 @@ def test_noalloc_rejects_oversized_shapes_on_the_host(lib):
     big = _shape(sa2, H=40, N=75600, stride_b=40 * 75600 * 128, stride_h=75600 * 128)
     assert lib.sa2_build_mask_noalloc(ctypes.byref(big), 256, 256, ctypes.c_float(0.1), ctypes.c_float(0.5),
                                       ctypes.byref(m), None) == WORKSPACE
-    no_mask = sa2.BlockMaskStruct(16, 16, 16, 16, None, None)
+    # the lists are required (the u8 mask and P-bar are optional outputs)
+    no_cols = sa2.BlockMaskStruct(16, 16, None, 16, None, None)
     assert lib.sa2_build_mask_noalloc(ctypes.byref(_shape(sa2)), 256, 256, ctypes.c_float(0.1), ctypes.c_float(0.5),
-                                      ctypes.byref(no_mask), None) == INVALID
+                                      ctypes.byref(no_cols), None) == INVALID
 
 
 def test_profiler_size_query_needs_no_gpu(lib):
