@@ -26,8 +26,9 @@
 // writing dS_j, so the tensor pipe never drains to let an MMA overwrite an operand.
 //
 // The CTAs are persistent, one per SM, and take query blocks from a counter until none is
-// left, head by head and within a head longest list first.  The producer publishes each block in a two-slot ring in shared memory that every
-// role reads; the K / V rings and the TMEM buffers run on across blocks.  So the set-up is
+// left, in the order of launch_item_order (head by head, longest list first within a head,
+// lists too long to start late in front).  The producer publishes each block in a two-slot
+// ring in shared memory that every role reads; the K / V rings and the TMEM buffers run on across blocks.  So the set-up is
 // paid once per SM, the next block's K_j / V_j stream in behind the current block's, its
 // Q and dO load as soon as the current block's S_j / dP_j MMAs have completed, and its
 // first S_j / dP_j MMAs run while the row threads store the current block's dQ.
@@ -121,10 +122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{abort_flag, s.wait_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Work items are query blocks (block x: block x % Tq of head x / Tq), taken head by head
-  // and longest first within a head: each CTA stays resident and takes items from a counter
-  // over that order, its first being order[blockIdx.x], the next order[gridDim.x + (counter
-  // value)].
+  // Work items are query blocks (block x: block x % Tq of head x / Tq), taken in the order of
+  // launch_item_order: each CTA stays resident and takes items from a counter over that
+  // order, its first being order[blockIdx.x], the next order[gridDim.x + (counter value)].
   const int num_items = s.B * s.H * s.Tq;
   // list length of item x, clamped to [0, Tk] (the producer reports a bad value)
   auto item_len = [&](int x, bool report) {
@@ -482,7 +482,7 @@ cudaError_t launch_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMa
   const long long items = (long long)s.B * s.H * s.Tq;
   const long long grid = items < sms ? items : sms;  // persistent: one CTA per SM
   prof_start(st, kAttnBwdDq);
-  e = launch_item_order(a.row_cnt, s.B * s.H, s.Tq, s.Tk, const_cast<int32_t*>(a.order), a.work_ctr, st);
+  e = launch_item_order(a.row_cnt, s.B * s.H, s.Tq, s.Tk, (int)grid, a.order, a.work_ctr, st);
   if (e == cudaSuccess) kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, mdo, mql, mkl, s, a);
   prof_stop(st, kAttnBwdDq);
   return e == cudaSuccess ? cudaGetLastError() : e;

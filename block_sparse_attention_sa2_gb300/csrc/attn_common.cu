@@ -158,30 +158,73 @@ static int grid_for(int64_t items) { return (int)std::min<int64_t>((items + 255)
 
 namespace {
 
-// Counting sort of each head's query blocks by descending list length, one CTA per head: a
-// histogram of Tk - length in shared memory, its exclusive scan, and a scatter through the
-// running bin offsets.  Heads stay in order, so the items in flight at any time come from one
-// or two heads and share their K / V blocks in L2.
+// The launch order of the query blocks.  Heads stay in order, each head's blocks by descending
+// list length, so the items in flight at any time come from one or two heads and share their
+// K / V blocks in L2.  A head's long lists would end after everything else when that head
+// comes late, so a list of head h longer than the work the heads from h on leave per slot,
+// (heads - h) * W_h / slots blocks with W_h the head's total, is taken out of its head and
+// put into one list in front, all heads' long lists together by descending length (the
+// longest-processing-time-first rule).  Two passes of one CTA per head: the first sets the
+// head's threshold and counts its long lists into a global histogram, the second places the
+// long lists from the global histogram and the rest of the head behind the long list and the
+// earlier heads.  Histograms are counting sorts over Tk - length in shared memory.
 constexpr int kOrderThreads = 1024;
 
-__global__ void __launch_bounds__(kOrderThreads) item_order_kernel(const int32_t* __restrict__ row_cnt, int Tq,
-                                                                   int Tk, int32_t* __restrict__ order,
-                                                                   int* __restrict__ work_ctr) {
-  extern __shared__ int bins[];  // Tk + 1
-  __shared__ int warp_sum[kOrderThreads / 32];
+struct OrderScratch {
+  int* hist;    // [Tk + 1] long lists of all heads by Tk - length (zeroed before the first pass)
+  int* cur;     // [Tk + 1] cursors into hist's bins (zeroed before the first pass)
+  int* thr;     // [heads] a list is long when its length is above this
+  int* nshort;  // [heads] the lists of the head that are not long
+};
+
+__device__ __forceinline__ int clamped_len(const int32_t* row_cnt, int64_t x, int Tk) {
+  const int n = row_cnt[x];
+  return n < 0 ? 0 : (n > Tk ? Tk : n);
+}
+
+__global__ void __launch_bounds__(kOrderThreads) item_split_kernel(const int32_t* __restrict__ row_cnt, int Tq,
+                                                                   int Tk, int slots, OrderScratch o) {
+  __shared__ unsigned long long work;
+  __shared__ int nlong;
+  const int tid = threadIdx.x, h = blockIdx.x;
+  const int64_t x0 = (int64_t)h * Tq;
+  if (tid == 0) {
+    work = 0;
+    nlong = 0;
+  }
+  __syncthreads();
+  unsigned long long w = 0;
+  for (int i = tid; i < Tq; i += kOrderThreads) w += (unsigned long long)clamped_len(row_cnt, x0 + i, Tk);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
+  if ((tid & 31) == 0) atomicAdd(&work, w);
+  __syncthreads();
+  const unsigned long long later = (unsigned long long)(gridDim.x - h) * work;
+  const unsigned long long t = (later + (unsigned long long)slots - 1) / (unsigned long long)slots;
+  const int thr = t > (unsigned long long)Tk ? Tk : (int)t;
+  int mine = 0;
+  for (int i = tid; i < Tq; i += kOrderThreads) {
+    const int n = clamped_len(row_cnt, x0 + i, Tk);
+    if (n > thr) {
+      atomicAdd(&o.hist[Tk - n], 1);
+      ++mine;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+  if ((tid & 31) == 0 && mine) atomicAdd(&nlong, mine);
+  __syncthreads();
+  if (tid == 0) {
+    o.thr[h] = thr;
+    o.nshort[h] = Tq - nlong;
+  }
+}
+
+// In-place exclusive scan of bins[0, nb) by the whole block; returns the total to every thread.
+__device__ int scan_bins(int* bins, int nb, int* warp_sum) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t x0 = (int64_t)blockIdx.x * Tq;  // the head's first item
-  const int nb = Tk + 1;
-  for (int i = tid; i < nb; i += kOrderThreads) bins[i] = 0;
-  __syncthreads();
-  auto bin_of = [&](int i) {
-    const int n = row_cnt[x0 + i];
-    return Tk - (n < 0 ? 0 : (n > Tk ? Tk : n));
-  };
-  for (int i = tid; i < Tq; i += kOrderThreads) atomicAdd(&bins[bin_of(i)], 1);
-  __syncthreads();
-  // exclusive scan: each thread sums a contiguous run of bins, the runs are scanned across
-  // the block, then each run is rewritten as offsets
+  // each thread sums a contiguous run of bins, the runs are scanned across the block, then
+  // each run is rewritten as offsets
   const int per = (nb + kOrderThreads - 1) / kOrderThreads;
   const int b0 = min(nb, tid * per), b1 = min(nb, b0 + per);
   int run = 0;
@@ -210,18 +253,73 @@ __global__ void __launch_bounds__(kOrderThreads) item_order_kernel(const int32_t
     bins[i] = base;
     base += c;
   }
+  const int total = warp_sum[kOrderThreads / 32 - 1];
   __syncthreads();
-  for (int i = tid; i < Tq; i += kOrderThreads) order[x0 + atomicAdd(&bins[bin_of(i)], 1)] = (int32_t)(x0 + i);
-  if (work_ctr && blockIdx.x == 0 && tid == 0) *work_ctr = 0;
+  return total;
+}
+
+__global__ void __launch_bounds__(kOrderThreads) item_order_kernel(const int32_t* __restrict__ row_cnt, int Tq,
+                                                                   int Tk, int32_t* __restrict__ order,
+                                                                   OrderScratch o, int* __restrict__ work_ctr) {
+  extern __shared__ int bins[];  // Tk + 1
+  __shared__ int warp_sum[kOrderThreads / 32];
+  __shared__ int earlier;
+  const int tid = threadIdx.x, h = blockIdx.x;
+  const int64_t x0 = (int64_t)h * Tq;
+  const int nb = Tk + 1;
+  const int thr = o.thr[h];
+  // the long lists of every head: global offsets from the global histogram
+  for (int i = tid; i < nb; i += kOrderThreads) bins[i] = o.hist[i];
+  if (tid == 0) earlier = 0;
+  __syncthreads();
+  const int nlong_all = scan_bins(bins, nb, warp_sum);
+  for (int i = tid; i < Tq; i += kOrderThreads) {
+    const int n = clamped_len(row_cnt, x0 + i, Tk);
+    if (n > thr) order[bins[Tk - n] + atomicAdd(&o.cur[Tk - n], 1)] = (int32_t)(x0 + i);
+  }
+  // the rest of this head, behind the long lists and the rest of the earlier heads
+  int e = 0;
+  for (int g = tid; g < h; g += kOrderThreads) e += o.nshort[g];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
+  __syncthreads();
+  if ((tid & 31) == 0 && e) atomicAdd(&earlier, e);
+  for (int i = tid; i < nb; i += kOrderThreads) bins[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < Tq; i += kOrderThreads) {
+    const int n = clamped_len(row_cnt, x0 + i, Tk);
+    if (n <= thr) atomicAdd(&bins[Tk - n], 1);
+  }
+  __syncthreads();
+  scan_bins(bins, nb, warp_sum);
+  const int base = nlong_all + earlier;
+  for (int i = tid; i < Tq; i += kOrderThreads) {
+    const int n = clamped_len(row_cnt, x0 + i, Tk);
+    if (n <= thr) order[base + atomicAdd(&bins[Tk - n], 1)] = (int32_t)(x0 + i);
+  }
+  if (work_ctr && h == 0 && tid == 0) *work_ctr = 0;
 }
 
 }  // namespace
 
-cudaError_t launch_item_order(const int32_t* row_cnt, int heads, int Tq, int Tk, int32_t* order, int* work_ctr,
-                              cudaStream_t st) {
+size_t item_order_ints(int heads, int Tq, int Tk) {
+  return (size_t)heads * Tq + 2 * ((size_t)Tk + 1) + 2 * (size_t)heads;
+}
+
+cudaError_t launch_item_order(const int32_t* row_cnt, int heads, int Tq, int Tk, int slots, int32_t* order,
+                              int* work_ctr, cudaStream_t st) {
   const size_t smem = (size_t)(Tk + 1) * sizeof(int);
   if (smem > 48 * 1024) return cudaErrorInvalidValue;  // Tk <= 12287
-  item_order_kernel<<<heads, kOrderThreads, smem, st>>>(row_cnt, Tq, Tk, order, work_ctr);
+  if (heads <= 0 || Tq <= 0) return cudaSuccess;
+  OrderScratch o;
+  o.hist = order + (size_t)heads * Tq;
+  o.cur = o.hist + (Tk + 1);
+  o.thr = o.cur + (Tk + 1);
+  o.nshort = o.thr + heads;
+  cudaError_t e = cudaMemsetAsync(o.hist, 0, sizeof(int) * 2 * ((size_t)Tk + 1), st);
+  if (e != cudaSuccess) return e;
+  item_split_kernel<<<heads, kOrderThreads, 0, st>>>(row_cnt, Tq, Tk, slots < 1 ? 1 : slots, o);
+  item_order_kernel<<<heads, kOrderThreads, smem, st>>>(row_cnt, Tq, Tk, order, o, work_ctr);
   return cudaGetLastError();
 }
 

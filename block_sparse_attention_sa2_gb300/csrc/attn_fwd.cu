@@ -119,8 +119,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const WaitCtl wc{abort_flag, s.wait_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // CTAs launch head by head, within a head longest list first: the CTAs in flight share
-  // their heads' K / V in L2, and the last wave holds the shortest lists
+  // CTAs launch in the order of launch_item_order: head by head, within a head longest list
+  // first, so the CTAs in flight share their heads' K / V in L2 and the last wave holds short
+  // lists; the lists too long to start late launch first of all
   const int x = a.order[blockIdx.x];
   const int bh = x / s.Tq;
   const int qi = x % s.Tq;
@@ -422,9 +423,14 @@ cudaError_t launch_fwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtens
   auto kern = attn_fwd_kernel<D, OutT, S_F16, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  if (e != cudaSuccess) return e;
   const long long grid = (long long)s.B * s.H * s.Tq;
   prof_start(st, kAttnFwd);
-  e = launch_item_order(a.row_cnt, s.B * s.H, s.Tq, s.Tk, a.order, nullptr, st);
+  e = launch_item_order(a.row_cnt, s.B * s.H, s.Tq, s.Tk, sms * (per_sm > 0 ? per_sm : 1), a.order, nullptr, st);
   if (e == cudaSuccess) kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, mql, mkl, s, a);
   prof_stop(st, kAttnFwd);
   return e == cudaSuccess ? cudaGetLastError() : e;

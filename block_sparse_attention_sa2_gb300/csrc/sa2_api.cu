@@ -128,7 +128,7 @@ FwdWs fwd_ws(const ShapeArgs& s) {
     w.total = 5 * t;
   }
   w.order = w.total;  // the launch order of the query blocks
-  w.total += align_up(sizeof(int32_t) * (size_t)s.B * s.H * s.Tq);
+  w.total += align_up(sizeof(int32_t) * item_order_ints(s.B * s.H, s.Tq, s.Tk));
   return w;
 }
 
@@ -149,7 +149,7 @@ BwdWs bwd_ws(const ShapeArgs& s) {
   w.do16 = w.v16 + t;
   w.ctr = w.do16 + t;
   w.order = w.ctr + align_up(sizeof(int) * kBwdWorkCounters);
-  w.total = w.order + align_up(sizeof(int32_t) * (size_t)s.B * s.H * s.Tq);
+  w.total = w.order + align_up(sizeof(int32_t) * item_order_ints(s.B * s.H, s.Tq, s.Tk));
   if (s.dtype == SA2_FP32) {  // fp16 residuals of Q and K (the split S product)
     w.q16lo = w.total;
     w.k16lo = w.q16lo + t;

@@ -77,12 +77,16 @@ bool make_token_map(CUtensorMap* map, const void* base, const ShapeArgs& s, int6
 cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsigned* status, cudaStream_t st,
                           __half* dst_lo = nullptr);
 
-// The B*H*Tq query blocks head by head, each head's blocks by descending kept-list length
-// (lengths clamped to [0, Tk]; equal lengths in no fixed order), for the persistent kernels
-// that take one query block per work item; also zeroes *work_ctr (when not null).  One CTA
-// per head.
-cudaError_t launch_item_order(const int32_t* row_cnt, int heads, int Tq, int Tk, int32_t* order, int* work_ctr,
-                              cudaStream_t st);
+// The launch order of the B*H*Tq query blocks for kernels that take one query block per
+// work item: head by head, each head's blocks by descending kept-list length (lengths clamped
+// to [0, Tk]; equal lengths in no fixed order), except that lists too long to start late
+// (longer than (heads - h) * W_h / slots blocks for head h with W_h its total, slots the CTAs
+// resident at once) come first, all heads' together by descending length.  order holds
+// item_order_ints(heads, Tq, Tk) integers: the order, then the scratch of the two passes.
+// Also zeroes *work_ctr (when not null).  One CTA per head and pass.
+size_t item_order_ints(int heads, int Tq, int Tk);
+cudaError_t launch_item_order(const int32_t* row_cnt, int heads, int Tq, int Tk, int slots, int32_t* order,
+                              int* work_ctr, cudaStream_t st);
 
 struct FwdArgs {
   const int32_t* row_cnt;
@@ -128,7 +132,7 @@ struct BwdArgs {
 struct DqArgs {
   const int32_t* row_cnt;
   const int32_t* row_idx;
-  const int32_t* order;  // query blocks, head by head, longest list first (launch_item_order)
+  int32_t* order;  // workspace: the launch order of the query blocks (launch_item_order)
   const float* stats;
   int* work_ctr;  // item counter of the persistent kernel (workspace; zeroed by launch_item_order)
   void* dq;
