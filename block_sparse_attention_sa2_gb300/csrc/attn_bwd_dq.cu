@@ -15,15 +15,25 @@
 // both work on every list entry (TMEM buffers j % 2), one query row per thread, group g on
 // key columns 32g .. 32g+31 of the entry, so that each entry's dS is ready in half the time.
 // Per kept key block j:
-//   S_j  = Q K_j^T     M = 128, N = 64, K = d     (A, B K-major, fp16)
+//   S_j  = Q K_j^T     M = 128, N = 64, K = d     (A = Q from TMEM, B = K_j K-major, fp16)
 //   dP_j = dO V_j^T    M = 128, N = 64, K = d     (A, B K-major, fp16)
 //   row threads: P = exp2(S * scale*log2e - LSE*log2e), dS = P (dP - D), dS as fp16 pairs
 //                into their own TMEM buffer
 //   dQ  += dS_j K_j    M = 128, N = d, K = 64     (A = dS from TMEM, B = K_j MN-major)
-// TMEM columns: S at 0 / 64, dP at 128 / 192, dS at 256 / 288 (all double-buffered), dQ at
-// 384 (d columns).  S_j / dP_j may overwrite their buffers as soon as the row threads have
-// read S_{j-2} / dP_{j-2} out; only the row threads wait for dQ_{j-2} to complete before
-// writing dS_j, so the tensor pipe never drains to let an MMA overwrite an operand.
+// TMEM columns: S at 0 / 64, dP at 128 / 192, dS at 256 / 288 (all double-buffered), the
+// query block's Q at 320 (d / 2 columns of fp16 pairs), dQ at 384 (d columns).  S_j / dP_j
+// may overwrite their buffers as soon as the row threads have read S_{j-2} / dP_{j-2} out;
+// only the row threads wait for dQ_{j-2} to complete before writing dS_j, so the tensor pipe
+// never drains to let an MMA overwrite an operand.
+//
+// Q sits in TMEM as the A operand of S_j because an M128 N64 product with both operands in
+// shared memory reads 6 KB per k-step, more than shared memory delivers in the 32 cycles of
+// the k-step's math; with A in TMEM it reads only the 2 KB of K_j.  The row threads copy
+// each query block's Q out of its shared-memory slot into TMEM (thread = row = TMEM lane),
+// which they do for the next block as soon as the current block's last S_j has been read,
+// before the current block's epilogue.  Q and dO load into a two-slot ring, so the next
+// block's tiles are in shared memory well before it starts.  fp32 calls (the split S
+// product reads Q's fp16 residual too) keep Q in shared memory and a one-slot ring.
 //
 // The CTAs are persistent, one per SM, and take query blocks from a counter until none is
 // left, in the order of launch_item_order (head by head, longest list first within a head,
@@ -44,25 +54,28 @@ constexpr int kItemReaders = 10;  // warps reading the item slot: 1, 2 and the 8
 constexpr int kKStages = 4;
 constexpr int kVStages = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 384;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColQ = 320, kColDQ = 384;
 
 // SPLIT (fp32 calls): Q and K also as fp16 residuals lo = fp16(x - hi) for the split S
 // product Qhi Khi^T + Qhi Klo^T + Qlo Khi^T; the K ring is then 2 deep to fit.
 template <int D, bool SPLIT>
 struct DqSmem {
+  static constexpr bool kQInTmem = !SPLIT;           // Q as the TMEM A operand of S_j
+  static constexpr int kQBuf = SPLIT ? 1 : 2;        // Q / dO ring depth
   static constexpr int kKSt = SPLIT ? 2 : kKStages;  // K ring depth
   static constexpr int kPanels = D / 64;
   static constexpr int kQBytes = 128 * 128 * kPanels;  // 128 rows x 128 B per panel
   static constexpr int kKVBytes = 64 * 128 * kPanels;
   static constexpr int kParts = SPLIT ? 2 : 1;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffQlo = kOffQ + kQBytes;
-  static constexpr int kOffDO = kOffQ + kParts * kQBytes;
-  static constexpr int kOffK = kOffDO + kQBytes;
+  // a Q / dO slot: Q, (Qlo,) dO
+  static constexpr int kQSlot = (kParts + 1) * kQBytes;
+  static constexpr int kSlotQ = 0, kSlotQlo = kQBytes, kSlotDO = kParts * kQBytes;
+  static constexpr int kOffK = kQBuf * kQSlot;
   static constexpr int kOffKlo = kOffK + kKSt * kKVBytes;
   static constexpr int kOffV = kOffK + kParts * kKSt * kKVBytes;
   static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
   static constexpr int kBytes = kOffBar + 512 + 1024;
+  static_assert(kBytes <= (int)kMaxDynSmem, "shared memory");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -100,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-  const uint32_t bar_q = smem_u32(&bars[0]);  // Q, dO of the current query block landed
+  auto bar_q = [&](int qs) { return smem_u32(&bars[qs == 0 ? 0 : 29]); };  // Q, dO of slot qs landed
   auto bar_kfull = [&](int st) { return smem_u32(&bars[1 + st]); };
   auto bar_kempty = [&](int st) { return smem_u32(&bars[5 + st]); };
   auto bar_vfull = [&](int st) { return smem_u32(&bars[9 + st]); };
@@ -112,10 +125,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_dq = smem_u32(&bars[21]);      // every dQ MMA of the query block completed
   const uint32_t bar_gdrain = smem_u32(&bars[22]);  // every dQ MMA of the CTA completed
   const uint32_t bar_sdrain = smem_u32(&bars[23]);  // every S_j / dP_j MMA of the CTA completed
-  const uint32_t bar_qfree = smem_u32(&bars[24]);   // every S_j / dP_j MMA of the query block completed
+  // every S_j / dP_j MMA of the query block in slot qs completed
+  auto bar_qfree = [&](int qs) { return smem_u32(&bars[qs == 0 ? 24 : 30]); };
   auto bar_item_full = [&](int i) { return smem_u32(&bars[25 + i]); };  // item slot i written
   auto bar_item_free = [&](int i) { return smem_u32(&bars[27 + i]); };  // ... and read by every role
-  // 29 barriers occupy the first 232 bytes of the 512-byte barrier area
+  const uint32_t bar_qt = smem_u32(&bars[31]);  // the query block's Q copied into TMEM
+  // 32 barriers occupy the first 256 bytes of the 512-byte barrier area
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffBar + 384);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffBar + 392);
   volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kOffBar + 400);
@@ -150,7 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     *abort_flag = 0;
-    mbar_init(bar_q, 1);
+    for (int qs = 0; qs < L::kQBuf; ++qs) {
+      mbar_init(bar_q(qs), 1);
+      mbar_init(bar_qfree(qs), 1);
+    }
+    mbar_init(bar_qt, 256);
     for (int st = 0; st < kKStages; ++st) {
       mbar_init(bar_kfull(st), 1);
       mbar_init(bar_kempty(st), 1);
@@ -170,7 +189,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_dq, 1);
     mbar_init(bar_gdrain, 1);
     mbar_init(bar_sdrain, 1);
-    mbar_init(bar_qfree, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -215,17 +233,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nkv > 0) {
           const int bh = qb / s.Tq, qi = qb - bh * s.Tq, b = bh / s.H, h = bh - b * s.H;
           const int32_t* list = a.row_idx + (int64_t)qb * s.Tk;
-          // Q, dO of the previous query block are free once its S_j / dP_j MMAs completed
-          if (qn >= 1 && !mbar_wait(bar_qfree, (qn - 1) & 1, wc)) {
+          // slot qs last held Q, dO of query block qn - kQBuf: free once its S_j / dP_j MMAs
+          // completed (the row threads copied that Q into TMEM before its first S_j)
+          const int qs = (int)(qn % L::kQBuf);
+          if (qn >= (uint32_t)L::kQBuf && !mbar_wait(bar_qfree(qs), ((qn / L::kQBuf) - 1) & 1, wc)) {
             ok = false;
             break;
           }
           ++qn;
-          mbar_arrive_expect_tx(bar_q, (1 + L::kParts) * L::kQBytes);
+          const uint32_t slot_base = sbase + qs * L::kQSlot;
+          mbar_arrive_expect_tx(bar_q(qs), L::kQSlot);
           for (int p = 0; p < L::kPanels; ++p) {
-            tma_load_4d(sbase + L::kOffQ + p * 16384, &mq, bar_q, p * 64, qi * s.bq, h, b);
-            if constexpr (SPLIT) tma_load_4d(sbase + L::kOffQlo + p * 16384, &mql, bar_q, p * 64, qi * s.bq, h, b);
-            tma_load_4d(sbase + L::kOffDO + p * 16384, &mdo, bar_q, p * 64, qi * s.bq, h, b);
+            tma_load_4d(slot_base + L::kSlotQ + p * 16384, &mq, bar_q(qs), p * 64, qi * s.bq, h, b);
+            if constexpr (SPLIT)
+              tma_load_4d(slot_base + L::kSlotQlo + p * 16384, &mql, bar_q(qs), p * 64, qi * s.bq, h, b);
+            tma_load_4d(slot_base + L::kSlotDO + p * 16384, &mdo, bar_q(qs), p * 64, qi * s.bq, h, b);
           }
           for (int j = 0; j < nkv; ++j, ++J) {
             const int ks = J % kKStages, vs = J % kVStages;
@@ -261,18 +283,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         x = xn;
       }
       // No copy may still be in flight when the CTA exits, whether the loop ran to its end or
-      // gave up: drain the last load of each stage and the last Q / dO load (each is its
+      // gave up: drain the last load of each stage and of each Q / dO slot (each is its
       // barrier's latest phase).
       for (uint32_t v = nk > kKStages ? nk - kKStages : 0; v < nk; ++v)
         mbar_drain(bar_kfull(v % kKStages), (v / kKStages) & 1, abort_flag);
       for (uint32_t v = nv > kVStages ? nv - kVStages : 0; v < nv; ++v)
         mbar_drain(bar_vfull(v % kVStages), (v / kVStages) & 1, abort_flag);
-      if (qn > 0) mbar_drain(bar_q, (qn - 1) & 1, abort_flag);
+      for (uint32_t v = qn > (uint32_t)L::kQBuf ? qn - L::kQBuf : 0; v < qn; ++v)
+        mbar_drain(bar_q((int)(v % L::kQBuf)), (v / L::kQBuf) & 1, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ S_j, dP_j issuer
     constexpr uint32_t idS = idesc_f16_f32(128, 64, false, false);
-    const uint64_t qd = smem_desc(sbase + L::kOffQ, 16, 1024), dod = smem_desc(sbase + L::kOffDO, 16, 1024);
     bool ok = true;
     uint32_t J = 0, qn = 0;
     for (int n = 0; ok; ++n) {
@@ -280,11 +302,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (x < 0) break;
       const int nkv = item_len(x, false);
       if (nkv == 0) continue;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_q, qn & 1, wc))) {
+      // Q, dO of the block landed in slot qs (and, for Q in TMEM, Q copied there)
+      const int qs = (int)(qn % L::kQBuf);
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_q(qs), (qn / L::kQBuf) & 1, wc) &&
+                                       (!L::kQInTmem || mbar_wait(bar_qt, qn & 1, wc)))) {
         ok = false;
         break;
       }
       ++qn;
+      const uint32_t slot_base = sbase + qs * L::kQSlot;
+      const uint64_t qd = smem_desc(slot_base + L::kSlotQ, 16, 1024), dod = smem_desc(slot_base + L::kSlotDO, 16, 1024);
       for (int j = 0; j < nkv; ++j, ++J) {
         const int ks = J % kKStages, vs = J % kVStages, bb = J & 1;
         // K_j and V_j present, and buffer bb (S_{j-2} / dP_{j-2}) read out by the row
@@ -300,10 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t kd = smem_desc(sbase + L::kOffK + ks * L::kKVBytes, 16, 1024);
         const uint64_t vd = smem_desc(sbase + L::kOffV + vs * L::kKVBytes, 16, 1024);
         if (elect_one()) {
-          mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qd, kd);
+          if constexpr (L::kQInTmem)
+            mma_ts_bkmajor<idS, 64, D / 16>(tmem + kColS + bb * 64, tmem + kColQ, kd);
+          else
+            mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qd, kd);
           if constexpr (SPLIT) {
             const uint64_t kld = smem_desc(sbase + L::kOffKlo + ks * L::kKVBytes, 16, 1024);
-            const uint64_t qld = smem_desc(sbase + L::kOffQlo, 16, 1024);
+            const uint64_t qld = smem_desc(slot_base + L::kSlotQlo, 16, 1024);
             mma_ss_kmajor_acc<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qd, kld);
             mma_ss_kmajor_acc<idS, 128, 64, D / 16>(tmem + kColS + bb * 64, qld, kd);
           }
@@ -314,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       if (!ok) break;
-      if (elect_one()) umma_commit(bar_qfree);
+      if (elect_one()) umma_commit(bar_qfree(qs));
       __syncwarp();
     }
     // no MMA of this warp may still run when TMEM is released, on the abort path too
@@ -368,10 +398,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * sub) << 16);
     const int c_begin = wg * (D / 2), c_end = c_begin + D / 2;
     bool ok = true;
-    uint32_t J = 0, an = 0;
-    for (int n = 0; ok; ++n) {
-      const int x = take_item(n, ok);
-      if (x < 0) break;
+    uint32_t J = 0, an = 0, qc = 0;
+    // Q of the next query block with a non-empty list into TMEM: thread = row = TMEM lane,
+    // group wg the 64 channels of panel wg (for d = 64 group 0 copies the one panel).  Every
+    // S_j MMA reading the TMEM copy of the previous block has completed: the rows read the
+    // last S_j of every earlier block before they get here.
+    auto copy_q = [&]() {
+      const int qs = (int)(qc % L::kQBuf);
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_q(qs), (qc / L::kQBuf) & 1, wc))) return false;
+      ++qc;
+      if (wg < L::kPanels) {
+        const uint8_t* src = smem + qs * L::kQSlot + L::kSlotQ + wg * 16384 + r * 128;
+        uint32_t v[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row sits at chunk c ^ (r % 8)
+          const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
+          v[4 * c] = w.x;
+          v[4 * c + 1] = w.y;
+          v[4 * c + 2] = w.z;
+          v[4 * c + 3] = w.w;
+        }
+        tmem_st32(trow + kColQ + 32 * wg, v);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar_qt);
+      return true;
+    };
+    int x = take_item(0, ok);
+    if (L::kQInTmem && ok && x >= 0 && item_len(x, false) > 0) ok = copy_q();
+    for (int n = 0; ok && x >= 0; ++n) {
       const int nkv = item_len(x, false);
       const int bh = x / s.Tq, qi = x - bh * s.Tq, b = bh / s.H, h = bh - b * s.H;
       const int32_t* list = a.row_idx + (int64_t)x * s.Tk;
@@ -427,6 +483,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar_pready(bb));
       }
       if (!ok) break;
+      // the next query block, so that its Q is in TMEM (and its S_j can start) before this
+      // block's epilogue
+      const int xn = take_item(n + 1, ok);
+      if (!ok) break;
+      if (L::kQInTmem && xn >= 0 && item_len(xn, false) > 0 && !copy_q()) {
+        ok = false;
+        break;
+      }
       // ---- epilogue: dQ = scale * (dS K) accumulated over the list; each group stores
       // half of the channels of every row
       OutT* dqrow = reinterpret_cast<OutT*>(a.dq) + (int64_t)b * a.g_sb + (int64_t)h * a.g_sh + tok * a.g_sn;
@@ -437,25 +501,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c) z[c] = 0.f;
           for (int c0 = c_begin; c0 < c_end; c0 += 32) store_chunk<OutT>(dqrow + c0, z);
         }
-        continue;
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, an & 1, wc))) {
-        ok = false;
-        break;
-      }
-      ++an;
-      tc_fence_after();
+      } else {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, an & 1, wc))) {
+          ok = false;
+          break;
+        }
+        ++an;
+        tc_fence_after();
 #pragma unroll 1
-      for (int c0 = c_begin; c0 < c_end; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(trow + kColDQ + c0, o);
-        tmem_ld_wait(o);
-        float v[32];
+        for (int c0 = c_begin; c0 < c_end; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(trow + kColDQ + c0, o);
+          tmem_ld_wait(o);
+          float v[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(o[c]) * a.scale;
-        if (row_valid) store_chunk<OutT>(dqrow + c0, v);
+          for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(o[c]) * a.scale;
+          if (row_valid) store_chunk<OutT>(dqrow + c0, v);
+        }
+        tc_fence_before();
       }
-      tc_fence_before();
+      x = xn;
     }
   }
   tc_fence_before();

@@ -400,14 +400,18 @@ class DkdvModel(Model):
             pass
 
 class DqModel(Model):
-    """attn_bwd_dq_kernel: items are query blocks with `items[x]` kept key blocks."""
+    """attn_bwd_dq_kernel: items are query blocks with `items[x]` kept key blocks.  Q and dO
+    load into a two-slot ring; the row warps copy each block's Q into TMEM (each warp its
+    part) for the S MMAs, the next block's right after the current block's last S was read."""
 
-    KST, VST = 4, 2
+    KST, VST, QBUF = 4, 2, 2
 
     def make_cta(self, cid):
         c = type("CTA", (), {})()
         c.cid = cid
-        c.q = Bar("q", 1)
+        c.q = [Bar(f"q{i}", 1) for i in range(self.QBUF)]
+        c.qfree = [Bar(f"qfree{i}", 1) for i in range(self.QBUF)]
+        c.qt = Bar("qt", NE)
         c.kfull = [Bar(f"kfull{i}", 1) for i in range(self.KST)]
         c.kempty = [Bar(f"kempty{i}", 1) for i in range(self.KST)]
         c.vfull = [Bar(f"vfull{i}", 1) for i in range(self.VST)]
@@ -416,11 +420,15 @@ class DqModel(Model):
         c.sfree = [Bar(f"sfree{i}", NE) for i in range(2)]
         c.pready = [Bar(f"pready{i}", NE) for i in range(2)]
         c.pfree = [Bar(f"pfree{i}", 1) for i in range(2)]
-        c.dq, c.gdrain, c.sdrain, c.qfree = Bar("dq", 1), Bar("gdrain", 1), Bar("sdrain", 1), Bar("qfree", 1)
+        c.dq, c.gdrain, c.sdrain = Bar("dq", 1), Bar("gdrain", 1), Bar("sdrain", 1)
         c.item_full = [Bar(f"item_full{i}", 1) for i in range(2)]
         c.item_free = [Bar(f"item_free{i}", 2 + NE) for i in range(2)]
         c.slot = [None, None]
-        c.qtag, c.q_readers = None, 0
+        # Q / dO slots: contents, S/dP MMAs reading them, row warps that copied its Q out
+        c.qtag, c.q_readers = [None] * self.QBUF, [0] * self.QBUF
+        c.q_copied = [set(ALL) for _ in range(self.QBUF)]
+        # Q in TMEM: the block each row warp's part holds, S MMAs reading it
+        c.tq, c.tq_readers = {}, 0
         c.ktag, c.k_readers = [None] * self.KST, [0] * self.KST
         c.vtag, c.v_readers = [None] * self.VST, [0] * self.VST
         c.S, c.S_read = [None, None], [set(ALL), set(ALL)]
@@ -436,9 +444,10 @@ class DqModel(Model):
     def complete_tma(self, job):
         c, kind, idx, tag = job
         if kind == "q":
-            check(c.q_readers == 0, "Q/dO overwritten while S/dP MMAs read them")
-            c.qtag = tag
-            c.q.complete_tx(1)
+            check(c.q_readers[idx] == 0, f"Q/dO slot {idx} overwritten while S/dP MMAs read it")
+            check(c.q_copied[idx] >= ALL, f"Q/dO slot {idx} overwritten before every row warp copied its Q")
+            c.qtag[idx], c.q_copied[idx] = tag, set()
+            c.q[idx].complete_tx(1)
         elif kind == "k":
             check(c.k_readers[idx] == 0, f"K stage {idx} overwritten while read")
             c.ktag[idx] = tag
@@ -452,11 +461,13 @@ class DqModel(Model):
         if op[0] == "commit":
             op[1].arrive()
         elif op[0] == "S":
-            _, J, ks, vs, bb, qk = op
-            check(c.qtag == qk and c.ktag[ks] == J and c.vtag[vs] == J, f"S/dP({J}): operands changed")
+            _, J, ks, vs, bb, qk, qs = op
+            check(c.qtag[qs] == qk and c.ktag[ks] == J and c.vtag[vs] == J, f"S/dP({J}): operands changed")
+            check(all(c.tq.get(g) == qk for g in range(NE)), f"S({J}) read a Q in TMEM that is not block {qk}'s")
             check(c.S_read[bb] >= ALL, f"S({J}) overwrote buffer {bb} before it was read")
             c.S[bb], c.S_read[bb] = J, set()
-            c.q_readers -= 1
+            c.q_readers[qs] -= 1
+            c.tq_readers -= 1
             c.k_readers[ks] -= 1
             c.v_readers[vs] -= 1
         else:
@@ -486,11 +497,12 @@ class DqModel(Model):
                 xn = self.fetch_next()
                 nkv = self.items[x]
                 if nkv > 0:
-                    if qn >= 1 and "qfree" not in self.drop:
-                        yield from self.wait(c.qfree, qn - 1)
-                    check(c.q_readers == 0, "Q/dO load issued while S/dP MMAs read them")
-                    c.q.expect_tx(1)
-                    self.tma.append((c, "q", 0, qn))
+                    qs = qn % self.QBUF
+                    if qn >= self.QBUF and "qfree" not in self.drop:
+                        yield from self.wait(c.qfree[qs], qn // self.QBUF - 1)
+                    check(c.q_readers[qs] == 0, f"Q/dO load into slot {qs} issued while S/dP MMAs read it")
+                    c.q[qs].expect_tx(1)
+                    self.tma.append((c, "q", qs, qn))
                     qn += 1
                     for _ in range(nkv):
                         ks, vs = J % self.KST, J % self.VST
@@ -515,8 +527,9 @@ class DqModel(Model):
             yield from self.drain(c.kfull[v % self.KST], v // self.KST)
         for v in range(max(0, nv - self.VST), nv):
             yield from self.drain(c.vfull[v % self.VST], v // self.VST)
-        if qn > 0:
-            yield from self.drain(c.q, qn - 1)
+        for v in range(max(0, qn - self.QBUF), qn):
+            yield from self.drain(c.q[v % self.QBUF], v // self.QBUF)
+
     def s_issuer(self, c):
         J = qn = n = 0
         try:
@@ -528,8 +541,10 @@ class DqModel(Model):
                 nkv = self.items[x]
                 if nkv == 0:
                     continue
-                yield from self.wait(c.q, qn)
-                qk = qn
+                qs, qk = qn % self.QBUF, qn
+                yield from self.wait(c.q[qs], qn // self.QBUF)
+                if "qt" not in self.drop:
+                    yield from self.wait(c.qt, qn)
                 qn += 1
                 for _ in range(nkv):
                     ks, vs, bb = J % self.KST, J % self.VST, J & 1
@@ -537,18 +552,21 @@ class DqModel(Model):
                     if J >= 2 and "sfree" not in self.drop:
                         yield from self.wait(c.sfree[bb], (J >> 1) - 1)
                     yield from self.wait(c.vfull[vs], J // self.VST)
-                    check(c.qtag == qk and c.ktag[ks] == J and c.vtag[vs] == J, f"S({J}) issued on the wrong operands")
-                    c.mmaq[1] += [("S", J, ks, vs, bb, qk), ("commit", c.sfull[bb]), ("commit", c.vempty[vs])]
-                    c.q_readers += 1
+                    check(c.qtag[qs] == qk and c.ktag[ks] == J and c.vtag[vs] == J,
+                          f"S({J}) issued on the wrong operands")
+                    c.mmaq[1] += [("S", J, ks, vs, bb, qk, qs), ("commit", c.sfull[bb]), ("commit", c.vempty[vs])]
+                    c.q_readers[qs] += 1
+                    c.tq_readers += 1
                     c.k_readers[ks] += 1
                     c.v_readers[vs] += 1
                     J += 1
                     yield ("step",)
-                c.mmaq[1].append(("commit", c.qfree))
+                c.mmaq[1].append(("commit", c.qfree[qs]))
         except Aborted:
             pass
         c.mmaq[1].append(("commit", c.sdrain))
         yield from self.mma_drain(c, c.sdrain)
+
     def dq_issuer(self, c):
         J = n = 0
         try:
@@ -575,14 +593,28 @@ class DqModel(Model):
             pass
         c.mmaq[2].append(("commit", c.gdrain))
         yield from self.mma_drain(c, c.gdrain)
+
     def rows(self, c, g):
-        J = an = n = 0
+        J = an = qc = 0
+
+        def copy_q():
+            nonlocal qc
+            qs = qc % self.QBUF
+            yield from self.wait(c.q[qs], qc // self.QBUF)
+            check(c.qtag[qs] == qc, f"row{g}: copies the Q of block {c.qtag[qs]} for block {qc}")
+            check(c.tq_readers == 0, f"row{g}: Q in TMEM overwritten while S MMAs read it")
+            c.tq[g] = qc
+            c.q_copied[qs].add(g)
+            c.qt.arrive()
+            qc += 1
+            yield ("step",)
+
         try:
-            while True:
-                x = yield from self.take(c, n)
-                n += 1
-                if x < 0:
-                    break
+            x = yield from self.take(c, 0)
+            if x >= 0 and self.items[x] > 0:
+                yield from copy_q()
+            n = 0
+            while x >= 0:
                 nkv = self.items[x]
                 for _ in range(nkv):
                     bb, jn = J & 1, J >> 1
@@ -598,16 +630,21 @@ class DqModel(Model):
                     c.pready[bb].arrive()
                     J += 1
                     yield ("step",)
-                if nkv == 0:
-                    continue
-                if "dq" not in self.drop:
-                    yield from self.wait(c.dq, an)
-                an += 1
-                check(c.acc == (x, nkv - 1) and c.acc_inflight == 0, f"row{g}: epilogue of item {x} sees {c.acc}")
-                c.acc_read.add(g)
-                if g == 0:
-                    self.processed.append(x)
-                yield ("step",)
+                n += 1
+                xn = yield from self.take(c, n)
+                if xn >= 0 and self.items[xn] > 0:
+                    yield from copy_q()
+                if nkv > 0:
+                    if "dq" not in self.drop:
+                        yield from self.wait(c.dq, an)
+                    an += 1
+                    check(c.acc == (x, nkv - 1) and c.acc_inflight == 0,
+                          f"row{g}: epilogue of item {x} sees {c.acc}")
+                    c.acc_read.add(g)
+                    if g == 0:
+                        self.processed.append(x)
+                    yield ("step",)
+                x = xn
         except Aborted:
             pass
 

@@ -20,7 +20,7 @@ def test_protocol_holds_on_random_schedules(model):
 @pytest.mark.parametrize("model,wait", [
     (DkdvModel, "kvfree"), (DkdvModel, "empty"), (DkdvModel, "sfree"), (DkdvModel, "pfree"), (DkdvModel, "drain"),
     (DqModel, "qfree"), (DqModel, "kempty"), (DqModel, "vempty"), (DqModel, "sfree"), (DqModel, "pfree"),
-    (DqModel, "dq"),
+    (DqModel, "dq"), (DqModel, "qt"),
     (PoolModel, "empty"), (PoolModel, "accfree"),
 ])
 def test_model_catches_a_missing_wait(model, wait):
