@@ -145,7 +145,9 @@ sa2_status sa2_build_mask_noalloc(const sa2_shape* shape, const void* q, const v
 
 /*
  * Bytes of device workspace sa2_attn_fwd needs: an fp16 copy of v, plus for SA2_FP32
- * inputs fp16 copies of q and k and their fp16 residuals fp16(x - fp16(x)).
+ * inputs fp16 copies of q and k and their fp16 residuals fp16(x - fp16(x)), and the launch
+ * order of the query blocks with its scratch (B*H*Tq + 2*(Tk + 1) + 2*B*H int32, rebuilt by
+ * every call).
  */
 size_t sa2_fwd_workspace_size(const sa2_shape* shape);
 
