@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=0,
                     help="steps of the end-to-end leg (0: the same as --steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager steps instead of replays of a CUDA graph of the step")
     ap.add_argument("--cpu-qblocks", type=int, default=4, help="query blocks of the oracle sample")
     ap.add_argument("--heads", type=int, default=0,
                     help="heads of the workload (default: all); a smaller case for profiler captures")
@@ -269,18 +271,20 @@ KERNEL_FLOPS = {"attn_fwd": 4, "attn_bwd_dkdv": 8, "attn_bwd_dq": 2}
 def phase_rooflines(prof, steps, pairs, d, peak_tflops):
     """Per-phase time and fraction of the bf16 peak, each phase with everything it launches.
 
-    forward  = attn_fwd + its fp16 copy of V (one of the step's three to_f16 launches);
+    forward  = attn_fwd + its fp16 copy of V (one of the step's three to_f16 launches) + its
+               launch order (one of the step's two item_order passes);
     backward = attn_bwd_dkdv + attn_bwd_dq + bwd_preprocess + bwd_pair_union + the fp16
-               copies of Q and K (two of the three to_f16 launches);
+               copies of Q and K (two of the three to_f16 launches) + the dQ kernel's order;
     algorithmic work 4 d (forward) and 10 d (backward) flops per kept pair."""
     def ms(name, share=1.0):
         return prof.get(name, (0, 0.0))[1] * share / steps
 
     conv = prof.get("to_f16", (0, 0.0))
     per_conv = conv[1] / conv[0] if conv[0] else 0.0  # the three copies are the same size
-    fwd_ms = ms("attn_fwd") + per_conv * (conv[0] / steps / 3.0 if conv[0] else 0.0)
+    order = ms("item_order", 0.5)  # two passes of the same size per step
+    fwd_ms = ms("attn_fwd") + per_conv * (conv[0] / steps / 3.0 if conv[0] else 0.0) + order
     bwd_ms = (ms("attn_bwd_dkdv") + ms("attn_bwd_dq") + ms("bwd_preprocess") + ms("bwd_pair_union")
-              + per_conv * (2.0 * conv[0] / steps / 3.0 if conv[0] else 0.0))
+              + per_conv * (2.0 * conv[0] / steps / 3.0 if conv[0] else 0.0) + order)
     out = {}
     for name, t, f in (("forward", fwd_ms, FWD_FLOPS), ("backward", bwd_ms, BWD_FLOPS)):
         tf = f * d * pairs / (t * 1e-3) / 1e12 if t > 0 else None
@@ -380,29 +384,50 @@ def run_native(a, rank, world):
         bus = torch.cuda.get_device_properties(dev).pci_bus_id
     except Exception:
         pass
+    # The timed leg replays one CUDA graph of the whole step (its launches, memsets and the
+    # mask builder's cross-stream waits, exactly the eager step's work) K times; --no-graph
+    # times K eager steps instead.  Per-kernel device times come from a separate leg of K
+    # eager steps under the library's launch profiler, whose events would otherwise sit
+    # inside the timed region.
+    graph = None
+    if not a.no_graph:
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(d)
+        graph.replay()
+        torch.cuda.synchronize()
+        sa2.check_device()
+
+    def timed(run):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(a.steps):
+            run()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        return reduce_max_over_ranks(t0.elapsed_time(t1), dev)
+
     clocks = ClockSampler(bus)
     if rank == 0:
         clocks.start()
+    clocks.mark(True)
+    ms_max = timed(graph.replay if graph is not None else (lambda: step(d)))
+    clocks.mark(False)
+    clk = clocks.stop() if rank == 0 else None
+    sa2.check_device()
+    eager_ms = timed(lambda: step(d)) if graph is not None else ms_max
     sa2.profiler_enable(True)
     sa2.profiler_collect()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks.mark(True)
-    ev0.record(stream)
-    for _ in range(a.steps):
-        step(d)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    clocks.mark(False)
-    if world > 1:
-        torch.distributed.barrier()
+    timed(lambda: step(d))
     sa2.profiler_enable(False)
     prof = sa2.profiler_collect()
     sa2.check_device()
-    ms_max = reduce_max_over_ranks(ev0.elapsed_time(ev1), dev)
-    clk = clocks.stop() if rank == 0 else None
 
     # ---- the mask builder timed on its own: wall time of sa2_build_mask on the stream (its
     # pooling and its second stream's scoring / selection overlap), inputs larger than L2
@@ -469,7 +494,8 @@ def run_native(a, rank, world):
     peaks = measured_peaks()
     value = job_flops_step * a.steps / (ms_max * 1e-3) / 1e12
     kernels = {n: {"launches": c, "ms_per_launch": (m / c if c else 0.0), "total_ms": m} for n, (c, m) in prof.items()}
-    launches = sum(c for c, _ in prof.values())
+    # kernels per profiled launch range: the launch order is two kernels (and a memset)
+    launches = sum(c * (2 if n == "item_order" else 1) for n, (c, _) in prof.items())
     ph = phase_rooflines(prof, a.steps, pairs, D, peaks["bf16_tflops"])
     roof = dominant_roofline(prof, pairs, D, peaks)
     if roof.get("kernel") == "attn_bwd_dkdv":
@@ -486,6 +512,9 @@ def run_native(a, rank, world):
         "metric": metric_name(a.sparsity), "metric_detail": METRIC_DETAIL,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": ms_max / a.steps, "higher_is_better": True,
+        "timing": (f"{a.steps} replays of one CUDA graph of the step (eager steps: {eager_ms / a.steps:.4f} ms); "
+                   if graph is not None else f"{a.steps} eager steps; ")
+                  + "per-kernel times from a separate profiled eager leg",
         "scaling": "strong" if sharded else "weak", "vs_baseline": None,
         "dtype": "bf16 in/out; tcgen05 MMAs bf16 (S) and fp16 (P, dS), fp32 accumulate", "data": "synthetic",
         "config": {"workload": f"{cfg.name} attention layer: B={cfg_job.B}, H={cfg_job.H}, N={N} (latent {'x'.join(map(str, cfg.grid))}), d={D}, bf16, "

@@ -316,11 +316,15 @@ cudaError_t launch_item_order(const int32_t* row_cnt, int heads, int Tq, int Tk,
   o.cur = o.hist + (Tk + 1);
   o.thr = o.cur + (Tk + 1);
   o.nshort = o.thr + heads;
+  prof_start(st, kItemOrder);
   cudaError_t e = cudaMemsetAsync(o.hist, 0, sizeof(int) * 2 * ((size_t)Tk + 1), st);
-  if (e != cudaSuccess) return e;
-  item_split_kernel<<<heads, kOrderThreads, 0, st>>>(row_cnt, Tq, Tk, slots < 1 ? 1 : slots, o);
-  item_order_kernel<<<heads, kOrderThreads, smem, st>>>(row_cnt, Tq, Tk, order, o, work_ctr);
-  return cudaGetLastError();
+  if (e == cudaSuccess) {
+    item_split_kernel<<<heads, kOrderThreads, 0, st>>>(row_cnt, Tq, Tk, slots < 1 ? 1 : slots, o);
+    item_order_kernel<<<heads, kOrderThreads, smem, st>>>(row_cnt, Tq, Tk, order, o, work_ctr);
+    e = cudaGetLastError();
+  }
+  prof_stop(st, kItemOrder);
+  return e;
 }
 
 cudaError_t launch_to_f16(const void* src, const ShapeArgs& s, __half* dst, unsigned* status, cudaStream_t st,

@@ -429,8 +429,8 @@ cudaError_t launch_fwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtens
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)s.B * s.H * s.Tq;
-  prof_start(st, kAttnFwd);
   e = launch_item_order(a.row_cnt, s.B * s.H, s.Tq, s.Tk, sms * (per_sm > 0 ? per_sm : 1), a.order, nullptr, st);
+  prof_start(st, kAttnFwd);
   if (e == cudaSuccess) kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, mql, mkl, s, a);
   prof_stop(st, kAttnFwd);
   return e == cudaSuccess ? cudaGetLastError() : e;

@@ -1417,7 +1417,11 @@ cudaError_t launch_build_mask(const ShapeArgs& s, const void* q, const void* k, 
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  for (int i = 0; i < kChains && e == cudaSuccess; ++i) {
+  // join the chains that took a chunk back into the caller's stream (only those: under stream
+  // capture a chain stream that took no work is not part of the capture, and waiting on an
+  // event recorded there would break it)
+  const int used = std::min(kChains, (BH + L.hc - 1) / L.hc);
+  for (int i = 0; i < used && e == cudaSuccess; ++i) {
     e = cudaEventRecord(aux->done[i], aux->stream[i]);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, aux->done[i], 0);
   }

@@ -25,7 +25,7 @@ std::vector<cudaEvent_t> g_pool;    // events ready for reuse
 
 const char* kNames[kNumKernelIds] = {"pool", "select", "csc", "to_f16", "attn_fwd",
                                      "bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq",
-                                     "bwd_pair_union", "vd_loss", "score_tc"};
+                                     "bwd_pair_union", "vd_loss", "score_tc", "item_order"};
 
 cudaEvent_t take_event() {
   if (!g_pool.empty()) {

@@ -17,7 +17,7 @@ constexpr size_t kMaxDynSmem = 227 * 1024;
 // Launch profiler (profiler.cu): kernel ids and the brackets every launch wrapper calls.
 enum KernelId {
   kPool = 0, kScoreSelect, kCsc, kToF16, kAttnFwd, kBwdPre, kAttnBwd, kAttnBwdDq, kBwdPairs, kVdLoss, kScoreTc,
-  kNumKernelIds
+  kItemOrder, kNumKernelIds
 };
 void prof_start(cudaStream_t st, int id);
 void prof_stop(cudaStream_t st, int id);

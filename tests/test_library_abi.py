@@ -135,7 +135,7 @@ def test_noalloc_rejects_oversized_shapes_on_the_host(lib):
 
 def test_profiler_size_query_needs_no_gpu(lib):
     lib.sa2_profiler_enable(0)
-    assert lib.sa2_profiler_collect(None, 0) == 11
+    assert lib.sa2_profiler_collect(None, 0) == 12
 
 
 def test_vd_loss_rejects_bad_arguments_before_any_launch(lib):
