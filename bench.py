@@ -272,19 +272,22 @@ def phase_rooflines(prof, steps, pairs, d, peak_tflops):
     """Per-phase time and fraction of the bf16 peak, each phase with everything it launches.
 
     forward  = attn_fwd + its fp16 copy of V (one of the step's three to_f16 launches) + its
-               launch order (one of the step's two item_order passes);
+               launch order (one item_order pass);
     backward = attn_bwd_dkdv + attn_bwd_dq + bwd_preprocess + bwd_pair_union + the fp16
-               copies of Q and K (two of the three to_f16 launches) + the dQ kernel's order;
+               copies of Q and K (two of the three to_f16 launches) + the dQ kernel's own launch
+               order when it builds one (a backward given the forward's workspace reuses the
+               forward's);
     algorithmic work 4 d (forward) and 10 d (backward) flops per kept pair."""
     def ms(name, share=1.0):
         return prof.get(name, (0, 0.0))[1] * share / steps
 
     conv = prof.get("to_f16", (0, 0.0))
     per_conv = conv[1] / conv[0] if conv[0] else 0.0  # the three copies are the same size
-    order = ms("item_order", 0.5)  # two passes of the same size per step
-    fwd_ms = ms("attn_fwd") + per_conv * (conv[0] / steps / 3.0 if conv[0] else 0.0) + order
+    passes = prof.get("item_order", (0, 0.0))[0] / steps  # item_order passes per step
+    order_pass = ms("item_order") / passes if passes else 0.0  # the passes are the same size
+    fwd_ms = ms("attn_fwd") + per_conv * (conv[0] / steps / 3.0 if conv[0] else 0.0) + order_pass
     bwd_ms = (ms("attn_bwd_dkdv") + ms("attn_bwd_dq") + ms("bwd_preprocess") + ms("bwd_pair_union")
-              + per_conv * (2.0 * conv[0] / steps / 3.0 if conv[0] else 0.0) + order)
+              + per_conv * (2.0 * conv[0] / steps / 3.0 if conv[0] else 0.0) + ms("item_order") - order_pass)
     out = {}
     for name, t, f in (("forward", fwd_ms, FWD_FLOPS), ("backward", bwd_ms, BWD_FLOPS)):
         tf = f * d * pairs / (t * 1e-3) / 1e12 if t > 0 else None
@@ -494,7 +497,7 @@ def run_native(a, rank, world):
     peaks = measured_peaks()
     value = job_flops_step * a.steps / (ms_max * 1e-3) / 1e12
     kernels = {n: {"launches": c, "ms_per_launch": (m / c if c else 0.0), "total_ms": m} for n, (c, m) in prof.items()}
-    # kernels per profiled launch range: the launch order is two kernels (and a memset)
+    # kernels per profiled launch range: a launch order is two kernels (and a memset)
     launches = sum(c * (2 if n == "item_order" else 1) for n, (c, _) in prof.items())
     ph = phase_rooflines(prof, a.steps, pairs, D, peaks["bf16_tflops"])
     roof = dominant_roofline(prof, pairs, D, peaks)

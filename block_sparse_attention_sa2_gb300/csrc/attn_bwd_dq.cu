@@ -546,7 +546,8 @@ cudaError_t launch_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMa
   if (e != cudaSuccess) return e;
   const long long items = (long long)s.B * s.H * s.Tq;
   const long long grid = items < sms ? items : sms;  // persistent: one CTA per SM
-  e = launch_item_order(a.row_cnt, s.B * s.H, s.Tq, s.Tk, (int)grid, a.order, a.work_ctr, st);
+  // the work counter is zeroed by the pair-list pass of the same call
+  if (!a.order_ready) e = launch_item_order(a.row_cnt, s.B * s.H, s.Tq, s.Tk, (int)grid, a.order, a.work_ctr, st);
   prof_start(st, kAttnBwdDq);
   if (e == cudaSuccess) kern<<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, mv, mdo, mql, mkl, s, a);
   prof_stop(st, kAttnBwdDq);

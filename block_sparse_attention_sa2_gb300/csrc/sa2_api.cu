@@ -319,10 +319,13 @@ sa2_status attn_bwd_impl(const sa2_shape* shape, const void* q, const void* k, c
                      split ? reinterpret_cast<__half*>(wsb + w.k16lo) : nullptr, nullptr};
   const void* src[3] = {q, k, v};
   bool copied[3] = {false, false, false};
+  int32_t* fwd_order = nullptr;
   if (fwd_workspace) {
-    // the forward's fp16 copies: v always, q and k (and their residuals) for fp32 inputs
+    // the forward's fp16 copies: v always, q and k (and their residuals) for fp32 inputs; and
+    // its launch order of the query blocks, a permutation the dQ kernel takes as it is
     const FwdWs fw = fwd_ws(s);
     const uint8_t* fb = static_cast<const uint8_t*>(fwd_workspace);
+    fwd_order = reinterpret_cast<int32_t*>(const_cast<uint8_t*>(fb + fw.order));
     c16[2] = reinterpret_cast<__half*>(const_cast<uint8_t*>(fb + fw.v16));
     copied[2] = true;
     if (split) {
@@ -369,7 +372,8 @@ sa2_status attn_bwd_impl(const sa2_shape* shape, const void* q, const void* k, c
   DqArgs g;
   g.row_cnt = mask->row_cnt;
   g.row_idx = mask->row_idx;
-  g.order = reinterpret_cast<int32_t*>(wsb + w.order);
+  g.order = fwd_order ? fwd_order : reinterpret_cast<int32_t*>(wsb + w.order);
+  g.order_ready = fwd_order != nullptr;
   g.stats = stats;
   g.work_ctr = a.work_ctr + 1;
   g.dq = dq;

@@ -132,9 +132,10 @@ struct BwdArgs {
 struct DqArgs {
   const int32_t* row_cnt;
   const int32_t* row_idx;
-  int32_t* order;  // workspace: the launch order of the query blocks (launch_item_order)
+  int32_t* order;    // workspace: the launch order of the query blocks (launch_item_order)
+  bool order_ready;  // order already holds a launch order (the forward's): not rebuilt
   const float* stats;
-  int* work_ctr;  // item counter of the persistent kernel (workspace; zeroed by launch_item_order)
+  int* work_ctr;  // item counter of the persistent kernel (workspace; zeroed by the pair-list pass)
   void* dq;
   int64_t g_sb, g_sh, g_sn;
   float scale;

@@ -219,7 +219,10 @@ sa2_status sa2_attn_bwd(const sa2_shape* shape, const void* q, const void* k, co
 /*
  * sa2_attn_bwd_with_fwd_ws -- sa2_attn_bwd that takes the fp16 copies the forward already
  * made instead of converting again: the copy of v, and for SA2_FP32 inputs those of q and
- * k and their residuals, which sa2_attn_fwd leaves in its workspace.  The result is the same, bit for bit.
+ * k and their residuals, which sa2_attn_fwd leaves in its workspace; the dQ kernel also
+ * takes the forward's launch order of the query blocks instead of building its own (any
+ * order gives the same dQ: every query block is one CTA's).  The result is the same, bit for
+ * bit.
  *
  *   fwd_ws, fwd_ws_bytes  the workspace of the sa2_attn_fwd call on the same shape, q, k
  *                         and v (the call that produced o, o_lo and lse), ordered before
