@@ -22,13 +22,15 @@
 // choice: they are whole warps), which is the price of the pairing -- about a fifth more
 // MMA work on the Wan-like masks -- against a tensor-core step that is twice as wide.
 //
-// TMEM (512 columns): S^T and dP^T (64 columns each, single), P^T and dS^T as fp16 pairs
-// (32 columns each, double-buffered), dV and dK accumulators (128 each, lanes = keys,
-// columns = channels).  S^T / dP^T are free again as soon as the element-wise warps hold
-// them in registers, so the next sub-tile's S^T, dP^T MMAs never wait for the dV, dK
-// MMAs to complete: the tensor pipe runs S/dP(u+1) behind dV/dK(u-1) without draining.
-// Shared memory: K and V of the pair (32 KB each) and a 4-deep ring of query sub-tiles
-// (Q 16 KB, dO 16 KB, and the sub-tile's log2(e)*LSE and D vectors, 512 B).
+// TMEM (512 columns): S^T and dP^T (64 columns each; single at d = 128, double-buffered at
+// d = 64), P^T and dS^T as fp16 pairs (32 columns each, double-buffered), dV and dK
+// accumulators (d columns each, lanes = keys, columns = channels).  S^T / dP^T are free
+// again as soon as the element-wise warps hold them in registers, so the next sub-tile's
+// S^T, dP^T MMAs never wait for the dV, dK MMAs to complete: the tensor pipe runs S/dP(u+1)
+// behind dV/dK(u-1) without draining (at d = 64, S/dP(u+1) need not even wait for sub-tile
+// u to be read out).  Shared memory: K and V of the pair (16 KB per 64-channel panel each)
+// and a 4-deep ring of query sub-tiles (Q and dO, 8 KB per panel each, and the sub-tile's
+// log2(e)*LSE and D vectors, 512 B).
 //
 // Roles (352 threads, 1 CTA per SM): warp 0 TMA producer, warp 1 TMEM owner and issuer
 // of the S^T / dP^T MMAs, warp 2 issuer of the dV / dK MMAs (each converged, one
@@ -47,9 +49,9 @@
 // inputs within the fp16 range) and P, dS are written as fp16, which keeps 11 significant
 // bits of P and dS against bf16's 8.
 //
-// The tiles are always 128 channels wide: for d = 64 the second channel panel is read past
-// the end of the tensor map and arrives as zeros, and the extra columns of the results are
-// not stored.
+// The channel dimension is a template parameter: d = 128 tiles hold two 64-channel panels,
+// d = 64 tiles one, so that a d = 64 call runs half the k-steps of Sᵀ / dPᵀ and dV / dK
+// products of N = 64 (the accumulators keep their 128 columns, half of them unused).
 #include "sa2_internal.h"
 
 namespace sa2 {
@@ -59,27 +61,41 @@ constexpr int kThreads = 352;
 constexpr int kItemReaders = 10;  // warps reading the item slot: 1, 2 and the 8 element-wise warps
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns
-constexpr uint32_t kColS = 0;     // 64: S^T
-constexpr uint32_t kColDP = 64;   // 64: dP^T
-constexpr uint32_t kColP = 128;   // 2 x 32: P^T, fp16 pairs
-constexpr uint32_t kColDS = 192;  // 2 x 32: dS^T, fp16 pairs
-constexpr uint32_t kColDV = 256;  // 128
-constexpr uint32_t kColDK = 384;  // 128
+// TMEM columns.  d = 128: S^T and dP^T once (64 each), P^T and dS^T as fp16 pairs
+// double-buffered (2 x 32 each), dV and dK (128 each).  d = 64: the accumulators take 64
+// columns each, which leaves room to double-buffer S^T and dP^T as well (buffer b of S^T at
+// 128 b, of dP^T at 128 b + 64), so that S^T(u+1) does not wait for the element-wise warps to
+// have read S^T(u) out.
+template <int D>
+struct DkdvCols {
+  static constexpr int kSBuf = D == 64 ? 2 : 1;  // S^T / dP^T buffers
+  static constexpr uint32_t S(int b) { return 128u * b; }
+  static constexpr uint32_t DP(int b) { return 128u * b + 64u; }
+  static constexpr uint32_t P = 128u * kSBuf, DS = P + 64u;  // 2 x 32 each, after the S^T / dP^T buffers
+  static constexpr uint32_t DV = DS + 64u, DK = DV + (uint32_t)D;
+  static_assert(DK + D <= 512, "TMEM columns");
+  static_assert(D != 128 || (P == 128 && DV == 256 && DK == 384), "the d = 128 layout");
+  static_assert(D != 64 || (P == 256 && DV == 384 && DK == 448), "the d = 64 layout");
+};
 
 // Shared memory (bytes from the 1024-aligned base).  SPLIT (fp32 calls): K and Q also as
 // fp16 residuals lo = fp16(x - hi) for the split product S^T = Khi Qhi^T + Khi Qlo^T +
 // Klo Qhi^T, with a 2-deep sub-tile ring to fit.
-template <bool SPLIT>
+template <bool SPLIT, int D>
 struct DkdvSmem {
+  static constexpr int kPanels = D / 64;          // 64-channel panels of 128 B rows
   static constexpr int kStages = SPLIT ? 2 : 4;
   static constexpr int kShift = SPLIT ? 1 : 2;  // log2(kStages)
-  static constexpr int kOffK = 0;               // 128 key rows x 2 channel panels of 128 B (panel = 16 KB)
-  static constexpr int kOffKlo = 32768;         // (SPLIT)
-  static constexpr int kOffV = SPLIT ? 65536 : 32768;
-  static constexpr int kOffStage = kOffV + 32768;  // stage: Q (2 panels x 64 rows x 128 B), dO (same), stats
-  static constexpr int kStageQ = 0, kStageDO = 16384, kStageStats = 32768, kStageQlo = 33792;
-  static constexpr int kStageBytes = SPLIT ? 33792 + 16384 : 33792;
-  static constexpr uint32_t kStageTx = (SPLIT ? 3 : 2) * 16384 + 512;
+  static constexpr int kKVBytes = 128 * 128 * kPanels;  // 128 key rows x panels (panel = 16 KB)
+  static constexpr int kOffK = 0;
+  static constexpr int kOffKlo = kKVBytes;  // (SPLIT)
+  static constexpr int kOffV = SPLIT ? 2 * kKVBytes : kKVBytes;
+  static constexpr int kOffStage = kOffV + kKVBytes;  // stage: Q (panels x 64 rows x 128 B), dO (same), stats
+  static constexpr int kTileBytes = 64 * 128 * kPanels;
+  static constexpr int kStageQ = 0, kStageDO = kTileBytes, kStageStats = 2 * kTileBytes;
+  static constexpr int kStageQlo = 2 * kTileBytes + 1024;  // (SPLIT)
+  static constexpr int kStageBytes = SPLIT ? kStageQlo + kTileBytes : 2 * kTileBytes + 1024;
+  static constexpr uint32_t kStageTx = (SPLIT ? 3 : 2) * kTileBytes + 512;
   static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
   static_assert(kSmemBytes <= (int)kMaxDynSmem, "shared memory");
@@ -137,13 +153,13 @@ __device__ __forceinline__ void zero_row64(GT* p) {
   for (int c = 0; c < 64 / kVec; ++c) *reinterpret_cast<uint4*>(p + kVec * c) = make_uint4(0, 0, 0, 0);
 }
 
-template <typename GT, bool SPLIT>
+template <typename GT, bool SPLIT, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                          const __grid_constant__ CUtensorMap mql, const __grid_constant__ CUtensorMap mkl,
                          ShapeArgs s, BwdArgs a) {
-  using L = DkdvSmem<SPLIT>;
+  using L = DkdvSmem<SPLIT, D>;
   constexpr int kStages = L::kStages, kStShift = L::kShift;
   constexpr int kOffK = L::kOffK, kOffKlo = L::kOffKlo, kOffV = L::kOffV, kOffStage = L::kOffStage;
   constexpr int kStageQ = L::kStageQ, kStageDO = L::kStageDO, kStageStats = L::kStageStats, kStageQlo = L::kStageQlo;
@@ -156,8 +172,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_kv = smem_u32(&bars[0]);  // K, V of the current pair landed
   auto bar_full = [&](int st) { return smem_u32(&bars[1 + st]); };
   auto bar_empty = [&](int st) { return smem_u32(&bars[5 + st]); };
-  const uint32_t bar_sfull = smem_u32(&bars[9]);   // S^T, dP^T of the current sub-tile in TMEM
-  const uint32_t bar_sfree = smem_u32(&bars[10]);  // ... and read out by the element-wise warps
+  using C = DkdvCols<D>;
+  constexpr int kSBuf = C::kSBuf;
+  // S^T, dP^T of a sub-tile in TMEM buffer b, and read out by the element-wise warps
+  auto bar_sfull = [&](int b) { return smem_u32(&bars[b == 0 ? 9 : 23]); };
+  auto bar_sfree = [&](int b) { return smem_u32(&bars[b == 0 ? 10 : 24]); };
   auto bar_pready = [&](int b) { return smem_u32(&bars[11 + b]); };  // P^T, dS^T buffer b written
   auto bar_pfree = [&](int b) { return smem_u32(&bars[13 + b]); };   // MMAs reading buffer b done
   const uint32_t bar_drain = smem_u32(&bars[15]);   // every dV / dK MMA of the pair completed
@@ -211,8 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_full(st), 1);
       mbar_init(bar_empty(st), 1);
     }
-    mbar_init(bar_sfull, 1);
-    mbar_init(bar_sfree, 256);
+    for (int sb = 0; sb < kSBuf; ++sb) {
+      mbar_init(bar_sfull(sb), 1);
+      mbar_init(bar_sfree(sb), 256);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_pready(i), 256);
       mbar_init(bar_pfree(i), 1);
@@ -272,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar_kv, SPLIT ? 3 * 32768 : 65536);
-          for (int p = 0; p < 2; ++p)
+          mbar_arrive_expect_tx(bar_kv, (SPLIT ? 3 : 2) * L::kKVBytes);
+          for (int p = 0; p < L::kPanels; ++p)
             for (int r = 0; r < 2; ++r) {
               tma_load_4d(sbase + kOffK + p * 16384 + r * 8192, &mk, bar_kv, p * 64, m * 128 + r * 64, h, b);
               if constexpr (SPLIT)
@@ -301,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t stg = sbase + kOffStage + st * kStageBytes;
             const int row = (qi << sub_shift) + hh;  // 64-row sub-tile index within the head
             mbar_arrive_expect_tx(bar_full(st), kStageTx);
-            for (int p = 0; p < 2; ++p) {
+            for (int p = 0; p < L::kPanels; ++p) {
               tma_load_4d(stg + kStageQ + p * 8192, &mq, bar_full(st), p * 64, row * 64, h, b);
               if constexpr (SPLIT) tma_load_4d(stg + kStageQlo + p * 8192, &mql, bar_full(st), p * 64, row * 64, h, b);
               tma_load_4d(stg + kStageDO + p * 8192, &mdo, bar_full(st), p * 64, row * 64, h, b);
@@ -343,9 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++kvn;
       for (int u = 0; u < nsub; ++u, ++U) {
         const int st = U & (kStages - 1);
-        // the stage landed, and S^T / dP^T of sub-tile U - 1 were read out of TMEM
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (U >> kStShift) & 1, wc) &&
-                                         (U == 0 || mbar_wait(bar_sfree, (U - 1) & 1, wc)))) {
+        const int sb = (int)(U % kSBuf);
+        // the stage landed, and S^T / dP^T of sub-tile U - kSBuf were read out of buffer sb
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(bar_full(st), (U >> kStShift) & 1, wc) &&
+                            (U < (uint32_t)kSBuf || mbar_wait(bar_sfree(sb), ((U / kSBuf) - 1) & 1, wc)))) {
           ok = false;
           break;
         }
@@ -353,14 +376,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stg = sbase + kOffStage + st * kStageBytes;
         const uint64_t qd = smem_desc(stg + kStageQ, 16, 1024), dod = smem_desc(stg + kStageDO, 16, 1024);
         if (elect_one()) {
-          mma_ss_kmajor<idS, 128, 64, 8>(tmem + kColS, kd, qd);
+          mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + C::S(sb), kd, qd);
           if constexpr (SPLIT) {
             const uint64_t kld = smem_desc(sbase + kOffKlo, 16, 1024), qld = smem_desc(stg + kStageQlo, 16, 1024);
-            mma_ss_kmajor_acc<idS, 128, 64, 8>(tmem + kColS, kd, qld);
-            mma_ss_kmajor_acc<idS, 128, 64, 8>(tmem + kColS, kld, qd);
+            mma_ss_kmajor_acc<idS, 128, 64, D / 16>(tmem + C::S(sb), kd, qld);
+            mma_ss_kmajor_acc<idS, 128, 64, D / 16>(tmem + C::S(sb), kld, qd);
           }
-          mma_ss_kmajor<idS, 128, 64, 8>(tmem + kColDP, vd, dod);
-          umma_commit(bar_sfull);
+          mma_ss_kmajor<idS, 128, 64, D / 16>(tmem + C::DP(sb), vd, dod);
+          umma_commit(bar_sfull(sb));
         }
         __syncwarp();
       }
@@ -374,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_drain(bar_sdrain, 0, abort_flag);
   } else if (warp == 2) {
     // --------------------------------------------------------- dV, dK issuer (warp 2)
-    constexpr uint32_t idG = idesc_f16_f32(128, 128, false, true);
+    constexpr uint32_t idG = idesc_f16_f32(128, D, false, true);
     bool ok = true;
     uint32_t W = 0;
     for (int n = 0; ok; ++n) {
@@ -398,8 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 8 KB apart; A = P^T / dS^T of buffer bb, 8 columns (16 queries) per k-step
         const uint64_t dod = smem_desc(stg + kStageDO, 8192, 1024), qd = smem_desc(stg + kStageQ, 8192, 1024);
         if (elect_one()) {
-          mma_ts_bmn<idG, 4>(tmem + kColDV, tmem + kColP + bb * 32, dod, w == 0);
-          mma_ts_bmn<idG, 4>(tmem + kColDK, tmem + kColDS + bb * 32, qd, w == 0);
+          mma_ts_bmn<idG, 4>(tmem + C::DV, tmem + C::P + bb * 32, dod, w == 0);
+          mma_ts_bmn<idG, 4>(tmem + C::DK, tmem + C::DS + bb * 32, qd, w == 0);
           umma_commit(bar_empty(st));
           umma_commit(bar_pfree(bb));
         }
@@ -443,23 +466,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           e_next = t + 1 < nu ? list[t + 1] : 0u;
         }
         const bool keep = ((e >> (30 + half)) & 1u) != 0;  // same for the whole warp
-        const int st = U & (kStages - 1), bb = U & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull, U & 1, wc) &&
+        const int st = U & (kStages - 1), bb = U & 1, sb = (int)(U % kSBuf);
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(sb), (U / kSBuf) & 1, wc) &&
                                          mbar_wait(bar_full(st), (U >> kStShift) & 1, wc))) {
           ok = false;
           break;
         }
         tc_fence_after();
         uint32_t sv[32], dv[32];
-        tmem_ld32(trow + kColS + 32 * g, sv);
-        tmem_ld32(trow + kColDP + 32 * g, dv);
+        tmem_ld32(trow + C::S(sb) + 32 * g, sv);
+        tmem_ld32(trow + C::DP(sb) + 32 * g, dv);
         const float4* l4 =
             reinterpret_cast<const float4*>(smem + kOffStage + st * kStageBytes + kStageStats) + 8 * g;
         const float4* d4 = l4 + 16;
         tmem_ld_wait(sv);
         tmem_ld_wait(dv);
         tc_fence_before();
-        mbar_arrive(bar_sfree);
+        mbar_arrive(bar_sfree(sb));
         uint32_t pw[16], dw[16];
         if (keep) {
 #pragma unroll
@@ -489,8 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        tmem_st16(trow + kColP + bb * 32 + 16 * g, pw);
-        tmem_st16(trow + kColDS + bb * 32 + 16 * g, dw);
+        tmem_st16(trow + C::P + bb * 32 + 16 * g, pw);
+        tmem_st16(trow + C::DS + bb * 32 + 16 * g, dw);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar_pready(bb));
@@ -513,18 +536,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++an;
       tc_fence_after();
-      uint32_t xv[32], yv[32];
-      tmem_ld32(trow + kColDK + c0, xv);
-      tmem_ld32(trow + kColDK + c0 + 32, yv);
-      tmem_ld_wait(xv);
-      tmem_ld_wait(yv);
-      if (store) store_row64<GT>(dkp, xv, yv, a.scale);
-      tmem_ld32(trow + kColDV + c0, xv);
-      tmem_ld32(trow + kColDV + c0 + 32, yv);
-      tmem_ld_wait(xv);
-      tmem_ld_wait(yv);
+      if (c0 < D) {  // (warp-uniform; at d = 64 the second group has no channels and no columns)
+        uint32_t xv[32], yv[32];
+        tmem_ld32(trow + C::DK + c0, xv);
+        tmem_ld32(trow + C::DK + c0 + 32, yv);
+        tmem_ld_wait(xv);
+        tmem_ld_wait(yv);
+        if (store) store_row64<GT>(dkp, xv, yv, a.scale);
+        tmem_ld32(trow + C::DV + c0, xv);
+        tmem_ld32(trow + C::DV + c0 + 32, yv);
+        tmem_ld_wait(xv);
+        tmem_ld_wait(yv);
+        if (store) store_row64<GT>(dvp, xv, yv, 1.f);
+      }
       tc_fence_before();
-      if (store) store_row64<GT>(dvp, xv, yv, 1.f);
     }
   }
   tc_fence_before();
@@ -606,11 +631,11 @@ __global__ void __launch_bounds__(32 * kUnionWarps) pair_union_kernel(const int3
   if (bad) report_error(status, kDevErrBounds);
 }
 
-template <typename GT, bool SPLIT>
+template <typename GT, bool SPLIT, int D>
 cudaError_t launch_bwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, const CUtensorMap& mql, const CUtensorMap& mkl, const BwdArgs& a,
                          cudaStream_t st) {
-  constexpr int kSmemBytes = DkdvSmem<SPLIT>::kSmemBytes;
+  constexpr int kSmemBytes = DkdvSmem<SPLIT, D>::kSmemBytes;
   const long long pairs = (long long)s.B * s.H * ((s.Tk + 1) / 2);
   prof_start(st, kBwdPairs);
   pair_union_kernel<<<(unsigned)((pairs + kUnionWarps - 1) / kUnionWarps), 32 * kUnionWarps, 0, st>>>(
@@ -618,7 +643,7 @@ cudaError_t launch_bwd_t(const ShapeArgs& s, const CUtensorMap& mq, const CUtens
   prof_stop(st, kBwdPairs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = attn_bwd_dkdv_kernel<GT, SPLIT>;
+  auto kern = attn_bwd_dkdv_kernel<GT, SPLIT, D>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -642,8 +667,11 @@ cudaError_t launch_attn_bwd(const ShapeArgs& s, const CUtensorMap& mq, const CUt
   if (s.Tq > 32 * kMaxTqWords || (long long)s.B * s.H * ((s.Tk + 1) / 2) > INT32_MAX) return cudaErrorInvalidValue;
   // fp32 calls take the split S product
   if (s.dtype != 0 && (!mql || !mkl)) return cudaErrorInvalidValue;
-  return s.dtype == 0 ? launch_bwd_t<__nv_bfloat16, false>(s, mq, mk, mv, mdo, mq, mk, a, st)
-                      : launch_bwd_t<float, true>(s, mq, mk, mv, mdo, *mql, *mkl, a, st);
+  if (s.d == 128)
+    return s.dtype == 0 ? launch_bwd_t<__nv_bfloat16, false, 128>(s, mq, mk, mv, mdo, mq, mk, a, st)
+                        : launch_bwd_t<float, true, 128>(s, mq, mk, mv, mdo, *mql, *mkl, a, st);
+  return s.dtype == 0 ? launch_bwd_t<__nv_bfloat16, false, 64>(s, mq, mk, mv, mdo, mq, mk, a, st)
+                      : launch_bwd_t<float, true, 64>(s, mq, mk, mv, mdo, *mql, *mkl, a, st);
 }
 
 }  // namespace sa2

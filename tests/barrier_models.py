@@ -195,14 +195,18 @@ ALL = frozenset(range(NE))
 
 
 class DkdvModel(Model):
-    """attn_bwd_dkdv_kernel: items are key-block pairs of `items[x]` 64-row query sub-tiles."""
+    """attn_bwd_dkdv_kernel: items are key-block pairs of `items[x]` 64-row query sub-tiles.
+    SBUF is the number of S^T / dP^T buffers in TMEM (1 at d = 128, 2 at d = 64)."""
 
     STAGES = 4
+    SBUF = 1
 
     def make_cta(self, cid):
         c = type("CTA", (), {})()
         c.cid = cid
-        c.kv, c.sfull, c.sfree = Bar("kv", 1), Bar("sfull", 1), Bar("sfree", NE)
+        c.kv = Bar("kv", 1)
+        c.sfull = [Bar(f"sfull{i}", 1) for i in range(self.SBUF)]
+        c.sfree = [Bar(f"sfree{i}", NE) for i in range(self.SBUF)]
         c.full = [Bar(f"full{i}", 1) for i in range(self.STAGES)]
         c.empty = [Bar(f"empty{i}", 1) for i in range(self.STAGES)]
         c.pready = [Bar(f"pready{i}", NE) for i in range(2)]
@@ -214,7 +218,7 @@ class DkdvModel(Model):
         c.stage = [None] * self.STAGES
         c.stage_readers = [set() for _ in range(self.STAGES)]
         c.kv_tag, c.kv_readers = None, 0
-        c.S, c.S_read, c.DP = None, set(), None
+        c.S, c.S_read, c.DP = [None] * self.SBUF, [set() for _ in range(self.SBUF)], [None] * self.SBUF
         c.P, c.P_readers = [dict(), dict()], [0, 0]
         c.acc, c.acc_read, c.acc_inflight = None, set(ALL), 0
         c.mmaq = {1: [], 2: []}
@@ -243,14 +247,15 @@ class DkdvModel(Model):
             op[1].arrive()
         elif kind in ("S", "DP"):
             _, U, st, kvk = op
+            sb = U % self.SBUF
             check(c.stage[st] == U and c.kv_tag == kvk, f"{kind}({U}): operands changed before completion")
             c.stage_readers[st].discard(kind)
             c.kv_readers -= 1
             if kind == "S":
-                check(c.S is None or c.S_read >= ALL, f"S({U}) overwrote S({c.S}) before it was read")
-                c.S, c.S_read = U, set()
+                check(c.S[sb] is None or c.S_read[sb] >= ALL, f"S({U}) overwrote S({c.S[sb]}) before it was read")
+                c.S[sb], c.S_read[sb] = U, set()
             else:
-                c.DP = U
+                c.DP[sb] = U
         else:
             _, W, st, bb, item, w = op
             check(c.stage[st] == W and all(c.P[bb].get(g) == W for g in range(NE)),
@@ -320,12 +325,12 @@ class DkdvModel(Model):
                 kvk = (x, kvn)
                 kvn += 1
                 for _ in range(nsub):
-                    st = U % self.STAGES
+                    st, sb = U % self.STAGES, U % self.SBUF
                     yield from self.wait(c.full[st], U // self.STAGES)
-                    if U >= 1 and "sfree" not in self.drop:
-                        yield from self.wait(c.sfree, U - 1)
+                    if U >= self.SBUF and "sfree" not in self.drop:
+                        yield from self.wait(c.sfree[sb], U // self.SBUF - 1)
                     check(c.stage[st] == U and c.kv_tag == kvk, f"S({U}) issued on the wrong operands")
-                    c.mmaq[1] += [("S", U, st, kvk), ("DP", U, st, kvk), ("commit", c.sfull)]
+                    c.mmaq[1] += [("S", U, st, kvk), ("DP", U, st, kvk), ("commit", c.sfull[sb])]
                     c.kv_readers += 2
                     U += 1
                     yield ("step",)
@@ -370,14 +375,14 @@ class DkdvModel(Model):
                     break
                 nsub = self.items[x]
                 for _ in range(nsub):
-                    st, bb = U % self.STAGES, U & 1
-                    yield from self.wait(c.sfull, U)
+                    st, bb, sb = U % self.STAGES, U & 1, U % self.SBUF
+                    yield from self.wait(c.sfull[sb], U // self.SBUF)
                     yield from self.wait(c.full[st], U // self.STAGES)
-                    check(c.S == U and c.DP == U, f"ew{g}: reads S({U}) while TMEM holds S({c.S})")
+                    check(c.S[sb] == U and c.DP[sb] == U, f"ew{g}: reads S({U}) while TMEM holds S({c.S[sb]})")
                     check(c.stage[st] == U, f"ew{g}: statistics of sub-tile {U} replaced")
-                    c.S_read.add(g)
+                    c.S_read[sb].add(g)
                     c.stage_readers[st].discard(f"ew{g}")
-                    c.sfree.arrive()
+                    c.sfree[sb].arrive()
                     yield ("step",)
                     if U >= 2 and "pfree" not in self.drop:
                         yield from self.wait(c.pfree[bb], (U >> 1) - 1)
@@ -398,6 +403,12 @@ class DkdvModel(Model):
                 yield ("step",)
         except Aborted:
             pass
+
+class DkdvModel64(DkdvModel):
+    """attn_bwd_dkdv_kernel at d = 64: S^T / dP^T double-buffered in TMEM."""
+
+    SBUF = 2
+
 
 class DqModel(Model):
     """attn_bwd_dq_kernel: items are query blocks with `items[x]` kept key blocks.  Q and dO

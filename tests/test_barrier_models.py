@@ -6,12 +6,12 @@ intended phase and never overwrite data before its readers are done.  Each model
 catch every wait that is taken out of it."""
 import pytest
 
-from tests.barrier_models import DkdvModel, DqModel, PoolModel, run_forward_trials, run_trials
+from tests.barrier_models import DkdvModel, DkdvModel64, DqModel, PoolModel, run_forward_trials, run_trials
 
 TRIALS = 150
 
 
-@pytest.mark.parametrize("model", [DkdvModel, DqModel, PoolModel], ids=["dkdv", "dq", "pool"])
+@pytest.mark.parametrize("model", [DkdvModel, DkdvModel64, DqModel, PoolModel], ids=["dkdv", "dkdv64", "dq", "pool"])
 def test_protocol_holds_on_random_schedules(model):
     err = run_trials(model, TRIALS)
     assert err is None, err
@@ -19,6 +19,7 @@ def test_protocol_holds_on_random_schedules(model):
 
 @pytest.mark.parametrize("model,wait", [
     (DkdvModel, "kvfree"), (DkdvModel, "empty"), (DkdvModel, "sfree"), (DkdvModel, "pfree"), (DkdvModel, "drain"),
+    (DkdvModel64, "sfree"), (DkdvModel64, "pfree"), (DkdvModel64, "empty"),
     (DqModel, "qfree"), (DqModel, "kempty"), (DqModel, "vempty"), (DqModel, "sfree"), (DqModel, "pfree"),
     (DqModel, "dq"), (DqModel, "qt"),
     (PoolModel, "empty"), (PoolModel, "accfree"),
@@ -40,7 +41,7 @@ def test_forward_model_catches_a_missing_wait(wait):
     assert run_forward_trials(TRIALS, drop={wait}) is not None, f"forward without {wait} passed"
 
 
-@pytest.mark.parametrize("model", [DkdvModel, DqModel, PoolModel], ids=["dkdv", "dq", "pool"])
+@pytest.mark.parametrize("model", [DkdvModel, DkdvModel64, DqModel, PoolModel], ids=["dkdv", "dkdv64", "dq", "pool"])
 def test_abort_path_leaves_nothing_in_flight(model):
     """Waits expire at random: every role leaves its loops, and when the CTA frees its tensor
     memory and exits no copy or MMA is still in flight (and no drain waits forever)."""
@@ -53,7 +54,7 @@ def test_forward_abort_path_leaves_nothing_in_flight():
     assert err is None, err
 
 
-@pytest.mark.parametrize("model", [DkdvModel, DqModel, PoolModel, "fwd"], ids=["dkdv", "dq", "pool", "fwd"])
+@pytest.mark.parametrize("model", [DkdvModel, DkdvModel64, DqModel, PoolModel, "fwd"], ids=["dkdv", "dkdv64", "dq", "pool", "fwd"])
 @pytest.mark.parametrize("skipped", ["abort_drain", "abort_mma_drain"])
 def test_model_catches_a_drain_skipped_on_abort(model, skipped):
     """Without the producer's drain of its issued copies, or with the issuers' drains giving
