@@ -37,10 +37,10 @@ from workload import CONFIGS, make_inputs  # noqa: E402
 FWD_FLOPS, BWD_FLOPS = 4, 10  # per kept (query, key) pair and channel
 
 # DRAM bytes (read + write) of one attn_bwd_dkdv launch per head of the Wan2.1-14B-720p
-# workload at its calibrated 95 % sparsity: an ncu capture of the 4-head case (761.7 MB read
-# + 141.1 MB written, profiles/) divided by its heads, the heads being independent.  Set to
+# workload at its calibrated 95 % sparsity: an ncu capture of the 4-head case (776.9 MB read
+# + 141.7 MB written, profiles/) divided by its heads, the heads being independent.  Set to
 # None whenever the kernel changes until it has been captured again.
-BWD_TRAFFIC_PER_HEAD = (761.684736e6 + 141.071872e6) / 4
+BWD_TRAFFIC_PER_HEAD = (776.931840e6 + 141.679616e6) / 4
 BWD_TRAFFIC_WORKLOAD = ("wan2.1-14b-720p", 0.95)
 
 
