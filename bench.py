@@ -395,11 +395,16 @@ def run_native(a, rank, world):
     graph = None
     if not a.no_graph:
         torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step(d)
-        graph.replay()
-        torch.cuda.synchronize()
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step(d)
+            graph.replay()
+            torch.cuda.synchronize()
+        except Exception as err:  # a capture this driver refuses: time eager steps instead
+            print(f"bench: CUDA graph capture failed ({err}); timing eager steps", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize()
         sa2.check_device()
 
     def timed(run):
