@@ -78,8 +78,8 @@ def test_bwd_random_masks_empty_rows_unused_keys_and_scale(sa2):
     _full_check(sa2, cfg, x, mask, scale=0.05)
 
 
-@pytest.mark.parametrize("d,bq", [(64, 128), (128, 64)])
-def test_bwd_many_items_per_persistent_cta(sa2, d, bq):
+@pytest.mark.parametrize("d,bq,dtype", [(64, 128, "bf16"), (128, 64, "bf16"), (64, 128, "fp32")])
+def test_bwd_many_items_per_persistent_cta(sa2, d, bq, dtype):
     """The dK/dV and dQ kernels keep one CTA per SM and take key-block pairs / query blocks
     from a counter.  48 short heads give 480 pairs and 480 or 912 query blocks, several per
     CTA, so barrier phases run across items.  Empty items sit between full ones: a head
@@ -87,7 +87,7 @@ def test_bwd_many_items_per_persistent_cta(sa2, d, bq):
     dense head with long lists.  Every gradient element is checked, and a second call must
     repeat the first bit for bit (the counter is reset per call, and each item is computed
     by one CTA whatever the assignment)."""
-    cfg, x = small_case(f"many-items-d{d}-bq{bq}", 2, 24, 1200, d, "bf16", bq, 64, seed=61)
+    cfg, x = small_case(f"many-items-d{d}-bq{bq}-{dtype}", 2, 24, 1200, d, dtype, bq, 64, seed=61)
     assert cfg.B * cfg.H * ((cfg.Tk + 1) // 2) == 480 and cfg.B * cfg.H * cfg.Tq >= 480
     rng = np.random.default_rng(17)
     mask = (rng.random((cfg.B, cfg.H, cfg.Tq, cfg.Tk)) < 0.2).astype(np.uint8)
